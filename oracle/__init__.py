@@ -1,0 +1,161 @@
+"""fp64 CPU oracle for the differentiable CSR conjugate-gradient solve (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY.  The oracle is the checker that the CUDA library is
+compared against; it is loaded only by the test suite, by the smoke check and
+by the benchmark's CPU-baseline leg, never by the library itself.  It shares no
+code with the CUDA path.
+
+Each function follows "torch-sla: Differentiable Sparse Linear Algebra with
+Adjoint Solvers and Sparse Tensor Parallelism for PyTorch" (Chi, Wen),
+technical summary, Methodology sections 1 (native iterative solver, .matvec /
+.solve) and 2 (adjoint differentiation framework, linear systems); see the C
+source ``sla_oracle.c`` for the readings taken where the pages are silent.
+
+Parity pins live in ``tests/test_oracle_*.py``.  Every oracle function is
+pinned there against something other than itself (dense linear algebra on
+tiny grids, closed-form eigenvalues and CG bounds, finite termination, the
+adjoint identity, central finite differences, exact scaling invariants).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sla_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+STATUS = {0: "OK", 1: "NOT_CONVERGED", 2: "BREAKDOWN", 5: "NONFINITE"}
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle with gcc (-O2 -ffp-contract=off: no fused multiply-add)."""
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        tmp = out + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+                        "-o", tmp, src, "-lm"], check=True)
+        os.replace(tmp, out)
+    return out
+
+
+def _bind(lib):
+    i64, p = ctypes.c_int64, ctypes.c_void_p
+    lib.orc_spmv.argtypes = [i64, p, p, p, p, p]
+    lib.orc_spmv.restype = None
+    lib.orc_dot.argtypes = [i64, p, p]
+    lib.orc_dot.restype = ctypes.c_double
+    lib.orc_diagonal.argtypes = [i64, p, p, p, p]
+    lib.orc_diagonal.restype = None
+    lib.orc_cg.argtypes = [i64, p, p, p, p, p, ctypes.c_double, i64, ctypes.c_int, p, p,
+                           ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]
+    lib.orc_cg.restype = ctypes.c_int
+    lib.orc_grad_values.argtypes = [i64, p, p, p, p, p]
+    lib.orc_grad_values.restype = None
+    lib.orc_cg_adjoint.argtypes = [i64, p, p, p, p, p, ctypes.c_double, i64, ctypes.c_int, p, p,
+                                   ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]
+    lib.orc_cg_adjoint.restype = ctypes.c_int
+    return lib
+
+
+def load(path: Optional[str] = None):
+    """Load (building if needed) the oracle shared library."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _csr(row_ptr, col_idx, values):
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int64)
+    ci = np.ascontiguousarray(col_idx, dtype=np.int32)
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    return rp, ci, v
+
+
+def spmv(row_ptr, col_idx, values, x, lib=None) -> np.ndarray:
+    lib = lib or load()
+    rp, ci, v = _csr(row_ptr, col_idx, values)
+    n = rp.shape[0] - 1
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty(n, dtype=np.float64)
+    lib.orc_spmv(n, _ptr(rp), _ptr(ci), _ptr(v), _ptr(x), _ptr(y))
+    return y
+
+
+def dot(a, b, lib=None) -> float:
+    lib = lib or load()
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    b = np.ascontiguousarray(b, dtype=np.float64)
+    return float(lib.orc_dot(a.shape[0], _ptr(a), _ptr(b)))
+
+
+def cg(row_ptr, col_idx, values, b, x0=None, rtol: float = 1e-10, maxit: int = 100000, precond: int = 0,
+       history: bool = False, lib=None) -> dict:
+    """Solve A x = b by CG; returns dict(x, iters, rel_res, status, history)."""
+    lib = lib or load()
+    rp, ci, v = _csr(row_ptr, col_idx, values)
+    n = rp.shape[0] - 1
+    b = np.ascontiguousarray(b, dtype=np.float64)
+    x0c = None if x0 is None else np.ascontiguousarray(x0, dtype=np.float64)
+    x = np.empty(n, dtype=np.float64)
+    h = np.full(maxit + 1, np.nan) if history else None
+    it = ctypes.c_int64(0)
+    rr = ctypes.c_double(0.0)
+    st = lib.orc_cg(n, _ptr(rp), _ptr(ci), _ptr(v), _ptr(b), _ptr(x0c), float(rtol), int(maxit), int(precond),
+                    _ptr(x), _ptr(h), ctypes.byref(it), ctypes.byref(rr))
+    out = {"x": x, "iters": int(it.value), "rel_res": float(rr.value), "status": int(st)}
+    if history:
+        out["history"] = h[: it.value + 1].copy()
+    return out
+
+
+def grad_values(row_ptr, col_idx, lam, x, lib=None) -> np.ndarray:
+    lib = lib or load()
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int64)
+    ci = np.ascontiguousarray(col_idx, dtype=np.int32)
+    n = rp.shape[0] - 1
+    lam = np.ascontiguousarray(lam, dtype=np.float64)
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    gv = np.empty(ci.shape[0], dtype=np.float64)
+    lib.orc_grad_values(n, _ptr(rp), _ptr(ci), _ptr(lam), _ptr(x), _ptr(gv))
+    return gv
+
+
+def cg_adjoint(row_ptr, col_idx, values, x, g, rtol: float = 1e-10, maxit: int = 100000, precond: int = 0,
+               lib=None) -> dict:
+    """Adjoint backward: dict(grad_b = lambda, grad_values, iters, rel_res, status)."""
+    lib = lib or load()
+    rp, ci, v = _csr(row_ptr, col_idx, values)
+    n = rp.shape[0] - 1
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    gb = np.empty(n, dtype=np.float64)
+    gv = np.empty(ci.shape[0], dtype=np.float64)
+    it = ctypes.c_int64(0)
+    rr = ctypes.c_double(0.0)
+    st = lib.orc_cg_adjoint(n, _ptr(rp), _ptr(ci), _ptr(v), _ptr(x), _ptr(g), float(rtol), int(maxit),
+                            int(precond), _ptr(gb), _ptr(gv), ctypes.byref(it), ctypes.byref(rr))
+    return {"grad_b": gb, "grad_values": gv, "iters": int(it.value), "rel_res": float(rr.value),
+            "status": int(st)}
+
+
+def cg_batched(row_ptr, col_idx, values_b, b_b, rtol, maxit, precond=0, history=False, lib=None) -> list:
+    """Batched shared-pattern solve: one fp64 CG per system on the (possibly fp32-rounded) inputs."""
+    return [cg(row_ptr, col_idx, values_b[s], b_b[s], None, rtol, maxit, precond, history, lib)
+            for s in range(values_b.shape[0])]
+
+
+def cg_adjoint_batched(row_ptr, col_idx, values_b, x_b, g_b, rtol, maxit, precond=0, lib=None) -> list:
+    return [cg_adjoint(row_ptr, col_idx, values_b[s], x_b[s], g_b[s], rtol, maxit, precond, lib)
+            for s in range(values_b.shape[0])]

@@ -1,0 +1,181 @@
+/*
+ * Plain fp64 CPU oracle for the differentiable CSR conjugate-gradient solve.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the checker, not the product: only
+ * the test suite, the smoke check and the benchmark's CPU-baseline leg load it.
+ * It shares no code, header or constant with the CUDA library.  It is written
+ * to be read against the method's description, not to be fast: one thread,
+ * sequential sums in index order, no blocking, no fusion.  Build with
+ * -ffp-contract=off so that a*b+c is always a rounded multiply then a rounded
+ * add on every host (x86_64 and aarch64 give identical results).
+ *
+ * Source of the method: "torch-sla: Differentiable Sparse Linear Algebra with
+ * Adjoint Solvers and Sparse Tensor Parallelism for PyTorch" (Chi, Wen),
+ * technical summary:
+ *   - Methodology, 1 "Unified backend abstraction": the PyTorch-native
+ *     iterative solver (conjugate gradient on the GPU) and the .matvec/.solve API;
+ *   - Methodology, 2 "Adjoint differentiation framework", linear systems: for
+ *     Ax=b the backward solves A^T lambda = dL/dx once, and the gradient with
+ *     respect to the matrix is -lambda_i x_j on the sparsity pattern only;
+ *     graph O(1), memory O(n + nnz);
+ *   - Significance: the native backend uses Jacobi preconditioning.
+ * The pages do not spell out the CG variant, the stopping rule or the
+ * treatment of breakdown.  Readings taken here (textbook Hestenes-Stiefel CG,
+ * stop when ||r_k||_2 <= rtol ||b||_2 on the recursively updated residual,
+ * Jacobi M = diag(A) applied as r_i / A_ii, breakdown when p.Ap <= 0):
+ *   iteration count = number of products A p inside the loop;
+ *   b == 0 gives x = 0 after 0 iterations;
+ *   a non-finite ||b||, r.r or p.Ap stops with status NONFINITE;
+ *   p.Ap <= 0 (finite) stops with BREAKDOWN, x left at the last iterate;
+ *   with Jacobi, a diagonal entry <= 0 or missing stops with BREAKDOWN before
+ *   the first iteration.
+ *
+ * Status codes returned: 0 converged, 1 not converged after maxit, 2 breakdown,
+ * 5 non-finite.
+ *
+ * Layout: CSR with int64 row_ptr[n+1], int32 col_idx[nnz], double values[nnz].
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_NOT_CONVERGED 1
+#define ORC_BREAKDOWN 2
+#define ORC_NONFINITE 5
+
+/* y = A x: for every row, the sum over its stored entries in storage order. */
+void orc_spmv(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const double *values,
+              const double *x, double *y) {
+  for (int64_t i = 0; i < n; ++i) {
+    double s = 0.0;
+    for (int64_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k) s += values[k] * x[col_idx[k]];
+    y[i] = s;
+  }
+}
+
+/* a . b, summed in index order. */
+double orc_dot(int64_t n, const double *a, const double *b) {
+  double s = 0.0;
+  for (int64_t i = 0; i < n; ++i) s += a[i] * b[i];
+  return s;
+}
+
+/* diag[i] = A_ii (0 when row i stores no diagonal entry). */
+void orc_diagonal(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const double *values,
+                  double *diag) {
+  for (int64_t i = 0; i < n; ++i) {
+    diag[i] = 0.0;
+    for (int64_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k)
+      if (col_idx[k] == i) diag[i] = values[k];
+  }
+}
+
+/*
+ * Conjugate gradient (Hestenes-Stiefel) for A x = b, optionally Jacobi
+ * preconditioned (precond = 1: M = diag(A), z = M^{-1} r computed as r_i / A_ii).
+ *
+ *   r = b - A x0 (r = b when x0 is NULL), z = M^{-1} r, p = z, rho = r.z
+ *   repeat: q = A p; alpha = rho / (p.q); x += alpha p; r -= alpha q;
+ *           stop when ||r|| <= rtol ||b||; z = M^{-1} r; rho' = r.z;
+ *           beta = rho'/rho; p = z + beta p; rho = rho'.
+ *
+ * x       : output, n entries (the last iterate on every exit).
+ * history : NULL or maxit+1 entries; history[k] = ||r_k|| / ||b|| for k = 0..iters.
+ * Returns the status; *iters and *rel_res (= ||r|| / ||b|| at exit) are set.
+ */
+int orc_cg(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const double *values,
+           const double *b, const double *x0, double rtol, int64_t maxit, int precond,
+           double *x, double *history, int64_t *iters, double *rel_res) {
+  double *r = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  double *z = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  double *p = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  double *q = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  double *d = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  int status = ORC_NOT_CONVERGED;
+  *iters = 0;
+  *rel_res = 0.0;
+
+  double nb = sqrt(orc_dot(n, b, b));
+  if (x0) memcpy(x, x0, sizeof(double) * (size_t)n);
+  else for (int64_t i = 0; i < n; ++i) x[i] = 0.0;
+  if (!isfinite(nb)) { status = ORC_NONFINITE; goto done; }
+  if (nb == 0.0) {
+    for (int64_t i = 0; i < n; ++i) x[i] = 0.0;
+    if (history) history[0] = 0.0;
+    status = ORC_OK;
+    goto done;
+  }
+  if (precond == 1) {
+    orc_diagonal(n, row_ptr, col_idx, values, d);
+    for (int64_t i = 0; i < n; ++i) {
+      if (!isfinite(d[i])) { status = ORC_NONFINITE; goto done; }
+      if (!(d[i] > 0.0)) { status = ORC_BREAKDOWN; goto done; }
+    }
+  }
+
+  if (x0) {
+    orc_spmv(n, row_ptr, col_idx, values, x, q);
+    for (int64_t i = 0; i < n; ++i) r[i] = b[i] - q[i];
+  } else {
+    for (int64_t i = 0; i < n; ++i) r[i] = b[i];
+  }
+  double rr = orc_dot(n, r, r);
+  *rel_res = sqrt(rr) / nb;
+  if (history) history[0] = *rel_res;
+  if (!isfinite(rr)) { status = ORC_NONFINITE; goto done; }
+  if (sqrt(rr) <= rtol * nb) { status = ORC_OK; goto done; }
+
+  for (int64_t i = 0; i < n; ++i) z[i] = (precond == 1) ? r[i] / d[i] : r[i];
+  for (int64_t i = 0; i < n; ++i) p[i] = z[i];
+  double rho = orc_dot(n, r, z);
+
+  for (int64_t k = 0; k < maxit; ++k) {
+    orc_spmv(n, row_ptr, col_idx, values, p, q);
+    double pq = orc_dot(n, p, q);
+    if (!isfinite(pq)) { status = ORC_NONFINITE; goto done; }
+    if (!(pq > 0.0)) { status = ORC_BREAKDOWN; goto done; }
+    double alpha = rho / pq;
+    for (int64_t i = 0; i < n; ++i) x[i] = x[i] + alpha * p[i];
+    for (int64_t i = 0; i < n; ++i) r[i] = r[i] - alpha * q[i];
+    rr = orc_dot(n, r, r);
+    *iters = k + 1;
+    *rel_res = sqrt(rr) / nb;
+    if (history) history[k + 1] = *rel_res;
+    if (!isfinite(rr)) { status = ORC_NONFINITE; goto done; }
+    if (sqrt(rr) <= rtol * nb) { status = ORC_OK; goto done; }
+    for (int64_t i = 0; i < n; ++i) z[i] = (precond == 1) ? r[i] / d[i] : r[i];
+    double rho_new = orc_dot(n, r, z);
+    double beta = rho_new / rho;
+    for (int64_t i = 0; i < n; ++i) p[i] = z[i] + beta * p[i];
+    rho = rho_new;
+  }
+  status = ORC_NOT_CONVERGED;
+
+done:
+  free(r); free(z); free(p); free(q); free(d);
+  return status;
+}
+
+/* grad_values[k] = -lambda[row(k)] * x[col(k)] for every stored entry, in CSR order. */
+void orc_grad_values(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const double *lambda,
+                     const double *x, double *grad_values) {
+  for (int64_t i = 0; i < n; ++i)
+    for (int64_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k) grad_values[k] = -(lambda[i] * x[col_idx[k]]);
+}
+
+/*
+ * Adjoint backward of x = A^{-1} b for an upstream gradient g = dL/dx:
+ * lambda solves A^T lambda = g (A is symmetric here, so the same CG routine
+ * with the same preconditioner, rtol and maxit, starting from lambda = 0);
+ * grad_b = lambda; grad_values = -lambda_i x_j on A's pattern.
+ * Returns the adjoint solve's status.
+ */
+int orc_cg_adjoint(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const double *values,
+                   const double *x, const double *g, double rtol, int64_t maxit, int precond,
+                   double *grad_b, double *grad_values, int64_t *iters, double *rel_res) {
+  int st = orc_cg(n, row_ptr, col_idx, values, g, NULL, rtol, maxit, precond, grad_b, NULL, iters, rel_res);
+  orc_grad_values(n, row_ptr, col_idx, grad_b, x, grad_values);
+  return st;
+}

@@ -1,0 +1,361 @@
+"""Pins of the fp64 oracle against facts fixed by the mathematics, not by the oracle itself.
+
+Each pin is a function ``pin_xxx(lib)`` that raises AssertionError when the
+oracle library ``lib`` (see ``oracle.load``) disagrees with:
+
+  * dense linear algebra on tiny grids (numpy.linalg.solve / exact rational
+    elimination with ``fractions.Fraction``);
+  * the closed-form eigenvalues of the five-point Laplacian,
+    4 - 2cos(i pi/(m+1)) - 2cos(j pi/(m+1)), and the CG iteration bound that
+    follows from the condition number;
+  * finite termination of CG after (number of distinct eigenvalues) steps;
+  * the relation between the recursively updated residual and the true
+    residual b - A x_k of the returned iterate;
+  * the adjoint identity <g, A^{-1} c> = <A^{-T} g, c>;
+  * central finite differences of L = <g, x(A, b)> with respect to b and to a
+    single stored entry of A (re-solved densely, since the perturbed matrix is
+    not symmetric);
+  * the exact scaling invariants sum_k gv_k values_k = -<g, x> and
+    <grad_b, b> = <g, x> (from x(tA) = x/t and x(tb) = t x);
+  * the Jacobi special case: with constant diagonal 4 the preconditioned
+    iterates equal the unpreconditioned ones bit for bit (scaling by 1/4 is
+    exact in binary floating point), and in general Jacobi PCG iterates equal
+    D^{-1/2} times the plain CG iterates of the symmetrically scaled system.
+
+The method is that of "torch-sla" (Chi, Wen), technical summary, Methodology
+section 2 (adjoint differentiation framework, linear systems).
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+
+import numpy as np
+
+import oracle
+from workloads import poisson_5pt, diffusion_dirichlet, diffusion_interior, random_spd, config1
+
+EPS = np.finfo(np.float64).eps
+
+
+def poisson_eigs(m: int) -> np.ndarray:
+    th = np.arange(1, m + 1) * np.pi / (m + 1)
+    return (4.0 - 2.0 * np.cos(th)[:, None] - 2.0 * np.cos(th)[None, :]).reshape(-1)
+
+
+def poisson_kappa(m: int) -> float:
+    th = np.pi / (m + 1)
+    lmin = 4.0 - 4.0 * np.cos(th)
+    lmax = 4.0 + 4.0 * np.cos(th)
+    return lmax / lmin
+
+
+def cg_residual_bound(kappa: float, rtol: float) -> int:
+    """Smallest k with 2 sqrt(kappa) ((sqrt(kappa)-1)/(sqrt(kappa)+1))^k <= rtol (x0 = 0)."""
+    s = math.sqrt(kappa)
+    return int(math.ceil(math.log(2.0 * s / rtol) / math.log((s + 1.0) / (s - 1.0))))
+
+
+# --------------------------------------------------------------------------- spmv / dot
+
+def pin_spmv_dense(lib):
+    for n, seed, hubs in [(1, 0, 0), (2, 1, 0), (17, 2, 0), (33, 3, 2), (257, 4, 3)]:
+        A = random_spd(n, 4.0, seed, long_rows=hubs)
+        x = np.random.default_rng(seed + 100).standard_normal(n)
+        y = oracle.spmv(A.row_ptr, A.col_idx, A.values, x, lib=lib)
+        D = A.dense()
+        yd = D @ x
+        bound = 4 * np.diff(A.row_ptr.astype(np.int64)).max() * EPS * (np.abs(D) @ np.abs(x)) + 1e-300
+        assert np.all(np.abs(y - yd) <= bound), (n, np.max(np.abs(y - yd) / bound))
+
+
+def pin_spmv_exact_integers(lib):
+    # small integers: every product and partial sum is exact, so y must equal the dense product exactly
+    A = poisson_5pt(7)
+    x = np.random.default_rng(5).integers(-50, 50, A.n).astype(np.float64)
+    y = oracle.spmv(A.row_ptr, A.col_idx, A.values, x, lib=lib)
+    assert np.array_equal(y, A.dense() @ x)
+    # empty matrix
+    y0 = oracle.spmv(np.zeros(1, np.int64), np.zeros(0, np.int32), np.zeros(0), np.zeros(0), lib=lib)
+    assert y0.shape == (0,)
+
+
+def pin_dot(lib):
+    rng = np.random.default_rng(7)
+    for n in [0, 1, 5, 1000]:
+        a, b = rng.standard_normal(n), rng.standard_normal(n)
+        exact = math.fsum((a * b).tolist()) if n else 0.0
+        got = oracle.dot(a, b, lib=lib)
+        assert abs(got - exact) <= n * EPS * float(np.abs(a) @ np.abs(b)) + 1e-300
+    assert oracle.dot(np.array([3.0, 4.0]), np.array([5.0, -2.0]), lib=lib) == 7.0
+
+
+# --------------------------------------------------------------------------- forward CG
+
+def pin_cg_vs_dense(lib):
+    cases = []
+    for m in [2, 3, 4, 8, 16, 24]:
+        cases.append(("poisson", poisson_5pt(m)))
+    rng = np.random.default_rng(11)
+    cases.append(("interior", diffusion_interior(9, rng.lognormal(0, 0.5, 2 * 9 * 8), 0.01)))
+    cases.append(("dirichlet", diffusion_dirichlet(10, rng.lognormal(0, 1.0, 2 * 10 * 11))))
+    cases.append(("random", random_spd(150, 5.0, 3, long_rows=2)))
+    for name, A in cases:
+        b = np.random.default_rng(A.n).standard_normal(A.n)
+        D = A.dense()
+        xs = np.linalg.solve(D, b)
+        ev = np.linalg.eigvalsh(D)
+        kappa = ev[-1] / ev[0]
+        for precond in (0, 1):
+            out = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-12, maxit=10000, precond=precond, lib=lib)
+            assert out["status"] == 0, (name, precond, out["status"])
+            err = np.linalg.norm(out["x"] - xs) / np.linalg.norm(xs)
+            assert err <= kappa * 1e-12 * 4 + 1e-13, (name, precond, err)
+            true_res = np.linalg.norm(b - D @ out["x"]) / np.linalg.norm(b)
+            assert true_res <= 1e-11, (name, precond, true_res)
+
+
+def pin_cg_exact_rational(lib):
+    # m = 2 Poisson: A^{-1} e1 = (7/24, 1/12, 1/12, 1/24), solved exactly over the rationals here
+    A = poisson_5pt(2)
+    D = [[Fraction(int(v)) for v in row] for row in A.dense()]
+    b = [Fraction(1), Fraction(0), Fraction(0), Fraction(0)]
+    n = 4
+    M = [row[:] + [b[i]] for i, row in enumerate(D)]
+    for c in range(n):
+        piv = next(r for r in range(c, n) if M[r][c] != 0)
+        M[c], M[piv] = M[piv], M[c]
+        for r in range(n):
+            if r != c and M[r][c] != 0:
+                f = M[r][c] / M[c][c]
+                M[r] = [M[r][k] - f * M[c][k] for k in range(n + 1)]
+    x_exact = [M[i][n] / M[i][i] for i in range(n)]
+    assert x_exact == [Fraction(7, 24), Fraction(1, 12), Fraction(1, 12), Fraction(1, 24)]
+    out = oracle.cg(A.row_ptr, A.col_idx, A.values, np.array([1.0, 0, 0, 0]), rtol=0.0, maxit=3, lib=lib)
+    assert np.max(np.abs(out["x"] - np.array([float(v) for v in x_exact]))) <= 8 * EPS
+    # m = 1: A = [4], one step gives b/4 exactly
+    A1 = poisson_5pt(1)
+    out1 = oracle.cg(A1.row_ptr, A1.col_idx, A1.values, np.array([3.0]), rtol=1e-14, maxit=10, lib=lib)
+    assert out1["iters"] == 1 and out1["x"][0] == 0.75 and out1["status"] == 0
+
+
+def pin_finite_termination(lib):
+    # CG terminates in at most (number of distinct eigenvalues) steps in exact arithmetic
+    for m in [2, 3, 4, 5]:
+        A = poisson_5pt(m)
+        ev = poisson_eigs(m)
+        distinct = len(np.unique(np.round(ev, 9)))
+        b = np.random.default_rng(m).standard_normal(A.n)
+        out = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=0.0, maxit=distinct, history=True, lib=lib)
+        assert out["rel_res"] < 1e-12, (m, distinct, out["rel_res"])
+        # and not before: with all eigen-components present one step fewer leaves a visible residual
+        out2 = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=0.0, maxit=distinct - 1, lib=lib)
+        assert out2["rel_res"] > 1e-10, (m, out2["rel_res"])
+
+
+def pin_eigen_closed_form_and_bound(lib):
+    for m in [3, 8, 16]:
+        A = poisson_5pt(m)
+        ev = np.linalg.eigvalsh(A.dense())
+        assert np.max(np.abs(np.sort(poisson_eigs(m)) - ev)) <= 1e-12
+    # iteration count within the residual bound derived from kappa (config 1: m = 64, rtol 1e-10)
+    w = config1()
+    out = oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=w.rtol, maxit=w.maxit, lib=lib)
+    kappa = poisson_kappa(64)
+    assert abs(kappa - 1711.7) < 0.1
+    assert out["status"] == 0 and 0 < out["iters"] <= cg_residual_bound(kappa, w.rtol)
+    # manufactured solution: ||x - x*|| / ||x*|| <= kappa * rtol
+    err = np.linalg.norm(out["x"] - w.x_star) / np.linalg.norm(w.x_star)
+    assert err <= kappa * w.rtol, err
+
+
+def pin_history_matches_true_residual(lib):
+    # the recursive residual history equals ||b - A x_k|| / ||b|| of the iterate after k steps
+    A = diffusion_dirichlet(12, np.random.default_rng(3).lognormal(0, 1.0, 2 * 12 * 13))
+    D = A.dense()
+    b = np.random.default_rng(4).standard_normal(A.n)
+    nb = np.linalg.norm(b)
+    for precond in (0, 1):
+        full = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=0.0, maxit=12, precond=precond, history=True,
+                         lib=lib)
+        assert full["history"][0] == 1.0
+        for k in [1, 2, 5, 12]:
+            part = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=0.0, maxit=k, precond=precond, lib=lib)
+            assert part["status"] == 1 and part["iters"] == k
+            true_rel = np.linalg.norm(b - D @ part["x"]) / nb
+            assert abs(true_rel - full["history"][k]) <= 1e-10 * max(true_rel, 1e-3), (precond, k)
+            assert part["rel_res"] == full["history"][k]
+
+
+def pin_x0_restart(lib):
+    A = poisson_5pt(10)
+    b = np.random.default_rng(8).standard_normal(A.n)
+    D = A.dense()
+    xs = np.linalg.solve(D, b)
+    first = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=0.0, maxit=7, lib=lib)
+    rest = oracle.cg(A.row_ptr, A.col_idx, A.values, b, x0=first["x"], rtol=1e-12, maxit=1000, lib=lib)
+    assert rest["status"] == 0
+    assert np.linalg.norm(rest["x"] - xs) / np.linalg.norm(xs) < 1e-9
+    # starting at the exact solution: 0 iterations
+    at = oracle.cg(A.row_ptr, A.col_idx, A.values, D @ xs, x0=xs, rtol=1e-8, maxit=10, lib=lib)
+    assert at["iters"] == 0 and at["status"] == 0
+
+
+def pin_jacobi_constant_diagonal(lib):
+    A = poisson_5pt(20)
+    b = np.random.default_rng(9).standard_normal(A.n)
+    a = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-10, maxit=5000, precond=0, history=True, lib=lib)
+    j = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-10, maxit=5000, precond=1, history=True, lib=lib)
+    assert a["iters"] == j["iters"]
+    assert np.array_equal(a["x"], j["x"])
+    assert np.array_equal(a["history"], j["history"])
+
+
+def pin_jacobi_equals_scaled_cg(lib):
+    # Jacobi PCG on (A, b) produces, step for step, x_k = D^{-1/2} y_k where y_k are the plain CG
+    # iterates on the symmetrically scaled system (D^{-1/2} A D^{-1/2}) y = D^{-1/2} b (exact algebra;
+    # agreement up to rounding).
+    A = diffusion_dirichlet(10, np.random.default_rng(61).lognormal(0, 1.0, 2 * 10 * 11))
+    b = np.random.default_rng(62).standard_normal(A.n)
+    rows = np.repeat(np.arange(A.n), np.diff(A.row_ptr.astype(np.int64)))
+    d = A.dense().diagonal()
+    s = 1.0 / np.sqrt(d)
+    vals_scaled = A.values * s[rows] * s[A.col_idx]
+    for k in [1, 2, 3, 6, 15]:
+        pc = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=0.0, maxit=k, precond=1, lib=lib)
+        sc = oracle.cg(A.row_ptr, A.col_idx, vals_scaled, s * b, rtol=0.0, maxit=k, precond=0, lib=lib)
+        x_from_scaled = s * sc["x"]
+        err = np.linalg.norm(pc["x"] - x_from_scaled) / np.linalg.norm(x_from_scaled)
+        assert err <= 1e-11, (k, err)
+
+
+def pin_status_codes(lib):
+    A = poisson_5pt(6)
+    n = A.n
+    b = np.random.default_rng(1).standard_normal(n)
+    z = oracle.cg(A.row_ptr, A.col_idx, A.values, np.zeros(n), x0=np.ones(n), rtol=1e-8, maxit=10, lib=lib)
+    assert z["status"] == 0 and z["iters"] == 0 and not z["x"].any()
+    m0 = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-8, maxit=0, lib=lib)
+    assert m0["status"] == 1 and m0["iters"] == 0 and not m0["x"].any()
+    neg = oracle.cg(A.row_ptr, A.col_idx, -A.values, b, rtol=1e-8, maxit=10, lib=lib)
+    assert neg["status"] == 2 and neg["iters"] == 0
+    bn = b.copy(); bn[3] = np.nan
+    assert oracle.cg(A.row_ptr, A.col_idx, A.values, bn, rtol=1e-8, maxit=10, lib=lib)["status"] == 5
+    vn = A.values.copy(); vn[7] = np.inf
+    assert oracle.cg(A.row_ptr, A.col_idx, vn, b, rtol=1e-8, maxit=10, lib=lib)["status"] == 5
+    vz = A.values.copy(); vz[0] = 0.0   # row 0's diagonal is its first stored entry
+    assert A.col_idx[0] == 0
+    assert oracle.cg(A.row_ptr, A.col_idx, vz, b, rtol=1e-8, maxit=10, precond=1, lib=lib)["status"] == 2
+    nc = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-12, maxit=3, lib=lib)
+    assert nc["status"] == 1 and nc["iters"] == 3
+
+
+# --------------------------------------------------------------------------- adjoint
+
+def _dense_L(D, b, g):
+    return float(g @ np.linalg.solve(D, b))
+
+
+def pin_adjoint_identity(lib):
+    A = diffusion_dirichlet(11, np.random.default_rng(21).lognormal(0, 1.0, 2 * 11 * 12))
+    rng = np.random.default_rng(22)
+    g, c = rng.standard_normal(A.n), rng.standard_normal(A.n)
+    for precond in (0, 1):
+        lam = oracle.cg(A.row_ptr, A.col_idx, A.values, g, rtol=1e-13, maxit=10000, precond=precond, lib=lib)["x"]
+        y = oracle.cg(A.row_ptr, A.col_idx, A.values, c, rtol=1e-13, maxit=10000, precond=precond, lib=lib)["x"]
+        lhs, rhs = float(g @ y), float(lam @ c)
+        assert abs(lhs - rhs) <= 1e-9 * (abs(lhs) + abs(rhs)), (lhs, rhs)
+
+
+def pin_adjoint_fd(lib):
+    A = diffusion_interior(4, np.random.default_rng(31).lognormal(0, 0.5, 2 * 4 * 3), 0.01)
+    D = A.dense()
+    rng = np.random.default_rng(32)
+    b, g = rng.standard_normal(A.n), rng.standard_normal(A.n)
+    fw = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-14, maxit=10000, lib=lib)
+    adj = oracle.cg_adjoint(A.row_ptr, A.col_idx, A.values, fw["x"], g, rtol=1e-14, maxit=10000, lib=lib)
+    assert adj["status"] == 0
+    # d/db_i by central differences
+    for i in [0, 5, A.n - 1]:
+        h = 1e-6 * max(1.0, abs(b[i]))
+        bp, bm = b.copy(), b.copy()
+        bp[i] += h; bm[i] -= h
+        fd = (_dense_L(D, bp, g) - _dense_L(D, bm, g)) / (2 * h)
+        assert abs(fd - adj["grad_b"][i]) <= 1e-7 * max(1.0, abs(fd)), (i, fd, adj["grad_b"][i])
+    # d/dvalues_k: perturb one stored entry only (the perturbed matrix is not symmetric)
+    rows = np.repeat(np.arange(A.n), np.diff(A.row_ptr.astype(np.int64)))
+    for k in [0, 1, 7, A.nnz // 2, A.nnz - 1]:
+        i, j = rows[k], A.col_idx[k]
+        h = 1e-6 * max(1.0, abs(A.values[k]))
+        Dp, Dm = D.copy(), D.copy()
+        Dp[i, j] += h; Dm[i, j] -= h
+        fd = (_dense_L(Dp, b, g) - _dense_L(Dm, b, g)) / (2 * h)
+        assert abs(fd - adj["grad_values"][k]) <= 1e-7 * max(1.0, abs(fd)), (k, fd, adj["grad_values"][k])
+
+
+def pin_adjoint_config1_loss(lib):
+    # config-1 loss L = 0.5 ||x - x_t||^2, so g = x - x_t; check a few gradient entries by FD (small grid)
+    A = poisson_5pt(6)
+    D = A.dense()
+    rng = np.random.default_rng(41)
+    x_star = rng.uniform(-1, 1, A.n)
+    b = D @ x_star
+    x_t = rng.uniform(-1, 1, A.n)
+    fw = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-14, maxit=1000, lib=lib)
+    adj = oracle.cg_adjoint(A.row_ptr, A.col_idx, A.values, fw["x"], fw["x"] - x_t, rtol=1e-14, maxit=1000,
+                            lib=lib)
+
+    def L(Dm, bm):
+        x = np.linalg.solve(Dm, bm)
+        return 0.5 * float((x - x_t) @ (x - x_t))
+
+    rows = np.repeat(np.arange(A.n), np.diff(A.row_ptr.astype(np.int64)))
+    for k in [3, 50, A.nnz - 2]:
+        i, j = rows[k], A.col_idx[k]
+        h = 1e-6
+        Dp, Dm = D.copy(), D.copy()
+        Dp[i, j] += h; Dm[i, j] -= h
+        fd = (L(Dp, b) - L(Dm, b)) / (2 * h)
+        assert abs(fd - adj["grad_values"][k]) <= 1e-7 * max(1.0, abs(fd))
+    for i in [0, 17]:
+        bp, bm = b.copy(), b.copy()
+        bp[i] += 1e-6; bm[i] -= 1e-6
+        fd = (L(D, bp) - L(D, bm)) / 2e-6
+        assert abs(fd - adj["grad_b"][i]) <= 1e-7 * max(1.0, abs(fd))
+
+
+def pin_adjoint_invariants(lib):
+    A = diffusion_dirichlet(16, np.random.default_rng(51).lognormal(0, 1.0, 2 * 16 * 17))
+    rng = np.random.default_rng(52)
+    b, g = rng.standard_normal(A.n), rng.standard_normal(A.n)
+    fw = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-13, maxit=10000, precond=1, lib=lib)
+    adj = oracle.cg_adjoint(A.row_ptr, A.col_idx, A.values, fw["x"], g, rtol=1e-13, maxit=10000, precond=1,
+                            lib=lib)
+    gx = float(g @ fw["x"])
+    s1 = float(adj["grad_values"] @ A.values)
+    s2 = float(adj["grad_b"] @ b)
+    assert abs(s1 + gx) <= 1e-9 * abs(gx), (s1, gx)
+    assert abs(s2 - gx) <= 1e-9 * abs(gx), (s2, gx)
+    # pattern: one gradient per stored entry, and -lambda_i x_j exactly on a hand-picked entry
+    assert adj["grad_values"].shape == (A.nnz,)
+    k = 5
+    i = int(np.searchsorted(A.row_ptr, k, side="right") - 1)
+    assert adj["grad_values"][k] == -(adj["grad_b"][i] * fw["x"][A.col_idx[k]])
+
+
+def pin_adjoint_zero_gradient(lib):
+    A = poisson_5pt(5)
+    x = np.random.default_rng(3).standard_normal(A.n)
+    adj = oracle.cg_adjoint(A.row_ptr, A.col_idx, A.values, x, np.zeros(A.n), rtol=1e-8, maxit=10, lib=lib)
+    assert adj["status"] == 0 and adj["iters"] == 0
+    assert not adj["grad_b"].any() and not adj["grad_values"].any()
+
+
+ALL_PINS = [
+    pin_spmv_dense, pin_spmv_exact_integers, pin_dot,
+    pin_cg_vs_dense, pin_cg_exact_rational, pin_finite_termination, pin_eigen_closed_form_and_bound,
+    pin_history_matches_true_residual, pin_x0_restart, pin_jacobi_constant_diagonal, pin_jacobi_equals_scaled_cg,
+    pin_status_codes,
+    pin_adjoint_identity, pin_adjoint_fd, pin_adjoint_config1_loss, pin_adjoint_invariants,
+    pin_adjoint_zero_gradient,
+]

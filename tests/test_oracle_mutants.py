@@ -1,0 +1,57 @@
+"""Planted mistakes in a copy of the oracle must each fail at least one pin (CPU only).
+
+Each case rewrites one expression of ``oracle/sla_oracle.c`` in a temporary
+copy (a dropped term, a wrong sign, a wrong index or a transposed operand),
+compiles it, and runs the pin battery of ``oracle_pins`` against it.  The
+unmodified oracle passes every pin (test_oracle_pins.py); every mutant must not.
+"""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "sla_oracle.c")
+
+MUTANTS = [
+    ("spmv_wrong_index", "s += values[k] * x[col_idx[k]];", "s += values[k] * x[i];"),
+    ("spmv_dropped_term", "for (int64_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k) s += values[k]",
+     "for (int64_t k = row_ptr[i] + 1; k < row_ptr[i + 1]; ++k) s += values[k]"),
+    ("dot_wrong_operand", "s += a[i] * b[i];", "s += a[i] * a[i];"),
+    ("x_update_sign", "x[i] = x[i] + alpha * p[i];", "x[i] = x[i] - alpha * p[i];"),
+    ("r_update_operand", "r[i] = r[i] - alpha * q[i];", "r[i] = r[i] - alpha * p[i];"),
+    ("alpha_transposed", "double alpha = rho / pq;", "double alpha = pq / rho;"),
+    ("beta_transposed", "double beta = rho_new / rho;", "double beta = rho / rho_new;"),
+    ("p_update_uses_r", "p[i] = z[i] + beta * p[i];", "p[i] = r[i] + beta * p[i];"),
+    ("jacobi_multiplies", "z[i] = (precond == 1) ? r[i] / d[i] : r[i];\n    double rho_new",
+     "z[i] = (precond == 1) ? r[i] * d[i] : r[i];\n    double rho_new"),
+    ("stop_rule_no_sqrt", "if (sqrt(rr) <= rtol * nb) { status = ORC_OK; goto done; }\n    for",
+     "if (rr <= rtol * nb) { status = ORC_OK; goto done; }\n    for"),
+    ("history_off_by_one", "if (history) history[k + 1] = *rel_res;", "if (history) history[k] = *rel_res;"),
+    ("grad_values_transposed", "grad_values[k] = -(lambda[i] * x[col_idx[k]]);",
+     "grad_values[k] = -(lambda[col_idx[k]] * x[i]);"),
+    ("grad_values_sign", "grad_values[k] = -(lambda[i] * x[col_idx[k]]);",
+     "grad_values[k] = (lambda[i] * x[col_idx[k]]);"),
+    ("adjoint_wrong_rhs", "orc_cg(n, row_ptr, col_idx, values, g, NULL,", "orc_cg(n, row_ptr, col_idx, values, x, NULL,"),
+    ("x0_residual_sign", "r[i] = b[i] - q[i];", "r[i] = b[i] + q[i];"),
+    ("breakdown_test_dropped", "if (!(pq > 0.0)) { status = ORC_BREAKDOWN; goto done; }", ""),
+]
+
+
+@pytest.mark.parametrize("name,orig,mut", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, orig, mut, tmp_path):
+    text = open(SRC).read()
+    assert text.count(orig) == 1, f"mutation site for {name} not unique"
+    src = tmp_path / f"{name}.c"
+    src.write_text(text.replace(orig, mut))
+    so = str(tmp_path / f"lib{name}.so")
+    oracle.build(force=True, src=str(src), out=so)
+    lib = oracle.load(so)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(lib)
+        except Exception as e:  # noqa: BLE001 - any failure counts as caught
+            caught.append((pin.__name__, type(e).__name__))
+    assert caught, f"mutant {name} passed every pin"

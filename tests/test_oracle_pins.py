@@ -1,0 +1,15 @@
+"""The oracle against its pins (CPU only).  See tests/oracle_pins.py for what each pin fixes."""
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return oracle.load()
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=[p.__name__ for p in ALL_PINS])
+def test_pin(pin, lib):
+    pin(lib)
