@@ -27,8 +27,9 @@
  *   b == 0 gives x = 0 after 0 iterations;
  *   a non-finite ||b||, r.r or p.Ap stops with status NONFINITE;
  *   p.Ap <= 0 (finite) stops with BREAKDOWN, x left at the last iterate;
- *   with Jacobi, a diagonal entry <= 0 or missing stops with BREAKDOWN before
- *   the first iteration.
+ *   with Jacobi, any non-finite diagonal entry stops with NONFINITE, else any
+ *   diagonal entry <= 0 or missing stops with BREAKDOWN, before the first
+ *   iteration (a symmetric positive definite matrix has a positive diagonal).
  *
  * Status codes returned: 0 converged, 1 not converged after maxit, 2 breakdown,
  * 5 non-finite.
@@ -109,10 +110,10 @@ int orc_cg(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const doub
   }
   if (precond == 1) {
     orc_diagonal(n, row_ptr, col_idx, values, d);
-    for (int64_t i = 0; i < n; ++i) {
+    for (int64_t i = 0; i < n; ++i)
       if (!isfinite(d[i])) { status = ORC_NONFINITE; goto done; }
+    for (int64_t i = 0; i < n; ++i)
       if (!(d[i] > 0.0)) { status = ORC_BREAKDOWN; goto done; }
-    }
   }
 
   if (x0) {

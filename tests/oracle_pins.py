@@ -246,6 +246,10 @@ def pin_status_codes(lib):
     vz = A.values.copy(); vz[0] = 0.0   # row 0's diagonal is its first stored entry
     assert A.col_idx[0] == 0
     assert oracle.cg(A.row_ptr, A.col_idx, vz, b, rtol=1e-8, maxit=10, precond=1, lib=lib)["status"] == 2
+    # a non-finite diagonal anywhere outranks a non-positive one earlier in the matrix
+    dpos = [k for k in range(int(A.row_ptr[A.n - 1]), int(A.row_ptr[A.n])) if A.col_idx[k] == A.n - 1][0]
+    vb = vz.copy(); vb[dpos] = np.nan
+    assert oracle.cg(A.row_ptr, A.col_idx, vb, b, rtol=1e-8, maxit=10, precond=1, lib=lib)["status"] == 5
     nc = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-12, maxit=3, lib=lib)
     assert nc["status"] == 1 and nc["iters"] == 3
 
