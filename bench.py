@@ -1,0 +1,380 @@
+"""Benchmark of the differentiable CSR CG solve (forward + adjoint backward) on GB300.
+
+One step = one pass of the whole hot path over one synthetic system: the CG solve
+A x = b (sla_cg_solve) and the adjoint backward (sla_cg_adjoint: A lambda = g,
+grad_b = lambda, grad_values = -lambda_i x_j on the pattern).  The default workload
+is the 1M-DOF 2D Poisson system in fp64 (m = 1000, nnz = 4,996,000), CG rtol 1e-8,
+b ~ N(0,1) seed 0, g ~ N(0,1) seed 1.
+
+Metric: CG iterations per second over the whole job (forward + adjoint iterations of
+all ranks / the max-over-ranks device time of the timed steps), plus the effective HBM
+GB/s of the fused CG iteration against the measured copy bandwidth, and the adjoint ms.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}] [--config configN]
+
+With N > 1 the script runs under torch.distributed.run; every rank solves its own
+independent system of the same size (the single-system solve has no exchange step:
+replicas, weak scaling).  --impl reference times the fp64 CPU oracle on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CG iters/sec and HBM GB/s (% of roofline), 1M-DOF 2D Poisson fp64; adjoint ms"
+
+
+def b_iter(n, nnz, s_v, s_p, jacobi):
+    """Algorithmic bytes of one fused CG iteration: matrix stream + row pointers + V vector passes."""
+    V = 11 if jacobi else 9
+    return nnz * (s_v + 4) + (n + 1) * s_p + V * n * s_v
+
+
+def b_gradvalues(n, nnz, s_v, s_p):
+    """One grad_values pass: col_idx read + gv write, row pointers, lambda and x reads."""
+    return nnz * (s_v + 4) + (n + 1) * s_p + 2 * n * s_v
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per CG iteration from the committed ncu summary, if it matches the current kernels."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows for j in range(4) if r[5 + j] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def flush_l2(buf):
+    buf.zero_()  # a write larger than the 129 MB L2 evicts the previous step's lines
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import differentiable_sparse_iterative_gb300 as sla
+    from workloads import config_by_name
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = config_by_name(args.config)
+    precond = w.precond
+    jac = precond == 1
+    batched = w.batch > 0
+    if batched:
+        raise SystemExit("bench.py times the single-system workloads (config1/2/4/5)")
+    A = sla.CSRMatrix.from_numpy(w.A.row_ptr, w.A.col_idx, w.A.values, dev)
+    b = torch.from_numpy(w.b).to(dev)
+    g_np = w.g if w.g is not None else np.random.default_rng(1).standard_normal(w.A.n)
+    g = torch.from_numpy(g_np).to(dev)
+    n, nnz = w.A.n, w.A.nnz
+    s_v, s_p = 8, w.A.row_ptr.dtype.itemsize
+    ws = torch.empty(sla.sla_cg_workspace_bytes(n, 1, torch.float64, precond), dtype=torch.uint8, device=dev)
+    x = torch.empty(n, dtype=torch.float64, device=dev)
+    gb = torch.empty(n, dtype=torch.float64, device=dev)
+    gv = torch.empty(nnz, dtype=torch.float64, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        _, fi, _ = sla.sla_cg_solve(A, b, rtol=w.rtol, maxit=w.maxit, precond=precond, x=x, workspace=ws)
+        e1.record(stream)
+        _, _, ai = sla.sla_cg_adjoint(A, x, g, rtol=w.rtol, maxit=w.maxit, precond=precond, grad_b=gb,
+                                      grad_values=gv, workspace=ws)
+        e2.record(stream)
+        return e0, e1, e2, fi, ai
+
+    for _ in range(args.warmup):
+        flush_l2(flush)
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats(dev)
+    mem0 = torch.cuda.memory_allocated(dev)
+    launches0 = sla.sla_launch_count()
+    recs = []
+    with ClockSampler(local_rank) as clk:
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            flush_l2(flush)
+            recs.append(step())
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    launches = sla.sla_launch_count() - launches0
+    fwd_ms = [r[0].elapsed_time(r[1]) for r in recs]
+    adj_ms = [r[1].elapsed_time(r[2]) for r in recs]
+    iters_f = [r[3].iters for r in recs]
+    iters_a = [r[4].iters for r in recs]
+    status = {r[3].status for r in recs} | {r[4].status for r in recs}
+    step_ms = [f + a for f, a in zip(fwd_ms, adj_ms)]
+    tot_s = sum(step_ms) / 1e3
+    tot_iters = sum(iters_f) + sum(iters_a)
+    peak_mem = torch.cuda.max_memory_allocated(dev) - mem0
+
+    if world > 1:
+        t = torch.tensor([tot_s], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        it = torch.tensor([float(tot_iters)], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(it, op=torch.distributed.ReduceOp.SUM)
+        tot_s_all, tot_iters_all = float(t.item()), float(it.item())
+    else:
+        tot_s_all, tot_iters_all = tot_s, float(tot_iters)
+
+    Bi = b_iter(n, nnz, s_v, s_p, jac)
+    Bg = b_gradvalues(n, nnz, s_v, s_p)
+    peak, peak_kind = measured_peaks()
+    # fused CG iteration (spmv_step + update_step): bytes per iteration / forward time per iteration
+    fwd_s = sum(fwd_ms) / 1e3
+    achieved = Bi * sum(iters_f) / fwd_s / 1e9
+    tr = profiled_traffic().get(args.config)
+    clocks = clk.summary()
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, dev, precond, sla, torch)
+
+    out = {
+        "metric": METRIC, "value": tot_iters_all / tot_s_all, "unit": "iters/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(step_ms),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generators; no dataset on the pages)",
+        "config": {"workload": w.name, "n": n, "nnz": nnz, "rtol": w.rtol, "precond": "jacobi" if jac else "none",
+                   "step": "forward CG solve + adjoint (grad_b, grad_values)",
+                   "l2": "flushed between steps (256 MB write); within a solve the iterations reuse L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "iters_forward": statistics.mean(iters_f), "iters_adjoint": statistics.mean(iters_a),
+        "time_to_tolerance_ms": statistics.mean(fwd_ms), "adjoint_ms": statistics.mean(adj_ms),
+        "status": sorted(status),
+        "effective_gbs_step": (Bi * tot_iters + Bg * args.steps) / tot_s / 1e9,
+        "peak_mem_mb": peak_mem / 2**20,
+        "roofline": {"kernel": "fused CG iteration (cg_spmv_step + cg_update_step)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": peak_kind,
+                     "bytes_per_iter": Bi,
+                     "traffic": (tr["dram_bytes_per_iter"] if tr else None),
+                     "traffic_source": (tr.get("source") if tr else None)},
+        "gpu_launches": int(launches),
+        "wall_s": wall,
+        "clocks": clocks,
+    }
+    if e2e:
+        out["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline(w, args.cpu_iters)
+    return out
+
+
+def run_e2e(args, w, dev, precond, sla, torch):
+    """The same step through the public autograd API, inputs from pinned host memory, results back."""
+    h_rp = torch.from_numpy(w.A.row_ptr).pin_memory()
+    h_ci = torch.from_numpy(w.A.col_idx).pin_memory()
+    h_v = torch.from_numpy(w.A.values).pin_memory()
+    h_b = torch.from_numpy(w.b).pin_memory()
+    g_np = w.g if w.g is not None else np.random.default_rng(1).standard_normal(w.A.n)
+    h_g = torch.from_numpy(g_np).pin_memory()
+    o_x = torch.empty(w.A.n, dtype=torch.float64).pin_memory()
+    o_gb = torch.empty(w.A.n, dtype=torch.float64).pin_memory()
+    o_gv = torch.empty(w.A.nnz, dtype=torch.float64).pin_memory()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (h_rp, h_ci, h_v, h_b, h_g))
+    d2h = sum(t.numel() * t.element_size() for t in (o_x, o_gb, o_gv))
+    stream = torch.cuda.current_stream(dev)
+    iters = []
+
+    def step():
+        rp = h_rp.to(dev, non_blocking=True)
+        ci = h_ci.to(dev, non_blocking=True)
+        v = h_v.to(dev, non_blocking=True).requires_grad_(True)
+        b = h_b.to(dev, non_blocking=True).requires_grad_(True)
+        g = h_g.to(dev, non_blocking=True)
+        A = sla.CSRMatrix(rp, ci, v)
+        xx = sla.solve(A, b, rtol=w.rtol, maxit=w.maxit, precond=precond)
+        xx.backward(g)
+        o_x.copy_(xx.detach(), non_blocking=True)
+        o_gb.copy_(b.grad, non_blocking=True)
+        o_gv.copy_(v.grad, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        flush_l2(flush)
+        step()
+    torch.cuda.synchronize()
+    total = 0.0
+    for _ in range(args.steps):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        total += e0.elapsed_time(e1) / 1e3
+    # iterations of the autograd path equal those of the direct calls on the same data
+    _, fi, _ = sla.sla_cg_solve(sla.CSRMatrix(h_rp.to(dev), h_ci.to(dev), h_v.to(dev)), h_b.to(dev), rtol=w.rtol,
+                                maxit=w.maxit, precond=precond)
+    _, _, ai = sla.sla_cg_adjoint(sla.CSRMatrix(h_rp.to(dev), h_ci.to(dev), h_v.to(dev)),
+                                  o_x.to(dev), h_g.to(dev), rtol=w.rtol, maxit=w.maxit, precond=precond)
+    per_step_iters = fi.iters + ai.iters
+    return {"value": per_step_iters * args.steps / total, "unit": "iters/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "api": "differentiable_sparse_iterative_gb300.solve + backward"}
+
+
+def cpu_baseline(w, iters):
+    """The fp64 oracle as it stands (one host thread) on a bounded sample: `iters` forward CG
+    iterations plus `iters` adjoint iterations on the same system."""
+    import oracle
+    oracle.load()
+    t0 = time.perf_counter()
+    f = oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=0.0, maxit=iters, precond=w.precond)
+    g = w.g if w.g is not None else np.random.default_rng(1).standard_normal(w.A.n)
+    a = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, w.A.values, f["x"], g, rtol=0.0, maxit=iters,
+                          precond=w.precond)
+    dt = time.perf_counter() - t0
+    return {"value": (f["iters"] + a["iters"]) / dt, "unit": "iters/s", "cores": 1, "kind": "oracle",
+            "sample": f"{w.name}: {iters} forward + {iters} adjoint CG iterations (rtol 0) and one grad_values "
+                      f"pass, {dt:.1f} s on one host core"}
+
+
+def run_reference(args, rank, world):
+    """The oracle arm: the fp64 CPU oracle timed on the host, on bounded samples of the workload."""
+    from workloads import config_by_name
+    import oracle
+    if rank != 0:
+        return None
+    w = config_by_name(args.config)
+    oracle.load()
+    g = w.g if w.g is not None else np.random.default_rng(1).standard_normal(w.A.n)
+    k = args.ref_iters
+
+    def step():
+        f = oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=0.0, maxit=k, precond=w.precond)
+        a = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, w.A.values, f["x"], g, rtol=0.0, maxit=k,
+                              precond=w.precond)
+        return f["iters"] + a["iters"]
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    its = sum(step() for _ in range(args.steps))
+    dt = time.perf_counter() - t0
+    v = its / dt
+    sample = f"{w.name}: each step {k} forward + {k} adjoint CG iterations (rtol 0) + grad_values, one host core"
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "iters/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generators)",
+            "config": {"workload": w.name, "n": w.A.n, "nnz": w.A.nnz, "rtol": w.rtol},
+            "cpu_baseline": {"value": v, "unit": "iters/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "iters/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="config2")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-iters", type=int, default=600)
+    ap.add_argument("--ref-iters", type=int, default=100)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,335 @@
+"""Differentiable sparse iterative solve on GB300: Python binding of libsla.
+
+The compute runs in libsla's CUDA kernels (``csrc/``, C ABI in ``include/sla.h``);
+this module only marshals torch tensors (device memory, the current stream) into
+the C calls, under the same names.  There is no CPU or PyTorch fallback: if
+libsla.so is missing or a tensor is not on a CUDA device the call raises.
+
+Method: "torch-sla: Differentiable Sparse Linear Algebra with Adjoint Solvers and
+Sparse Tensor Parallelism for PyTorch" (Chi, Wen), technical summary —
+Methodology 1 (autograd-aware .matvec / .solve; one matrix or a batch sharing a
+pattern), Methodology 2 (adjoint: one A^T lambda = dL/dx solve, grad_b = lambda,
+grad_A = -lambda_i x_j on the pattern, O(1) graph nodes), Significance (Jacobi
+preconditioning).
+
+    A = CSRMatrix(row_ptr, col_idx, values)          # CUDA tensors
+    x = solve(A, b, rtol=1e-8)                       # autograd: grads to values and b
+"""
+from __future__ import annotations
+
+import ctypes
+import warnings
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _abi
+from ._abi import (SLA_OK, SLA_NOT_CONVERGED, SLA_BREAKDOWN, SLA_INVALID_ARG, SLA_BAD_CSR, SLA_NONFINITE,
+                   SLA_WORKSPACE_TOO_SMALL, SLA_CUDA_ERROR, SLA_PRECOND_NONE, SLA_PRECOND_JACOBI)
+
+__all__ = [
+    "CSRMatrix", "SlaError", "CGInfo", "lib", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
+    "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_validate_csr", "sla_cg_workspace_bytes",
+    "sla_status_string", "sla_launch_count", "sla_version", "CGSolve", "solve", "matvec",
+    "SLA_PRECOND_NONE", "SLA_PRECOND_JACOBI",
+]
+
+_lib = None
+
+
+def lib():
+    """The loaded libsla (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        _lib = _abi.load()
+    return _lib
+
+
+class SlaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = f"{where}: {sla_status_string(status)}"
+        if status == SLA_CUDA_ERROR:
+            msg += f" ({lib().sla_last_cuda_error().decode()})"
+        super().__init__(msg)
+        self.status = status
+
+
+@dataclass
+class CGInfo:
+    iters: int
+    rel_res: float
+    status: int
+    kernels: int
+
+    @property
+    def status_name(self) -> str:
+        return sla_status_string(self.status)
+
+
+@dataclass
+class CSRMatrix:
+    """Square CSR matrix on a CUDA device: row_ptr (int32/int64, n+1), col_idx (int32), values (f32/f64)."""
+    row_ptr: torch.Tensor
+    col_idx: torch.Tensor
+    values: torch.Tensor
+
+    @property
+    def n(self) -> int:
+        return self.row_ptr.shape[0] - 1
+
+    @property
+    def nnz(self) -> int:
+        return self.col_idx.shape[0]
+
+    @classmethod
+    def from_numpy(cls, row_ptr, col_idx, values, device="cuda"):
+        return cls(torch.as_tensor(row_ptr).to(device), torch.as_tensor(col_idx).to(device),
+                   torch.as_tensor(values).to(device))
+
+    def with_values(self, values: torch.Tensor) -> "CSRMatrix":
+        return CSRMatrix(self.row_ptr, self.col_idx, values)
+
+
+_DT = {torch.float32: _abi.SLA_F32, torch.float64: _abi.SLA_F64}
+_IT = {torch.int32: _abi.SLA_I32, torch.int64: _abi.SLA_I64}
+
+
+def _dev_ptr(t: Optional[torch.Tensor], dtype=None, name="tensor") -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (libsla has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _csr_struct(A: CSRMatrix, values: Optional[torch.Tensor] = None) -> _abi.sla_csr:
+    vals = A.values if values is None else values
+    if vals.dtype not in _DT:
+        raise ValueError("values must be float32 or float64")
+    if A.row_ptr.dtype not in _IT or A.col_idx.dtype != torch.int32:
+        raise ValueError("row_ptr must be int32/int64 and col_idx int32")
+    s = _abi.sla_csr()
+    s.n = A.n
+    s.nnz = A.nnz
+    s.rowptr_type = _IT[A.row_ptr.dtype]
+    s.dtype = _DT[vals.dtype]
+    s.row_ptr = _dev_ptr(A.row_ptr, name="row_ptr")
+    s.col_idx = _dev_ptr(A.col_idx, name="col_idx")
+    s.values = _dev_ptr(vals, name="values") if vals.dim() == 1 else None
+    return s
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _opts(rtol, maxit, precond, unroll=0) -> _abi.sla_cg_opts:
+    o = _abi.sla_cg_opts()
+    o.rtol = float(rtol)
+    o.maxit = int(maxit)
+    o.precond = int(precond)
+    o.unroll = int(unroll)
+    return o
+
+
+def _check(st: int, where: str):
+    if st != SLA_OK:
+        raise SlaError(st, where)
+
+
+def sla_status_string(status: int) -> str:
+    return lib().sla_status_string(int(status)).decode()
+
+
+def sla_version() -> int:
+    return lib().sla_version()
+
+
+def sla_launch_count() -> int:
+    return lib().sla_launch_count()
+
+
+def sla_cg_workspace_bytes(n: int, batch: int, dtype: torch.dtype, precond: int) -> int:
+    return lib().sla_cg_workspace_bytes(int(n), int(batch), _DT[dtype], int(precond))
+
+
+def _workspace(n, batch, dtype, precond, device, ws: Optional[torch.Tensor]) -> torch.Tensor:
+    need = sla_cg_workspace_bytes(n, batch, dtype, precond)
+    if ws is not None and ws.numel() * ws.element_size() >= need:
+        return ws
+    return torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+
+
+def sla_validate_csr(A: CSRMatrix, check_symmetric: bool = False) -> int:
+    """Returns -1 when A is canonical (and symmetric if asked), else the first offending row."""
+    ws = torch.empty(256, dtype=torch.uint8, device=A.row_ptr.device)
+    bad = ctypes.c_int64(-1)
+    st = lib().sla_validate_csr(ctypes.byref(_csr_struct(A)), int(bool(check_symmetric)), ctypes.byref(bad),
+                                ws.data_ptr(), 256, _stream(A.row_ptr.device))
+    if st not in (SLA_OK, SLA_BAD_CSR):
+        _check(st, "sla_validate_csr")
+    return int(bad.value)
+
+
+def sla_spmv(A: CSRMatrix, x: torch.Tensor, y: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """y = A x (asynchronous on the current stream)."""
+    if y is None:
+        y = torch.empty(A.n, dtype=A.values.dtype, device=A.values.device)
+    _check(lib().sla_spmv(ctypes.byref(_csr_struct(A)), _dev_ptr(x, A.values.dtype, "x"),
+                          _dev_ptr(y, A.values.dtype, "y"), _stream(A.values.device)), "sla_spmv")
+    return y
+
+
+def sla_grad_values(A: CSRMatrix, lam: torch.Tensor, x: torch.Tensor,
+                    out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """grad_values[k] = -lam[row(k)] * x[col(k)] on A's pattern (asynchronous)."""
+    if out is None:
+        out = torch.empty(A.nnz, dtype=A.values.dtype, device=A.values.device)
+    _check(lib().sla_grad_values(ctypes.byref(_csr_struct(A)), _dev_ptr(lam, A.values.dtype, "lambda"),
+                                 _dev_ptr(x, A.values.dtype, "x"), _dev_ptr(out, A.values.dtype, "grad_values"),
+                                 _stream(A.values.device)), "sla_grad_values")
+    return out
+
+
+def _info(ci: _abi.sla_cg_info) -> CGInfo:
+    return CGInfo(int(ci.iters), float(ci.rel_res), int(ci.status), int(ci.kernels))
+
+
+def sla_cg_solve(A: CSRMatrix, b: torch.Tensor, x0: Optional[torch.Tensor] = None, rtol: float = 1e-8,
+                 maxit: int = 10000, precond: int = SLA_PRECOND_NONE, x: Optional[torch.Tensor] = None,
+                 history: bool = False, workspace: Optional[torch.Tensor] = None, sync: bool = True,
+                 unroll: int = 0):
+    """CG solve of A x = b.  Returns (x, CGInfo or None, history tensor or None).
+
+    With sync=False the call is asynchronous and returns info=None.
+    """
+    dt, dev = A.values.dtype, A.values.device
+    if x is None:
+        x = torch.empty(A.n, dtype=dt, device=dev)
+    hist = torch.full((int(maxit) + 1,), float("nan"), dtype=torch.float64, device=dev) if history else None
+    ws = _workspace(A.n, 1, dt, precond, dev, workspace)
+    info = _abi.sla_cg_info()
+    st = lib().sla_cg_solve(ctypes.byref(_csr_struct(A)), _dev_ptr(b, dt, "b"), _dev_ptr(x0, dt, "x0"),
+                            ctypes.byref(_opts(rtol, maxit, precond, unroll)), _dev_ptr(x, dt, "x"),
+                            ctypes.byref(info) if sync else None, _dev_ptr(hist, torch.float64, "history"),
+                            ws.data_ptr(), ws.numel(), _stream(dev))
+    _check(st, "sla_cg_solve")
+    return x, (_info(info) if sync else None), hist
+
+
+def sla_cg_adjoint(A: CSRMatrix, x: torch.Tensor, g: torch.Tensor, rtol: float = 1e-8, maxit: int = 10000,
+                   precond: int = SLA_PRECOND_NONE, grad_b: Optional[torch.Tensor] = None,
+                   grad_values: Optional[torch.Tensor] = None, want_grad_values: bool = True,
+                   workspace: Optional[torch.Tensor] = None, sync: bool = True, unroll: int = 0):
+    """Adjoint backward: returns (grad_b = lambda, grad_values or None, CGInfo or None)."""
+    dt, dev = A.values.dtype, A.values.device
+    if grad_b is None:
+        grad_b = torch.empty(A.n, dtype=dt, device=dev)
+    if grad_values is None and want_grad_values:
+        grad_values = torch.empty(A.nnz, dtype=dt, device=dev)
+    ws = _workspace(A.n, 1, dt, precond, dev, workspace)
+    info = _abi.sla_cg_info()
+    st = lib().sla_cg_adjoint(ctypes.byref(_csr_struct(A)), _dev_ptr(x, dt, "x"), _dev_ptr(g, dt, "g"),
+                              ctypes.byref(_opts(rtol, maxit, precond, unroll)), _dev_ptr(grad_b, dt, "grad_b"),
+                              _dev_ptr(grad_values, dt, "grad_values"), ctypes.byref(info) if sync else None,
+                              ws.data_ptr(), ws.numel(), _stream(dev))
+    _check(st, "sla_cg_adjoint")
+    return grad_b, grad_values, (_info(info) if sync else None)
+
+
+def sla_cg_solve_batched(pattern: CSRMatrix, values: torch.Tensor, b: torch.Tensor,
+                         x0: Optional[torch.Tensor] = None, rtol: float = 1e-5, maxit: int = 10000,
+                         precond: int = SLA_PRECOND_NONE, x: Optional[torch.Tensor] = None, history: bool = False,
+                         workspace: Optional[torch.Tensor] = None, sync: bool = True, unroll: int = 0):
+    """Batched shared-pattern CG: values [B, nnz], b [B, n].  Returns (x [B, n], [CGInfo]*B, history)."""
+    B = values.shape[0]
+    dt, dev = values.dtype, values.device
+    if x is None:
+        x = torch.empty(B, pattern.n, dtype=dt, device=dev)
+    hist = (torch.full((B, int(maxit) + 1), float("nan"), dtype=torch.float64, device=dev) if history else None)
+    ws = _workspace(pattern.n, B, dt, precond, dev, workspace)
+    infos = (_abi.sla_cg_info * max(B, 1))()
+    st = lib().sla_cg_solve_batched(ctypes.byref(_csr_struct(pattern, values)), B, _dev_ptr(values, dt, "values"),
+                                    _dev_ptr(b, dt, "b"), _dev_ptr(x0, dt, "x0"),
+                                    ctypes.byref(_opts(rtol, maxit, precond, unroll)), _dev_ptr(x, dt, "x"),
+                                    infos if sync else None, _dev_ptr(hist, torch.float64, "history"),
+                                    ws.data_ptr(), ws.numel(), _stream(dev))
+    _check(st, "sla_cg_solve_batched")
+    return x, ([_info(infos[s]) for s in range(B)] if sync else None), hist
+
+
+def sla_cg_adjoint_batched(pattern: CSRMatrix, values: torch.Tensor, x: torch.Tensor, g: torch.Tensor,
+                           rtol: float = 1e-5, maxit: int = 10000, precond: int = SLA_PRECOND_NONE,
+                           grad_b: Optional[torch.Tensor] = None, grad_values: Optional[torch.Tensor] = None,
+                           want_grad_values: bool = True, workspace: Optional[torch.Tensor] = None,
+                           sync: bool = True, unroll: int = 0):
+    """Batched adjoint: returns (grad_b [B, n], grad_values [B, nnz] or None, [CGInfo]*B)."""
+    B = values.shape[0]
+    dt, dev = values.dtype, values.device
+    if grad_b is None:
+        grad_b = torch.empty(B, pattern.n, dtype=dt, device=dev)
+    if grad_values is None and want_grad_values:
+        grad_values = torch.empty(B, pattern.nnz, dtype=dt, device=dev)
+    ws = _workspace(pattern.n, B, dt, precond, dev, workspace)
+    infos = (_abi.sla_cg_info * max(B, 1))()
+    st = lib().sla_cg_adjoint_batched(ctypes.byref(_csr_struct(pattern, values)), B, _dev_ptr(values, dt, "values"),
+                                      _dev_ptr(x, dt, "x"), _dev_ptr(g, dt, "g"),
+                                      ctypes.byref(_opts(rtol, maxit, precond, unroll)),
+                                      _dev_ptr(grad_b, dt, "grad_b"), _dev_ptr(grad_values, dt, "grad_values"),
+                                      infos if sync else None, ws.data_ptr(), ws.numel(), _stream(dev))
+    _check(st, "sla_cg_adjoint_batched")
+    return grad_b, grad_values, ([_info(infos[s]) for s in range(B)] if sync else None)
+
+
+def _raise_on_failure(info: CGInfo, where: str):
+    if info.status == SLA_NOT_CONVERGED:
+        warnings.warn(f"{where}: CG did not reach rtol in {info.iters} iterations (rel_res {info.rel_res:.3e})")
+    elif info.status != SLA_OK:
+        raise SlaError(info.status, where)
+
+
+class CGSolve(torch.autograd.Function):
+    """x = A^{-1} b with the adjoint backward (one node in the autograd graph).
+
+    Saved for backward: x and A (pattern and values): O(n + nnz), whatever the
+    iteration count.  Backward solves A lambda = dL/dx with the same rtol, maxit
+    and preconditioner and returns grad_values = -lambda_i x_j on the pattern and
+    grad_b = lambda.
+    """
+
+    @staticmethod
+    def forward(ctx, row_ptr, col_idx, values, b, rtol, maxit, precond):
+        A = CSRMatrix(row_ptr, col_idx, values)
+        x, info, _ = sla_cg_solve(A, b, rtol=rtol, maxit=maxit, precond=precond)
+        _raise_on_failure(info, "CGSolve.forward")
+        ctx.save_for_backward(row_ptr, col_idx, values, x)
+        ctx.opts = (rtol, maxit, precond)
+        ctx.fwd_info = info
+        return x
+
+    @staticmethod
+    def backward(ctx, g):
+        row_ptr, col_idx, values, x = ctx.saved_tensors
+        rtol, maxit, precond = ctx.opts
+        A = CSRMatrix(row_ptr, col_idx, values)
+        need_v, need_b = ctx.needs_input_grad[2], ctx.needs_input_grad[3]
+        grad_b, grad_v, info = sla_cg_adjoint(A, x, g.contiguous(), rtol=rtol, maxit=maxit, precond=precond,
+                                              want_grad_values=need_v)
+        _raise_on_failure(info, "CGSolve.backward")
+        return None, None, (grad_v if need_v else None), (grad_b if need_b else None), None, None, None
+
+
+def solve(A: CSRMatrix, b: torch.Tensor, rtol: float = 1e-8, maxit: int = 10000,
+          precond: int = SLA_PRECOND_NONE) -> torch.Tensor:
+    """Differentiable x = A^{-1} b (gradients flow to A.values and b)."""
+    return CGSolve.apply(A.row_ptr, A.col_idx, A.values, b, rtol, maxit, precond)
+
+
+def matvec(A: CSRMatrix, x: torch.Tensor) -> torch.Tensor:
+    """y = A x through libsla (not differentiable; see solve for the differentiable path)."""
+    return sla_spmv(A, x)

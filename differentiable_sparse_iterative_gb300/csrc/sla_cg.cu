@@ -1,0 +1,594 @@
+// Conjugate-gradient solve and adjoint backward on the GPU (libsla).
+//
+// Method: "torch-sla: Differentiable Sparse Linear Algebra with Adjoint Solvers
+// and Sparse Tensor Parallelism for PyTorch" (Chi, Wen), technical summary:
+//   Methodology 1 - the GPU iterative backend (CG) behind .solve, one matrix
+//     or a batch sharing one pattern;
+//   Methodology 2 - linear-system adjoint: A^T lambda = dL/dx, grad_b = lambda,
+//     grad_A = -lambda_i x_j on the pattern, O(n + nnz) memory;
+//   Significance - Jacobi preconditioning of the native backend.
+// Hestenes-Stiefel CG with the stopping rule ||r_k|| <= rtol ||b|| on the
+// recursive residual (textbook reading; the summary gives no variant).
+//
+// GB300 design.  fp64 FMA issues at about 2 per clock per SM on this part, so
+// one fp64 operation costs as much time as ~11 bytes of HBM traffic; each
+// iteration is two fused kernels that keep the fp64 work near its minimum
+// (about 10 operations per row for a five-point matrix) while streaming the
+// matrix once:
+//   K_A (spmv_step):   p_k = z_k + beta p_{k-1} for the block's rows (kept in
+//                      shared memory), x += alpha_{k-1} p_{k-1} (delayed by one
+//                      iteration so p_{k-1} is read once), q = A p_k with
+//                      neighbours outside the tile recomputed from r and
+//                      p_{k-1}, and the partial sums of p.q;
+//   K_B (update_step): r -= alpha q and the partial sums of r.r (and r.z).
+// Each kernel ends with a deterministic two-level reduction: every block
+// publishes its partial sum, the last block to arrive adds all partials in a
+// fixed order and computes alpha (K_A) or beta and the stopping test (K_B) on
+// the device.  The loop itself is a CUDA graph: an init and a setup kernel,
+// then a device-side conditional WHILE node whose body holds U iterations and a
+// one-thread control kernel that ends the loop when every system has stopped,
+// then a finish kernel that applies the last delayed x update.  The host
+// launches one graph per solve and synchronises once to read the status.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "sla_common.cuh"
+#include "sla_host.h"
+
+namespace sla {
+
+// ------------------------------------------------------------------------ kernels
+
+template <typename V, typename I>
+__global__ void __launch_bounds__(kBlock) cg_init(Prob<V, I> P) {
+  // zero the control blocks; every system starts active
+  for (int s = threadIdx.x; s < P.batch; s += kBlock) {
+    Ctl c;
+    memset(&c, 0, sizeof(c));
+    P.ctl[s] = c;
+  }
+  if (threadIdx.x == 0) {
+    P.glob->active = (uint32_t)P.batch;
+    P.glob->bodies = 0;
+    P.glob->kernels = 1ull;
+    P.glob->safety_stop = 0;
+    P.glob->bad_csr = 0;
+  }
+}
+
+// Setup: x = x0 (or 0), r = b - A x0 (or b), Jacobi 1/A_ii, ||b||, r.r, r.z; then the
+// stopping decisions of iteration 0.
+template <typename V, typename I, bool JAC>
+__global__ void __launch_bounds__(kBlock) cg_setup(Prob<V, I> P) {
+  count_kernel(P.glob);
+  const int s = blockIdx.y, bx = blockIdx.x;
+  const int64_t vo = (int64_t)s * P.n;
+  const V *val = P.val + s * P.val_stride;
+  const V *b = P.b + vo;
+  V *x = P.x + vo;
+  V *r = P.r + vo;
+  V *dinv = JAC ? P.dinv + vo : nullptr;
+  const V *x0 = P.x0 ? P.x0 + vo : nullptr;
+  int64_t c0, c1;
+  chunk_of(P.n, P.G, bx, c0, c1);
+  double acc[5] = {0.0, 0.0, 0.0, 0.0, 0.0};  // b.b, r.r, r.z, #non-finite diag, #diag <= 0
+  for (int64_t i = c0 + threadIdx.x; i < c1; i += kBlock) {
+    const V bi = b[i];
+    V ri = bi;
+    int64_t e0, e1;
+    row_range(P.rp, i, P.nnz, e0, e1, &P.glob->bad_csr);
+    if (x0) {
+      V s_ = V(0);
+      for (int64_t e = e0; e < e1; ++e) {
+        const int32_t c = P.ci[e];
+        if (col_ok(c, P.n, &P.glob->bad_csr)) s_ = fmav<V>(val[e], x0[c], s_);
+      }
+      ri = bi - s_;
+      x[i] = x0[i];
+    } else {
+      x[i] = V(0);
+    }
+    r[i] = ri;
+    acc[0] = fma((double)bi, (double)bi, acc[0]);
+    acc[1] = fma((double)ri, (double)ri, acc[1]);
+    if (JAC) {
+      V d = V(0);
+      for (int64_t e = e0; e < e1; ++e)
+        if (P.ci[e] == (int32_t)i) d = val[e];
+      if (!isfinite((double)d)) acc[3] += 1.0;
+      else if (!(d > V(0))) acc[4] += 1.0;
+      const V di = V(1) / d;
+      dinv[i] = di;
+      acc[2] = fma((double)ri, (double)(di * ri), acc[2]);
+    }
+  }
+  block_sum<5>(acc);
+  double *part = P.partials + (size_t)s * kRedSlots * kMaxBlocksPerSystem;
+  Ctl *C = P.ctl + s;
+  if (!publish_last<5>(acc, part, &C->ticket, P.G, bx)) return;
+  double tot[5];
+  reduce_partials<5>(part, P.G, &C->ticket, tot);
+  if (threadIdx.x != 0) return;
+  const double nb = sqrt(tot[0]);
+  double *hist = P.history ? P.history + (size_t)s * (size_t)(P.maxit + 1) : nullptr;
+  C->nb = nb;
+  C->k = 0;
+  int done = 1;
+  if (!isfinite(nb)) {
+    C->status = SLA_NONFINITE;
+  } else if (nb == 0.0) {
+    C->status = SLA_OK;
+    C->pending = 2;
+    C->rel_res = 0.0;
+    if (hist) hist[0] = 0.0;
+  } else if (JAC && tot[3] > 0.0) {
+    C->status = SLA_NONFINITE;
+  } else if (JAC && tot[4] > 0.0) {
+    C->status = SLA_BREAKDOWN;
+  } else {
+    const double rr = tot[1];
+    C->rel_res = sqrt(rr) / nb;
+    if (hist) hist[0] = C->rel_res;
+    if (!isfinite(rr)) {
+      C->status = SLA_NONFINITE;
+    } else if (sqrt(rr) <= P.rtol * nb) {
+      C->status = SLA_OK;
+    } else if (P.maxit == 0) {
+      C->status = SLA_NOT_CONVERGED;
+    } else {
+      C->rho = JAC ? tot[2] : rr;
+      C->status = SLA_NOT_CONVERGED;
+      done = 0;
+    }
+  }
+  if (done) {
+    C->done = 1;
+    atomicSub(&P.glob->active, 1u);
+  }
+}
+
+// z_c = M^{-1} r_c and p_k[c] = z_c + beta p_{k-1}[c]: the same expression for rows of the tile
+// (kept in shared memory) and for neighbours recomputed from global memory.
+template <typename V, bool JAC>
+__device__ __forceinline__ V p_of(const V *__restrict__ r, const V *__restrict__ dinv, const V *__restrict__ po,
+                                  int64_t c, bool first, V beta) {
+  const V rc = r[c];
+  const V zc = JAC ? dinv[c] * rc : rc;
+  return first ? zc : fmav<V>(beta, po[c], zc);
+}
+
+template <typename V, typename I, bool JAC, int RPT>
+__global__ void __launch_bounds__(kBlock) cg_spmv_step(Prob<V, I> P, int par) {
+  count_kernel(P.glob);
+  const int s = blockIdx.y, bx = blockIdx.x;
+  Ctl *C = P.ctl + s;
+  if (C->done) return;
+  const int64_t k = C->k;
+  const bool first = (k == 0);
+  const V beta = (V)C->beta;
+  const V alpha_prev = (V)C->alpha;
+  const int64_t vo = (int64_t)s * P.n;
+  const V *__restrict__ val = P.val + s * P.val_stride;
+  const I *__restrict__ rp = P.rp;
+  const int32_t *__restrict__ ci = P.ci;
+  const V *__restrict__ r = P.r + vo;
+  const V *__restrict__ dinv = JAC ? P.dinv + vo : nullptr;
+  const V *__restrict__ po = P.p[par ^ 1] + vo;
+  V *__restrict__ pn = P.p[par] + vo;
+  V *__restrict__ q = P.q + vo;
+  V *__restrict__ x = P.x + vo;
+  __shared__ V sp[kBlock * RPT];
+
+  int64_t c0, c1;
+  chunk_of(P.n, P.G, bx, c0, c1);
+  const int64_t chunk = c1 - c0;
+  const int nsub = (int)((chunk + kBlock * RPT - 1) / (kBlock * RPT));
+  double pq = 0.0;
+  int64_t s0 = c0;
+  for (int sub = 0; sub < nsub; ++sub) {
+    const int len = (int)((chunk * (sub + 1)) / nsub - (chunk * sub) / nsub);
+    s0 = c0 + (chunk * sub) / nsub;
+    // p_k for the tile's rows, and the delayed x update with p_{k-1}
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+      const int li = j * kBlock + threadIdx.x;
+      if (li < len) {
+        const int64_t i = s0 + li;
+        const V ri = r[i];
+        const V zi = JAC ? dinv[i] * ri : ri;
+        V pv = zi;
+        if (!first) {
+          const V pold = po[i];
+          pv = fmav<V>(beta, pold, zi);
+          x[i] = fmav<V>(alpha_prev, pold, x[i]);
+        }
+        sp[li] = pv;
+        pn[i] = pv;
+      }
+    }
+    __syncthreads();
+    V part = V(0);
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+      const int li = j * kBlock + threadIdx.x;
+      if (li < len) {
+        const int64_t i = s0 + li;
+        int64_t e0, e1;
+        row_range(rp, i, P.nnz, e0, e1, &P.glob->bad_csr);
+        V acc = V(0);
+        for (int64_t e = e0; e < e1; ++e) {
+          const int32_t c = ci[e];
+          const V v = val[e];
+          const uint32_t off = (uint32_t)((int64_t)c - s0);
+          V pc;
+          if (off < (uint32_t)len) pc = sp[off];
+          else pc = col_ok(c, P.n, &P.glob->bad_csr) ? p_of<V, JAC>(r, dinv, po, c, first, beta) : V(0);
+          acc = fmav<V>(v, pc, acc);
+        }
+        q[i] = acc;
+        part = fmav<V>(sp[li], acc, part);
+      }
+    }
+    pq += (double)part;
+    __syncthreads();
+  }
+  double v1[1] = {pq};
+  block_sum<1>(v1);
+  double *pp = P.partials + (size_t)s * kRedSlots * kMaxBlocksPerSystem;
+  if (!publish_last<1>(v1, pp, &C->ticket, P.G, bx)) return;
+  double tot[1];
+  reduce_partials<1>(pp, P.G, &C->ticket, tot);
+  if (threadIdx.x != 0) return;
+  const double pqt = tot[0];
+  int stop = 0;
+  if (!isfinite(pqt)) {
+    C->status = SLA_NONFINITE;
+    stop = 1;
+  } else if (!(pqt > 0.0)) {
+    C->status = SLA_BREAKDOWN;
+    stop = 1;
+  } else {
+    C->alpha = C->rho / pqt;
+  }
+  if (stop) {
+    C->done = 1;
+    C->pending = 0;
+    atomicSub(&P.glob->active, 1u);
+  }
+}
+
+template <typename V, typename I, bool JAC>
+__global__ void __launch_bounds__(kBlock) cg_update_step(Prob<V, I> P, int par) {
+  count_kernel(P.glob);
+  const int s = blockIdx.y, bx = blockIdx.x;
+  Ctl *C = P.ctl + s;
+  if (C->done) return;
+  const V alpha = (V)C->alpha;
+  const int64_t vo = (int64_t)s * P.n;
+  V *__restrict__ r = P.r + vo;
+  const V *__restrict__ q = P.q + vo;
+  const V *__restrict__ dinv = JAC ? P.dinv + vo : nullptr;
+  int64_t c0, c1;
+  chunk_of(P.n, P.G, bx, c0, c1);
+  double acc[2] = {0.0, 0.0};
+  V rr = V(0), rz = V(0);
+  int cnt = 0;
+  for (int64_t i = c0 + threadIdx.x; i < c1; i += kBlock) {
+    const V ri = fmav<V>(-alpha, q[i], r[i]);
+    r[i] = ri;
+    rr = fmav<V>(ri, ri, rr);
+    if (JAC) rz = fmav<V>(ri, dinv[i] * ri, rz);
+    if constexpr (sizeof(V) == 4) {  // float data: fold into the fp64 sums every few rows
+      if (++cnt == 8) {
+        acc[0] += (double)rr;
+        acc[1] += (double)rz;
+        rr = V(0);
+        rz = V(0);
+        cnt = 0;
+      }
+    }
+  }
+  acc[0] += (double)rr;
+  acc[1] += (double)rz;
+  block_sum<2>(acc);
+  double *pp = P.partials + (size_t)s * kRedSlots * kMaxBlocksPerSystem;
+  if (!publish_last<2>(acc, pp, &C->ticket, P.G, bx)) return;
+  double tot[2];
+  reduce_partials<2>(pp, P.G, &C->ticket, tot);
+  if (threadIdx.x != 0) return;
+  const double rrt = tot[0];
+  const int64_t k1 = C->k + 1;
+  C->k = k1;
+  C->rel_res = sqrt(rrt) / C->nb;
+  if (P.history) P.history[(size_t)s * (size_t)(P.maxit + 1) + (size_t)k1] = C->rel_res;
+  C->last_parity = par;
+  int stop = 1;
+  if (!isfinite(rrt)) {
+    C->status = SLA_NONFINITE;
+  } else if (sqrt(rrt) <= P.rtol * C->nb) {
+    C->status = SLA_OK;
+  } else if (k1 >= P.maxit) {
+    C->status = SLA_NOT_CONVERGED;
+  } else {
+    const double rho_new = JAC ? tot[1] : rrt;
+    C->beta = rho_new / C->rho;
+    C->rho = rho_new;
+    stop = 0;
+  }
+  if (stop) {
+    C->done = 1;
+    C->pending = 1;  // x += alpha_k p_k still to apply
+    atomicSub(&P.glob->active, 1u);
+  }
+}
+
+// Ends the device-side loop once every system has stopped (or, as a guard that should never
+// fire, after more bodies than maxit allows).
+__global__ void cg_loop_control(Glob *g, cudaGraphConditionalHandle h, uint32_t max_bodies) {
+  if (threadIdx.x == 0) {
+    atomicAdd(&g->kernels, 1ull);
+    const uint32_t bodies = ++g->bodies;
+    const uint32_t active = *(volatile uint32_t *)&g->active;
+    if (active == 0u || bodies >= max_bodies) {
+      if (active != 0u) g->safety_stop = 1u;
+      cudaGraphSetConditional(h, 0u);
+    }
+  }
+}
+
+template <typename V, typename I>
+__global__ void __launch_bounds__(kBlock) cg_finish(Prob<V, I> P) {
+  count_kernel(P.glob);
+  const int s = blockIdx.y, bx = blockIdx.x;
+  const Ctl *C = P.ctl + s;
+  const int pending = C->pending;
+  if (pending == 0) return;
+  const int64_t vo = (int64_t)s * P.n;
+  V *x = P.x + vo;
+  const V *p = P.p[C->last_parity] + vo;
+  const V alpha = (V)C->alpha;
+  int64_t c0, c1;
+  chunk_of(P.n, P.G, bx, c0, c1);
+  for (int64_t i = c0 + threadIdx.x; i < c1; i += kBlock)
+    x[i] = pending == 1 ? fmav<V>(alpha, p[i], x[i]) : V(0);
+}
+
+// ------------------------------------------------------------------------ host side
+
+namespace {
+
+constexpr int kRPT = 4;       // rows per thread per tile of the SpMV step
+constexpr int kDefaultUnroll = 8;
+
+struct GraphEntry {
+  std::vector<char> key;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  uint64_t stamp = 0;
+};
+
+std::mutex g_mu;
+std::vector<GraphEntry> g_cache;
+uint64_t g_stamp = 0;
+constexpr size_t kCacheCap = 32;
+
+template <typename V, typename I, bool JAC>
+struct Kernels {
+  static void *init() { return (void *)cg_init<V, I>; }
+  static void *setup() { return (void *)cg_setup<V, I, JAC>; }
+  static void *spmv_step() { return (void *)cg_spmv_step<V, I, JAC, kRPT>; }
+  static void *update_step() { return (void *)cg_update_step<V, I, JAC>; }
+  static void *finish() { return (void *)cg_finish<V, I>; }
+};
+
+cudaError_t add_kernel(cudaGraphNode_t *node, cudaGraph_t g, const cudaGraphNode_t *dep, size_t ndep, void *fn,
+                       dim3 grid, dim3 block, void **args) {
+  cudaKernelNodeParams kp;
+  memset(&kp, 0, sizeof(kp));
+  kp.func = fn;
+  kp.gridDim = grid;
+  kp.blockDim = block;
+  kp.sharedMemBytes = 0;
+  kp.kernelParams = args;
+  kp.extra = nullptr;
+  return cudaGraphAddKernelNode(node, g, dep, ndep, &kp);
+}
+
+template <typename V, typename I, bool JAC>
+cudaError_t build_graph(const Prob<V, I> &P0, int unroll, cudaGraph_t *out_graph, cudaGraphExec_t *out_exec) {
+  using K = Kernels<V, I, JAC>;
+  Prob<V, I> P = P0;
+  cudaGraph_t g = nullptr;
+  cudaError_t e = cudaGraphCreate(&g, 0);
+  if (e != cudaSuccess) return e;
+  cudaGraphConditionalHandle h;
+  dim3 grid(P.G, P.batch), block(kBlock);
+  cudaGraphNode_t n_init, n_setup, n_while, n_fin, prev = nullptr;
+  void *args_p[] = {(void *)&P};
+  int par[2] = {0, 1};
+  void *args_pp[2][2] = {{(void *)&P, (void *)&par[0]}, {(void *)&P, (void *)&par[1]}};
+  const uint32_t max_bodies = (uint32_t)std::min<int64_t>((P.maxit + unroll - 1) / unroll + 2, 0x7fffffff);
+  cudaGraphNodeParams cp = {cudaGraphNodeTypeConditional};
+  do {
+    if ((e = cudaGraphConditionalHandleCreate(&h, g, 1u, cudaGraphCondAssignDefault)) != cudaSuccess) break;
+    if ((e = add_kernel(&n_init, g, nullptr, 0, K::init(), dim3(1), block, args_p)) != cudaSuccess) break;
+    if ((e = add_kernel(&n_setup, g, &n_init, 1, K::setup(), grid, block, args_p)) != cudaSuccess) break;
+    cp.type = cudaGraphNodeTypeConditional;
+    cp.conditional.handle = h;
+    cp.conditional.type = cudaGraphCondTypeWhile;
+    cp.conditional.size = 1;
+    if ((e = cudaGraphAddNode(&n_while, g, &n_setup, nullptr, 1, &cp)) != cudaSuccess) break;
+    cudaGraph_t body = cp.conditional.phGraph_out[0];
+    for (int u = 0; u < unroll && e == cudaSuccess; ++u) {
+      cudaGraphNode_t na, nb;
+      e = add_kernel(&na, body, prev ? &prev : nullptr, prev ? 1 : 0, K::spmv_step(), grid, block, args_pp[u & 1]);
+      if (e != cudaSuccess) break;
+      e = add_kernel(&nb, body, &na, 1, K::update_step(), grid, block, args_pp[u & 1]);
+      prev = nb;
+    }
+    if (e != cudaSuccess) break;
+    Glob *gp = P.glob;
+    void *args_c[] = {(void *)&gp, (void *)&h, (void *)&max_bodies};
+    cudaGraphNode_t nc;
+    if ((e = add_kernel(&nc, body, &prev, 1, (void *)cg_loop_control, dim3(1), dim3(32), args_c)) != cudaSuccess)
+      break;
+    if ((e = add_kernel(&n_fin, g, &n_while, 1, K::finish(), grid, block, args_p)) != cudaSuccess) break;
+    e = cudaGraphInstantiate(out_exec, g, 0);
+  } while (0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return e;
+  }
+  *out_graph = g;
+  return cudaSuccess;
+}
+
+int occupancy_blocks(const void *fn) {
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, kBlock, 0) != cudaSuccess || nb < 1) nb = 1;
+  return nb;
+}
+
+struct DeviceInfo {
+  int dev = -1;
+  int sms = 0;
+};
+
+DeviceInfo device_info() {
+  DeviceInfo d;
+  cudaGetDevice(&d.dev);
+  cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, d.dev);
+  if (d.sms < 1) d.sms = 1;
+  return d;
+}
+
+// Blocks per system: fill the GPU once (SMs x resident blocks), at least 256 rows per block.
+int choose_G(int64_t n, int64_t batch, int sms, int occ) {
+  int64_t total = (int64_t)sms * occ;
+  int64_t g = std::max<int64_t>(1, total / std::max<int64_t>(1, batch));
+  g = std::min<int64_t>(g, (n + kBlock - 1) / kBlock);
+  g = std::min<int64_t>(g, kMaxBlocksPerSystem);
+  return (int)std::max<int64_t>(1, g);
+}
+
+template <typename V, typename I, bool JAC>
+sla_status run_cg(Prob<V, I> P, int unroll, cudaStream_t stream, sla_cg_info *info, int64_t batch) {
+  const DeviceInfo di = device_info();
+  static std::atomic<int> occ_cache{0};
+  int occ = occ_cache.load();
+  if (occ == 0) {
+    occ = std::min(occupancy_blocks(Kernels<V, I, JAC>::spmv_step()),
+                   occupancy_blocks(Kernels<V, I, JAC>::update_step()));
+    occ_cache.store(occ);
+  }
+  P.G = choose_G(P.n, batch, di.sms, occ);
+  if (unroll <= 0) unroll = kDefaultUnroll;
+  if (unroll & 1) unroll += 1;  // the ping-pong parity of the body must repeat
+
+  std::vector<char> key(sizeof(P) + 4 * sizeof(int));
+  int tag[4] = {(int)sizeof(V), (int)sizeof(I), (int)JAC, unroll};
+  memcpy(key.data(), &P, sizeof(P));
+  memcpy(key.data() + sizeof(P), tag, sizeof(tag));
+  int dev = di.dev;
+  key.insert(key.end(), (char *)&dev, (char *)&dev + sizeof(dev));
+
+  cudaGraphExec_t exec = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto &en : g_cache)
+      if (en.key == key) {
+        en.stamp = ++g_stamp;
+        exec = en.exec;
+        break;
+      }
+    if (!exec) {
+      GraphEntry en;
+      en.key = key;
+      cudaError_t e = build_graph<V, I, JAC>(P, unroll, &en.graph, &en.exec);
+      if (e != cudaSuccess) return fail(e);
+      if (g_cache.size() >= kCacheCap) {
+        auto it = std::min_element(g_cache.begin(), g_cache.end(),
+                                   [](const GraphEntry &a, const GraphEntry &b) { return a.stamp < b.stamp; });
+        cudaGraphExecDestroy(it->exec);
+        cudaGraphDestroy(it->graph);
+        g_cache.erase(it);
+      }
+      en.stamp = ++g_stamp;
+      exec = en.exec;
+      g_cache.push_back(std::move(en));
+    }
+    cudaError_t e = cudaGraphLaunch(exec, stream);
+    if (e != cudaSuccess) return fail(e);
+  }
+  if (!info) return SLA_OK;
+  return read_info(P.ctl, P.glob, batch, stream, info);
+}
+
+template <typename V, typename I>
+sla_status dispatch_precond(const Prob<V, I> &P, int precond, int unroll, cudaStream_t st, sla_cg_info *info,
+                            int64_t batch) {
+  if (precond == SLA_PRECOND_JACOBI) return run_cg<V, I, true>(P, unroll, st, info, batch);
+  return run_cg<V, I, false>(P, unroll, st, info, batch);
+}
+
+template <typename V, typename I>
+Prob<V, I> make_prob(const sla_csr *A, int64_t batch, const void *values, int64_t val_stride, const void *b,
+                     const void *x0, const sla_cg_opts *o, void *x, double *history, void *ws, bool jacobi) {
+  Prob<V, I> P;
+  memset(&P, 0, sizeof(P));
+  Layout L = make_layout(A->n, batch, sizeof(V), jacobi);
+  char *w = (char *)ws;
+  P.rp = (const I *)A->row_ptr;
+  P.ci = A->col_idx;
+  P.val = (const V *)values;
+  P.b = (const V *)b;
+  P.x0 = (const V *)x0;
+  P.x = (V *)x;
+  P.r = (V *)(w + L.r);
+  P.p[0] = (V *)(w + L.p0);
+  P.p[1] = (V *)(w + L.p1);
+  P.q = (V *)(w + L.q);
+  P.dinv = jacobi ? (V *)(w + L.dinv) : nullptr;
+  P.partials = (double *)(w + L.partials);
+  P.ctl = (Ctl *)(w + L.ctl);
+  P.glob = (Glob *)(w + L.glob);
+  P.history = history;
+  P.val_stride = val_stride;
+  P.nnz = A->nnz;
+  P.maxit = o->maxit;
+  P.rtol = o->rtol;
+  P.n = (int32_t)A->n;
+  P.batch = (int32_t)batch;
+  return P;
+}
+
+}  // namespace
+
+sla_status cg_entry(const sla_csr *A, int64_t batch, const void *values, int64_t val_stride, const void *b,
+                    const void *x0, const sla_cg_opts *o, void *x, sla_cg_info *info, double *history, void *ws,
+                    cudaStream_t st) {
+  const bool jac = o->precond == SLA_PRECOND_JACOBI;
+  if (A->dtype == SLA_F64) {
+    if (A->rowptr_type == SLA_I64)
+      return dispatch_precond(make_prob<double, int64_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac),
+                              o->precond, o->unroll, st, info, batch);
+    return dispatch_precond(make_prob<double, int32_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac),
+                            o->precond, o->unroll, st, info, batch);
+  }
+  if (A->rowptr_type == SLA_I64)
+    return dispatch_precond(make_prob<float, int64_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac),
+                            o->precond, o->unroll, st, info, batch);
+  return dispatch_precond(make_prob<float, int32_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac),
+                          o->precond, o->unroll, st, info, batch);
+}
+
+size_t workspace_bytes(int64_t n, int64_t batch, int dtype, int precond) {
+  return make_layout(n, batch, dtype == SLA_F64 ? 8 : 4, precond == SLA_PRECOND_JACOBI).total;
+}
+
+}  // namespace sla

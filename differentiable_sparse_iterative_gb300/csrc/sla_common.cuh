@@ -1,0 +1,192 @@
+// Shared device-side definitions of libsla: control block, workspace layout,
+// deterministic reductions and the "last block reduces" protocol.
+//
+// The library solves the CSR systems of "torch-sla: Differentiable Sparse
+// Linear Algebra with Adjoint Solvers and Sparse Tensor Parallelism for
+// PyTorch" (Chi, Wen), technical summary, Methodology 1-2, on one GB300.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sla.h"
+
+namespace sla {
+
+constexpr int kBlock = 256;                  // threads per block of every row kernel
+constexpr int kWarps = kBlock / 32;
+constexpr int kMaxBlocksPerSystem = 2048;    // partial-sum slots per system and reduction
+constexpr int kRedSlots = 5;                 // reductions per kernel: at most 5 sums
+
+// Per-system solver state, resident on the device for the whole solve.
+struct Ctl {
+  double rho;        // r.z of the current iterate
+  double alpha;      // step length of the current (or last) iteration
+  double beta;       // beta of the last completed iteration
+  double nb;         // ||b||_2
+  double rel_res;    // ||r|| / ||b|| of the latest residual
+  int64_t k;         // completed iterations
+  int32_t status;    // sla_status
+  int32_t done;      // 1 once this system has stopped
+  int32_t pending;   // 0: nothing; 1: x += alpha * p[last_parity] at finish; 2: x = 0 at finish
+  int32_t last_parity;
+  uint32_t ticket;   // arrival counter of the last-block reduction (returns to 0 after each use)
+  uint32_t pad;
+};
+static_assert(sizeof(Ctl) % 8 == 0, "Ctl must stay 8-byte aligned");
+
+// Whole-call state.
+struct Glob {
+  uint32_t active;                // systems still iterating
+  uint32_t bodies;                // loop bodies executed
+  unsigned long long kernels;     // kernel executions of this call
+  uint32_t safety_stop;           // 1 if the loop was cut by the body bound (never expected)
+  uint32_t bad_csr;               // 1 if a row range or column index was out of bounds (entry skipped)
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace layout (offsets in bytes from the workspace base).
+struct Layout {
+  size_t glob, ctl, partials, r, p0, p1, q, dinv, total;
+};
+
+__host__ __device__ inline Layout make_layout(int64_t n, int64_t batch, size_t vbytes, bool jacobi) {
+  Layout L;
+  size_t off = 0;
+  L.glob = off; off += align256(sizeof(Glob));
+  L.ctl = off; off += align256(sizeof(Ctl) * (size_t)batch);
+  L.partials = off; off += align256(sizeof(double) * (size_t)kRedSlots * kMaxBlocksPerSystem * (size_t)batch);
+  size_t vec = align256(vbytes * (size_t)n * (size_t)batch);
+  L.r = off; off += vec;
+  L.p0 = off; off += vec;
+  L.p1 = off; off += vec;
+  L.q = off; off += vec;
+  L.dinv = off; off += jacobi ? vec : 0;
+  L.total = off;
+  return L;
+}
+
+// Everything a solve kernel needs, passed by value (it lives in the kernel's parameter bank).
+template <typename V, typename I>
+struct Prob {
+  const I *rp;
+  const int32_t *ci;
+  const V *val;          // values of system 0
+  const V *b;            // right-hand side of system 0
+  const V *x0;           // NULL: start from 0
+  V *x;                  // solution of system 0
+  V *r;
+  V *p[2];               // ping-pong search directions
+  V *q;
+  V *dinv;               // Jacobi: 1 / A_ii
+  double *partials;      // [batch][kRedSlots][kMaxBlocksPerSystem]
+  Ctl *ctl;              // [batch]
+  Glob *glob;
+  double *history;       // [batch][maxit+1] or NULL
+  int64_t val_stride;    // nnz for batched values, 0 when all systems share one value array
+  int64_t nnz;
+  int64_t maxit;
+  double rtol;
+  int32_t n;
+  int32_t G;             // blocks per system
+  int32_t batch;
+  int32_t pad;
+};
+
+template <typename V> __device__ __forceinline__ V fmav(V a, V b, V c);
+template <> __device__ __forceinline__ double fmav<double>(double a, double b, double c) { return fma(a, b, c); }
+template <> __device__ __forceinline__ float fmav<float>(float a, float b, float c) { return fmaf(a, b, c); }
+
+// Rows [c0, c1) of block bx out of G equal contiguous chunks.
+__device__ __forceinline__ void chunk_of(int64_t n, int G, int bx, int64_t &c0, int64_t &c1) {
+  c0 = n * bx / G;
+  c1 = n * (bx + 1) / G;
+}
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Block-wide sum of NV values in a fixed order (lane tree, then warp tree); result in thread 0.
+template <int NV>
+__device__ __forceinline__ void block_sum(double (&v)[NV]) {
+  __shared__ double sred[NV][kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    double w = warp_sum(v[j]);
+    if (lane == 0) sred[j][warp] = w;
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      double w = lane < kWarps ? sred[j][lane] : 0.0;
+      w = warp_sum(w);
+      v[j] = w;
+    }
+  }
+  __syncthreads();
+}
+
+// Publishes this block's sums (valid in thread 0) as partials[j][bx] and returns true in the
+// block that arrives last.  The last block then reads all G partials with reduce_partials().
+template <int NV>
+__device__ __forceinline__ bool publish_last(const double (&v)[NV], double *part, uint32_t *ticket, int G,
+                                             int bx) {
+  __shared__ int s_last;
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) part[(size_t)j * kMaxBlocksPerSystem + bx] = v[j];
+    __threadfence();
+    unsigned t = atomicAdd(ticket, 1u);
+    s_last = (t == (unsigned)(G - 1));
+  }
+  __syncthreads();
+  if (!s_last) return false;
+  __threadfence();
+  return true;
+}
+
+// Sum of the G partials of each reduction in a fixed order: thread t adds slots t, t+kBlock, ...
+// in that order, then block_sum.  Independent of which block came last.  Result in thread 0;
+// the ticket is returned to 0 for the next kernel.
+template <int NV>
+__device__ __forceinline__ void reduce_partials(const double *part, int G, uint32_t *ticket, double (&tot)[NV]) {
+#pragma unroll
+  for (int j = 0; j < NV; ++j) tot[j] = 0.0;
+  for (int i = threadIdx.x; i < G; i += kBlock) {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) tot[j] += __ldcg(part + (size_t)j * kMaxBlocksPerSystem + i);
+  }
+  block_sum<NV>(tot);
+  if (threadIdx.x == 0) *ticket = 0u;
+}
+
+// Row range [e0, e1) of row i, or an empty range (and the bad-CSR flag) if row_ptr is out of bounds.
+template <typename I>
+__device__ __forceinline__ void row_range(const I *rp, int64_t i, int64_t nnz, int64_t &e0, int64_t &e1,
+                                          uint32_t *bad) {
+  e0 = (int64_t)rp[i];
+  e1 = (int64_t)rp[i + 1];
+  if (e0 < 0 || e1 < e0 || e1 > nnz) {
+    if (bad) atomicOr(bad, 1u);
+    e0 = e1 = 0;
+  }
+}
+
+// True when column c is inside [0, n); otherwise raises the bad-CSR flag.
+__device__ __forceinline__ bool col_ok(int32_t c, int32_t n, uint32_t *bad) {
+  const bool ok = (uint32_t)c < (uint32_t)n;
+  if (!ok && bad) atomicOr(bad, 1u);
+  return ok;
+}
+
+__device__ __forceinline__ void count_kernel(Glob *g) {
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicAdd(&g->kernels, 1ull);
+}
+
+}  // namespace sla

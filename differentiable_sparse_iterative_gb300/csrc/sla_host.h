@@ -1,0 +1,33 @@
+// Host-side internals shared by the libsla translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sla.h"
+
+namespace sla {
+
+// Records a CUDA error for sla_last_cuda_error() and returns SLA_CUDA_ERROR.
+sla_status fail(cudaError_t e);
+
+// Adds host-side kernel launches to the process-wide count.
+void count_launches(uint64_t k);
+
+// Copies the per-system control blocks back, synchronises the stream and fills info[batch].
+struct Ctl;
+struct Glob;
+sla_status read_info(const Ctl *ctl, const Glob *glob, int64_t batch, cudaStream_t stream, sla_cg_info *info);
+
+// Device-resident CG for `batch` systems sharing A's pattern (values at values + s*val_stride).
+sla_status cg_entry(const sla_csr *A, int64_t batch, const void *values, int64_t val_stride, const void *b,
+                    const void *x0, const sla_cg_opts *o, void *x, sla_cg_info *info, double *history, void *ws,
+                    cudaStream_t st);
+
+size_t workspace_bytes(int64_t n, int64_t batch, int dtype, int precond);
+
+// grad_values[s][k] = -lambda_s[row(k)] * x_s[col(k)] for `batch` systems (asynchronous).
+sla_status grad_values_entry(const sla_csr *A, int64_t batch, const void *lambda, const void *x, void *gv,
+                             cudaStream_t st);
+
+}  // namespace sla

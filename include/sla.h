@@ -1,0 +1,218 @@
+/*
+ * libsla — differentiable CSR conjugate-gradient solve for one GB300 (sm_103a).
+ *
+ * The method is the one described in "torch-sla: Differentiable Sparse Linear
+ * Algebra with Adjoint Solvers and Sparse Tensor Parallelism for PyTorch"
+ * (Chi, Wen), technical summary ("TS" below):
+ *   - TS Methodology 1, "Unified backend abstraction": an autograd-aware
+ *     .matvec / .solve API whose GPU iterative backend is conjugate gradient;
+ *     four sparse tensor kinds, among them one matrix and a batch of matrices
+ *     sharing one sparsity pattern;
+ *   - TS Methodology 2, "Adjoint differentiation framework", linear systems:
+ *     for A x = b the backward pass solves A^T lambda = dL/dx once; the
+ *     gradient with respect to the matrix is -lambda_i x_j on the sparsity
+ *     pattern only, so the autograd graph is O(1) and its memory O(n + nnz),
+ *     independent of the iteration count;
+ *   - TS Significance: the native iterative backend is Jacobi preconditioned.
+ * Where the summary leaves a step open the library takes the textbook reading:
+ * Hestenes-Stiefel CG, stopping when ||r_k||_2 <= rtol * ||b||_2 on the
+ * recursively updated residual (unpreconditioned norm also under Jacobi),
+ * iteration count = number of products A p in the loop, b = 0 giving x = 0.
+ *
+ * Conventions for every entry point
+ *   - Pointers named "device" are CUDA device (or managed) memory on the
+ *     current device; "host" pointers are ordinary host memory.  The library
+ *     allocates no device memory: scratch space is the caller's workspace,
+ *     sized by sla_cg_workspace_bytes().  The caller keeps ownership of
+ *     every buffer.
+ *   - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Work is enqueued on it in order.
+ *   - Matrices are square CSR, canonical: row_ptr[0] = 0, row_ptr[n] = nnz,
+ *     non-decreasing; within a row, col_idx strictly increasing and in
+ *     [0, n); every diagonal entry stored.  The solvers assume A symmetric
+ *     positive definite (so A^T = A).  sla_validate_csr() checks the
+ *     structural part.
+ *   - Row pointers are int32 or int64 (sla_itype); column indices int32 (so
+ *     n < 2^31); values and vectors are float32 or float64 (sla_dtype), all
+ *     of one type within a call.  Float32 data is updated in float32; dot
+ *     products are summed in float32 over a few rows per thread and in
+ *     float64 from there on, and every scalar of the iteration (alpha, beta,
+ *     norms) is float64.
+ *   - Kernels never read outside the caller's buffers: an out-of-range row
+ *     pointer or column index is skipped (SpMV and grad_values then treat the
+ *     entry as absent; a solve reports SLA_BAD_CSR).
+ *   - Errors never leave a kernel waiting: invalid arguments are rejected on
+ *     the host before any launch (SLA_INVALID_ARG / SLA_WORKSPACE_TOO_SMALL);
+ *     numerical failures are reported through sla_cg_info.status; a CUDA
+ *     runtime failure returns SLA_CUDA_ERROR (sla_last_cuda_error() names it).
+ */
+#ifndef SLA_H_
+#define SLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SLA_API __attribute__((visibility("default")))
+#else
+#define SLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sla_status {
+  SLA_OK = 0,                  /* converged (or nothing to do) */
+  SLA_NOT_CONVERGED = 1,       /* maxit iterations done without reaching rtol; x holds the last iterate */
+  SLA_BREAKDOWN = 2,           /* p.Ap <= 0, or a Jacobi diagonal <= 0: A is not SPD; x = last iterate */
+  SLA_INVALID_ARG = 3,         /* null pointer, negative size, unknown enum, misaligned buffer */
+  SLA_BAD_CSR = 4,             /* non-canonical CSR (sla_validate_csr), or a solve met an out-of-range
+                                  row pointer or column index (such entries are skipped, never read) */
+  SLA_NONFINITE = 5,           /* ||b||, r.r, p.Ap or a Jacobi diagonal is NaN or infinite */
+  SLA_WORKSPACE_TOO_SMALL = 6, /* ws_bytes < sla_cg_workspace_bytes(...) */
+  SLA_TIMEOUT = 7,             /* reserved: no current entry point waits on other blocks */
+  SLA_CUDA_ERROR = 8           /* a CUDA runtime call failed */
+} sla_status;
+
+typedef enum sla_dtype { SLA_F32 = 0, SLA_F64 = 1 } sla_dtype;
+typedef enum sla_itype { SLA_I32 = 0, SLA_I64 = 1 } sla_itype;
+typedef enum sla_precond { SLA_PRECOND_NONE = 0, SLA_PRECOND_JACOBI = 1 } sla_precond;
+
+/* A square CSR matrix on the device (TS Methodology 1: "SparseTensor"). */
+typedef struct sla_csr {
+  int64_t n;              /* rows = columns, 0 <= n < 2^31 */
+  int64_t nnz;            /* stored entries */
+  int32_t rowptr_type;    /* sla_itype of row_ptr */
+  int32_t dtype;          /* sla_dtype of values */
+  const void *row_ptr;    /* device, n+1 entries */
+  const int32_t *col_idx; /* device, nnz entries */
+  const void *values;     /* device, nnz entries (ignored by the batched calls: values come separately) */
+} sla_csr;
+
+typedef struct sla_cg_opts {
+  double rtol;            /* stop when ||r|| <= rtol * ||b||; 0 runs exactly maxit iterations */
+  int64_t maxit;          /* iteration cap, >= 0 */
+  int32_t precond;        /* sla_precond */
+  int32_t unroll;         /* iterations per device-side loop body; 0 = library default */
+} sla_cg_opts;
+
+/* Result of one solve (host memory).  Filled after the call has synchronised the stream. */
+typedef struct sla_cg_info {
+  int64_t iters;          /* completed iterations (products A p inside the loop) */
+  double rel_res;         /* ||r|| / ||b|| of the recursive residual at exit (0 when b = 0) */
+  int32_t status;         /* sla_status of this system */
+  int32_t reserved;
+  int64_t kernels;        /* kernel executions of this call on the GPU, counted on the device */
+} sla_cg_info;
+
+/* ---------------------------------------------------------------- housekeeping */
+
+/* Human-readable name of a status code (static storage). */
+SLA_API const char *sla_status_string(int32_t status);
+
+/* Name of the last CUDA runtime error seen by this thread ("no error" if none). */
+SLA_API const char *sla_last_cuda_error(void);
+
+/* Library ABI version: 100 * major + minor. */
+SLA_API int32_t sla_version(void);
+
+/* Total kernels launched by this process through the library (host-side count of launches,
+ * plus the device-counted kernel executions of every solve whose info was read back). */
+SLA_API uint64_t sla_launch_count(void);
+
+/*
+ * Bytes of device workspace a solve or adjoint call needs, for `batch` systems of n unknowns
+ * (batch = 1 for the single-system calls).  Returns 0 for invalid arguments.
+ * Ownership: the caller allocates it (any 256-byte aligned device buffer) and may reuse it
+ * across calls; calls sharing one workspace must not overlap on the GPU.
+ */
+SLA_API size_t sla_cg_workspace_bytes(int64_t n, int64_t batch, int32_t dtype, int32_t precond);
+
+/*
+ * Structural check of a CSR matrix (TS Methodology 1: the matrix types the solvers accept).
+ * Checks row_ptr bounds and monotonicity, column range, strictly increasing columns within
+ * each row and a stored diagonal; with check_symmetric != 0 also that the pattern and values
+ * are symmetric (A_ij == A_ji bit for bit).  Synchronises the stream.
+ * workspace: device, >= 256 bytes.  Returns SLA_OK or SLA_BAD_CSR; *bad_row (host, may be NULL)
+ * receives the first offending row or -1.
+ */
+SLA_API sla_status sla_validate_csr(const sla_csr *A, int32_t check_symmetric, int64_t *bad_row,
+                            void *workspace, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------- the hot path */
+
+/*
+ * y = A x (TS Methodology 1: ".matvec").  x, y: device, n entries of A->dtype; x and y must not
+ * overlap.  Each row is summed in storage order with fused multiply-adds.  Asynchronous.
+ */
+SLA_API sla_status sla_spmv(const sla_csr *A, const void *x, void *y, void *stream);
+
+/*
+ * Solve A x = b by conjugate gradient (TS Methodology 1: the GPU iterative backend; Jacobi
+ * preconditioning per TS Significance when opts->precond = SLA_PRECOND_JACOBI).
+ *   b        device, n entries.
+ *   x0       device, n entries, or NULL for x0 = 0.  May equal x (in-place restart).
+ *   x        device, n entries: the solution (the last iterate on every exit).
+ *   info     host, or NULL.  With info the call synchronises the stream once and fills it; with
+ *            NULL the call is fully asynchronous and the status stays on the device.
+ *   history  device, opts->maxit + 1 doubles, or NULL: history[k] = ||r_k|| / ||b|| for
+ *            k = 0..iters (entries past iters are not written).
+ *   workspace/ws_bytes: device scratch, >= sla_cg_workspace_bytes(n, 1, dtype, precond).
+ * The whole iteration runs on the device (a CUDA graph whose loop is a device-side
+ * conditional); the host does not take part between the first and the last iteration.
+ */
+SLA_API sla_status sla_cg_solve(const sla_csr *A, const void *b, const void *x0, const sla_cg_opts *opts,
+                        void *x, sla_cg_info *info, double *history, void *workspace, size_t ws_bytes,
+                        void *stream);
+
+/*
+ * Adjoint backward of x = A^{-1} b (TS Methodology 2, linear systems): solve A^T lambda = g
+ * (A symmetric, so the same CG with the same opts, from lambda = 0), then
+ *   grad_b[i]       = lambda[i]                          (written directly: grad_b is lambda)
+ *   grad_values[k]  = -lambda[row(k)] * x[col_idx[k]]    (one entry per stored entry, CSR order)
+ *   x, g        device, n entries (x: the forward solution; g: dL/dx).
+ *   grad_b      device, n entries.  grad_values: device, nnz entries, or NULL to skip.
+ *   info        as for sla_cg_solve (status of the adjoint solve).
+ */
+SLA_API sla_status sla_cg_adjoint(const sla_csr *A, const void *x, const void *g, const sla_cg_opts *opts,
+                          void *grad_b, void *grad_values, sla_cg_info *info, void *workspace,
+                          size_t ws_bytes, void *stream);
+
+/*
+ * grad_values[k] = -lambda[row(k)] * x[col_idx[k]] for every stored entry (TS Methodology 2: the
+ * matrix gradient "only on the sparsity pattern").  lambda, x: device, n entries; grad_values:
+ * device, nnz entries.  Asynchronous.
+ */
+SLA_API sla_status sla_grad_values(const sla_csr *A, const void *lambda, const void *x, void *grad_values,
+                           void *stream);
+
+/*
+ * Batched solve over one shared pattern (TS Methodology 1: one "SparseTensor" holding a shared
+ * pattern with a batch of value arrays; "thousands of systems at once").  Each system runs its
+ * own CG (own alpha, beta, stopping test); a converged system stops changing.
+ *   pattern   CSR whose row_ptr/col_idx are shared; pattern->values is ignored.
+ *   values    device, batch x nnz, row-major (system s at values + s*nnz).
+ *   b, x0, x  device, batch x n (x0 may be NULL).
+ *   info      host, batch entries, or NULL.
+ *   history   device, batch x (maxit+1) doubles, or NULL.
+ *   workspace >= sla_cg_workspace_bytes(n, batch, dtype, precond).
+ */
+SLA_API sla_status sla_cg_solve_batched(const sla_csr *pattern, int64_t batch, const void *values, const void *b,
+                                const void *x0, const sla_cg_opts *opts, void *x, sla_cg_info *info,
+                                double *history, void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Batched adjoint: for every system s, lambda_s = A_s^{-1} g_s, grad_b[s] = lambda_s,
+ * grad_values[s][k] = -lambda_s[row(k)] * x_s[col_idx[k]].  Shapes as in sla_cg_solve_batched;
+ * grad_values is batch x nnz (or NULL).
+ */
+SLA_API sla_status sla_cg_adjoint_batched(const sla_csr *pattern, int64_t batch, const void *values, const void *x,
+                                  const void *g, const sla_cg_opts *opts, void *grad_b, void *grad_values,
+                                  sla_cg_info *info, void *workspace, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SLA_H_ */

@@ -1,0 +1,102 @@
+"""libsla loads and exports every symbol include/sla.h declares; host-side argument checks (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from differentiable_sparse_iterative_gb300 import _abi, build as sla_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sla_build.build()
+    return _abi.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "sla.h")).read()
+    return sorted(set(re.findall(r"SLA_API\s+[\w\s\*]*?\b(sla_\w+)\s*\(", text)))
+
+
+def test_header_matches_binding():
+    assert declared_symbols() == sorted(_abi.EXPORTS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    # and nothing else of ours is visible
+    out = os.popen(f"nm -D --defined-only {_abi.LIB_PATH}").read()
+    ours = sorted(set(re.findall(r" T (sla_\w+)", out)))
+    assert ours == declared_symbols()
+
+
+def test_status_strings_and_version(lib):
+    assert lib.sla_version() == 100
+    assert lib.sla_status_string(0) == b"SLA_OK"
+    assert lib.sla_status_string(2) == b"SLA_BREAKDOWN"
+    assert lib.sla_status_string(99) == b"SLA_UNKNOWN_STATUS"
+
+
+def test_workspace_bytes(lib):
+    f = lib.sla_cg_workspace_bytes
+    assert f(-1, 1, 1, 0) == 0 and f(10, 0, 1, 0) == 0 and f(10, 1, 7, 0) == 0 and f(10, 1, 1, 5) == 0
+    a, j = f(1000, 1, 1, 0), f(1000, 1, 1, 1)
+    assert j > a > 4 * 1000 * 8
+    assert f(1000, 1, 0, 0) < a                 # float32 vectors are half the size
+    assert f(1000, 4, 1, 0) > 3 * (a - 200000)  # batch scales the vectors
+    assert a % 256 == 0
+
+
+def _csr(n=4, nnz=10, rt=0, dt=1, ptr=0x10000):
+    A = _abi.sla_csr()
+    A.n, A.nnz, A.rowptr_type, A.dtype = n, nnz, rt, dt
+    A.row_ptr = A.col_idx = A.values = ptr
+    return A
+
+
+def _opts(rtol=1e-8, maxit=10, precond=0):
+    o = _abi.sla_cg_opts()
+    o.rtol, o.maxit, o.precond, o.unroll = rtol, maxit, precond, 0
+    return o
+
+
+def test_argument_rejection_without_gpu(lib):
+    P = 0x10000  # never dereferenced: every case is rejected before any CUDA call
+    solve = lib.sla_cg_solve
+    assert solve(None, P, None, ctypes.byref(_opts()), P, None, None, P, 1 << 20, None) == _abi.SLA_INVALID_ARG
+    assert solve(ctypes.byref(_csr(dt=7)), P, None, ctypes.byref(_opts()), P, None, None, P, 1 << 20, None) == 3
+    assert solve(ctypes.byref(_csr(rt=9)), P, None, ctypes.byref(_opts()), P, None, None, P, 1 << 20, None) == 3
+    assert solve(ctypes.byref(_csr(n=-1)), P, None, ctypes.byref(_opts()), P, None, None, P, 1 << 20, None) == 3
+    assert solve(ctypes.byref(_csr(n=1 << 31)), P, None, ctypes.byref(_opts()), P, None, None, P, 1 << 20,
+                 None) == 3
+    assert solve(ctypes.byref(_csr()), P, None, None, P, None, None, P, 1 << 20, None) == 3
+    assert solve(ctypes.byref(_csr()), P, None, ctypes.byref(_opts(rtol=-1.0)), P, None, None, P, 1 << 20,
+                 None) == 3
+    assert solve(ctypes.byref(_csr()), P, None, ctypes.byref(_opts(rtol=float("nan"))), P, None, None, P,
+                 1 << 20, None) == 3
+    assert solve(ctypes.byref(_csr()), P, None, ctypes.byref(_opts(maxit=-1)), P, None, None, P, 1 << 20,
+                 None) == 3
+    assert solve(ctypes.byref(_csr()), P, None, ctypes.byref(_opts(precond=3)), P, None, None, P, 1 << 20,
+                 None) == 3
+    assert solve(ctypes.byref(_csr()), None, None, ctypes.byref(_opts()), P, None, None, P, 1 << 20, None) == 3
+    assert solve(ctypes.byref(_csr()), P + 4, None, ctypes.byref(_opts()), P, None, None, P, 1 << 20, None) == 3
+    assert solve(ctypes.byref(_csr()), P, None, ctypes.byref(_opts()), P, None, None, P + 16, 1 << 20, None) == 3
+    assert solve(ctypes.byref(_csr()), P, None, ctypes.byref(_opts()), P, None, None, P, 16,
+                 None) == _abi.SLA_WORKSPACE_TOO_SMALL
+    assert lib.sla_cg_solve_batched(ctypes.byref(_csr()), -1, P, P, None, ctypes.byref(_opts()), P, None, None,
+                                    P, 1 << 20, None) == 3
+    assert lib.sla_spmv(ctypes.byref(_csr(rt=0, nnz=1 << 31)), P, P, None) == 3
+
+
+def test_empty_system_needs_no_gpu(lib):
+    info = _abi.sla_cg_info()
+    info.status = 77
+    st = lib.sla_cg_solve(ctypes.byref(_csr(n=0, nnz=0)), None, None, ctypes.byref(_opts()), None,
+                          ctypes.byref(info), None, None, 0, None)
+    assert st == 0 and info.status == 0 and info.iters == 0
+    assert lib.sla_cg_solve_batched(ctypes.byref(_csr()), 0, 0x10000, 0x10000, None, ctypes.byref(_opts()),
+                                    0x10000, None, None, 0x10000, 1 << 20, None) == 0

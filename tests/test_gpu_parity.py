@@ -1,0 +1,272 @@
+"""libsla (CUDA, through the C ABI) against the fp64 oracle: small and ragged cases, edge cases.
+
+Sizes span several blocks and tiles with ragged tails; every case is seeded.
+"""
+import numpy as np
+import pytest
+
+from gpu_helpers import (sla, oracle, torch, rel, to_dev, t, spmv_bound, check_history, X_TOL_F64, GRAD_TOL_F64,
+                         TOL_F32, ITER_SLACK_F64, ITER_SLACK_F32)
+from workloads import poisson_5pt, diffusion_dirichlet, diffusion_interior, random_spd, config1, config3
+
+pytestmark = pytest.mark.gpu
+
+EPS64 = np.finfo(np.float64).eps
+EPS32 = np.finfo(np.float32).eps
+
+
+def _cases():
+    rng = np.random.default_rng(100)
+    return {
+        "poisson1": poisson_5pt(1),
+        "poisson2": poisson_5pt(2),
+        "poisson17": poisson_5pt(17),
+        "poisson33_i64": poisson_5pt(33, rowptr64=True),
+        "poisson90": poisson_5pt(90),
+        "dirichlet45": diffusion_dirichlet(45, rng.lognormal(0, 1.0, 2 * 45 * 46)),
+        "interior31": diffusion_interior(31, rng.lognormal(0, 0.5, 2 * 31 * 30), 0.01),
+        "random1025": random_spd(1025, 6.0, 7, long_rows=4),
+        "random3": random_spd(3, 1.0, 8),
+    }
+
+
+CASES = _cases()
+
+
+@pytest.mark.parametrize("name", list(CASES))
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_spmv(name, dtype):
+    A = CASES[name]
+    Ad = A.astype(dtype)
+    x = np.random.default_rng(1).standard_normal(A.n).astype(dtype)
+    y = sla.sla_spmv(to_dev(Ad), t(x)).cpu().numpy()
+    yo = oracle.spmv(A.row_ptr, A.col_idx, Ad.values.astype(np.float64), x.astype(np.float64))
+    eps = EPS64 if dtype == np.float64 else EPS32
+    assert np.all(np.abs(y - yo) <= spmv_bound(Ad, x, eps))
+
+
+def test_spmv_exact_integers():
+    A = poisson_5pt(50)
+    x = np.random.default_rng(2).integers(-1000, 1000, A.n).astype(np.float64)
+    y = sla.sla_spmv(to_dev(A), t(x)).cpu().numpy()
+    assert np.array_equal(y, oracle.spmv(A.row_ptr, A.col_idx, A.values, x))
+
+
+@pytest.mark.parametrize("name", list(CASES))
+@pytest.mark.parametrize("precond", [0, 1])
+def test_cg_and_adjoint_f64(name, precond):
+    A = CASES[name]
+    rng = np.random.default_rng(A.n + precond)
+    b, g = rng.standard_normal(A.n), rng.standard_normal(A.n)
+    rtol, maxit = 1e-10, 20000
+    dA = to_dev(A)
+    x, info, hist = sla.sla_cg_solve(dA, t(b), rtol=rtol, maxit=maxit, precond=precond, history=True)
+    ref = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=rtol, maxit=maxit, precond=precond, history=True)
+    assert info.status == ref["status"] == 0
+    assert abs(info.iters - ref["iters"]) <= ITER_SLACK_F64
+    assert rel(x.cpu().numpy(), ref["x"]) <= X_TOL_F64
+    h = hist.cpu().numpy()
+    check_history(h, ref["history"])
+    assert np.isnan(h[info.iters + 1:]).all()  # entries past iters are not written
+    gb, gv, ainfo = sla.sla_cg_adjoint(dA, x, t(g), rtol=rtol, maxit=maxit, precond=precond)
+    adj = oracle.cg_adjoint(A.row_ptr, A.col_idx, A.values, ref["x"], g, rtol=rtol, maxit=maxit, precond=precond)
+    assert ainfo.status == adj["status"] == 0
+    assert abs(ainfo.iters - adj["iters"]) <= ITER_SLACK_F64
+    assert rel(gb.cpu().numpy(), adj["grad_b"]) <= GRAD_TOL_F64
+    assert gv.shape == (A.nnz,)
+    assert rel(gv.cpu().numpy(), adj["grad_values"]) <= GRAD_TOL_F64
+
+
+def test_grad_values_exact_on_given_vectors():
+    # one rounded product per entry: bit-exact against the oracle given the same lambda and x
+    A = random_spd(777, 5.0, 3, long_rows=2)
+    rng = np.random.default_rng(4)
+    lam, x = rng.standard_normal(A.n), rng.standard_normal(A.n)
+    gv = sla.sla_grad_values(to_dev(A), t(lam), t(x)).cpu().numpy()
+    assert np.array_equal(gv, oracle.grad_values(A.row_ptr, A.col_idx, lam, x))
+
+
+def test_config1_manufactured_and_loss_adjoint():
+    w = config1()
+    dA = to_dev(w.A)
+    x, info, hist = sla.sla_cg_solve(dA, t(w.b), rtol=w.rtol, maxit=w.maxit, history=True)
+    ref = oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=w.rtol, maxit=w.maxit, history=True)
+    assert info.status == 0 and abs(info.iters - ref["iters"]) <= ITER_SLACK_F64
+    xs = x.cpu().numpy()
+    assert rel(xs, ref["x"]) <= X_TOL_F64
+    check_history(hist.cpu().numpy(), ref["history"])
+    # L = 0.5 ||x - x_t||^2  ->  g = x - x_t
+    g_gpu = x - t(w.x_target)
+    gb, gv, ainfo = sla.sla_cg_adjoint(dA, x, g_gpu, rtol=w.rtol, maxit=w.maxit)
+    adj = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, w.A.values, ref["x"], ref["x"] - w.x_target, rtol=w.rtol,
+                            maxit=w.maxit)
+    assert rel(gb.cpu().numpy(), adj["grad_b"]) <= GRAD_TOL_F64
+    assert rel(gv.cpu().numpy(), adj["grad_values"]) <= GRAD_TOL_F64
+
+
+@pytest.mark.parametrize("m,batch,precond", [(16, 5, 0), (24, 3, 1), (128, 64, 0)])
+def test_batched_f32(m, batch, precond):
+    w = config3(m=m, batch=batch)
+    P = to_dev(w.A, np.float32)
+    vals, b, g = t(w.values_b), t(w.b), t(w.g)
+    x, infos, hist = sla.sla_cg_solve_batched(P, vals, b, rtol=w.rtol, maxit=5000, precond=precond, history=True)
+    gb, gv, ainfos = sla.sla_cg_adjoint_batched(P, vals, x, g, rtol=w.rtol, maxit=5000, precond=precond)
+    xs, gbs, gvs, hs = x.cpu().numpy(), gb.cpu().numpy(), gv.cpu().numpy(), hist.cpu().numpy()
+    for s in range(batch):
+        v64 = w.values_b[s].astype(np.float64)
+        ref = oracle.cg(w.A.row_ptr, w.A.col_idx, v64, w.b[s].astype(np.float64), rtol=w.rtol, maxit=5000,
+                        precond=precond, history=True)
+        assert infos[s].status == ref["status"] == 0
+        assert abs(infos[s].iters - ref["iters"]) <= max(1, ITER_SLACK_F32 * ref["iters"])
+        assert rel(xs[s], ref["x"]) <= TOL_F32
+        check_history(hs[s], ref["history"], k=10, tol=1e-4)
+        adj = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, v64, xs[s].astype(np.float64),
+                                w.g[s].astype(np.float64), rtol=w.rtol, maxit=5000, precond=precond)
+        assert ainfos[s].status == 0
+        assert rel(gbs[s], adj["grad_b"]) <= TOL_F32
+        assert rel(gvs[s], adj["grad_values"]) <= TOL_F32
+
+
+def test_batched_f64_equals_single_systems():
+    # each system of a batched solve equals the single-system solve of that system
+    w = config3(m=20, batch=4)
+    v64 = w.values_b.astype(np.float64)
+    P = to_dev(w.A)
+    xb, infos, _ = sla.sla_cg_solve_batched(P, t(v64), t(w.b.astype(np.float64)), rtol=1e-10, maxit=5000)
+    for s in range(4):
+        As = sla.CSRMatrix(P.row_ptr, P.col_idx, t(v64[s]))
+        xs, info, _ = sla.sla_cg_solve(As, t(w.b[s].astype(np.float64)), rtol=1e-10, maxit=5000)
+        assert info.iters == infos[s].iters
+        assert rel(xb[s].cpu().numpy(), xs.cpu().numpy()) <= 1e-12
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+
+def _solve_both(A, b, **kw):
+    x, info, _ = sla.sla_cg_solve(to_dev(A), t(b), **kw)
+    ref = oracle.cg(A.row_ptr, A.col_idx, A.values, b, **kw)
+    return x.cpu().numpy(), info, ref
+
+
+def test_zero_rhs_gives_zero():
+    A = poisson_5pt(12)
+    x0 = t(np.ones(A.n))
+    x, info, _ = sla.sla_cg_solve(to_dev(A), t(np.zeros(A.n)), x0=x0, rtol=1e-8, maxit=10)
+    assert info.status == 0 and info.iters == 0 and not x.cpu().numpy().any()
+
+
+def test_maxit_zero_and_not_converged():
+    A = poisson_5pt(30)
+    b = np.random.default_rng(3).standard_normal(A.n)
+    x, info, ref = _solve_both(A, b, rtol=1e-8, maxit=0)
+    assert info.status == ref["status"] == 1 and info.iters == 0 and not x.any()
+    x, info, ref = _solve_both(A, b, rtol=1e-12, maxit=7)
+    assert info.status == ref["status"] == 1 and info.iters == ref["iters"] == 7
+    assert rel(x, ref["x"]) <= 1e-12
+
+
+@pytest.mark.parametrize("maxit", [1, 2, 3, 8, 9, 17])
+def test_fixed_iterations_any_count(maxit):
+    # rtol = 0 runs exactly maxit iterations, whatever the loop body's unroll
+    A = diffusion_dirichlet(20, np.random.default_rng(5).lognormal(0, 1, 2 * 20 * 21))
+    b = np.random.default_rng(6).standard_normal(A.n)
+    for unroll in (2, 8):
+        x, info, _ = sla.sla_cg_solve(to_dev(A), t(b), rtol=0.0, maxit=maxit, unroll=unroll)
+        ref = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=0.0, maxit=maxit)
+        assert info.iters == ref["iters"] == maxit and info.status == 1
+        assert rel(x.cpu().numpy(), ref["x"]) <= 1e-12
+
+
+def test_breakdown_on_negative_definite():
+    A = poisson_5pt(10)
+    An = A.astype(np.float64)
+    An.values = -A.values
+    b = np.random.default_rng(1).standard_normal(A.n)
+    x, info, ref = _solve_both(An, b, rtol=1e-8, maxit=50)
+    assert info.status == ref["status"] == 2 and info.iters == ref["iters"] == 0
+
+
+def test_nonfinite_inputs():
+    A = poisson_5pt(10)
+    b = np.random.default_rng(1).standard_normal(A.n)
+    bn = b.copy()
+    bn[5] = np.nan
+    _, info, ref = _solve_both(A, bn, rtol=1e-8, maxit=50)
+    assert info.status == ref["status"] == 5
+    Av = A.astype(np.float64)
+    Av.values = A.values.copy()
+    Av.values[11] = np.inf
+    _, info, ref = _solve_both(Av, b, rtol=1e-8, maxit=50)
+    assert info.status == ref["status"] == 5
+
+
+def test_jacobi_bad_diagonal():
+    A = poisson_5pt(10)
+    b = np.random.default_rng(1).standard_normal(A.n)
+    Az = A.astype(np.float64)
+    Az.values = A.values.copy()
+    Az.values[0] = 0.0
+    _, info, ref = _solve_both(Az, b, rtol=1e-8, maxit=50, precond=1)
+    assert info.status == ref["status"] == 2
+    dpos = [k for k in range(int(A.row_ptr[A.n - 1]), int(A.row_ptr[A.n])) if A.col_idx[k] == A.n - 1][0]
+    Az.values[dpos] = np.nan
+    _, info, ref = _solve_both(Az, b, rtol=1e-8, maxit=50, precond=1)
+    assert info.status == ref["status"] == 5
+
+
+def test_x0_restart_and_in_place():
+    A = poisson_5pt(25)
+    b = np.random.default_rng(9).standard_normal(A.n)
+    first = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=0.0, maxit=11)
+    dA = to_dev(A)
+    x0 = t(first["x"])
+    x, info, _ = sla.sla_cg_solve(dA, t(b), x0=x0, rtol=1e-10, maxit=5000)
+    ref = oracle.cg(A.row_ptr, A.col_idx, A.values, b, x0=first["x"], rtol=1e-10, maxit=5000)
+    assert info.status == 0 and abs(info.iters - ref["iters"]) <= 1
+    assert rel(x.cpu().numpy(), ref["x"]) <= X_TOL_F64
+    # in place: x0 and x are the same buffer
+    xi = t(first["x"])
+    sla.sla_cg_solve(dA, t(b), x0=xi, x=xi, rtol=1e-10, maxit=5000)
+    assert rel(xi.cpu().numpy(), ref["x"]) <= X_TOL_F64
+
+
+def test_empty_and_single():
+    A = poisson_5pt(1)
+    x, info, _ = sla.sla_cg_solve(to_dev(A), t(np.array([3.0])), rtol=1e-14, maxit=10)
+    assert info.iters == 1 and x.item() == 0.75
+
+
+def test_validate_csr():
+    A = random_spd(300, 4.0, 2, long_rows=1)
+    dA = to_dev(A)
+    assert sla.sla_validate_csr(dA, check_symmetric=True) == -1
+    ci = A.col_idx.copy()
+    k = int(A.row_ptr[40])
+    ci[k], ci[k + 1] = ci[k + 1], ci[k]  # unsorted row 40
+    bad = sla.CSRMatrix(dA.row_ptr, t(ci), dA.values)
+    assert sla.sla_validate_csr(bad) == 40
+    v = A.values.copy()
+    k7 = [k for k in range(int(A.row_ptr[7]), int(A.row_ptr[8])) if A.col_idx[k] != 7][0]
+    v[k7] += 1.0  # breaks symmetry between row 7 and its partner row
+    assert sla.sla_validate_csr(sla.CSRMatrix(dA.row_ptr, dA.col_idx, t(v)), check_symmetric=True) in (
+        7, int(A.col_idx[k7]))
+    ci2 = A.col_idx.copy()
+    ci2[-1] = A.n  # out of range in the last row
+    assert sla.sla_validate_csr(sla.CSRMatrix(dA.row_ptr, t(ci2), dA.values)) == A.n - 1
+
+
+def test_deterministic_repeat():
+    A = diffusion_dirichlet(60, np.random.default_rng(7).lognormal(0, 1, 2 * 60 * 61))
+    b = t(np.random.default_rng(8).standard_normal(A.n))
+    dA = to_dev(A)
+    x1, i1, _ = sla.sla_cg_solve(dA, b, rtol=1e-9, maxit=5000, precond=1)
+    x2, i2, _ = sla.sla_cg_solve(dA, b, rtol=1e-9, maxit=5000, precond=1)
+    assert i1.iters == i2.iters and torch.equal(x1, x2)
+
+
+def test_no_cpu_tensors():
+    A = poisson_5pt(4)
+    with pytest.raises(ValueError):
+        sla.sla_cg_solve(sla.CSRMatrix.from_numpy(A.row_ptr, A.col_idx, A.values, "cpu"),
+                         torch.zeros(A.n, dtype=torch.float64))
