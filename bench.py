@@ -56,13 +56,28 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def profiled_traffic():
-    """DRAM bytes per CG iteration from the committed ncu summary, if it matches the current kernels."""
+def csrc_sha256():
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "differentiable_sparse_iterative_gb300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(config):
+    """DRAM bytes per CG iteration from the committed ncu summary, or None when the kernel
+    sources changed since the counters were taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            return json.load(f)
+            rec = json.load(f).get(config)
     except (OSError, ValueError):
-        return {}
+        return None
+    if not rec or rec.get("csrc_sha256") != csrc_sha256():
+        return None
+    return rec
 
 
 class ClockSampler:
@@ -146,14 +161,16 @@ def run_ours(args, rank, world, local_rank):
     gv = torch.empty(nnz, dtype=torch.float64, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    loop = sla.SLA_LOOP_HOST if args.loop == "host" else sla.SLA_LOOP_GRAPH
 
     def step():
         e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         e0.record(stream)
-        _, fi, _ = sla.sla_cg_solve(A, b, rtol=w.rtol, maxit=w.maxit, precond=precond, x=x, workspace=ws)
+        _, fi, _ = sla.sla_cg_solve(A, b, rtol=w.rtol, maxit=w.maxit, precond=precond, x=x, workspace=ws,
+                                    loop=loop)
         e1.record(stream)
         _, _, ai = sla.sla_cg_adjoint(A, x, g, rtol=w.rtol, maxit=w.maxit, precond=precond, grad_b=gb,
-                                      grad_values=gv, workspace=ws)
+                                      grad_values=gv, workspace=ws, loop=loop)
         e2.record(stream)
         return e0, e1, e2, fi, ai
 
@@ -203,7 +220,7 @@ def run_ours(args, rank, world, local_rank):
     # fused CG iteration (spmv_step + update_step): bytes per iteration / forward time per iteration
     fwd_s = sum(fwd_ms) / 1e3
     achieved = Bi * sum(iters_f) / fwd_s / 1e9
-    tr = profiled_traffic().get(args.config)
+    tr = profiled_traffic(args.config)
     clocks = clk.summary()
 
     e2e = None
@@ -218,7 +235,8 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": w.name, "n": n, "nnz": nnz, "rtol": w.rtol, "precond": "jacobi" if jac else "none",
                    "step": "forward CG solve + adjoint (grad_b, grad_values)",
                    "l2": "flushed between steps (256 MB write); within a solve the iterations reuse L2",
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "loop": args.loop},
         "iters_forward": statistics.mean(iters_f), "iters_adjoint": statistics.mean(iters_a),
         "time_to_tolerance_ms": statistics.mean(fwd_ms), "adjoint_ms": statistics.mean(adj_ms),
         "status": sorted(status),
@@ -354,6 +372,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-iters", type=int, default=600)
     ap.add_argument("--ref-iters", type=int, default=100)
+    ap.add_argument("--loop", choices=["graph", "host"], default="graph",
+                    help="graph: device-side loop (default); host: host-driven loop, e.g. for per-kernel ncu")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

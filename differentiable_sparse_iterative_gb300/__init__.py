@@ -26,13 +26,14 @@ import torch
 
 from . import _abi
 from ._abi import (SLA_OK, SLA_NOT_CONVERGED, SLA_BREAKDOWN, SLA_INVALID_ARG, SLA_BAD_CSR, SLA_NONFINITE,
-                   SLA_WORKSPACE_TOO_SMALL, SLA_CUDA_ERROR, SLA_PRECOND_NONE, SLA_PRECOND_JACOBI)
+                   SLA_WORKSPACE_TOO_SMALL, SLA_CUDA_ERROR, SLA_PRECOND_NONE, SLA_PRECOND_JACOBI, SLA_LOOP_GRAPH,
+                   SLA_LOOP_HOST)
 
 __all__ = [
     "CSRMatrix", "SlaError", "CGInfo", "lib", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
     "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_validate_csr", "sla_cg_workspace_bytes",
     "sla_status_string", "sla_launch_count", "sla_version", "CGSolve", "solve", "matvec",
-    "SLA_PRECOND_NONE", "SLA_PRECOND_JACOBI",
+    "SLA_PRECOND_NONE", "SLA_PRECOND_JACOBI", "SLA_LOOP_GRAPH", "SLA_LOOP_HOST",
 ]
 
 _lib = None
@@ -128,12 +129,14 @@ def _stream(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
-def _opts(rtol, maxit, precond, unroll=0) -> _abi.sla_cg_opts:
+def _opts(rtol, maxit, precond, unroll=0, loop=SLA_LOOP_GRAPH) -> _abi.sla_cg_opts:
     o = _abi.sla_cg_opts()
     o.rtol = float(rtol)
     o.maxit = int(maxit)
     o.precond = int(precond)
     o.unroll = int(unroll)
+    o.loop = int(loop)
+    o.reserved = 0
     return o
 
 
@@ -203,7 +206,7 @@ def _info(ci: _abi.sla_cg_info) -> CGInfo:
 def sla_cg_solve(A: CSRMatrix, b: torch.Tensor, x0: Optional[torch.Tensor] = None, rtol: float = 1e-8,
                  maxit: int = 10000, precond: int = SLA_PRECOND_NONE, x: Optional[torch.Tensor] = None,
                  history: bool = False, workspace: Optional[torch.Tensor] = None, sync: bool = True,
-                 unroll: int = 0):
+                 unroll: int = 0, loop: int = SLA_LOOP_GRAPH):
     """CG solve of A x = b.  Returns (x, CGInfo or None, history tensor or None).
 
     With sync=False the call is asynchronous and returns info=None.
@@ -215,7 +218,7 @@ def sla_cg_solve(A: CSRMatrix, b: torch.Tensor, x0: Optional[torch.Tensor] = Non
     ws = _workspace(A.n, 1, dt, precond, dev, workspace)
     info = _abi.sla_cg_info()
     st = lib().sla_cg_solve(ctypes.byref(_csr_struct(A)), _dev_ptr(b, dt, "b"), _dev_ptr(x0, dt, "x0"),
-                            ctypes.byref(_opts(rtol, maxit, precond, unroll)), _dev_ptr(x, dt, "x"),
+                            ctypes.byref(_opts(rtol, maxit, precond, unroll, loop)), _dev_ptr(x, dt, "x"),
                             ctypes.byref(info) if sync else None, _dev_ptr(hist, torch.float64, "history"),
                             ws.data_ptr(), ws.numel(), _stream(dev))
     _check(st, "sla_cg_solve")
@@ -225,7 +228,8 @@ def sla_cg_solve(A: CSRMatrix, b: torch.Tensor, x0: Optional[torch.Tensor] = Non
 def sla_cg_adjoint(A: CSRMatrix, x: torch.Tensor, g: torch.Tensor, rtol: float = 1e-8, maxit: int = 10000,
                    precond: int = SLA_PRECOND_NONE, grad_b: Optional[torch.Tensor] = None,
                    grad_values: Optional[torch.Tensor] = None, want_grad_values: bool = True,
-                   workspace: Optional[torch.Tensor] = None, sync: bool = True, unroll: int = 0):
+                   workspace: Optional[torch.Tensor] = None, sync: bool = True, unroll: int = 0,
+                   loop: int = SLA_LOOP_GRAPH):
     """Adjoint backward: returns (grad_b = lambda, grad_values or None, CGInfo or None)."""
     dt, dev = A.values.dtype, A.values.device
     if grad_b is None:
@@ -235,7 +239,7 @@ def sla_cg_adjoint(A: CSRMatrix, x: torch.Tensor, g: torch.Tensor, rtol: float =
     ws = _workspace(A.n, 1, dt, precond, dev, workspace)
     info = _abi.sla_cg_info()
     st = lib().sla_cg_adjoint(ctypes.byref(_csr_struct(A)), _dev_ptr(x, dt, "x"), _dev_ptr(g, dt, "g"),
-                              ctypes.byref(_opts(rtol, maxit, precond, unroll)), _dev_ptr(grad_b, dt, "grad_b"),
+                              ctypes.byref(_opts(rtol, maxit, precond, unroll, loop)), _dev_ptr(grad_b, dt, "grad_b"),
                               _dev_ptr(grad_values, dt, "grad_values"), ctypes.byref(info) if sync else None,
                               ws.data_ptr(), ws.numel(), _stream(dev))
     _check(st, "sla_cg_adjoint")
@@ -245,7 +249,8 @@ def sla_cg_adjoint(A: CSRMatrix, x: torch.Tensor, g: torch.Tensor, rtol: float =
 def sla_cg_solve_batched(pattern: CSRMatrix, values: torch.Tensor, b: torch.Tensor,
                          x0: Optional[torch.Tensor] = None, rtol: float = 1e-5, maxit: int = 10000,
                          precond: int = SLA_PRECOND_NONE, x: Optional[torch.Tensor] = None, history: bool = False,
-                         workspace: Optional[torch.Tensor] = None, sync: bool = True, unroll: int = 0):
+                         workspace: Optional[torch.Tensor] = None, sync: bool = True, unroll: int = 0,
+                         loop: int = SLA_LOOP_GRAPH):
     """Batched shared-pattern CG: values [B, nnz], b [B, n].  Returns (x [B, n], [CGInfo]*B, history)."""
     B = values.shape[0]
     dt, dev = values.dtype, values.device
@@ -256,7 +261,7 @@ def sla_cg_solve_batched(pattern: CSRMatrix, values: torch.Tensor, b: torch.Tens
     infos = (_abi.sla_cg_info * max(B, 1))()
     st = lib().sla_cg_solve_batched(ctypes.byref(_csr_struct(pattern, values)), B, _dev_ptr(values, dt, "values"),
                                     _dev_ptr(b, dt, "b"), _dev_ptr(x0, dt, "x0"),
-                                    ctypes.byref(_opts(rtol, maxit, precond, unroll)), _dev_ptr(x, dt, "x"),
+                                    ctypes.byref(_opts(rtol, maxit, precond, unroll, loop)), _dev_ptr(x, dt, "x"),
                                     infos if sync else None, _dev_ptr(hist, torch.float64, "history"),
                                     ws.data_ptr(), ws.numel(), _stream(dev))
     _check(st, "sla_cg_solve_batched")
@@ -267,7 +272,7 @@ def sla_cg_adjoint_batched(pattern: CSRMatrix, values: torch.Tensor, x: torch.Te
                            rtol: float = 1e-5, maxit: int = 10000, precond: int = SLA_PRECOND_NONE,
                            grad_b: Optional[torch.Tensor] = None, grad_values: Optional[torch.Tensor] = None,
                            want_grad_values: bool = True, workspace: Optional[torch.Tensor] = None,
-                           sync: bool = True, unroll: int = 0):
+                           sync: bool = True, unroll: int = 0, loop: int = SLA_LOOP_GRAPH):
     """Batched adjoint: returns (grad_b [B, n], grad_values [B, nnz] or None, [CGInfo]*B)."""
     B = values.shape[0]
     dt, dev = values.dtype, values.device
@@ -279,7 +284,7 @@ def sla_cg_adjoint_batched(pattern: CSRMatrix, values: torch.Tensor, x: torch.Te
     infos = (_abi.sla_cg_info * max(B, 1))()
     st = lib().sla_cg_adjoint_batched(ctypes.byref(_csr_struct(pattern, values)), B, _dev_ptr(values, dt, "values"),
                                       _dev_ptr(x, dt, "x"), _dev_ptr(g, dt, "g"),
-                                      ctypes.byref(_opts(rtol, maxit, precond, unroll)),
+                                      ctypes.byref(_opts(rtol, maxit, precond, unroll, loop)),
                                       _dev_ptr(grad_b, dt, "grad_b"), _dev_ptr(grad_values, dt, "grad_values"),
                                       infos if sync else None, ws.data_ptr(), ws.numel(), _stream(dev))
     _check(st, "sla_cg_adjoint_batched")

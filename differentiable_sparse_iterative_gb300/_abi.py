@@ -12,6 +12,7 @@ SLA_WORKSPACE_TOO_SMALL, SLA_TIMEOUT, SLA_CUDA_ERROR = 6, 7, 8
 SLA_F32, SLA_F64 = 0, 1
 SLA_I32, SLA_I64 = 0, 1
 SLA_PRECOND_NONE, SLA_PRECOND_JACOBI = 0, 1
+SLA_LOOP_GRAPH, SLA_LOOP_HOST = 0, 1
 
 # every symbol include/sla.h declares
 EXPORTS = [
@@ -29,7 +30,7 @@ class sla_csr(ctypes.Structure):
 
 class sla_cg_opts(ctypes.Structure):
     _fields_ = [("rtol", ctypes.c_double), ("maxit", ctypes.c_int64), ("precond", ctypes.c_int32),
-                ("unroll", ctypes.c_int32)]
+                ("unroll", ctypes.c_int32), ("loop", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class sla_cg_info(ctypes.Structure):

@@ -90,7 +90,9 @@ __global__ void __launch_bounds__(kBlock) grad_values_kernel(int64_t n, int64_t 
     int64_t e_begin = __shfl_sync(0xffffffffu, my_start, 0);
     int64_t e_end = (int64_t)rp[rend];
     if (e_begin < 0 || e_end > nnz || e_end < e_begin) e_begin = e_end = 0;  // malformed row_ptr: skip
-    for (int64_t e = e_begin + lane; e < e_end; e += 32) {
+    // warp-uniform trip count: every lane takes part in every shuffle
+    for (int64_t base = e_begin; base < e_end; base += 32) {
+      const int64_t e = base + lane;
       // row of e: the last lane j with start_j <= e (binary search via shuffles)
       int lo = 0;
 #pragma unroll
@@ -99,8 +101,10 @@ __global__ void __launch_bounds__(kBlock) grad_values_kernel(int64_t n, int64_t 
         if (st <= e) lo += step;
       }
       const V li = __shfl_sync(0xffffffffu, my_lam, lo);
-      const int32_t c = ci[e];
-      gv[e] = (uint32_t)c < (uint32_t)n ? -(li * x[c]) : V(0);
+      if (e < e_end) {
+        const int32_t c = ci[e];
+        gv[e] = (uint32_t)c < (uint32_t)n ? -(li * x[c]) : V(0);
+      }
     }
   }
 }
@@ -196,6 +200,8 @@ sla_status check_opts(const sla_cg_opts *o) {
   if (o->maxit < 0 || o->maxit > ((int64_t)1 << 40)) return SLA_INVALID_ARG;
   if (o->precond != SLA_PRECOND_NONE && o->precond != SLA_PRECOND_JACOBI) return SLA_INVALID_ARG;
   if (o->unroll < 0 || o->unroll > 64) return SLA_INVALID_ARG;
+  if (o->loop != SLA_LOOP_GRAPH && o->loop != SLA_LOOP_HOST) return SLA_INVALID_ARG;
+  if (o->reserved != 0) return SLA_INVALID_ARG;
   return SLA_OK;
 }
 

@@ -476,8 +476,40 @@ int choose_G(int64_t n, int64_t batch, int sms, int occ) {
   return (int)std::max<int64_t>(1, g);
 }
 
+// Host-driven loop: the same kernels launched directly; the host reads the number of active
+// systems every `unroll` iterations (one 4-byte copy and one stream synchronisation).
 template <typename V, typename I, bool JAC>
-sla_status run_cg(Prob<V, I> P, int unroll, cudaStream_t stream, sla_cg_info *info, int64_t batch) {
+sla_status run_cg_host_loop(Prob<V, I> P, int unroll, cudaStream_t stream, sla_cg_info *info, int64_t batch) {
+  using K = Kernels<V, I, JAC>;
+  dim3 grid(P.G, P.batch), block(kBlock);
+  uint64_t launched = 0;
+  cg_init<V, I><<<1, block, 0, stream>>>(P);
+  cg_setup<V, I, JAC><<<grid, block, 0, stream>>>(P);
+  launched += 2;
+  uint32_t active = 1;
+  for (int64_t k = 0; k < P.maxit && active; k += unroll) {
+    const int64_t upto = std::min<int64_t>(P.maxit - k, unroll);
+    for (int64_t u = 0; u < upto; ++u) {
+      const int par = (int)((k + u) & 1);
+      cg_spmv_step<V, I, JAC, kRPT><<<grid, block, 0, stream>>>(P, par);
+      cg_update_step<V, I, JAC><<<grid, block, 0, stream>>>(P, par);
+    }
+    launched += 2 * (uint64_t)upto;
+    cudaError_t e = cudaMemcpyAsync(&active, &P.glob->active, sizeof(active), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail(e);
+  }
+  cg_finish<V, I><<<grid, block, 0, stream>>>(P);
+  launched += 1;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(e);
+  (void)launched;
+  if (!info) return SLA_OK;
+  return read_info(P.ctl, P.glob, batch, stream, info);
+}
+
+template <typename V, typename I, bool JAC>
+sla_status run_cg(Prob<V, I> P, int unroll, int loop, cudaStream_t stream, sla_cg_info *info, int64_t batch) {
   const DeviceInfo di = device_info();
   static std::atomic<int> occ_cache{0};
   int occ = occ_cache.load();
@@ -489,6 +521,7 @@ sla_status run_cg(Prob<V, I> P, int unroll, cudaStream_t stream, sla_cg_info *in
   P.G = choose_G(P.n, batch, di.sms, occ);
   if (unroll <= 0) unroll = kDefaultUnroll;
   if (unroll & 1) unroll += 1;  // the ping-pong parity of the body must repeat
+  if (loop == SLA_LOOP_HOST) return run_cg_host_loop<V, I, JAC>(P, unroll, stream, info, batch);
 
   std::vector<char> key(sizeof(P) + 4 * sizeof(int));
   int tag[4] = {(int)sizeof(V), (int)sizeof(I), (int)JAC, unroll};
@@ -530,10 +563,10 @@ sla_status run_cg(Prob<V, I> P, int unroll, cudaStream_t stream, sla_cg_info *in
 }
 
 template <typename V, typename I>
-sla_status dispatch_precond(const Prob<V, I> &P, int precond, int unroll, cudaStream_t st, sla_cg_info *info,
+sla_status dispatch_precond(const Prob<V, I> &P, const sla_cg_opts *o, cudaStream_t st, sla_cg_info *info,
                             int64_t batch) {
-  if (precond == SLA_PRECOND_JACOBI) return run_cg<V, I, true>(P, unroll, st, info, batch);
-  return run_cg<V, I, false>(P, unroll, st, info, batch);
+  if (o->precond == SLA_PRECOND_JACOBI) return run_cg<V, I, true>(P, o->unroll, o->loop, st, info, batch);
+  return run_cg<V, I, false>(P, o->unroll, o->loop, st, info, batch);
 }
 
 template <typename V, typename I>
@@ -576,15 +609,15 @@ sla_status cg_entry(const sla_csr *A, int64_t batch, const void *values, int64_t
   if (A->dtype == SLA_F64) {
     if (A->rowptr_type == SLA_I64)
       return dispatch_precond(make_prob<double, int64_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac),
-                              o->precond, o->unroll, st, info, batch);
+                              o, st, info, batch);
     return dispatch_precond(make_prob<double, int32_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac),
-                            o->precond, o->unroll, st, info, batch);
+                            o, st, info, batch);
   }
   if (A->rowptr_type == SLA_I64)
     return dispatch_precond(make_prob<float, int64_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac),
-                            o->precond, o->unroll, st, info, batch);
+                            o, st, info, batch);
   return dispatch_precond(make_prob<float, int32_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac),
-                          o->precond, o->unroll, st, info, batch);
+                          o, st, info, batch);
 }
 
 size_t workspace_bytes(int64_t n, int64_t batch, int dtype, int precond) {

@@ -90,11 +90,20 @@ typedef struct sla_csr {
   const void *values;     /* device, nnz entries (ignored by the batched calls: values come separately) */
 } sla_csr;
 
+typedef enum sla_loop {
+  SLA_LOOP_GRAPH = 0,     /* one CUDA graph per solve; the loop is a device-side conditional WHILE node */
+  SLA_LOOP_HOST = 1       /* the host launches the same kernels directly and reads the device status
+                             every `unroll` iterations (for profilers that cannot see inside
+                             conditional graphs, and for drivers without conditional nodes) */
+} sla_loop;
+
 typedef struct sla_cg_opts {
   double rtol;            /* stop when ||r|| <= rtol * ||b||; 0 runs exactly maxit iterations */
   int64_t maxit;          /* iteration cap, >= 0 */
   int32_t precond;        /* sla_precond */
-  int32_t unroll;         /* iterations per device-side loop body; 0 = library default */
+  int32_t unroll;         /* iterations per loop body (graph) or per status read (host); 0 = default */
+  int32_t loop;           /* sla_loop */
+  int32_t reserved;       /* must be 0 */
 } sla_cg_opts;
 
 /* Result of one solve (host memory).  Filled after the call has synchronised the stream. */

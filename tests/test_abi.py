@@ -58,9 +58,9 @@ def _csr(n=4, nnz=10, rt=0, dt=1, ptr=0x10000):
     return A
 
 
-def _opts(rtol=1e-8, maxit=10, precond=0):
+def _opts(rtol=1e-8, maxit=10, precond=0, loop=0, reserved=0, unroll=0):
     o = _abi.sla_cg_opts()
-    o.rtol, o.maxit, o.precond, o.unroll = rtol, maxit, precond, 0
+    o.rtol, o.maxit, o.precond, o.unroll, o.loop, o.reserved = rtol, maxit, precond, unroll, loop, reserved
     return o
 
 
@@ -81,6 +81,11 @@ def test_argument_rejection_without_gpu(lib):
     assert solve(ctypes.byref(_csr()), P, None, ctypes.byref(_opts(maxit=-1)), P, None, None, P, 1 << 20,
                  None) == 3
     assert solve(ctypes.byref(_csr()), P, None, ctypes.byref(_opts(precond=3)), P, None, None, P, 1 << 20,
+                 None) == 3
+    assert solve(ctypes.byref(_csr()), P, None, ctypes.byref(_opts(loop=2)), P, None, None, P, 1 << 20, None) == 3
+    assert solve(ctypes.byref(_csr()), P, None, ctypes.byref(_opts(reserved=1)), P, None, None, P, 1 << 20,
+                 None) == 3
+    assert solve(ctypes.byref(_csr()), P, None, ctypes.byref(_opts(unroll=65)), P, None, None, P, 1 << 20,
                  None) == 3
     assert solve(ctypes.byref(_csr()), None, None, ctypes.byref(_opts()), P, None, None, P, 1 << 20, None) == 3
     assert solve(ctypes.byref(_csr()), P + 4, None, ctypes.byref(_opts()), P, None, None, P, 1 << 20, None) == 3

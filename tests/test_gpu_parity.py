@@ -5,8 +5,8 @@ Sizes span several blocks and tiles with ragged tails; every case is seeded.
 import numpy as np
 import pytest
 
-from gpu_helpers import (sla, oracle, torch, rel, to_dev, t, spmv_bound, check_history, X_TOL_F64, GRAD_TOL_F64,
-                         TOL_F32, ITER_SLACK_F64, ITER_SLACK_F32)
+from gpu_helpers import (sla, oracle, torch, rel, to_dev, t, spmv_bound, check_history, rounding_sensitivity,
+                         X_TOL_F64, GRAD_TOL_F64, TOL_F32, ITER_SLACK_F64, ITER_SLACK_F32)
 from workloads import poisson_5pt, diffusion_dirichlet, diffusion_interior, random_spd, config1, config3
 
 pytestmark = pytest.mark.gpu
@@ -62,16 +62,19 @@ def test_cg_and_adjoint_f64(name, precond):
     dA = to_dev(A)
     x, info, hist = sla.sla_cg_solve(dA, t(b), rtol=rtol, maxit=maxit, precond=precond, history=True)
     ref = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=rtol, maxit=maxit, precond=precond, history=True)
+    horizon, spread = rounding_sensitivity(A, b, precond, rtol, maxit)
     assert info.status == ref["status"] == 0
-    assert abs(info.iters - ref["iters"]) <= ITER_SLACK_F64
+    assert abs(info.iters - ref["iters"]) <= max(ITER_SLACK_F64, 2 * spread + 1)
     assert rel(x.cpu().numpy(), ref["x"]) <= X_TOL_F64
     h = hist.cpu().numpy()
-    check_history(h, ref["history"])
+    assert horizon >= 8, horizon
+    check_history(h, ref["history"], k=min(50, horizon - 1))
     assert np.isnan(h[info.iters + 1:]).all()  # entries past iters are not written
     gb, gv, ainfo = sla.sla_cg_adjoint(dA, x, t(g), rtol=rtol, maxit=maxit, precond=precond)
     adj = oracle.cg_adjoint(A.row_ptr, A.col_idx, A.values, ref["x"], g, rtol=rtol, maxit=maxit, precond=precond)
+    _, aspread = rounding_sensitivity(A, g, precond, rtol, maxit, k=0)
     assert ainfo.status == adj["status"] == 0
-    assert abs(ainfo.iters - adj["iters"]) <= ITER_SLACK_F64
+    assert abs(ainfo.iters - adj["iters"]) <= max(ITER_SLACK_F64, 2 * aspread + 1)
     assert rel(gb.cpu().numpy(), adj["grad_b"]) <= GRAD_TOL_F64
     assert gv.shape == (A.nnz,)
     assert rel(gv.cpu().numpy(), adj["grad_values"]) <= GRAD_TOL_F64
@@ -270,3 +273,21 @@ def test_no_cpu_tensors():
     with pytest.raises(ValueError):
         sla.sla_cg_solve(sla.CSRMatrix.from_numpy(A.row_ptr, A.col_idx, A.values, "cpu"),
                          torch.zeros(A.n, dtype=torch.float64))
+
+
+@pytest.mark.parametrize("precond", [0, 1])
+def test_host_loop_equals_graph_loop(precond):
+    # the two loop drivers run the same kernels in the same order: identical results, bit for bit
+    A = diffusion_dirichlet(40, np.random.default_rng(11).lognormal(0, 1, 2 * 40 * 41))
+    b = t(np.random.default_rng(12).standard_normal(A.n))
+    dA = to_dev(A)
+    xg, ig, hg = sla.sla_cg_solve(dA, b, rtol=1e-9, maxit=3000, precond=precond, history=True,
+                                  loop=sla.SLA_LOOP_GRAPH)
+    for unroll in (2, 6):
+        xh, ih, hh = sla.sla_cg_solve(dA, b, rtol=1e-9, maxit=3000, precond=precond, history=True,
+                                      loop=sla.SLA_LOOP_HOST, unroll=unroll)
+        assert ih.iters == ig.iters and ih.status == ig.status == 0
+        assert torch.equal(xh, xg) and torch.equal(hh[: ih.iters + 1], hg[: ig.iters + 1])
+    gb, gv, _ = sla.sla_cg_adjoint(dA, xg, b, rtol=1e-9, maxit=3000, precond=precond, loop=sla.SLA_LOOP_HOST)
+    gb2, gv2, _ = sla.sla_cg_adjoint(dA, xg, b, rtol=1e-9, maxit=3000, precond=precond)
+    assert torch.equal(gb, gb2) and torch.equal(gv, gv2)
