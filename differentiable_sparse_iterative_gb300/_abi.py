@@ -18,7 +18,7 @@ SLA_LOOP_GRAPH, SLA_LOOP_HOST = 0, 1
 EXPORTS = [
     "sla_status_string", "sla_last_cuda_error", "sla_version", "sla_launch_count", "sla_cg_workspace_bytes",
     "sla_validate_csr", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values", "sla_cg_solve_batched",
-    "sla_cg_adjoint_batched",
+    "sla_cg_adjoint_batched", "sla_cg_solve_static",
 ]
 
 
@@ -58,8 +58,9 @@ def bind(lib):
     lib.sla_grad_values.argtypes = [C, P, P, P, P]
     lib.sla_cg_solve_batched.argtypes = [C, i64, P, P, P, O, P, I, P, P, sz, P]
     lib.sla_cg_adjoint_batched.argtypes = [C, i64, P, P, P, O, P, P, I, P, sz, P]
+    lib.sla_cg_solve_static.argtypes = [C, P, P, O, P, I, P, P]
     for name in ["sla_validate_csr", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
-                 "sla_cg_solve_batched", "sla_cg_adjoint_batched"]:
+                 "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_cg_solve_static"]:
         getattr(lib, name).restype = i32
     return lib
 

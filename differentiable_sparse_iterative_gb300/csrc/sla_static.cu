@@ -1,0 +1,120 @@
+// sla_cg_solve_static: the CG solve for callers that cannot allocate device memory.
+//
+// Some callers can neither call cudaMalloc nor hand the library a workspace: plugins
+// loaded into a host application that owns and budgets every byte of device memory,
+// code on latency-critical paths where an allocation (and the device synchronisation
+// it can imply) is not allowed, and thin bindings that have no device allocator at
+// all.  For them this entry point keeps its scratch in a fixed array in the library's
+// own device memory, reserved when the library is loaded on a GPU and held until the
+// process exits.  The caller still passes the matrix, b, x0 and x.
+//
+// Limits: one system (no batch) of at most kStaticMaxN = 65,536 unknowns, fp32 or fp64,
+// with or without Jacobi; larger systems are rejected with SLA_WORKSPACE_TOO_SMALL
+// before anything is launched.  The iteration runs the same kernels as sla_cg_solve,
+// driven from the host (no graph is instantiated, since that may allocate).
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "sla_common.cuh"
+#include "sla_host.h"
+
+namespace sla {
+
+namespace {
+
+constexpr int64_t kStaticMaxN = 65536;
+// Workspace layout for n = 65,536, one system, fp64 values, Jacobi: Glob (256 B) + Ctl (256 B)
+// + partial sums (5 x 2048 doubles = 81,920 B) + 5 vectors of 65,536 doubles (524,288 B each).
+constexpr size_t kStaticScratchBytes = 256 + 256 + 81920 + 5 * 524288;  // 2,703,872 bytes
+constexpr int kMaxDevices = 64;
+
+// The shared scratch.  In host code this name is only a stand-in for the device symbol:
+// never pass it to a kernel; use the address returned by cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+void *g_static_addr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device, looked up once per device (with that
+// device current) and cached.
+sla_status static_scratch(void **out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return SLA_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return fail(e);
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return SLA_OK;
+}
+
+bool is_aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+}  // namespace
+
+}  // namespace sla
+
+using namespace sla;
+
+extern "C" SLA_API sla_status sla_cg_solve_static(const sla_csr *A, const void *b, const void *x0,
+                                                  const sla_cg_opts *opts, void *x, sla_cg_info *info,
+                                                  double *history, void *stream) {
+  // argument checks first: they need no GPU
+  if (!A || !opts) return SLA_INVALID_ARG;
+  if (A->n < 0 || A->nnz < 0) return SLA_INVALID_ARG;
+  if (A->n > kStaticMaxN) return SLA_WORKSPACE_TOO_SMALL;  // beyond the static scratch
+  if (A->dtype != SLA_F32 && A->dtype != SLA_F64) return SLA_INVALID_ARG;
+  if (A->rowptr_type != SLA_I32 && A->rowptr_type != SLA_I64) return SLA_INVALID_ARG;
+  if (opts->precond != SLA_PRECOND_NONE && opts->precond != SLA_PRECOND_JACOBI) return SLA_INVALID_ARG;
+  if (!(opts->rtol >= 0.0) || opts->rtol > 1e300 || opts->maxit < 0 || opts->maxit > ((int64_t)1 << 40))
+    return SLA_INVALID_ARG;
+  if (opts->unroll < 0 || opts->unroll > 64 || opts->reserved != 0) return SLA_INVALID_ARG;
+  const size_t vsz = A->dtype == SLA_F64 ? 8 : 4, isz = A->rowptr_type == SLA_I64 ? 8 : 4;
+  if (A->n > 0 && (!A->row_ptr || !b || !x)) return SLA_INVALID_ARG;
+  if (A->nnz > 0 && (!A->col_idx || !A->values)) return SLA_INVALID_ARG;
+  if (!is_aligned(A->row_ptr, isz) || !is_aligned(A->col_idx, 4) || !is_aligned(A->values, vsz) ||
+      !is_aligned(b, vsz) || !is_aligned(x0, vsz) || !is_aligned(x, vsz) || !is_aligned(history, 8))
+    return SLA_INVALID_ARG;
+  const bool jac = opts->precond == SLA_PRECOND_JACOBI;
+  const Layout L = make_layout(A->n, 1, vsz, jac);
+  if (L.total > kStaticScratchBytes) return SLA_WORKSPACE_TOO_SMALL;
+  if (A->n == 0) {
+    if (info) {
+      info->iters = 0;
+      info->rel_res = 0.0;
+      info->status = SLA_OK;
+      info->reserved = 0;
+      info->kernels = 0;
+    }
+    return SLA_OK;
+  }
+  void *ws = nullptr;
+  sla_status s = static_scratch(&ws);
+  if (s != SLA_OK) return s;
+  sla_cg_opts o = *opts;
+  o.loop = SLA_LOOP_HOST;
+  cudaStream_t st = (cudaStream_t)stream;
+  // The init kernel of the solve zeroes the control block and the loop state in the scratch, so
+  // nothing left by an earlier call is read; vectors are written before they are read.
+  s = cg_entry(A, 1, A->values, 0, b, x0, &o, x, nullptr, history, ws, st);
+  if (s != SLA_OK || !info) return s;
+  Ctl hc;
+  Glob hg;
+  cudaError_t e = cudaMemcpyAsync(&hc, (const char *)ws + L.ctl, sizeof(Ctl), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&hg, (const char *)ws + L.glob, sizeof(Glob), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail(e);
+  count_launches(hg.kernels);
+  info->iters = hc.k;
+  info->rel_res = hc.rel_res;
+  info->status = hg.bad_csr ? SLA_BAD_CSR : hc.status;
+  info->reserved = 0;
+  info->kernels = (int64_t)hg.kernels;
+  return SLA_OK;
+}

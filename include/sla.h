@@ -220,6 +220,29 @@ SLA_API sla_status sla_cg_adjoint_batched(const sla_csr *pattern, int64_t batch,
                                   const void *g, const sla_cg_opts *opts, void *grad_b, void *grad_values,
                                   sla_cg_info *info, void *workspace, size_t ws_bytes, void *stream);
 
+/* ---------------------------------------------------------------- allocation-free variant */
+
+/*
+ * sla_cg_solve without a workspace argument, for callers that cannot allocate device memory
+ * (plugins inside a host application that owns all device memory, latency-critical paths where
+ * an allocation is not allowed, bindings with no device allocator).  The paper has no
+ * counterpart: this is a library convenience, not part of the method.
+ *   Scratch: a fixed 2,703,872-byte array in the library's own device memory, reserved on every
+ *   GPU that loads the library and held until the process exits.  Systems of up to 65,536
+ *   unknowns (one system, fp32 or fp64, with or without Jacobi) fit; larger n returns
+ *   SLA_WORKSPACE_TOO_SMALL before anything is launched.
+ *   Set-up: the first call on a device looks up the array's device address on the current
+ *   device (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *   Sharing: every call uses the same array.  Each call resets the state it needs, but calls
+ *   whose GPU work overlaps (on different streams or threads) race on the array: serialise them.
+ *   Allocation: none, neither cudaMalloc/cudaFree nor any allocating library routine; the loop
+ *   is driven from the host with plain kernel launches (one 4-byte status read every
+ *   opts->unroll iterations; opts->loop is ignored).
+ *   Arguments and results as for sla_cg_solve.
+ */
+SLA_API sla_status sla_cg_solve_static(const sla_csr *A, const void *b, const void *x0, const sla_cg_opts *opts,
+                                       void *x, sla_cg_info *info, double *history, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
