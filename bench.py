@@ -161,7 +161,8 @@ def run_ours(args, rank, world, local_rank):
     gv = torch.empty(nnz, dtype=torch.float64, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    loop = sla.SLA_LOOP_HOST if args.loop == "host" else sla.SLA_LOOP_GRAPH
+    loop = {"auto": sla.SLA_LOOP_AUTO, "resident": sla.SLA_LOOP_RESIDENT, "graph": sla.SLA_LOOP_GRAPH,
+            "host": sla.SLA_LOOP_HOST}[args.loop]
 
     def step():
         e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
@@ -372,8 +373,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-iters", type=int, default=600)
     ap.add_argument("--ref-iters", type=int, default=100)
-    ap.add_argument("--loop", choices=["graph", "host"], default="graph",
-                    help="graph: device-side loop (default); host: host-driven loop, e.g. for per-kernel ncu")
+    ap.add_argument("--loop", choices=["auto", "resident", "graph", "host"], default="auto",
+                    help="auto (default): resident kernel when the system fits on chip, else graph; "
+                         "host: host-driven loop, e.g. for per-kernel ncu")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

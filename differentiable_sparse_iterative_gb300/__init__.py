@@ -26,14 +26,15 @@ import torch
 
 from . import _abi
 from ._abi import (SLA_OK, SLA_NOT_CONVERGED, SLA_BREAKDOWN, SLA_INVALID_ARG, SLA_BAD_CSR, SLA_NONFINITE,
-                   SLA_WORKSPACE_TOO_SMALL, SLA_CUDA_ERROR, SLA_PRECOND_NONE, SLA_PRECOND_JACOBI, SLA_LOOP_GRAPH,
-                   SLA_LOOP_HOST)
+                   SLA_WORKSPACE_TOO_SMALL, SLA_CUDA_ERROR, SLA_PRECOND_NONE, SLA_PRECOND_JACOBI, SLA_LOOP_AUTO,
+                   SLA_LOOP_HOST, SLA_LOOP_GRAPH, SLA_LOOP_RESIDENT)
 
 __all__ = [
     "CSRMatrix", "SlaError", "CGInfo", "lib", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
     "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_validate_csr", "sla_cg_workspace_bytes",
     "sla_status_string", "sla_launch_count", "sla_version", "CGSolve", "solve", "matvec",
-    "SLA_PRECOND_NONE", "SLA_PRECOND_JACOBI", "SLA_LOOP_GRAPH", "SLA_LOOP_HOST",
+    "SLA_PRECOND_NONE", "SLA_PRECOND_JACOBI", "SLA_LOOP_AUTO", "SLA_LOOP_HOST", "SLA_LOOP_GRAPH",
+    "SLA_LOOP_RESIDENT",
 ]
 
 _lib = None
@@ -129,7 +130,7 @@ def _stream(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
-def _opts(rtol, maxit, precond, unroll=0, loop=SLA_LOOP_GRAPH) -> _abi.sla_cg_opts:
+def _opts(rtol, maxit, precond, unroll=0, loop=SLA_LOOP_AUTO) -> _abi.sla_cg_opts:
     o = _abi.sla_cg_opts()
     o.rtol = float(rtol)
     o.maxit = int(maxit)
@@ -206,7 +207,7 @@ def _info(ci: _abi.sla_cg_info) -> CGInfo:
 def sla_cg_solve(A: CSRMatrix, b: torch.Tensor, x0: Optional[torch.Tensor] = None, rtol: float = 1e-8,
                  maxit: int = 10000, precond: int = SLA_PRECOND_NONE, x: Optional[torch.Tensor] = None,
                  history: bool = False, workspace: Optional[torch.Tensor] = None, sync: bool = True,
-                 unroll: int = 0, loop: int = SLA_LOOP_GRAPH):
+                 unroll: int = 0, loop: int = SLA_LOOP_AUTO):
     """CG solve of A x = b.  Returns (x, CGInfo or None, history tensor or None).
 
     With sync=False the call is asynchronous and returns info=None.
@@ -229,7 +230,7 @@ def sla_cg_adjoint(A: CSRMatrix, x: torch.Tensor, g: torch.Tensor, rtol: float =
                    precond: int = SLA_PRECOND_NONE, grad_b: Optional[torch.Tensor] = None,
                    grad_values: Optional[torch.Tensor] = None, want_grad_values: bool = True,
                    workspace: Optional[torch.Tensor] = None, sync: bool = True, unroll: int = 0,
-                   loop: int = SLA_LOOP_GRAPH):
+                   loop: int = SLA_LOOP_AUTO):
     """Adjoint backward: returns (grad_b = lambda, grad_values or None, CGInfo or None)."""
     dt, dev = A.values.dtype, A.values.device
     if grad_b is None:
@@ -250,7 +251,7 @@ def sla_cg_solve_batched(pattern: CSRMatrix, values: torch.Tensor, b: torch.Tens
                          x0: Optional[torch.Tensor] = None, rtol: float = 1e-5, maxit: int = 10000,
                          precond: int = SLA_PRECOND_NONE, x: Optional[torch.Tensor] = None, history: bool = False,
                          workspace: Optional[torch.Tensor] = None, sync: bool = True, unroll: int = 0,
-                         loop: int = SLA_LOOP_GRAPH):
+                         loop: int = SLA_LOOP_AUTO):
     """Batched shared-pattern CG: values [B, nnz], b [B, n].  Returns (x [B, n], [CGInfo]*B, history)."""
     B = values.shape[0]
     dt, dev = values.dtype, values.device
@@ -272,7 +273,7 @@ def sla_cg_adjoint_batched(pattern: CSRMatrix, values: torch.Tensor, x: torch.Te
                            rtol: float = 1e-5, maxit: int = 10000, precond: int = SLA_PRECOND_NONE,
                            grad_b: Optional[torch.Tensor] = None, grad_values: Optional[torch.Tensor] = None,
                            want_grad_values: bool = True, workspace: Optional[torch.Tensor] = None,
-                           sync: bool = True, unroll: int = 0, loop: int = SLA_LOOP_GRAPH):
+                           sync: bool = True, unroll: int = 0, loop: int = SLA_LOOP_AUTO):
     """Batched adjoint: returns (grad_b [B, n], grad_values [B, nnz] or None, [CGInfo]*B)."""
     B = values.shape[0]
     dt, dev = values.dtype, values.device

@@ -508,8 +508,20 @@ sla_status run_cg_host_loop(Prob<V, I> P, int unroll, cudaStream_t stream, sla_c
   return read_info(P.ctl, P.glob, batch, stream, info);
 }
 
+}  // namespace
+
+// Resident persistent kernel (sla_resident.cu).
+template <typename V, typename I, bool JAC>
+sla_status run_resident(Prob<V, I> P, cudaStream_t stream, sla_cg_info *info);
+
+namespace {
+
 template <typename V, typename I, bool JAC>
 sla_status run_cg(Prob<V, I> P, int unroll, int loop, cudaStream_t stream, sla_cg_info *info, int64_t batch) {
+  if (loop == SLA_LOOP_RESIDENT ||
+      (loop == SLA_LOOP_AUTO && resident_fits(P.n, batch, sizeof(V) == 8 ? SLA_F64 : SLA_F32,
+                                              JAC ? SLA_PRECOND_JACOBI : SLA_PRECOND_NONE, P.maxit)))
+    return run_resident<V, I, JAC>(P, stream, info);
   const DeviceInfo di = device_info();
   static std::atomic<int> occ_cache{0};
   int occ = occ_cache.load();

@@ -16,7 +16,7 @@ namespace sla {
 constexpr int kBlock = 256;                  // threads per block of every row kernel
 constexpr int kWarps = kBlock / 32;
 constexpr int kMaxBlocksPerSystem = 2048;    // partial-sum slots per system and reduction
-constexpr int kRedSlots = 5;                 // reductions per kernel: at most 5 sums
+constexpr int kRedSlots = 6;                 // partial-sum rows: 5 (setup / r.r, r.z) + 1 (p.q, resident kernel)
 
 // Per-system solver state, resident on the device for the whole solve.
 struct Ctl {
@@ -42,6 +42,8 @@ struct Glob {
   unsigned long long kernels;     // kernel executions of this call
   uint32_t safety_stop;           // 1 if the loop was cut by the body bound (never expected)
   uint32_t bad_csr;               // 1 if a row range or column index was out of bounds (entry skipped)
+  uint32_t barrier;               // arrival counter of the resident kernel's grid barrier
+  uint32_t timeout;               // 1 if a bounded grid-barrier wait expired
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -110,26 +112,35 @@ __device__ __forceinline__ double warp_sum(double v) {
   return v;
 }
 
-// Block-wide sum of NV values in a fixed order (lane tree, then warp tree); result in thread 0.
-template <int NV>
-__device__ __forceinline__ void block_sum(double (&v)[NV]) {
-  __shared__ double sred[NV][kWarps];
+// Block-wide sum of NV values per thread of a BLOCK-thread block, in a fixed order; the result
+// is in thread 0.  fp64 instructions are the scarce resource on this GPU (2 FMA per SM per clock,
+// so one 32-lane fp64 instruction holds an SM sub-partition for 64 cycles): instead of a shuffle
+// tree in every warp, the values go through shared memory and warp 0 alone adds them, lane l
+// summing entries l, l+32, ... in order, then a 5-step shuffle tree.  That is BLOCK/32 + 4
+// fp64 warp-instructions per value instead of 5 * BLOCK/32 + 5.
+template <int NV, int BLOCK>
+__device__ __forceinline__ void block_sum_n(double (&v)[NV]) {
+  static_assert(BLOCK % 32 == 0, "block size must be a multiple of 32");
+  __shared__ double sbuf[NV][BLOCK];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    double w = warp_sum(v[j]);
-    if (lane == 0) sred[j][warp] = w;
-  }
+  for (int j = 0; j < NV; ++j) sbuf[j][threadIdx.x] = v[j];
   __syncthreads();
   if (warp == 0) {
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      double w = lane < kWarps ? sred[j][lane] : 0.0;
-      w = warp_sum(w);
-      v[j] = w;
+      double t = sbuf[j][lane];
+#pragma unroll
+      for (int k = 1; k < BLOCK / 32; ++k) t += sbuf[j][lane + 32 * k];
+      v[j] = warp_sum(t);
     }
   }
   __syncthreads();
+}
+
+template <int NV>
+__device__ __forceinline__ void block_sum(double (&v)[NV]) {
+  block_sum_n<NV, kBlock>(v);
 }
 
 // Publishes this block's sums (valid in thread 0) as partials[j][bx] and returns true in the
@@ -156,13 +167,15 @@ __device__ __forceinline__ bool publish_last(const double (&v)[NV], double *part
 // the ticket is returned to 0 for the next kernel.
 template <int NV>
 __device__ __forceinline__ void reduce_partials(const double *part, int G, uint32_t *ticket, double (&tot)[NV]) {
+  // warp 0 alone: lane l adds partials l, l+32, ... in order, then the shuffle tree
+  if (threadIdx.x < 32) {
 #pragma unroll
-  for (int j = 0; j < NV; ++j) tot[j] = 0.0;
-  for (int i = threadIdx.x; i < G; i += kBlock) {
-#pragma unroll
-    for (int j = 0; j < NV; ++j) tot[j] += __ldcg(part + (size_t)j * kMaxBlocksPerSystem + i);
+    for (int j = 0; j < NV; ++j) {
+      double t = 0.0;
+      for (int i = threadIdx.x; i < G; i += 32) t += __ldcg(part + (size_t)j * kMaxBlocksPerSystem + i);
+      tot[j] = warp_sum(t);
+    }
   }
-  block_sum<NV>(tot);
   if (threadIdx.x == 0) *ticket = 0u;
 }
 

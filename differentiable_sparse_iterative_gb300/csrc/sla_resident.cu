@@ -1,0 +1,437 @@
+// Resident CG: the whole solve in one persistent kernel, vectors kept in shared memory.
+//
+// Method as in sla_cg.cu ("torch-sla" technical summary, Methodology 1-2 and Significance:
+// Hestenes-Stiefel CG with optional Jacobi preconditioning; same recurrences, same stopping
+// rule, same status decisions).
+//
+// GB300 design.  When one system fits on chip (x, r, p, q and, with Jacobi, 1/diag for a
+// 1/G share of the rows in one SM's 227 KB of shared memory), one 1024-thread block per SM
+// owns a contiguous row chunk for the whole solve and its vectors never leave the SM.  Per
+// iteration only the matrix is streamed (from L2 when it fits there) and two values per row
+// are published for the neighbouring blocks: r_k and p_k, from which a block recomputes
+// p_k = z + beta p_{k-1} for the few columns outside its chunk.  The two global dependencies
+// of an iteration (alpha needs p.Ap, beta needs r.r) are two grid barriers, each carrying
+// a deterministic all-reduce: every block writes its block sum, and after the barrier every
+// block adds the G block sums in the same fixed order, so all blocks hold bit-identical
+// scalars and take the same branch.  The launch is cooperative (all blocks co-resident);
+// each barrier wait is bounded and ends the solve with SLA_TIMEOUT if it ever expires.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+
+#include "sla_common.cuh"
+#include "sla_host.h"
+
+namespace sla {
+
+namespace {
+
+constexpr int kResBlock = 1024;
+constexpr long long kSpinLimit = 1ll << 26;  // ~seconds of polling before a barrier gives up
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded grid barrier over a monotone arrival counter.  Returns false (after raising the
+// timeout flag) if the other blocks did not arrive in time, or if another block timed out.
+__device__ __forceinline__ bool grid_barrier(unsigned *arrive, unsigned *timeout, unsigned G, unsigned &epoch) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ++epoch;
+    const unsigned target = epoch * G;
+    __threadfence();
+    atomicAdd(arrive, 1u);
+    int ok = 1;
+    long long spins = 0;
+    while (ld_acquire(arrive) < target) {
+      if (*(volatile unsigned *)timeout) { ok = 0; break; }
+      if (++spins > kSpinLimit) {
+        atomicExch(timeout, 1u);
+        ok = 0;
+        break;
+      }
+      if (spins > 64) __nanosleep(32);
+    }
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+// Deterministic all-reduce across the G blocks.  Block level: every thread's value goes through
+// shared memory and warp 0 adds them (lane l: entries l, l+32, ... in order, then a shuffle
+// tree), so the reduction costs few fp64 warp-instructions.  Grid level: thread 0 writes the
+// block sum to part[j][bid]; after the barrier warp 0 of every block adds part[j][0..G) in the
+// same order, so every block obtains bit-identical totals.  The totals end in s_tot[] (shared),
+// valid for all threads after the call.
+template <int NV>
+__device__ __forceinline__ bool grid_allreduce(const double (&v)[NV], double *sbuf, double *s_tot, double *part,
+                                               unsigned *arrive, unsigned *timeout, unsigned &epoch) {
+  const int G = gridDim.x;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    sbuf[threadIdx.x] = v[j];
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      double t = sbuf[lane];
+#pragma unroll
+      for (int k = 1; k < kResBlock / 32; ++k) t += sbuf[lane + 32 * k];
+      t = warp_sum(t);
+      if (lane == 0) part[(size_t)j * kMaxBlocksPerSystem + blockIdx.x] = t;
+    }
+    __syncthreads();
+  }
+  if (!grid_barrier(arrive, timeout, (unsigned)G, epoch)) return false;
+  if (threadIdx.x < 32) {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      double t = 0.0;
+      for (int b = lane; b < G; b += 32) t += __ldcg(part + (size_t)j * kMaxBlocksPerSystem + b);
+      t = warp_sum(t);
+      if (lane == 0) s_tot[j] = t;
+    }
+  }
+  __syncthreads();
+  return true;
+}
+
+// p_k at a column outside the block's chunk, from the published r_k and p_{k-1}.
+template <typename V, bool JAC>
+__device__ __forceinline__ V p_remote(const V *r, const V *dinv, const V *po, int32_t c, bool first, V beta) {
+  const V rc = __ldcg(r + c);
+  const V zc = JAC ? __ldcg(dinv + c) * rc : rc;
+  return first ? zc : fmav<V>(beta, __ldcg(po + c), zc);
+}
+
+// Scalars of the iteration, decided by thread 0 and read by every thread from shared memory
+// (fp64 divisions and square roots are far too expensive to repeat in every thread).
+struct ResScalars {
+  double alpha, beta, alpha_prev;
+  int go;  // 1: keep iterating
+};
+
+template <typename V, typename I, bool JAC>
+__global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int cap) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  // shared: reduction buffer (kResBlock doubles), then r, p (and 1/diag) of the block's rows
+  double *sbuf = reinterpret_cast<double *>(smem_raw);
+  V *sr = reinterpret_cast<V *>(sbuf + kResBlock);
+  V *sp = sr + cap;
+  V *sd = JAC ? sp + cap : nullptr;
+  __shared__ double s_tot[5];
+  __shared__ ResScalars S;
+  const unsigned G = gridDim.x;
+  const int bid = blockIdx.x, tid = threadIdx.x;
+  const int64_t c0 = (int64_t)P.n * bid / G, c1 = (int64_t)P.n * (bid + 1) / G;
+  const int len = (int)(c1 - c0);
+  Glob *glob = P.glob;
+  Ctl *C = P.ctl;
+  unsigned *arrive = &glob->barrier;  // zeroed before the launch
+  unsigned *timeout = &glob->timeout;
+  // Partial-sum rows: 0..4 for the setup sums and later r.r, r.z (a block writes those only after
+  // the p.q barrier, when every block has read the setup sums); row 5 for p.q.
+  static_assert(kRedSlots >= 6, "the resident kernel needs 6 partial-sum rows");
+  double *partB = P.partials;
+  double *partA = P.partials + (size_t)5 * kMaxBlocksPerSystem;
+  const I *__restrict__ rp = P.rp;
+  const int32_t *__restrict__ ci = P.ci;
+  const V *__restrict__ val = P.val;
+  V *rpub = P.r;        // published r_k (read by the neighbouring blocks)
+  V *dpub = P.dinv;     // published 1/diag (Jacobi)
+  V *xg = P.x;          // x stays in global memory (L2): read and written once per iteration
+  V *qg = P.q;          // q likewise, between the SpMV and the r update
+  unsigned epoch = 0;
+  if (bid == 0 && tid == 0) atomicAdd(&glob->kernels, 1ull);
+
+  // ---- setup: x = x0 (or 0), r = b - A x0, 1/diag; sums b.b, r.r, r.z, #non-finite, #non-positive
+  double acc5[5] = {0.0, 0.0, 0.0, 0.0, 0.0};
+  for (int li = tid; li < len; li += kResBlock) {
+    const int64_t i = c0 + li;
+    int64_t e0, e1;
+    row_range(rp, i, P.nnz, e0, e1, &glob->bad_csr);
+    const V bi = P.b[i];
+    V ri = bi;
+    if (P.x0) {
+      V s_ = V(0);
+      for (int64_t e = e0; e < e1; ++e) {
+        const int32_t c = ci[e];
+        if (col_ok(c, P.n, &glob->bad_csr)) s_ = fmav<V>(val[e], P.x0[c], s_);
+      }
+      ri = bi - s_;
+    }
+    sr[li] = ri;
+    rpub[i] = ri;
+    acc5[0] = fma((double)bi, (double)bi, acc5[0]);
+    acc5[1] = fma((double)ri, (double)ri, acc5[1]);
+    if (JAC) {
+      V d = V(0);
+      for (int64_t e = e0; e < e1; ++e)
+        if (ci[e] == (int32_t)i) d = val[e];
+      if (!isfinite((double)d)) acc5[3] += 1.0;
+      else if (!(d > V(0))) acc5[4] += 1.0;
+      const V di = V(1) / d;
+      sd[li] = di;
+      dpub[i] = di;
+      acc5[2] = fma((double)ri, (double)(di * ri), acc5[2]);
+    }
+  }
+  // x = x0 (or 0) after every block has read x0 (x0 may be the same buffer as x)
+  const bool ok0 = grid_allreduce<5>(acc5, sbuf, s_tot, partB, arrive, timeout, epoch);
+  for (int li = tid; li < len; li += kResBlock) xg[c0 + li] = P.x0 ? P.x0[c0 + li] : V(0);
+
+  // thread 0 of every block takes the same decisions from the same totals
+  int status = SLA_NOT_CONVERGED, pending = 0;
+  int64_t k = 0;
+  double nb = 0.0, rel = 0.0, rho = 0.0;
+  if (tid == 0) {
+    nb = sqrt(s_tot[0]);
+    int go = 0;
+    if (!ok0) {
+      status = SLA_TIMEOUT;
+    } else if (!isfinite(nb)) {
+      status = SLA_NONFINITE;
+    } else if (nb == 0.0) {
+      status = SLA_OK;
+      pending = 2;
+      if (bid == 0 && P.history) P.history[0] = 0.0;
+    } else if (JAC && s_tot[3] > 0.0) {
+      status = SLA_NONFINITE;
+    } else if (JAC && s_tot[4] > 0.0) {
+      status = SLA_BREAKDOWN;
+    } else {
+      const double rr = s_tot[1];
+      rel = sqrt(rr) / nb;
+      if (bid == 0 && P.history) P.history[0] = rel;
+      if (!isfinite(rr)) status = SLA_NONFINITE;
+      else if (sqrt(rr) <= P.rtol * nb) status = SLA_OK;
+      else if (P.maxit == 0) status = SLA_NOT_CONVERGED;
+      else {
+        rho = JAC ? s_tot[2] : rr;
+        go = 1;
+      }
+    }
+    S.go = go;
+    S.alpha = 0.0;
+    S.beta = 0.0;
+    S.alpha_prev = 0.0;
+  }
+  __syncthreads();
+
+  // ---- iterations
+  while (S.go) {
+    const int par = (int)(k & 1);
+    const bool first = (k == 0);
+    const V vb = (V)S.beta, va_prev = (V)S.alpha_prev;
+    V *pn_pub = P.p[par];
+    const V *po_pub = P.p[par ^ 1];
+    // p_k = z_k + beta p_{k-1} for the own rows; x += alpha_{k-1} p_{k-1}; publish p_k
+    for (int li = tid; li < len; li += kResBlock) {
+      const V rl = sr[li];
+      const V z = JAC ? sd[li] * rl : rl;
+      V pv = z;
+      if (!first) {
+        const V po = sp[li];
+        pv = fmav<V>(vb, po, z);
+        xg[c0 + li] = fmav<V>(va_prev, po, xg[c0 + li]);
+      }
+      sp[li] = pv;
+      pn_pub[c0 + li] = pv;
+    }
+    __syncthreads();
+    // q = A p_k and the block's share of p.q
+    V part = V(0);
+    for (int li = tid; li < len; li += kResBlock) {
+      const int64_t i = c0 + li;
+      int64_t e0, e1;
+      row_range(rp, i, P.nnz, e0, e1, &glob->bad_csr);
+      V acc = V(0);
+      for (int64_t e = e0; e < e1; ++e) {
+        const int32_t c = __ldg(ci + e);
+        const V v = __ldg(val + e);
+        const uint32_t off = (uint32_t)((int64_t)c - c0);
+        V pc;
+        if (off < (uint32_t)len) pc = sp[off];
+        else pc = col_ok(c, P.n, &glob->bad_csr) ? p_remote<V, JAC>(rpub, dpub, po_pub, c, first, vb) : V(0);
+        acc = fmav<V>(v, pc, acc);
+      }
+      qg[i] = acc;
+      part = fmav<V>(sp[li], acc, part);
+    }
+    const double v1[1] = {(double)part};
+    const bool ok1 = grid_allreduce<1>(v1, sbuf, s_tot, partA, arrive, timeout, epoch);
+    if (tid == 0) {
+      const double pq = s_tot[0];
+      int go = 1;
+      if (!ok1) { status = SLA_TIMEOUT; go = 0; }
+      else if (!isfinite(pq)) { status = SLA_NONFINITE; go = 0; }
+      else if (!(pq > 0.0)) { status = SLA_BREAKDOWN; go = 0; }
+      else S.alpha = rho / pq;
+      S.go = go;
+    }
+    __syncthreads();
+    if (!S.go) break;
+    // r -= alpha q; publish r; sums r.r and r.z
+    const V va = (V)S.alpha;
+    V rr_t = V(0), rz_t = V(0);
+    double acc2[2] = {0.0, 0.0};
+    int cnt = 0;
+    for (int li = tid; li < len; li += kResBlock) {
+      const V ri = fmav<V>(-va, qg[c0 + li], sr[li]);
+      sr[li] = ri;
+      rpub[c0 + li] = ri;
+      rr_t = fmav<V>(ri, ri, rr_t);
+      if (JAC) rz_t = fmav<V>(ri, sd[li] * ri, rz_t);
+      if constexpr (sizeof(V) == 4) {
+        if (++cnt == 8) {
+          acc2[0] += (double)rr_t;
+          acc2[1] += (double)rz_t;
+          rr_t = rz_t = V(0);
+          cnt = 0;
+        }
+      }
+    }
+    acc2[0] += (double)rr_t;
+    acc2[1] += (double)rz_t;
+    const bool ok2 = grid_allreduce<2>(acc2, sbuf, s_tot, partB, arrive, timeout, epoch);
+    ++k;
+    if (tid == 0) {
+      const double rrt = s_tot[0];
+      int go = 0;
+      if (!ok2) {
+        status = SLA_TIMEOUT;
+      } else {
+        rel = sqrt(rrt) / nb;
+        if (bid == 0 && P.history) P.history[k] = rel;
+        pending = 1;
+        if (!isfinite(rrt)) status = SLA_NONFINITE;
+        else if (sqrt(rrt) <= P.rtol * nb) status = SLA_OK;
+        else if (k >= P.maxit) status = SLA_NOT_CONVERGED;
+        else {
+          const double rho_new = JAC ? s_tot[1] : rrt;
+          S.beta = rho_new / rho;
+          rho = rho_new;
+          S.alpha_prev = S.alpha;
+          pending = 0;
+          go = 1;
+        }
+      }
+      S.go = go;
+    }
+    __syncthreads();
+  }
+
+  // ---- finish: the last delayed x update (or x = 0 for b = 0)
+  __shared__ int s_pending;
+  if (tid == 0) s_pending = pending;
+  __syncthreads();
+  const V va = (V)S.alpha;
+  if (s_pending == 1) {
+    for (int li = tid; li < len; li += kResBlock) xg[c0 + li] = fmav<V>(va, sp[li], xg[c0 + li]);
+  } else if (s_pending == 2) {
+    for (int li = tid; li < len; li += kResBlock) xg[c0 + li] = V(0);
+  }
+  if (bid == 0 && tid == 0) {
+    C->k = k;
+    C->status = status;
+    C->rel_res = rel;
+    C->nb = nb;
+    C->alpha = S.alpha;
+    C->beta = S.beta;
+    C->rho = rho;
+    C->done = 1;
+  }
+}
+
+struct ResidentLimits {
+  int sms = 0;
+  int max_smem = 0;
+};
+
+ResidentLimits limits() {
+  ResidentLimits L;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&L.sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(&L.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  return L;
+}
+
+constexpr size_t kResStaticSmem = 4096;  // reduction scratch and flags of the kernel itself
+
+// Blocks and rows per block for the resident kernel, or G = 0 if the system does not fit.
+void resident_shape(int64_t n, size_t vbytes, bool jac, const ResidentLimits &L, int64_t maxit, int &G,
+                    int &cap, size_t &smem) {
+  G = 0;
+  cap = 0;
+  smem = 0;
+  if (n <= 0 || L.sms <= 0) return;
+  const int nvec = jac ? 3 : 2;  // r, p (and 1/diag) stay in shared memory; x and q live in L2
+  int g = (int)std::min<int64_t>(L.sms, std::max<int64_t>(1, (n + 255) / 256));
+  g = std::min(g, kMaxBlocksPerSystem);
+  const int64_t rows = (n + g - 1) / g;
+  const size_t need = (size_t)kResBlock * sizeof(double) + (size_t)rows * nvec * vbytes;
+  if (need + kResStaticSmem > (size_t)L.max_smem) return;
+  // the barrier counter counts 2 barriers per iteration plus setup, G arrivals each
+  if ((double)(2 * maxit + 2) * g >= 4.0e9) return;
+  G = g;
+  cap = (int)rows;
+  smem = need;
+}
+
+}  // namespace
+
+bool resident_fits(int64_t n, int64_t batch, int dtype, int precond, int64_t maxit) {
+  if (batch != 1) return false;
+  int G, cap;
+  size_t smem;
+  resident_shape(n, dtype == SLA_F64 ? 8 : 4, precond == SLA_PRECOND_JACOBI, limits(), maxit, G, cap, smem);
+  return G > 0;
+}
+
+template <typename V, typename I, bool JAC>
+sla_status run_resident(Prob<V, I> P, cudaStream_t stream, sla_cg_info *info) {
+  int G, cap;
+  size_t smem;
+  if (P.batch != 1) return SLA_INVALID_ARG;  // one system per resident launch
+  resident_shape(P.n, sizeof(V), JAC, limits(), P.maxit, G, cap, smem);
+  if (G == 0) return SLA_INVALID_ARG;
+  P.G = G;
+  void *fn = (void *)cg_resident<V, I, JAC>;
+  static std::atomic<size_t> smem_set{0};
+  if (smem_set.load() < smem) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fail(e);
+    smem_set.store(smem);
+  }
+  // fresh loop state: counters, flags and the control block start at zero
+  cudaError_t e = cudaMemsetAsync(P.glob, 0, sizeof(Glob), stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(P.ctl, 0, sizeof(Ctl), stream);
+  if (e != cudaSuccess) return fail(e);
+  void *args[] = {(void *)&P, (void *)&cap};
+  e = cudaLaunchCooperativeKernel(fn, dim3(G), dim3(kResBlock), args, smem, stream);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(e);
+  if (!info) return SLA_OK;
+  sla_status s = read_info(P.ctl, P.glob, 1, stream, info);
+  return s;
+}
+
+#define SLA_INSTANTIATE_RESIDENT(V, I, J) \
+  template sla_status run_resident<V, I, J>(Prob<V, I>, cudaStream_t, sla_cg_info *);
+SLA_INSTANTIATE_RESIDENT(double, int32_t, false)
+SLA_INSTANTIATE_RESIDENT(double, int32_t, true)
+SLA_INSTANTIATE_RESIDENT(double, int64_t, false)
+SLA_INSTANTIATE_RESIDENT(double, int64_t, true)
+SLA_INSTANTIATE_RESIDENT(float, int32_t, false)
+SLA_INSTANTIATE_RESIDENT(float, int32_t, true)
+SLA_INSTANTIATE_RESIDENT(float, int64_t, false)
+SLA_INSTANTIATE_RESIDENT(float, int64_t, true)
+
+}  // namespace sla

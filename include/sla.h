@@ -71,7 +71,7 @@ typedef enum sla_status {
                                   row pointer or column index (such entries are skipped, never read) */
   SLA_NONFINITE = 5,           /* ||b||, r.r, p.Ap or a Jacobi diagonal is NaN or infinite */
   SLA_WORKSPACE_TOO_SMALL = 6, /* ws_bytes < sla_cg_workspace_bytes(...) */
-  SLA_TIMEOUT = 7,             /* reserved: no current entry point waits on other blocks */
+  SLA_TIMEOUT = 7,             /* a bounded wait of the resident kernel's grid barrier expired */
   SLA_CUDA_ERROR = 8           /* a CUDA runtime call failed */
 } sla_status;
 
@@ -91,10 +91,16 @@ typedef struct sla_csr {
 } sla_csr;
 
 typedef enum sla_loop {
-  SLA_LOOP_GRAPH = 0,     /* one CUDA graph per solve; the loop is a device-side conditional WHILE node */
-  SLA_LOOP_HOST = 1       /* the host launches the same kernels directly and reads the device status
-                             every `unroll` iterations (for profilers that cannot see inside
+  SLA_LOOP_AUTO = 0,      /* RESIDENT when one system fits on chip, else GRAPH */
+  SLA_LOOP_HOST = 1,      /* the host launches the streaming kernels directly and reads the device
+                             status every `unroll` iterations (for profilers that cannot see inside
                              conditional graphs, and for drivers without conditional nodes) */
+  SLA_LOOP_GRAPH = 2,     /* streaming kernels in one CUDA graph per solve; the loop is a device-side
+                             conditional WHILE node */
+  SLA_LOOP_RESIDENT = 3   /* one persistent cooperative kernel per solve, each SM keeping its rows'
+                             vectors in shared memory (one system whose 1/#SM share of x, r, p, q
+                             [, 1/diag] fits one SM's shared memory: about 1.4M fp64 unknowns on
+                             GB300); SLA_INVALID_ARG when it does not fit */
 } sla_loop;
 
 typedef struct sla_cg_opts {
@@ -168,8 +174,9 @@ SLA_API sla_status sla_spmv(const sla_csr *A, const void *x, void *y, void *stre
  *   history  device, opts->maxit + 1 doubles, or NULL: history[k] = ||r_k|| / ||b|| for
  *            k = 0..iters (entries past iters are not written).
  *   workspace/ws_bytes: device scratch, >= sla_cg_workspace_bytes(n, 1, dtype, precond).
- * The whole iteration runs on the device (a CUDA graph whose loop is a device-side
- * conditional); the host does not take part between the first and the last iteration.
+ * The whole iteration runs on the device (opts->loop: one resident kernel, or a CUDA graph whose
+ * loop is a device-side conditional); the host does not take part between the first and the
+ * last iteration (except with SLA_LOOP_HOST).
  */
 SLA_API sla_status sla_cg_solve(const sla_csr *A, const void *b, const void *x0, const sla_cg_opts *opts,
                         void *x, sla_cg_info *info, double *history, void *workspace, size_t ws_bytes,
@@ -227,7 +234,7 @@ SLA_API sla_status sla_cg_adjoint_batched(const sla_csr *pattern, int64_t batch,
  * (plugins inside a host application that owns all device memory, latency-critical paths where
  * an allocation is not allowed, bindings with no device allocator).  The paper has no
  * counterpart: this is a library convenience, not part of the method.
- *   Scratch: a fixed 2,703,872-byte array in the library's own device memory, reserved on every
+ *   Scratch: a fixed 2,720,256-byte array in the library's own device memory, reserved on every
  *   GPU that loads the library and held until the process exits.  Systems of up to 65,536
  *   unknowns (one system, fp32 or fp64, with or without Jacobi) fit; larger n returns
  *   SLA_WORKSPACE_TOO_SMALL before anything is launched.

@@ -52,15 +52,20 @@ def test_spmv_exact_integers():
     assert np.array_equal(y, oracle.spmv(A.row_ptr, A.col_idx, A.values, x))
 
 
+LOOPS = {"auto": 0, "graph": 2}  # auto = the resident kernel for systems that fit on chip
+
+
+@pytest.mark.parametrize("loop", list(LOOPS))
 @pytest.mark.parametrize("name", list(CASES))
 @pytest.mark.parametrize("precond", [0, 1])
-def test_cg_and_adjoint_f64(name, precond):
+def test_cg_and_adjoint_f64(name, precond, loop):
     A = CASES[name]
     rng = np.random.default_rng(A.n + precond)
     b, g = rng.standard_normal(A.n), rng.standard_normal(A.n)
     rtol, maxit = 1e-10, 20000
     dA = to_dev(A)
-    x, info, hist = sla.sla_cg_solve(dA, t(b), rtol=rtol, maxit=maxit, precond=precond, history=True)
+    x, info, hist = sla.sla_cg_solve(dA, t(b), rtol=rtol, maxit=maxit, precond=precond, history=True,
+                                     loop=LOOPS[loop])
     ref = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=rtol, maxit=maxit, precond=precond, history=True)
     horizon, spread = rounding_sensitivity(A, b, precond, rtol, maxit)
     assert info.status == ref["status"] == 0
@@ -70,7 +75,7 @@ def test_cg_and_adjoint_f64(name, precond):
     assert horizon >= 8, horizon
     check_history(h, ref["history"], k=min(50, horizon - 1))
     assert np.isnan(h[info.iters + 1:]).all()  # entries past iters are not written
-    gb, gv, ainfo = sla.sla_cg_adjoint(dA, x, t(g), rtol=rtol, maxit=maxit, precond=precond)
+    gb, gv, ainfo = sla.sla_cg_adjoint(dA, x, t(g), rtol=rtol, maxit=maxit, precond=precond, loop=LOOPS[loop])
     adj = oracle.cg_adjoint(A.row_ptr, A.col_idx, A.values, ref["x"], g, rtol=rtol, maxit=maxit, precond=precond)
     _, aspread = rounding_sensitivity(A, g, precond, rtol, maxit, k=0)
     assert ainfo.status == adj["status"] == 0
@@ -138,7 +143,8 @@ def test_batched_f64_equals_single_systems():
     xb, infos, _ = sla.sla_cg_solve_batched(P, t(v64), t(w.b.astype(np.float64)), rtol=1e-10, maxit=5000)
     for s in range(4):
         As = sla.CSRMatrix(P.row_ptr, P.col_idx, t(v64[s]))
-        xs, info, _ = sla.sla_cg_solve(As, t(w.b[s].astype(np.float64)), rtol=1e-10, maxit=5000)
+        xs, info, _ = sla.sla_cg_solve(As, t(w.b[s].astype(np.float64)), rtol=1e-10, maxit=5000,
+                                       loop=sla.SLA_LOOP_GRAPH)
         assert info.iters == infos[s].iters
         assert rel(xb[s].cpu().numpy(), xs.cpu().numpy()) <= 1e-12
 
@@ -289,5 +295,33 @@ def test_host_loop_equals_graph_loop(precond):
         assert ih.iters == ig.iters and ih.status == ig.status == 0
         assert torch.equal(xh, xg) and torch.equal(hh[: ih.iters + 1], hg[: ig.iters + 1])
     gb, gv, _ = sla.sla_cg_adjoint(dA, xg, b, rtol=1e-9, maxit=3000, precond=precond, loop=sla.SLA_LOOP_HOST)
-    gb2, gv2, _ = sla.sla_cg_adjoint(dA, xg, b, rtol=1e-9, maxit=3000, precond=precond)
+    gb2, gv2, _ = sla.sla_cg_adjoint(dA, xg, b, rtol=1e-9, maxit=3000, precond=precond, loop=sla.SLA_LOOP_GRAPH)
     assert torch.equal(gb, gb2) and torch.equal(gv, gv2)
+
+
+@pytest.mark.parametrize("precond", [0, 1])
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_resident_matches_graph(precond, dtype):
+    # the resident kernel and the streaming kernels partition rows differently (so dot products
+    # round differently) but follow the same recurrences
+    A = diffusion_dirichlet(120, np.random.default_rng(21).lognormal(0, 0.5, 2 * 120 * 121)).astype(dtype)
+    b = np.random.default_rng(22).standard_normal(A.n).astype(dtype)
+    dA = to_dev(A)
+    rtol = 1e-9 if dtype == np.float64 else 1e-5
+    xr, ir, hr = sla.sla_cg_solve(dA, t(b), rtol=rtol, maxit=20000, precond=precond, history=True,
+                                  loop=sla.SLA_LOOP_RESIDENT)
+    xg, ig, hg = sla.sla_cg_solve(dA, t(b), rtol=rtol, maxit=20000, precond=precond, history=True,
+                                  loop=sla.SLA_LOOP_GRAPH)
+    assert ir.status == ig.status == 0
+    tol = X_TOL_F64 if dtype == np.float64 else TOL_F32
+    assert abs(ir.iters - ig.iters) <= (1 if dtype == np.float64 else max(2, 0.05 * ig.iters))
+    assert rel(xr.cpu().numpy(), xg.cpu().numpy()) <= tol
+    check_history(hr.cpu().numpy(), hg.cpu().numpy(), k=20, tol=1e-8 if dtype == np.float64 else 1e-4)
+    assert ir.kernels == 1  # the whole solve is one launch
+
+
+def test_resident_rejects_what_does_not_fit():
+    w = config3(m=8, batch=2)
+    P = to_dev(w.A, np.float32)
+    with pytest.raises(sla.SlaError):
+        sla.sla_cg_solve_batched(P, t(w.values_b), t(w.b), rtol=1e-5, maxit=100, loop=sla.SLA_LOOP_RESIDENT)
