@@ -29,6 +29,7 @@ namespace sla {
 namespace {
 
 constexpr int kResBlock = 1024;
+constexpr int kStage = 8;  // rows per thread whose global loads are issued together
 constexpr long long kSpinLimit = 1ll << 26;  // ~seconds of polling before a barrier gives up
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
@@ -64,42 +65,60 @@ __device__ __forceinline__ bool grid_barrier(unsigned *arrive, unsigned *timeout
   return s_ok != 0;
 }
 
-// Deterministic all-reduce across the G blocks.  Block level: every thread's value goes through
-// shared memory and warp 0 adds them (lane l: entries l, l+32, ... in order, then a shuffle
-// tree), so the reduction costs few fp64 warp-instructions.  Grid level: thread 0 writes the
-// block sum to part[j][bid]; after the barrier warp 0 of every block adds part[j][0..G) in the
-// same order, so every block obtains bit-identical totals.  The totals end in s_tot[] (shared),
-// valid for all threads after the call.
+// Deterministic all-reduce across the G blocks, in three steps so that the fp64 work on the
+// critical path is short:
+//  1. block_publish: every thread's value goes through shared memory; warps 0-3 (one per SM
+//     sub-partition) each add 256 of them (a depth-3 pairwise tree per lane, then a shuffle
+//     tree) and thread 0 adds the four warp sums; the block sum goes to part[j][bid];
+//  2. grid_barrier;
+//  3. warp_totals (warp 0 only): lane l adds part[j][l], part[j][l+32], ... in order, then a
+//     butterfly leaves the identical total in every lane.
+// Every block adds the same numbers in the same order, so all blocks hold bit-identical totals.
 template <int NV>
-__device__ __forceinline__ bool grid_allreduce(const double (&v)[NV], double *sbuf, double *s_tot, double *part,
-                                               unsigned *arrive, unsigned *timeout, unsigned &epoch) {
-  const int G = gridDim.x;
+__device__ __forceinline__ void block_publish(const double (&v)[NV], double *sbuf, double *part) {
+  static_assert(kResBlock == 1024, "four warps of 256 values each");
+  __shared__ double s4[2][4];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+#pragma unroll
+  for (int j0 = 0; j0 < NV; j0 += 2) {
+    const int nj = (NV - j0) < 2 ? (NV - j0) : 2;
+#pragma unroll
+    for (int j = 0; j < nj; ++j) sbuf[j * kResBlock + tid] = v[j0 + j];
+    __syncthreads();
+    if (warp < 4) {
+#pragma unroll
+      for (int j = 0; j < nj; ++j) {
+        const double *b = sbuf + j * kResBlock + warp * 256 + lane;
+        const double a0 = b[0] + b[32], a1 = b[64] + b[96], a2 = b[128] + b[160], a3 = b[192] + b[224];
+        const double t = warp_sum((a0 + a1) + (a2 + a3));
+        if (lane == 0) s4[j][warp] = t;
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+      for (int j = 0; j < nj; ++j)
+        part[(size_t)(j0 + j) * kMaxBlocksPerSystem + blockIdx.x] = (s4[j][0] + s4[j][1]) + (s4[j][2] + s4[j][3]);
+    }
+  }
+}
+
+__device__ __forceinline__ double warp_allsum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Warp 0 only: the grid totals, identical in every lane.
+template <int NV>
+__device__ __forceinline__ void warp_totals(const double *part, int G, double (&tot)[NV]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
-    sbuf[threadIdx.x] = v[j];
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      double t = sbuf[lane];
-#pragma unroll
-      for (int k = 1; k < kResBlock / 32; ++k) t += sbuf[lane + 32 * k];
-      t = warp_sum(t);
-      if (lane == 0) part[(size_t)j * kMaxBlocksPerSystem + blockIdx.x] = t;
-    }
-    __syncthreads();
+    double t = 0.0;
+    for (int b = lane; b < G; b += 32) t += __ldcg(part + (size_t)j * kMaxBlocksPerSystem + b);
+    tot[j] = warp_allsum(t);
   }
-  if (!grid_barrier(arrive, timeout, (unsigned)G, epoch)) return false;
-  if (threadIdx.x < 32) {
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      double t = 0.0;
-      for (int b = lane; b < G; b += 32) t += __ldcg(part + (size_t)j * kMaxBlocksPerSystem + b);
-      t = warp_sum(t);
-      if (lane == 0) s_tot[j] = t;
-    }
-  }
-  __syncthreads();
-  return true;
 }
 
 // p_k at a column outside the block's chunk, from the published r_k and p_{k-1}.
@@ -113,19 +132,18 @@ __device__ __forceinline__ V p_remote(const V *r, const V *dinv, const V *po, in
 // Scalars of the iteration, decided by thread 0 and read by every thread from shared memory
 // (fp64 divisions and square roots are far too expensive to repeat in every thread).
 struct ResScalars {
-  double alpha, beta, alpha_prev;
+  double alpha, beta, alpha_prev, rho, nb;
   int go;  // 1: keep iterating
 };
 
 template <typename V, typename I, bool JAC>
 __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int cap) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  // shared: reduction buffer (kResBlock doubles), then r, p (and 1/diag) of the block's rows
+  // shared: reduction buffer (2 x kResBlock doubles), then r, p (and 1/diag) of the block's rows
   double *sbuf = reinterpret_cast<double *>(smem_raw);
-  V *sr = reinterpret_cast<V *>(sbuf + kResBlock);
+  V *sr = reinterpret_cast<V *>(sbuf + 2 * kResBlock);
   V *sp = sr + cap;
   V *sd = JAC ? sp + cap : nullptr;
-  __shared__ double s_tot[5];
   __shared__ ResScalars S;
   const unsigned G = gridDim.x;
   const int bid = blockIdx.x, tid = threadIdx.x;
@@ -183,44 +201,51 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
     }
   }
   // x = x0 (or 0) after every block has read x0 (x0 may be the same buffer as x)
-  const bool ok0 = grid_allreduce<5>(acc5, sbuf, s_tot, partB, arrive, timeout, epoch);
+  block_publish<5>(acc5, sbuf, partB);
+  const bool ok0 = grid_barrier(arrive, timeout, G, epoch);
   for (int li = tid; li < len; li += kResBlock) xg[c0 + li] = P.x0 ? P.x0[c0 + li] : V(0);
 
   // thread 0 of every block takes the same decisions from the same totals
   int status = SLA_NOT_CONVERGED, pending = 0;
   int64_t k = 0;
   double nb = 0.0, rel = 0.0, rho = 0.0;
-  if (tid == 0) {
-    nb = sqrt(s_tot[0]);
-    int go = 0;
-    if (!ok0) {
-      status = SLA_TIMEOUT;
-    } else if (!isfinite(nb)) {
-      status = SLA_NONFINITE;
-    } else if (nb == 0.0) {
-      status = SLA_OK;
-      pending = 2;
-      if (bid == 0 && P.history) P.history[0] = 0.0;
-    } else if (JAC && s_tot[3] > 0.0) {
-      status = SLA_NONFINITE;
-    } else if (JAC && s_tot[4] > 0.0) {
-      status = SLA_BREAKDOWN;
-    } else {
-      const double rr = s_tot[1];
-      rel = sqrt(rr) / nb;
-      if (bid == 0 && P.history) P.history[0] = rel;
-      if (!isfinite(rr)) status = SLA_NONFINITE;
-      else if (sqrt(rr) <= P.rtol * nb) status = SLA_OK;
-      else if (P.maxit == 0) status = SLA_NOT_CONVERGED;
-      else {
-        rho = JAC ? s_tot[2] : rr;
-        go = 1;
+  if (tid < 32) {
+    double t5[5];
+    warp_totals<5>(partB, (int)G, t5);
+    if (tid == 0) {
+      nb = sqrt(t5[0]);
+      int go = 0;
+      if (!ok0) {
+        status = SLA_TIMEOUT;
+      } else if (!isfinite(nb)) {
+        status = SLA_NONFINITE;
+      } else if (nb == 0.0) {
+        status = SLA_OK;
+        pending = 2;
+        if (bid == 0 && P.history) P.history[0] = 0.0;
+      } else if (JAC && t5[3] > 0.0) {
+        status = SLA_NONFINITE;
+      } else if (JAC && t5[4] > 0.0) {
+        status = SLA_BREAKDOWN;
+      } else {
+        const double rr = t5[1];
+        rel = sqrt(rr) / nb;
+        if (bid == 0 && P.history) P.history[0] = rel;
+        if (!isfinite(rr)) status = SLA_NONFINITE;
+        else if (sqrt(rr) <= P.rtol * nb) status = SLA_OK;
+        else if (P.maxit == 0) status = SLA_NOT_CONVERGED;
+        else {
+          rho = JAC ? t5[2] : rr;
+          go = 1;
+        }
       }
+      S.go = go;
+      S.alpha = 0.0;
+      S.beta = 0.0;
+      S.alpha_prev = 0.0;
+      S.rho = rho;
+      S.nb = nb;
     }
-    S.go = go;
-    S.alpha = 0.0;
-    S.beta = 0.0;
-    S.alpha_prev = 0.0;
   }
   __syncthreads();
 
@@ -231,26 +256,56 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
     const V vb = (V)S.beta, va_prev = (V)S.alpha_prev;
     V *pn_pub = P.p[par];
     const V *po_pub = P.p[par ^ 1];
-    // p_k = z_k + beta p_{k-1} for the own rows; x += alpha_{k-1} p_{k-1}; publish p_k
-    for (int li = tid; li < len; li += kResBlock) {
-      const V rl = sr[li];
-      const V z = JAC ? sd[li] * rl : rl;
-      V pv = z;
+    // p_k = z_k + beta p_{k-1} for the own rows; x += alpha_{k-1} p_{k-1}; publish p_k.
+    // Rows are taken kStage at a time with their global loads issued first, so each group waits
+    // for memory once instead of once per row.
+    for (int j0 = tid; j0 < len; j0 += kStage * kResBlock) {
+      V xv[kStage];
       if (!first) {
-        const V po = sp[li];
-        pv = fmav<V>(vb, po, z);
-        xg[c0 + li] = fmav<V>(va_prev, po, xg[c0 + li]);
+#pragma unroll
+        for (int u = 0; u < kStage; ++u) {
+          const int li = j0 + u * kResBlock;
+          xv[u] = li < len ? xg[c0 + li] : V(0);
+        }
       }
-      sp[li] = pv;
-      pn_pub[c0 + li] = pv;
+#pragma unroll
+      for (int u = 0; u < kStage; ++u) {
+        const int li = j0 + u * kResBlock;
+        if (li < len) {
+          const V rl = sr[li];
+          const V z = JAC ? sd[li] * rl : rl;
+          V pv = z;
+          if (!first) {
+            const V po = sp[li];
+            pv = fmav<V>(vb, po, z);
+            xg[c0 + li] = fmav<V>(va_prev, po, xv[u]);
+          }
+          sp[li] = pv;
+          pn_pub[c0 + li] = pv;
+        }
+      }
     }
     __syncthreads();
-    // q = A p_k and the block's share of p.q
+    // q = A p_k and the block's share of p.q (row pointers of a group loaded up front)
     V part = V(0);
-    for (int li = tid; li < len; li += kResBlock) {
+    for (int j0 = tid; j0 < len; j0 += kStage * kResBlock) {
+      I rpa[kStage], rpb[kStage];
+#pragma unroll
+      for (int u = 0; u < kStage; ++u) {
+        const int li = j0 + u * kResBlock;
+        rpa[u] = li < len ? __ldg(rp + c0 + li) : I(0);
+        rpb[u] = li < len ? __ldg(rp + c0 + li + 1) : I(0);
+      }
+#pragma unroll
+      for (int u = 0; u < kStage; ++u) {
+      const int li = j0 + u * kResBlock;
+      if (li >= len) continue;
       const int64_t i = c0 + li;
-      int64_t e0, e1;
-      row_range(rp, i, P.nnz, e0, e1, &glob->bad_csr);
+      int64_t e0 = (int64_t)rpa[u], e1 = (int64_t)rpb[u];
+      if (e0 < 0 || e1 < e0 || e1 > P.nnz) {
+        atomicOr(&glob->bad_csr, 1u);
+        e0 = e1 = 0;
+      }
       V acc = V(0);
       for (int64_t e = e0; e < e1; ++e) {
         const int32_t c = __ldg(ci + e);
@@ -263,66 +318,107 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
       }
       qg[i] = acc;
       part = fmav<V>(sp[li], acc, part);
+      }
     }
     const double v1[1] = {(double)part};
-    const bool ok1 = grid_allreduce<1>(v1, sbuf, s_tot, partA, arrive, timeout, epoch);
-    if (tid == 0) {
-      const double pq = s_tot[0];
-      int go = 1;
-      if (!ok1) { status = SLA_TIMEOUT; go = 0; }
-      else if (!isfinite(pq)) { status = SLA_NONFINITE; go = 0; }
-      else if (!(pq > 0.0)) { status = SLA_BREAKDOWN; go = 0; }
-      else S.alpha = rho / pq;
-      S.go = go;
+    block_publish<1>(v1, sbuf, partA);
+    const bool ok1 = grid_barrier(arrive, timeout, G, epoch);
+    if (tid < 32) {
+      double t1[1];
+      warp_totals<1>(partA, (int)G, t1);
+      if (tid == 0) {
+        const double pq = t1[0];
+        int go = 1;
+        if (!ok1) { status = SLA_TIMEOUT; go = 0; }
+        else if (!isfinite(pq)) { status = SLA_NONFINITE; go = 0; }
+        else if (!(pq > 0.0)) { status = SLA_BREAKDOWN; go = 0; }
+        else S.alpha = rho / pq;
+        S.go = go;
+      }
     }
     __syncthreads();
     if (!S.go) break;
-    // r -= alpha q; publish r; sums r.r and r.z
+    // r -= alpha q; publish r; sums r.r (and r.z).  float data: each group of kStage rows is
+    // summed in float, then added to the fp64 sums.
     const V va = (V)S.alpha;
-    V rr_t = V(0), rz_t = V(0);
     double acc2[2] = {0.0, 0.0};
-    int cnt = 0;
-    for (int li = tid; li < len; li += kResBlock) {
-      const V ri = fmav<V>(-va, qg[c0 + li], sr[li]);
-      sr[li] = ri;
-      rpub[c0 + li] = ri;
-      rr_t = fmav<V>(ri, ri, rr_t);
-      if (JAC) rz_t = fmav<V>(ri, sd[li] * ri, rz_t);
-      if constexpr (sizeof(V) == 4) {
-        if (++cnt == 8) {
-          acc2[0] += (double)rr_t;
-          acc2[1] += (double)rz_t;
-          rr_t = rz_t = V(0);
-          cnt = 0;
+    for (int j0 = tid; j0 < len; j0 += kStage * kResBlock) {
+      V qv[kStage];
+#pragma unroll
+      for (int u = 0; u < kStage; ++u) {
+        const int li = j0 + u * kResBlock;
+        qv[u] = li < len ? qg[c0 + li] : V(0);
+      }
+      V rr_t = V(0), rz_t = V(0);
+#pragma unroll
+      for (int u = 0; u < kStage; ++u) {
+        const int li = j0 + u * kResBlock;
+        if (li < len) {
+          const V ri = fmav<V>(-va, qv[u], sr[li]);
+          sr[li] = ri;
+          rpub[c0 + li] = ri;
+          rr_t = fmav<V>(ri, ri, rr_t);
+          if (JAC) rz_t = fmav<V>(ri, sd[li] * ri, rz_t);
         }
+      }
+      if constexpr (sizeof(V) == 8) {
+        acc2[0] = (j0 == tid) ? (double)rr_t : acc2[0] + (double)rr_t;
+        if (JAC) acc2[1] = (j0 == tid) ? (double)rz_t : acc2[1] + (double)rz_t;
+      } else {
+        acc2[0] += (double)rr_t;
+        if (JAC) acc2[1] += (double)rz_t;
       }
     }
-    acc2[0] += (double)rr_t;
-    acc2[1] += (double)rz_t;
-    const bool ok2 = grid_allreduce<2>(acc2, sbuf, s_tot, partB, arrive, timeout, epoch);
+    if (JAC) {
+      block_publish<2>(acc2, sbuf, partB);
+    } else {
+      const double v1r[1] = {acc2[0]};
+      block_publish<1>(v1r, sbuf, partB);
+    }
+    const bool ok2 = grid_barrier(arrive, timeout, G, epoch);
     ++k;
-    if (tid == 0) {
-      const double rrt = s_tot[0];
-      int go = 0;
-      if (!ok2) {
-        status = SLA_TIMEOUT;
-      } else {
-        rel = sqrt(rrt) / nb;
-        if (bid == 0 && P.history) P.history[k] = rel;
-        pending = 1;
-        if (!isfinite(rrt)) status = SLA_NONFINITE;
-        else if (sqrt(rrt) <= P.rtol * nb) status = SLA_OK;
-        else if (k >= P.maxit) status = SLA_NOT_CONVERGED;
+    if (tid < 32) {
+      double t2[2] = {0.0, 0.0};
+      if (JAC) warp_totals<2>(partB, (int)G, t2);
+      else {
+        double t1[1];
+        warp_totals<1>(partB, (int)G, t1);
+        t2[0] = t1[0];
+      }
+      // the scalars in parallel lanes: lane 0 the stopping test, lane 1 beta, lane 2 the history
+      const double rrt = t2[0];
+      const double rho_new = JAC ? t2[1] : rrt;
+      double lane_val = 0.0;
+      if (tid == 1) lane_val = rho_new / S.rho;
+      if (tid == 2) {
+        lane_val = sqrt(rrt) / S.nb;
+        if (bid == 0 && P.history) P.history[k] = lane_val;
+      }
+      int stop_code = 0;  // 0 go on, 1 converged, 2 non-finite, 3 maxit, 4 timeout
+      if (tid == 0) {
+        if (!ok2) stop_code = 4;
+        else if (!isfinite(rrt)) stop_code = 2;
+        else if (sqrt(rrt) <= P.rtol * S.nb) stop_code = 1;
+        else if (k >= P.maxit) stop_code = 3;
+      }
+      const double beta_new = __shfl_sync(0xffffffffu, lane_val, 1);
+      const double rel_k = __shfl_sync(0xffffffffu, lane_val, 2);
+      if (tid == 0) {
+        rel = rel_k;
+        int go = 0;
+        if (stop_code == 4) status = SLA_TIMEOUT;
+        else if (stop_code == 2) { status = SLA_NONFINITE; pending = 1; }
+        else if (stop_code == 1) { status = SLA_OK; pending = 1; }
+        else if (stop_code == 3) { status = SLA_NOT_CONVERGED; pending = 1; }
         else {
-          const double rho_new = JAC ? s_tot[1] : rrt;
-          S.beta = rho_new / rho;
+          S.beta = beta_new;
+          S.rho = rho_new;
           rho = rho_new;
           S.alpha_prev = S.alpha;
-          pending = 0;
           go = 1;
         }
+        S.go = go;
       }
-      S.go = go;
     }
     __syncthreads();
   }
@@ -376,7 +472,7 @@ void resident_shape(int64_t n, size_t vbytes, bool jac, const ResidentLimits &L,
   int g = (int)std::min<int64_t>(L.sms, std::max<int64_t>(1, (n + 255) / 256));
   g = std::min(g, kMaxBlocksPerSystem);
   const int64_t rows = (n + g - 1) / g;
-  const size_t need = (size_t)kResBlock * sizeof(double) + (size_t)rows * nvec * vbytes;
+  const size_t need = (size_t)2 * kResBlock * sizeof(double) + (size_t)rows * nvec * vbytes;
   if (need + kResStaticSmem > (size_t)L.max_smem) return;
   // the barrier counter counts 2 barriers per iteration plus setup, G arrivals each
   if ((double)(2 * maxit + 2) * g >= 4.0e9) return;

@@ -37,7 +37,9 @@ def test_static_scratch_matches_workspace_entry_point_twice_in_a_row():
     rng = np.random.default_rng(6)
     cases = [(t(rng.standard_normal(A.n)), 0), (t(rng.standard_normal(A.n)), 1)]
     for b, precond in cases:  # two calls in a row share the scratch array
-        x_ref, info_ref, _ = sla.sla_cg_solve(dA, b, rtol=1e-10, maxit=20000, precond=precond)
+        # the existing entry point, driven by the same kernels (the host loop) as the static one
+        x_ref, info_ref, _ = sla.sla_cg_solve(dA, b, rtol=1e-10, maxit=20000, precond=precond,
+                                              loop=sla.SLA_LOOP_HOST)
         x = torch.full((A.n,), float("nan"), dtype=torch.float64, device=b.device)
         info = _static_solve(dA, b, 1e-10, 20000, precond, x)
         assert info.status == info_ref.status == 0
