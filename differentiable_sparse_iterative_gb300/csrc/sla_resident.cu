@@ -26,6 +26,36 @@
 
 namespace sla {
 
+#ifdef SLA_PHASE_TIMING
+// Profiling build only (compiled out of the library): cycles per phase, summed over iterations,
+// for every block: [p-update, spmv, p.q reduce, r-update, r.r reduce, scalars, -, iterations].
+__device__ unsigned long long g_phase_cycles[kMaxBlocksPerSystem][8];
+#define SLA_PHASE_INIT() unsigned long long ph_[6] = {0, 0, 0, 0, 0, 0}; long long ph_t = clock64()
+#define SLA_PHASE(q)                \
+  do {                              \
+    const long long t_ = clock64(); \
+    ph_[q] += t_ - ph_t;            \
+    ph_t = t_;                      \
+  } while (0)
+#define SLA_PHASE_STORE(k)                                                    \
+  do {                                                                        \
+    if (threadIdx.x == 0) {                                                   \
+      for (int q_ = 0; q_ < 6; ++q_) g_phase_cycles[blockIdx.x][q_] = ph_[q_]; \
+      g_phase_cycles[blockIdx.x][7] = (unsigned long long)(k);                \
+    }                                                                         \
+  } while (0)
+#else
+#define SLA_PHASE_INIT() \
+  do {                   \
+  } while (0)
+#define SLA_PHASE(q) \
+  do {               \
+  } while (0)
+#define SLA_PHASE_STORE(k) \
+  do {                     \
+  } while (0)
+#endif
+
 namespace {
 
 constexpr int kResBlock = 1024;
@@ -38,16 +68,21 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
   return v;
 }
 
-// Bounded grid barrier over a monotone arrival counter.  Returns false (after raising the
-// timeout flag) if the other blocks did not arrive in time, or if another block timed out.
-__device__ __forceinline__ bool grid_barrier(unsigned *arrive, unsigned *timeout, unsigned G, unsigned &epoch) {
-  __shared__ int s_ok;
+// Split-phase grid barrier over a monotone arrival counter.  grid_arrive: after the block's
+// writes (ordered by __syncthreads), thread 0 adds 1 with release semantics (no round trip).
+// grid_wait: thread 0 polls with acquire loads until all G blocks of this epoch have arrived, then
+// the block synchronises.  The wait is bounded: on expiry (or when another block has timed out) it
+// raises the timeout flag and returns false.  Work that needs neither side may run in between.
+__device__ __forceinline__ void grid_arrive(unsigned *arrive, unsigned &epoch) {
   __syncthreads();
+  ++epoch;
+  if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(arrive), "r"(1u) : "memory");
+}
+
+__device__ __forceinline__ bool grid_wait(unsigned *arrive, unsigned *timeout, unsigned G, unsigned epoch) {
+  __shared__ int s_ok;
   if (threadIdx.x == 0) {
-    ++epoch;
     const unsigned target = epoch * G;
-    __threadfence();
-    atomicAdd(arrive, 1u);
     int ok = 1;
     long long spins = 0;
     while (ld_acquire(arrive) < target) {
@@ -57,12 +92,17 @@ __device__ __forceinline__ bool grid_barrier(unsigned *arrive, unsigned *timeout
         ok = 0;
         break;
       }
-      if (spins > 64) __nanosleep(32);
+      if (spins > 256) __nanosleep(32);
     }
     s_ok = ok;
   }
   __syncthreads();
   return s_ok != 0;
+}
+
+__device__ __forceinline__ bool grid_barrier(unsigned *arrive, unsigned *timeout, unsigned G, unsigned &epoch) {
+  grid_arrive(arrive, epoch);
+  return grid_wait(arrive, timeout, G, epoch);
 }
 
 // Deterministic all-reduce across the G blocks, in three steps so that the fp64 work on the
@@ -133,8 +173,18 @@ __device__ __forceinline__ V p_remote(const V *r, const V *dinv, const V *po, in
 // (fp64 divisions and square roots are far too expensive to repeat in every thread).
 struct ResScalars {
   double alpha, beta, alpha_prev, rho, nb;
-  int go;  // 1: keep iterating
+  double tol, rr_lo, rr_hi;  // stopping test sqrt(r.r) <= tol, decided by comparison outside [lo, hi]
+  int go;                    // 1: keep iterating
 };
+
+// sqrt(rr) <= tol exactly as the fp64 expression evaluates, without the square root in the common
+// case: lo and hi bracket tol^2 with a few ulps of margin (rr <= lo implies sqrt(rr) < tol and
+// rr > hi implies sqrt(rr) > tol for correctly rounded sqrt); only rr in between takes the sqrt.
+__device__ __forceinline__ bool stop_test(double rr, const ResScalars &S) {
+  if (rr <= S.rr_lo) return true;
+  if (rr > S.rr_hi) return false;
+  return sqrt(rr) <= S.tol;
+}
 
 template <typename V, typename I, bool JAC>
 __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int cap) {
@@ -208,7 +258,7 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
   // thread 0 of every block takes the same decisions from the same totals
   int status = SLA_NOT_CONVERGED, pending = 0;
   int64_t k = 0;
-  double nb = 0.0, rel = 0.0, rho = 0.0;
+  double nb = 0.0, rel = 0.0, rho = 0.0, rr_last = -1.0;
   if (tid < 32) {
     double t5[5];
     warp_totals<5>(partB, (int)G, t5);
@@ -245,47 +295,33 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
       S.alpha_prev = 0.0;
       S.rho = rho;
       S.nb = nb;
+      const double tol = P.rtol * nb, e4 = 4.0 * 2.220446049250313e-16;
+      const double t1 = tol * (1.0 - e4), t2 = tol * (1.0 + e4);
+      S.tol = tol;
+      S.rr_lo = t1 * t1;
+      S.rr_hi = t2 * t2;
     }
   }
   __syncthreads();
 
   // ---- iterations
+  SLA_PHASE_INIT();
   while (S.go) {
     const int par = (int)(k & 1);
     const bool first = (k == 0);
     const V vb = (V)S.beta, va_prev = (V)S.alpha_prev;
     V *pn_pub = P.p[par];
     const V *po_pub = P.p[par ^ 1];
-    // p_k = z_k + beta p_{k-1} for the own rows; x += alpha_{k-1} p_{k-1}; publish p_k.
-    // Rows are taken kStage at a time with their global loads issued first, so each group waits
-    // for memory once instead of once per row.
-    for (int j0 = tid; j0 < len; j0 += kStage * kResBlock) {
-      V xv[kStage];
-      if (!first) {
-#pragma unroll
-        for (int u = 0; u < kStage; ++u) {
-          const int li = j0 + u * kResBlock;
-          xv[u] = li < len ? xg[c0 + li] : V(0);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kStage; ++u) {
-        const int li = j0 + u * kResBlock;
-        if (li < len) {
-          const V rl = sr[li];
-          const V z = JAC ? sd[li] * rl : rl;
-          V pv = z;
-          if (!first) {
-            const V po = sp[li];
-            pv = fmav<V>(vb, po, z);
-            xg[c0 + li] = fmav<V>(va_prev, po, xv[u]);
-          }
-          sp[li] = pv;
-          pn_pub[c0 + li] = pv;
-        }
-      }
+    // p_k = z_k + beta p_{k-1} for the own rows; publish p_k
+    for (int li = tid; li < len; li += kResBlock) {
+      const V rl = sr[li];
+      const V z = JAC ? sd[li] * rl : rl;
+      const V pv = first ? z : fmav<V>(vb, sp[li], z);
+      sp[li] = pv;
+      pn_pub[c0 + li] = pv;
     }
     __syncthreads();
+    SLA_PHASE(0);
     // q = A p_k and the block's share of p.q (row pointers of a group loaded up front)
     V part = V(0);
     for (int j0 = tid; j0 < len; j0 += kStage * kResBlock) {
@@ -321,8 +357,29 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
       }
     }
     const double v1[1] = {(double)part};
+    SLA_PHASE(1);
     block_publish<1>(v1, sbuf, partA);
-    const bool ok1 = grid_barrier(arrive, timeout, G, epoch);
+    grid_arrive(arrive, epoch);
+    // while the other blocks arrive: the delayed update x += alpha_{k-1} p_{k-1} (p_{k-1} is this
+    // block's own published copy), which needs neither reduction
+    if (!first) {
+      for (int j0 = tid; j0 < len; j0 += kStage * kResBlock) {
+        V xv[kStage], pv[kStage];
+#pragma unroll
+        for (int u = 0; u < kStage; ++u) {
+          const int li = j0 + u * kResBlock;
+          xv[u] = li < len ? xg[c0 + li] : V(0);
+          pv[u] = li < len ? po_pub[c0 + li] : V(0);
+        }
+#pragma unroll
+        for (int u = 0; u < kStage; ++u) {
+          const int li = j0 + u * kResBlock;
+          if (li < len) xg[c0 + li] = fmav<V>(va_prev, pv[u], xv[u]);
+        }
+      }
+    }
+    const bool ok1 = grid_wait(arrive, timeout, G, epoch);
+    SLA_PHASE(2);
     if (tid < 32) {
       double t1[1];
       warp_totals<1>(partA, (int)G, t1);
@@ -369,6 +426,7 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
         if (JAC) acc2[1] += (double)rz_t;
       }
     }
+    SLA_PHASE(3);
     if (JAC) {
       block_publish<2>(acc2, sbuf, partB);
     } else {
@@ -376,6 +434,7 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
       block_publish<1>(v1r, sbuf, partB);
     }
     const bool ok2 = grid_barrier(arrive, timeout, G, epoch);
+    SLA_PHASE(4);
     ++k;
     if (tid < 32) {
       double t2[2] = {0.0, 0.0};
@@ -385,26 +444,23 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
         warp_totals<1>(partB, (int)G, t1);
         t2[0] = t1[0];
       }
-      // the scalars in parallel lanes: lane 0 the stopping test, lane 1 beta, lane 2 the history
+      // lane 0 the stopping test, lane 1 beta (in parallel); the history keeps r.r for now and is
+      // turned into ||r|| / ||b|| after the loop
       const double rrt = t2[0];
       const double rho_new = JAC ? t2[1] : rrt;
       double lane_val = 0.0;
       if (tid == 1) lane_val = rho_new / S.rho;
-      if (tid == 2) {
-        lane_val = sqrt(rrt) / S.nb;
-        if (bid == 0 && P.history) P.history[k] = lane_val;
-      }
+      if (tid == 2 && bid == 0 && P.history) P.history[k] = rrt;
       int stop_code = 0;  // 0 go on, 1 converged, 2 non-finite, 3 maxit, 4 timeout
       if (tid == 0) {
         if (!ok2) stop_code = 4;
         else if (!isfinite(rrt)) stop_code = 2;
-        else if (sqrt(rrt) <= P.rtol * S.nb) stop_code = 1;
+        else if (stop_test(rrt, S)) stop_code = 1;
         else if (k >= P.maxit) stop_code = 3;
       }
       const double beta_new = __shfl_sync(0xffffffffu, lane_val, 1);
-      const double rel_k = __shfl_sync(0xffffffffu, lane_val, 2);
       if (tid == 0) {
-        rel = rel_k;
+        rr_last = rrt;
         int go = 0;
         if (stop_code == 4) status = SLA_TIMEOUT;
         else if (stop_code == 2) { status = SLA_NONFINITE; pending = 1; }
@@ -421,7 +477,9 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
       }
     }
     __syncthreads();
+    SLA_PHASE(5);
   }
+  SLA_PHASE_STORE(k);
 
   // ---- finish: the last delayed x update (or x = 0 for b = 0)
   __shared__ int s_pending;
@@ -433,7 +491,13 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
   } else if (s_pending == 2) {
     for (int li = tid; li < len; li += kResBlock) xg[c0 + li] = V(0);
   }
+  // history entries 1..k hold r.r: convert them to ||r|| / ||b|| (block 0, all threads)
+  if (bid == 0 && P.history && S.nb > 0.0) {
+    const double nbs = S.nb;
+    for (int64_t j = 1 + tid; j <= k; j += kResBlock) P.history[j] = sqrt(P.history[j]) / nbs;
+  }
   if (bid == 0 && tid == 0) {
+    if (rr_last >= 0.0 || rr_last != rr_last) rel = sqrt(rr_last) / nb;
     C->k = k;
     C->status = status;
     C->rel_res = rel;
@@ -531,3 +595,9 @@ SLA_INSTANTIATE_RESIDENT(float, int64_t, false)
 SLA_INSTANTIATE_RESIDENT(float, int64_t, true)
 
 }  // namespace sla
+
+#ifdef SLA_PHASE_TIMING
+extern "C" SLA_API int sla_phase_cycles(unsigned long long *host, int nblocks) {
+  return (int)cudaMemcpyFromSymbol(host, sla::g_phase_cycles, sizeof(unsigned long long) * 8 * (size_t)nblocks);
+}
+#endif
