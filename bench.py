@@ -143,7 +143,7 @@ def run_ours(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = config_by_name(args.config)
+    w = config_by_name(args.config, **({"m": args.grid_m} if args.grid_m else {}))
     precond = w.precond
     jac = precond == 1
     batched = w.batch > 0
@@ -373,6 +373,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-iters", type=int, default=600)
     ap.add_argument("--ref-iters", type=int, default=100)
+    ap.add_argument("--grid-m", type=int, default=0,
+                    help="override the grid side m of the chosen workload (smaller cases for profiling)")
     ap.add_argument("--loop", choices=["auto", "resident", "graph", "host"], default="auto",
                     help="auto (default): resident kernel when the system fits on chip, else graph; "
                          "host: host-driven loop, e.g. for per-kernel ncu")

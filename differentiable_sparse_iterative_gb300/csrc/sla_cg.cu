@@ -104,7 +104,9 @@ __global__ void __launch_bounds__(kBlock) cg_setup(Prob<V, I> P) {
       else if (!(d > V(0))) acc[4] += 1.0;
       const V di = V(1) / d;
       dinv[i] = di;
-      acc[2] = fma((double)ri, (double)(di * ri), acc[2]);
+      const V zi = di * ri;
+      P.z[vo + i] = zi;
+      acc[2] = fma((double)ri, (double)zi, acc[2]);
     }
   }
   block_sum<5>(acc);
@@ -154,11 +156,9 @@ __global__ void __launch_bounds__(kBlock) cg_setup(Prob<V, I> P) {
 
 // z_c = M^{-1} r_c and p_k[c] = z_c + beta p_{k-1}[c]: the same expression for rows of the tile
 // (kept in shared memory) and for neighbours recomputed from global memory.
-template <typename V, bool JAC>
-__device__ __forceinline__ V p_of(const V *__restrict__ r, const V *__restrict__ dinv, const V *__restrict__ po,
-                                  int64_t c, bool first, V beta) {
-  const V rc = r[c];
-  const V zc = JAC ? dinv[c] * rc : rc;
+template <typename V>
+__device__ __forceinline__ V p_of(const V *__restrict__ zs, const V *__restrict__ po, int64_t c, bool first, V beta) {
+  const V zc = zs[c];
   return first ? zc : fmav<V>(beta, po[c], zc);
 }
 
@@ -176,8 +176,8 @@ __global__ void __launch_bounds__(kBlock) cg_spmv_step(Prob<V, I> P, int par) {
   const V *__restrict__ val = P.val + s * P.val_stride;
   const I *__restrict__ rp = P.rp;
   const int32_t *__restrict__ ci = P.ci;
-  const V *__restrict__ r = P.r + vo;
-  const V *__restrict__ dinv = JAC ? P.dinv + vo : nullptr;
+  // z = M^{-1} r (r itself without a preconditioner)
+  const V *__restrict__ zs = JAC ? P.z + vo : P.r + vo;
   const V *__restrict__ po = P.p[par ^ 1] + vo;
   V *__restrict__ pn = P.p[par] + vo;
   V *__restrict__ q = P.q + vo;
@@ -193,19 +193,29 @@ __global__ void __launch_bounds__(kBlock) cg_spmv_step(Prob<V, I> P, int par) {
   for (int sub = 0; sub < nsub; ++sub) {
     const int len = (int)((chunk * (sub + 1)) / nsub - (chunk * sub) / nsub);
     s0 = c0 + (chunk * sub) / nsub;
-    // p_k for the tile's rows, and the delayed x update with p_{k-1}
+    // loads of the tile's rows first (vectors and row pointers), then p_k, the delayed x update
+    V zv[RPT], pov[RPT], xv[RPT];
+    I rpa[RPT], rpb[RPT];
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+      const int li = j * kBlock + threadIdx.x;
+      const bool in = li < len;
+      const int64_t i = s0 + li;
+      zv[j] = in ? zs[i] : V(0);
+      pov[j] = (in && !first) ? po[i] : V(0);
+      xv[j] = (in && !first) ? x[i] : V(0);
+      rpa[j] = in ? rp[i] : I(0);
+      rpb[j] = in ? rp[i + 1] : I(0);
+    }
 #pragma unroll
     for (int j = 0; j < RPT; ++j) {
       const int li = j * kBlock + threadIdx.x;
       if (li < len) {
         const int64_t i = s0 + li;
-        const V ri = r[i];
-        const V zi = JAC ? dinv[i] * ri : ri;
-        V pv = zi;
+        V pv = zv[j];
         if (!first) {
-          const V pold = po[i];
-          pv = fmav<V>(beta, pold, zi);
-          x[i] = fmav<V>(alpha_prev, pold, x[i]);
+          pv = fmav<V>(beta, pov[j], zv[j]);
+          x[i] = fmav<V>(alpha_prev, pov[j], xv[j]);
         }
         sp[li] = pv;
         pn[i] = pv;
@@ -218,8 +228,11 @@ __global__ void __launch_bounds__(kBlock) cg_spmv_step(Prob<V, I> P, int par) {
       const int li = j * kBlock + threadIdx.x;
       if (li < len) {
         const int64_t i = s0 + li;
-        int64_t e0, e1;
-        row_range(rp, i, P.nnz, e0, e1, &P.glob->bad_csr);
+        int64_t e0 = (int64_t)rpa[j], e1 = (int64_t)rpb[j];
+        if (e0 < 0 || e1 < e0 || e1 > P.nnz) {
+          atomicOr(&P.glob->bad_csr, 1u);
+          e0 = e1 = 0;
+        }
         V acc = V(0);
         for (int64_t e = e0; e < e1; ++e) {
           const int32_t c = ci[e];
@@ -227,7 +240,7 @@ __global__ void __launch_bounds__(kBlock) cg_spmv_step(Prob<V, I> P, int par) {
           const uint32_t off = (uint32_t)((int64_t)c - s0);
           V pc;
           if (off < (uint32_t)len) pc = sp[off];
-          else pc = col_ok(c, P.n, &P.glob->bad_csr) ? p_of<V, JAC>(r, dinv, po, c, first, beta) : V(0);
+          else pc = col_ok(c, P.n, &P.glob->bad_csr) ? p_of<V>(zs, po, c, first, beta) : V(0);
           acc = fmav<V>(v, pc, acc);
         }
         q[i] = acc;
@@ -273,28 +286,50 @@ __global__ void __launch_bounds__(kBlock) cg_update_step(Prob<V, I> P, int par) 
   V *__restrict__ r = P.r + vo;
   const V *__restrict__ q = P.q + vo;
   const V *__restrict__ dinv = JAC ? P.dinv + vo : nullptr;
+  V *__restrict__ z = JAC ? P.z + vo : nullptr;
   int64_t c0, c1;
   chunk_of(P.n, P.G, bx, c0, c1);
   double acc[2] = {0.0, 0.0};
-  V rr = V(0), rz = V(0);
-  int cnt = 0;
-  for (int64_t i = c0 + threadIdx.x; i < c1; i += kBlock) {
-    const V ri = fmav<V>(-alpha, q[i], r[i]);
-    r[i] = ri;
-    rr = fmav<V>(ri, ri, rr);
-    if (JAC) rz = fmav<V>(ri, dinv[i] * ri, rz);
-    if constexpr (sizeof(V) == 4) {  // float data: fold into the fp64 sums every few rows
-      if (++cnt == 8) {
-        acc[0] += (double)rr;
-        acc[1] += (double)rz;
-        rr = V(0);
-        rz = V(0);
-        cnt = 0;
+  // groups of kUpd rows per thread: all loads of a group first, then the arithmetic
+  constexpr int kUpd = 8;
+  for (int64_t g0 = c0 + threadIdx.x; g0 < c1; g0 += (int64_t)kUpd * kBlock) {
+    V qv[kUpd], rv[kUpd], dv[kUpd];
+#pragma unroll
+    for (int u = 0; u < kUpd; ++u) {
+      const int64_t i = g0 + (int64_t)u * kBlock;
+      const bool in = i < c1;
+      qv[u] = in ? q[i] : V(0);
+      rv[u] = in ? r[i] : V(0);
+      if (JAC) dv[u] = in ? dinv[i] : V(0);
+    }
+    // fp64 data accumulates straight into the fp64 sums; fp32 data per group in fp32 first
+    V rr = V(0), rz = V(0);
+    if constexpr (sizeof(V) == 8) {
+      rr = acc[0];
+      rz = acc[1];
+    }
+#pragma unroll
+    for (int u = 0; u < kUpd; ++u) {
+      const int64_t i = g0 + (int64_t)u * kBlock;
+      if (i < c1) {
+        const V ri = fmav<V>(-alpha, qv[u], rv[u]);
+        r[i] = ri;
+        rr = fmav<V>(ri, ri, rr);
+        if (JAC) {
+          const V zi = dv[u] * ri;
+          z[i] = zi;
+          rz = fmav<V>(ri, zi, rz);
+        }
       }
     }
+    if constexpr (sizeof(V) == 8) {
+      acc[0] = rr;
+      acc[1] = rz;
+    } else {
+      acc[0] += (double)rr;
+      if (JAC) acc[1] += (double)rz;
+    }
   }
-  acc[0] += (double)rr;
-  acc[1] += (double)rz;
   block_sum<2>(acc);
   double *pp = P.partials + (size_t)s * kRedSlots * kMaxBlocksPerSystem;
   if (!publish_last<2>(acc, pp, &C->ticket, P.G, bx)) return;
@@ -599,6 +634,7 @@ Prob<V, I> make_prob(const sla_csr *A, int64_t batch, const void *values, int64_
   P.p[1] = (V *)(w + L.p1);
   P.q = (V *)(w + L.q);
   P.dinv = jacobi ? (V *)(w + L.dinv) : nullptr;
+  P.z = jacobi ? (V *)(w + L.z) : nullptr;
   P.partials = (double *)(w + L.partials);
   P.ctl = (Ctl *)(w + L.ctl);
   P.glob = (Glob *)(w + L.glob);

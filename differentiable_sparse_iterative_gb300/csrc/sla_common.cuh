@@ -50,7 +50,7 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size
 
 // Workspace layout (offsets in bytes from the workspace base).
 struct Layout {
-  size_t glob, ctl, partials, r, p0, p1, q, dinv, total;
+  size_t glob, ctl, partials, r, p0, p1, q, dinv, z, total;
 };
 
 __host__ __device__ inline Layout make_layout(int64_t n, int64_t batch, size_t vbytes, bool jacobi) {
@@ -65,6 +65,7 @@ __host__ __device__ inline Layout make_layout(int64_t n, int64_t batch, size_t v
   L.p1 = off; off += vec;
   L.q = off; off += vec;
   L.dinv = off; off += jacobi ? vec : 0;
+  L.z = off; off += jacobi ? vec : 0;  // z = M^{-1} r, kept so the SpMV step reads one vector
   L.total = off;
   return L;
 }
@@ -82,6 +83,7 @@ struct Prob {
   V *p[2];               // ping-pong search directions
   V *q;
   V *dinv;               // Jacobi: 1 / A_ii
+  V *z;                  // Jacobi: z = dinv * r (written with r; the SpMV step reads z, not r and dinv)
   double *partials;      // [batch][kRedSlots][kMaxBlocksPerSystem]
   Ctl *ctl;              // [batch]
   Glob *glob;

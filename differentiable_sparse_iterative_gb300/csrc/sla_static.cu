@@ -25,8 +25,9 @@ namespace {
 
 constexpr int64_t kStaticMaxN = 65536;
 // Workspace layout for n = 65,536, one system, fp64 values, Jacobi: Glob (256 B) + Ctl (256 B)
-// + partial sums (6 x 2048 doubles = 98,304 B) + 5 vectors of 65,536 doubles (524,288 B each).
-constexpr size_t kStaticScratchBytes = 256 + 256 + 98304 + 5 * 524288;  // 2,720,256 bytes
+// + partial sums (6 x 2048 doubles = 98,304 B) + 6 vectors of 65,536 doubles (524,288 B each:
+// r, p0, p1, q, 1/diag, z).
+constexpr size_t kStaticScratchBytes = 256 + 256 + 98304 + 6 * 524288;  // 3,244,544 bytes
 constexpr int kMaxDevices = 64;
 
 // The shared scratch.  In host code this name is only a stand-in for the device symbol:

@@ -234,7 +234,7 @@ SLA_API sla_status sla_cg_adjoint_batched(const sla_csr *pattern, int64_t batch,
  * (plugins inside a host application that owns all device memory, latency-critical paths where
  * an allocation is not allowed, bindings with no device allocator).  The paper has no
  * counterpart: this is a library convenience, not part of the method.
- *   Scratch: a fixed 2,720,256-byte array in the library's own device memory, reserved on every
+ *   Scratch: a fixed 3,244,544-byte array in the library's own device memory, reserved on every
  *   GPU that loads the library and held until the process exits.  Systems of up to 65,536
  *   unknowns (one system, fp32 or fp64, with or without Jacobi) fit; larger n returns
  *   SLA_WORKSPACE_TOO_SMALL before anything is launched.
