@@ -33,12 +33,14 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
 
 #include "sla_common.cuh"
 #include "sla_host.h"
+#include "sla_tma.cuh"
 
 namespace sla {
 
@@ -275,6 +277,266 @@ __global__ void __launch_bounds__(kBlock) cg_spmv_step(Prob<V, I> P, int par) {
   }
 }
 
+// ---- TMA-staged SpMV step (same arithmetic as cg_spmv_step, same results bit for bit)
+//
+// The block walks its chunk in tiles of kTmaRows rows.  Thread 0 streams each tile's CSR
+// entries (col_idx, values) and row vectors (z, p_{k-1}, x) into a shared-memory stage with
+// 1-D bulk copies, two stages deep, so the copy of tile t+1 overlaps the arithmetic of tile t and
+// the matrix stream never waits on per-thread loads.  Bulk copies need 16-byte alignment: each
+// array's aligned interior is copied, the ragged ends (a few entries) are read from global
+// memory directly, and a tile with more than kTmaCap entries reads its CSR entries from global
+// memory.  A stage wait that exceeds its bound also falls back to global memory and raises the
+// timeout flag, so results never depend on a copy completing.
+constexpr int kTmaBlock = 512;         // threads per block of the TMA-staged step
+constexpr int kTmaRows = kTmaBlock;    // rows per tile, one per thread
+constexpr int kTmaCap = 6 * kTmaRows;  // CSR entries a stage holds
+constexpr int kTmaRemote = 4;          // off-tile columns per row whose p is gathered ahead
+constexpr long long kTmaWaitLimit = 1ll << 22;
+
+template <typename V>
+struct __align__(16) TmaStage {
+  static constexpr int kEv = 16 / (int)sizeof(V);  // elements per 16 bytes
+  alignas(16) int32_t ci[kTmaCap + 8];
+  alignas(16) V val[kTmaCap + 2 * kEv];
+  alignas(16) V zv[kTmaRows + 2 * kEv];
+  alignas(16) V pov[kTmaRows + 2 * kEv];
+  alignas(16) V xv[kTmaRows + 2 * kEv];
+};
+
+// What a stage holds: aligned interiors [a, b) of the entry range and of the row range, with the
+// index of element 0 of each staged array (base).  Written by thread 0 before the copies.
+struct TmaPlan {
+  int64_t cbase, ca, cb;   // col_idx entries
+  int64_t vbase, va, vb;   // values entries
+  int64_t rbase, ra, rb;   // rows (z, p_{k-1}, x)
+  int fallback;            // 1: CSR entries not staged for this tile
+};
+
+__device__ __forceinline__ int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+__device__ __forceinline__ int64_t round_dn(int64_t v, int64_t m) { return v / m * m; }
+
+template <typename V>
+__host__ __device__ constexpr size_t tma_smem_bytes() {
+  return 2 * sizeof(TmaStage<V>) + (size_t)kTmaRows * sizeof(V);
+}
+
+// Thread 0: plan and issue the copies of one tile into one stage.
+template <typename V>
+__device__ __forceinline__ void tma_issue(TmaStage<V> &st, TmaPlan &pl, uint64_t *bar, const int32_t *ci,
+                                          const V *val, const V *zs, const V *po, const V *x, int64_t s0, int len,
+                                          int64_t e_lo, int64_t e_hi, int64_t nnz, bool first) {
+  constexpr int kEv = TmaStage<V>::kEv;
+  uint32_t bytes = 0;
+  // never copy outside [0, nnz): a malformed row_ptr makes the tile read global memory, where
+  // the per-row checks skip out-of-range entries
+  pl.fallback = (e_hi - e_lo > kTmaCap || e_lo < 0 || e_hi < e_lo || e_hi > nnz) ? 1 : 0;
+  if (pl.fallback) e_lo = e_hi = 0;
+  pl.cbase = round_dn(e_lo, 4);
+  pl.ca = round_up(e_lo, 4);
+  pl.cb = round_dn(e_hi, 4);
+  pl.vbase = round_dn(e_lo, kEv);
+  pl.va = round_up(e_lo, kEv);
+  pl.vb = round_dn(e_hi, kEv);
+  if (pl.fallback || pl.cb < pl.ca) pl.cb = pl.ca;
+  if (pl.fallback || pl.vb < pl.va) pl.vb = pl.va;
+  pl.rbase = round_dn(s0, kEv);
+  pl.ra = round_up(s0, kEv);
+  pl.rb = round_dn(s0 + len, kEv);
+  if (pl.rb < pl.ra) pl.rb = pl.ra;
+  const uint32_t cbytes = (uint32_t)((pl.cb - pl.ca) * 4);
+  const uint32_t vbytes = (uint32_t)((pl.vb - pl.va) * (int64_t)sizeof(V));
+  const uint32_t rbytes = (uint32_t)((pl.rb - pl.ra) * (int64_t)sizeof(V));
+  bytes = cbytes + vbytes + rbytes * (first ? 1u : 3u);
+  fence_proxy_async_smem();
+  mbar_arrive_expect_tx(bar, bytes);
+  if (cbytes) bulk_g2s(st.ci + (pl.ca - pl.cbase), ci + pl.ca, cbytes, bar);
+  if (vbytes) bulk_g2s(st.val + (pl.va - pl.vbase), val + pl.va, vbytes, bar);
+  if (rbytes) {
+    bulk_g2s(st.zv + (pl.ra - pl.rbase), zs + pl.ra, rbytes, bar);
+    if (!first) {
+      bulk_g2s(st.pov + (pl.ra - pl.rbase), po + pl.ra, rbytes, bar);
+      bulk_g2s(st.xv + (pl.ra - pl.rbase), x + pl.ra, rbytes, bar);
+    }
+  }
+}
+
+template <typename V, typename I, bool JAC>
+__global__ void __launch_bounds__(kTmaBlock, 2) cg_spmv_step_tma(Prob<V, I> P, int par) {
+  count_kernel(P.glob);
+  const int s = blockIdx.y, bx = blockIdx.x;
+  Ctl *C = P.ctl + s;
+  if (C->done) return;
+  extern __shared__ __align__(16) unsigned char tma_smem[];
+  TmaStage<V> *stage = reinterpret_cast<TmaStage<V> *>(tma_smem);
+  V *sp = reinterpret_cast<V *>(tma_smem + 2 * sizeof(TmaStage<V>));
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ TmaPlan plan[2];
+
+  const int64_t k = C->k;
+  const bool first = (k == 0);
+  const V beta = (V)C->beta;
+  const V alpha_prev = (V)C->alpha;
+  const int64_t vo = (int64_t)s * P.n;
+  const V *__restrict__ val = P.val + s * P.val_stride;
+  const I *__restrict__ rp = P.rp;
+  const int32_t *__restrict__ ci = P.ci;
+  const V *__restrict__ zs = JAC ? P.z + vo : P.r + vo;
+  const V *__restrict__ po = P.p[par ^ 1] + vo;
+  V *__restrict__ pn = P.p[par] + vo;
+  V *__restrict__ q = P.q + vo;
+  V *__restrict__ x = P.x + vo;
+
+  int64_t c0, c1;
+  chunk_of(P.n, P.G, bx, c0, c1);
+  const int ntiles = (int)((c1 - c0 + kTmaRows - 1) / kTmaRows);
+  auto tile_s0 = [&](int t) { return c0 + (int64_t)t * kTmaRows; };
+  auto tile_len = [&](int t) { return (int)min((int64_t)kTmaRows, c1 - tile_s0(t)); };
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_proxy_async_smem();
+    for (int t = 0; t < 2 && t < ntiles; ++t) {
+      const int64_t a = tile_s0(t);
+      const int l = tile_len(t);
+      tma_issue<V>(stage[t], plan[t], &bar[t], ci, val, zs, po, x, a, l, (int64_t)rp[a], (int64_t)rp[a + l], P.nnz,
+                   first);
+    }
+  }
+  __syncthreads();
+
+  bool late = false;  // a stage wait ran out: read global memory for that tile
+  double pq = 0.0;
+  const int li = threadIdx.x;  // the thread's row within each tile
+  for (int t = 0; t < ntiles; ++t) {
+    const int sidx = t & 1;
+    const uint32_t parity = (uint32_t)((t >> 1) & 1);
+    const int64_t s0 = tile_s0(t);
+    const int len = tile_len(t);
+    const bool mine = li < len;
+    const int64_t i = s0 + li;
+    // bounds of tile t+2 for the producer, and this row's pointers, before the wait
+    int64_t nlo = 0, nhi = 0;
+    if (threadIdx.x == 0 && t + 2 < ntiles) {
+      const int64_t a = tile_s0(t + 2);
+      nlo = (int64_t)rp[a];
+      nhi = (int64_t)rp[a + tile_len(t + 2)];
+    }
+    int64_t e0 = mine ? (int64_t)rp[i] : 0, e1 = mine ? (int64_t)rp[i + 1] : 0;
+    if (e0 < 0 || e1 < e0 || e1 > P.nnz) {
+      atomicOr(&P.glob->bad_csr, 1u);
+      e0 = e1 = 0;
+    }
+    const bool ok = mbar_wait_bounded(&bar[sidx], parity, kTmaWaitLimit);
+    if (!ok) {
+      late = true;
+      atomicOr(&P.glob->timeout, 1u);
+    }
+    const TmaStage<V> &st = stage[sidx];
+    const TmaPlan pl = plan[sidx];
+    const bool staged_csr = ok && !pl.fallback;
+    // gather ahead: z and p_{k-1} at this row's first kTmaRemote off-tile columns
+    V rz[kTmaRemote], rpo[kTmaRemote];
+    int nrem = 0;
+    for (int64_t e = e0; e < e1 && nrem < kTmaRemote; ++e) {
+      const int32_t c = (staged_csr && e >= pl.ca && e < pl.cb) ? st.ci[e - pl.cbase] : ci[e];
+      if ((uint32_t)((int64_t)c - s0) >= (uint32_t)len && (uint32_t)c < (uint32_t)P.n) {
+#pragma unroll
+        for (int u = 0; u < kTmaRemote; ++u)
+          if (u == nrem) {
+            rz[u] = zs[c];
+            rpo[u] = first ? V(0) : po[c];
+          }
+        ++nrem;
+      }
+    }
+    // p_k for the row and the delayed x update
+    if (mine) {
+      const bool in = ok && i >= pl.ra && i < pl.rb;
+      const V zi = in ? st.zv[i - pl.rbase] : zs[i];
+      V pv = zi;
+      if (!first) {
+        const V pold = in ? st.pov[i - pl.rbase] : po[i];
+        const V xo = in ? st.xv[i - pl.rbase] : x[i];
+        pv = fmav<V>(beta, pold, zi);
+        x[i] = fmav<V>(alpha_prev, pold, xo);
+      }
+      sp[li] = pv;
+      pn[i] = pv;
+    }
+    __syncthreads();
+    V part = V(0);
+    if (mine) {
+      V acc = V(0);
+      int used = 0;
+      for (int64_t e = e0; e < e1; ++e) {
+        const int32_t c = (staged_csr && e >= pl.ca && e < pl.cb) ? st.ci[e - pl.cbase] : ci[e];
+        const V v = (staged_csr && e >= pl.va && e < pl.vb) ? st.val[e - pl.vbase] : val[e];
+        const uint32_t off = (uint32_t)((int64_t)c - s0);
+        V pc;
+        if (off < (uint32_t)len) {
+          pc = sp[off];
+        } else if (!col_ok(c, P.n, &P.glob->bad_csr)) {
+          pc = V(0);
+        } else if (used < nrem) {
+          V zc = rz[0], pc0 = rpo[0];
+#pragma unroll
+          for (int u = 1; u < kTmaRemote; ++u)
+            if (u == used) {
+              zc = rz[u];
+              pc0 = rpo[u];
+            }
+          pc = first ? zc : fmav<V>(beta, pc0, zc);
+          ++used;
+        } else {
+          pc = p_of<V>(zs, po, c, first, beta);
+        }
+        acc = fmav<V>(v, pc, acc);
+      }
+      q[i] = acc;
+      part = fmav<V>(sp[li], acc, part);
+    }
+    pq += (double)part;
+    __syncthreads();  // the stage and sp are free again
+    if (threadIdx.x == 0 && t + 2 < ntiles) {
+      if (late) {
+        // the previous copy into this stage may still be in flight: let it land first
+        mbar_wait_bounded(&bar[sidx], parity, kTmaWaitLimit);
+      }
+      tma_issue<V>(stage[sidx], plan[sidx], &bar[sidx], ci, val, zs, po, x, tile_s0(t + 2), tile_len(t + 2), nlo,
+                   nhi, P.nnz, first);
+    }
+  }
+  if (late && threadIdx.x == 0) {
+    // no copy may outlive the block
+    for (int t = ntiles - 2; t < ntiles; ++t)
+      if (t >= 0) mbar_wait_bounded(&bar[t & 1], (uint32_t)((t >> 1) & 1), kTmaWaitLimit);
+  }
+  double v1[1] = {pq};
+  block_sum_n<1, kTmaBlock>(v1);
+  double *pp = P.partials + (size_t)s * kRedSlots * kMaxBlocksPerSystem;
+  if (!publish_last<1>(v1, pp, &C->ticket, P.G, bx)) return;
+  double tot[1];
+  reduce_partials<1>(pp, P.G, &C->ticket, tot);
+  if (threadIdx.x != 0) return;
+  const double pqt = tot[0];
+  int stop = 0;
+  if (!isfinite(pqt)) {
+    C->status = SLA_NONFINITE;
+    stop = 1;
+  } else if (!(pqt > 0.0)) {
+    C->status = SLA_BREAKDOWN;
+    stop = 1;
+  } else {
+    C->alpha = C->rho / pqt;
+  }
+  if (stop) {
+    C->done = 1;
+    C->pending = 0;
+    atomicSub(&P.glob->active, 1u);
+  }
+}
+
 template <typename V, typename I, bool JAC>
 __global__ void __launch_bounds__(kBlock) cg_update_step(Prob<V, I> P, int par) {
   count_kernel(P.glob);
@@ -417,27 +679,44 @@ struct Kernels {
   static void *init() { return (void *)cg_init<V, I>; }
   static void *setup() { return (void *)cg_setup<V, I, JAC>; }
   static void *spmv_step() { return (void *)cg_spmv_step<V, I, JAC, kRPT>; }
+  static void *spmv_step_tma() { return (void *)cg_spmv_step_tma<V, I, JAC>; }
   static void *update_step() { return (void *)cg_update_step<V, I, JAC>; }
   static void *finish() { return (void *)cg_finish<V, I>; }
 };
 
 cudaError_t add_kernel(cudaGraphNode_t *node, cudaGraph_t g, const cudaGraphNode_t *dep, size_t ndep, void *fn,
-                       dim3 grid, dim3 block, void **args) {
+                       dim3 grid, dim3 block, void **args, unsigned smem = 0) {
   cudaKernelNodeParams kp;
   memset(&kp, 0, sizeof(kp));
   kp.func = fn;
   kp.gridDim = grid;
   kp.blockDim = block;
-  kp.sharedMemBytes = 0;
+  kp.sharedMemBytes = smem;
   kp.kernelParams = args;
   kp.extra = nullptr;
   return cudaGraphAddKernelNode(node, g, dep, ndep, &kp);
 }
 
+// Launch shape of the streaming path: blocks per system for the SpMV step and for the other
+// kernels, and whether the SpMV step is the TMA-staged one (with its dynamic shared memory).
+struct Launch {
+  int G_main = 1;
+  int G_spmv = 1;
+  bool tma = false;
+  unsigned tma_smem = 0;
+};
+
 template <typename V, typename I, bool JAC>
-cudaError_t build_graph(const Prob<V, I> &P0, int unroll, cudaGraph_t *out_graph, cudaGraphExec_t *out_exec) {
+cudaError_t build_graph(const Prob<V, I> &P0, const Launch &Lc, int unroll, cudaGraph_t *out_graph,
+                        cudaGraphExec_t *out_exec) {
   using K = Kernels<V, I, JAC>;
   Prob<V, I> P = P0;
+  Prob<V, I> Ps = P0;
+  P.G = Lc.G_main;
+  Ps.G = Lc.G_spmv;
+  const dim3 grid_s(Ps.G, P.batch);
+  void *fn_s = Lc.tma ? K::spmv_step_tma() : K::spmv_step();
+  const unsigned smem_s = Lc.tma ? Lc.tma_smem : 0u;
   cudaGraph_t g = nullptr;
   cudaError_t e = cudaGraphCreate(&g, 0);
   if (e != cudaSuccess) return e;
@@ -447,6 +726,7 @@ cudaError_t build_graph(const Prob<V, I> &P0, int unroll, cudaGraph_t *out_graph
   void *args_p[] = {(void *)&P};
   int par[2] = {0, 1};
   void *args_pp[2][2] = {{(void *)&P, (void *)&par[0]}, {(void *)&P, (void *)&par[1]}};
+  void *args_ps[2][2] = {{(void *)&Ps, (void *)&par[0]}, {(void *)&Ps, (void *)&par[1]}};
   const uint32_t max_bodies = (uint32_t)std::min<int64_t>((P.maxit + unroll - 1) / unroll + 2, 0x7fffffff);
   cudaGraphNodeParams cp = {cudaGraphNodeTypeConditional};
   do {
@@ -461,7 +741,8 @@ cudaError_t build_graph(const Prob<V, I> &P0, int unroll, cudaGraph_t *out_graph
     cudaGraph_t body = cp.conditional.phGraph_out[0];
     for (int u = 0; u < unroll && e == cudaSuccess; ++u) {
       cudaGraphNode_t na, nb;
-      e = add_kernel(&na, body, prev ? &prev : nullptr, prev ? 1 : 0, K::spmv_step(), grid, block, args_pp[u & 1]);
+      e = add_kernel(&na, body, prev ? &prev : nullptr, prev ? 1 : 0, fn_s, grid_s, dim3(Lc.tma ? kTmaBlock : kBlock),
+                     args_ps[u & 1], smem_s);
       if (e != cudaSuccess) break;
       e = add_kernel(&nb, body, &na, 1, K::update_step(), grid, block, args_pp[u & 1]);
       prev = nb;
@@ -481,6 +762,19 @@ cudaError_t build_graph(const Prob<V, I> &P0, int unroll, cudaGraph_t *out_graph
   }
   *out_graph = g;
   return cudaSuccess;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// The TMA-staged SpMV step is opt-in (SLA_SPMV=tma in the environment): measured on GB300 it is
+// slower than the plain step on the five-point workloads (its per-entry staging bookkeeping
+// makes it instruction-bound), so the plain step is the default.  Both compute the same rows.
+bool tma_enabled() {
+  static const int on = [] {
+    const char *e = getenv("SLA_SPMV");
+    return (e && strcmp(e, "tma") == 0) ? 1 : 0;
+  }();
+  return on != 0;
 }
 
 int occupancy_blocks(const void *fn) {
@@ -514,9 +808,12 @@ int choose_G(int64_t n, int64_t batch, int sms, int occ) {
 // Host-driven loop: the same kernels launched directly; the host reads the number of active
 // systems every `unroll` iterations (one 4-byte copy and one stream synchronisation).
 template <typename V, typename I, bool JAC>
-sla_status run_cg_host_loop(Prob<V, I> P, int unroll, cudaStream_t stream, sla_cg_info *info, int64_t batch) {
-  using K = Kernels<V, I, JAC>;
-  dim3 grid(P.G, P.batch), block(kBlock);
+sla_status run_cg_host_loop(Prob<V, I> P, const Launch &Lc, int unroll, cudaStream_t stream, sla_cg_info *info,
+                            int64_t batch) {
+  P.G = Lc.G_main;
+  Prob<V, I> Ps = P;
+  Ps.G = Lc.G_spmv;
+  dim3 grid(P.G, P.batch), grid_s(Ps.G, P.batch), block(kBlock);
   uint64_t launched = 0;
   cg_init<V, I><<<1, block, 0, stream>>>(P);
   cg_setup<V, I, JAC><<<grid, block, 0, stream>>>(P);
@@ -526,7 +823,10 @@ sla_status run_cg_host_loop(Prob<V, I> P, int unroll, cudaStream_t stream, sla_c
     const int64_t upto = std::min<int64_t>(P.maxit - k, unroll);
     for (int64_t u = 0; u < upto; ++u) {
       const int par = (int)((k + u) & 1);
-      cg_spmv_step<V, I, JAC, kRPT><<<grid, block, 0, stream>>>(P, par);
+      if (Lc.tma)
+        cg_spmv_step_tma<V, I, JAC><<<grid_s, dim3(kTmaBlock), Lc.tma_smem, stream>>>(Ps, par);
+      else
+        cg_spmv_step<V, I, JAC, kRPT><<<grid_s, block, 0, stream>>>(Ps, par);
       cg_update_step<V, I, JAC><<<grid, block, 0, stream>>>(P, par);
     }
     launched += 2 * (uint64_t)upto;
@@ -558,20 +858,38 @@ sla_status run_cg(Prob<V, I> P, int unroll, int loop, cudaStream_t stream, sla_c
                                               JAC ? SLA_PRECOND_JACOBI : SLA_PRECOND_NONE, P.maxit)))
     return run_resident<V, I, JAC>(P, stream, info);
   const DeviceInfo di = device_info();
-  static std::atomic<int> occ_cache{0};
-  int occ = occ_cache.load();
-  if (occ == 0) {
-    occ = std::min(occupancy_blocks(Kernels<V, I, JAC>::spmv_step()),
-                   occupancy_blocks(Kernels<V, I, JAC>::update_step()));
-    occ_cache.store(occ);
+  Launch Lc;
+  // TMA-staged SpMV step when every array it copies from is 16-byte aligned (per system too)
+  const bool per_sys_ok = batch == 1 || (((size_t)P.n * sizeof(V)) % 16 == 0 &&
+                                         ((size_t)P.val_stride * sizeof(V)) % 16 == 0);
+  Lc.tma = tma_enabled() && per_sys_ok && aligned16(P.ci) && aligned16(P.val) && aligned16(P.x) &&
+           aligned16(P.r) && aligned16(P.p[0]) && aligned16(P.p[1]) && (!JAC || aligned16(P.z));
+  Lc.tma_smem = (unsigned)tma_smem_bytes<V>();
+  static std::atomic<int> occ_u_cache{0}, occ_s_cache{0}, occ_t_cache{0};
+  int occ_u = occ_u_cache.load(), occ_s = occ_s_cache.load(), occ_t = occ_t_cache.load();
+  if (occ_u == 0) {
+    occ_u = occupancy_blocks(Kernels<V, I, JAC>::update_step());
+    occ_s = occupancy_blocks(Kernels<V, I, JAC>::spmv_step());
+    void *ft = Kernels<V, I, JAC>::spmv_step_tma();
+    occ_t = 0;
+    if (cudaFuncSetAttribute(ft, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lc.tma_smem) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_t, ft, kTmaBlock, Lc.tma_smem) != cudaSuccess)
+      occ_t = 0;
+    cudaGetLastError();  // clear a refused attribute, if any
+    occ_u_cache.store(occ_u);
+    occ_s_cache.store(occ_s);
+    occ_t_cache.store(occ_t);
   }
-  P.G = choose_G(P.n, batch, di.sms, occ);
+  if (occ_t < 1) Lc.tma = false;
+  Lc.G_main = choose_G(P.n, batch, di.sms, occ_u);
+  Lc.G_spmv = choose_G(P.n, batch, di.sms, Lc.tma ? occ_t : occ_s);
+  P.G = Lc.G_main;
   if (unroll <= 0) unroll = kDefaultUnroll;
   if (unroll & 1) unroll += 1;  // the ping-pong parity of the body must repeat
-  if (loop == SLA_LOOP_HOST) return run_cg_host_loop<V, I, JAC>(P, unroll, stream, info, batch);
+  if (loop == SLA_LOOP_HOST) return run_cg_host_loop<V, I, JAC>(P, Lc, unroll, stream, info, batch);
 
   std::vector<char> key(sizeof(P) + 4 * sizeof(int));
-  int tag[4] = {(int)sizeof(V), (int)sizeof(I), (int)JAC, unroll};
+  int tag[4] = {(int)sizeof(V), (int)sizeof(I), (int)JAC + 2 * (int)Lc.tma + 4 * Lc.G_spmv, unroll};
   memcpy(key.data(), &P, sizeof(P));
   memcpy(key.data() + sizeof(P), tag, sizeof(tag));
   int dev = di.dev;
@@ -589,7 +907,7 @@ sla_status run_cg(Prob<V, I> P, int unroll, int loop, cudaStream_t stream, sla_c
     if (!exec) {
       GraphEntry en;
       en.key = key;
-      cudaError_t e = build_graph<V, I, JAC>(P, unroll, &en.graph, &en.exec);
+      cudaError_t e = build_graph<V, I, JAC>(P, Lc, unroll, &en.graph, &en.exec);
       if (e != cudaSuccess) return fail(e);
       if (g_cache.size() >= kCacheCap) {
         auto it = std::min_element(g_cache.begin(), g_cache.end(),

@@ -325,3 +325,40 @@ def test_resident_rejects_what_does_not_fit():
     P = to_dev(w.A, np.float32)
     with pytest.raises(sla.SlaError):
         sla.sla_cg_solve_batched(P, t(w.values_b), t(w.b), rtol=1e-5, maxit=100, loop=sla.SLA_LOOP_RESIDENT)
+
+
+_SPMV_SCRIPT = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import differentiable_sparse_iterative_gb300 as sla
+from workloads import diffusion_dirichlet, random_spd
+out = []
+for A, pc in [(diffusion_dirichlet(300, np.random.default_rng(3).lognormal(0, 1, 2 * 300 * 301)), 1),
+              (random_spd(5000, 6.0, 4, long_rows=5), 0)]:
+    dA = sla.CSRMatrix.from_numpy(A.row_ptr, A.col_idx, A.values, "cuda")
+    b = torch.from_numpy(np.random.default_rng(5).standard_normal(A.n)).cuda()
+    x, info, _ = sla.sla_cg_solve(dA, b, rtol=1e-9, maxit=4000, precond=pc, loop=sla.SLA_LOOP_GRAPH)
+    out.append(x.cpu().numpy())
+np.save(sys.argv[2], np.concatenate(out))
+"""
+
+
+def test_tma_spmv_step_equals_plain(tmp_path):
+    # the TMA-staged SpMV step and the plain one do the same per-row arithmetic; they run at
+    # different occupancy, so the blocks (and the order of the p.q block sums) differ
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    script = tmp_path / "spmv_variant.py"
+    script.write_text(_SPMV_SCRIPT)
+    res = {}
+    for mode in ("tma", "plain"):
+        env = dict(os.environ)
+        env.pop("SLA_SPMV", None)
+        if mode == "tma":
+            env["SLA_SPMV"] = "tma"
+        outp = tmp_path / f"{mode}.npy"
+        subprocess.run([sys.executable, str(script), root, str(outp)], check=True, env=env, timeout=600)
+        res[mode] = np.load(outp)
+    assert rel(res["tma"], res["plain"]) <= 1e-11
