@@ -148,7 +148,7 @@ def run_ours(args, rank, world, local_rank):
     jac = precond == 1
     batched = w.batch > 0
     if batched:
-        raise SystemExit("bench.py times the single-system workloads (config1/2/4/5)")
+        return run_batched(args, w, dev, rank, world)
     A = sla.CSRMatrix.from_numpy(w.A.row_ptr, w.A.col_idx, w.A.values, dev)
     b = torch.from_numpy(w.b).to(dev)
     g_np = w.g if w.g is not None else np.random.default_rng(1).standard_normal(w.A.n)
@@ -161,7 +161,8 @@ def run_ours(args, rank, world, local_rank):
     gv = torch.empty(nnz, dtype=torch.float64, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    loop = {"auto": sla.SLA_LOOP_AUTO, "resident": sla.SLA_LOOP_RESIDENT, "graph": sla.SLA_LOOP_GRAPH,
+    loop = {"auto": sla.SLA_LOOP_AUTO, "cluster": sla.SLA_LOOP_CLUSTER, "resident": sla.SLA_LOOP_RESIDENT,
+            "graph": sla.SLA_LOOP_GRAPH,
             "host": sla.SLA_LOOP_HOST}[args.loop]
 
     def step():
@@ -258,6 +259,78 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(w, args.cpu_iters)
     return out
+
+
+def run_batched(args, w, dev, rank, world):
+    """Batched shared-pattern workload (config 3): forward + adjoint of all systems per step.
+    The metric counts system-iterations (each system's CG iterations, summed over the batch)."""
+    import torch
+    import differentiable_sparse_iterative_gb300 as sla
+    dt = torch.float32 if w.dtype == "f32" else torch.float64
+    P = sla.CSRMatrix.from_numpy(w.A.row_ptr, w.A.col_idx, w.A.values.astype(np.float32 if dt == torch.float32
+                                                                              else np.float64), dev)
+    vals = torch.from_numpy(w.values_b).to(dev)
+    b = torch.from_numpy(w.b).to(dev)
+    g = torch.from_numpy(w.g).to(dev)
+    B, n, nnz = w.batch, w.A.n, w.A.nnz
+    loop = {"auto": sla.SLA_LOOP_AUTO, "cluster": sla.SLA_LOOP_CLUSTER, "resident": sla.SLA_LOOP_RESIDENT,
+            "graph": sla.SLA_LOOP_GRAPH,
+            "host": sla.SLA_LOOP_HOST}[args.loop]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        x, fi, _ = sla.sla_cg_solve_batched(P, vals, b, rtol=w.rtol, maxit=w.maxit, precond=w.precond, loop=loop)
+        e1.record(stream)
+        _, _, ai = sla.sla_cg_adjoint_batched(P, vals, x, g, rtol=w.rtol, maxit=w.maxit, precond=w.precond,
+                                              loop=loop)
+        e2.record(stream)
+        return e0, e1, e2, fi, ai
+
+    for _ in range(args.warmup):
+        flush_l2(flush)
+        step()
+    torch.cuda.synchronize()
+    launches0 = sla.sla_launch_count()
+    recs = []
+    with ClockSampler(local_rank_of(dev)) as clk:
+        for _ in range(args.steps):
+            flush_l2(flush)
+            recs.append(step())
+        torch.cuda.synchronize()
+    launches = sla.sla_launch_count() - launches0
+    fwd_ms = [r[0].elapsed_time(r[1]) for r in recs]
+    adj_ms = [r[1].elapsed_time(r[2]) for r in recs]
+    it_f = [sum(i.iters for i in r[3]) for r in recs]
+    it_a = [sum(i.iters for i in r[4]) for r in recs]
+    tot_s = (sum(fwd_ms) + sum(adj_ms)) / 1e3
+    s_v = 4 if dt == torch.float32 else 8
+    Bi_sys = nnz * s_v + 9 * n * s_v  # per system-iteration; the shared pattern is read once per iteration
+    peak, peak_kind = measured_peaks()
+    max_it = [max(i.iters for i in r[3]) for r in recs]
+    # bytes of one batched iteration (all systems): B values+vectors, one pattern read
+    Bi_batch = B * Bi_sys + nnz * 4 + (n + 1) * 4
+    achieved = Bi_batch * sum(max_it) / (sum(fwd_ms) / 1e3) / 1e9
+    return {
+        "metric": METRIC, "value": (sum(it_f) + sum(it_a)) / tot_s, "unit": "system-iters/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": (sum(fwd_ms) + sum(adj_ms)) / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32" if s_v == 4 else "f64",
+        "data": "synthetic (seeded generators; no dataset on the pages)",
+        "config": {"workload": w.name, "n": n, "nnz": nnz, "batch": B, "rtol": w.rtol, "loop": args.loop,
+                   "step": "batched forward CG + batched adjoint"},
+        "iters_forward_max": statistics.mean(max_it), "time_to_tolerance_ms": statistics.mean(fwd_ms),
+        "adjoint_ms": statistics.mean(adj_ms),
+        "roofline": {"kernel": "batched CG iteration", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind, "bytes_per_iter": Bi_batch,
+                     "traffic": None},
+        "gpu_launches": int(launches), "clocks": clk.summary(),
+    }
+
+
+def local_rank_of(dev):
+    return dev.index if dev.index is not None else 0
 
 
 def run_e2e(args, w, dev, precond, sla, torch):
@@ -375,7 +448,7 @@ def main():
     ap.add_argument("--ref-iters", type=int, default=100)
     ap.add_argument("--grid-m", type=int, default=0,
                     help="override the grid side m of the chosen workload (smaller cases for profiling)")
-    ap.add_argument("--loop", choices=["auto", "resident", "graph", "host"], default="auto",
+    ap.add_argument("--loop", choices=["auto", "cluster", "resident", "graph", "host"], default="auto",
                     help="auto (default): resident kernel when the system fits on chip, else graph; "
                          "host: host-driven loop, e.g. for per-kernel ncu")
     args = ap.parse_args()

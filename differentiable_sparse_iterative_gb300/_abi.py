@@ -12,7 +12,7 @@ SLA_WORKSPACE_TOO_SMALL, SLA_TIMEOUT, SLA_CUDA_ERROR = 6, 7, 8
 SLA_F32, SLA_F64 = 0, 1
 SLA_I32, SLA_I64 = 0, 1
 SLA_PRECOND_NONE, SLA_PRECOND_JACOBI = 0, 1
-SLA_LOOP_AUTO, SLA_LOOP_HOST, SLA_LOOP_GRAPH, SLA_LOOP_RESIDENT = 0, 1, 2, 3
+SLA_LOOP_AUTO, SLA_LOOP_HOST, SLA_LOOP_GRAPH, SLA_LOOP_RESIDENT, SLA_LOOP_CLUSTER = 0, 1, 2, 3, 4
 
 # every symbol include/sla.h declares
 EXPORTS = [

@@ -200,7 +200,7 @@ sla_status check_opts(const sla_cg_opts *o) {
   if (o->maxit < 0 || o->maxit > ((int64_t)1 << 40)) return SLA_INVALID_ARG;
   if (o->precond != SLA_PRECOND_NONE && o->precond != SLA_PRECOND_JACOBI) return SLA_INVALID_ARG;
   if (o->unroll < 0 || o->unroll > 64) return SLA_INVALID_ARG;
-  if (o->loop < SLA_LOOP_AUTO || o->loop > SLA_LOOP_RESIDENT) return SLA_INVALID_ARG;
+  if (o->loop < SLA_LOOP_AUTO || o->loop > SLA_LOOP_CLUSTER) return SLA_INVALID_ARG;
   if (o->reserved != 0) return SLA_INVALID_ARG;
   return SLA_OK;
 }

@@ -845,17 +845,24 @@ sla_status run_cg_host_loop(Prob<V, I> P, const Launch &Lc, int unroll, cudaStre
 
 }  // namespace
 
-// Resident persistent kernel (sla_resident.cu).
+// Resident persistent kernel and cluster-resident kernel (sla_resident.cu).
 template <typename V, typename I, bool JAC>
 sla_status run_resident(Prob<V, I> P, cudaStream_t stream, sla_cg_info *info);
+template <typename V, typename I, bool JAC>
+sla_status run_cluster(Prob<V, I> P, int64_t batch, cudaStream_t stream, sla_cg_info *info);
 
 namespace {
 
 template <typename V, typename I, bool JAC>
 sla_status run_cg(Prob<V, I> P, int unroll, int loop, cudaStream_t stream, sla_cg_info *info, int64_t batch) {
-  if (loop == SLA_LOOP_RESIDENT ||
-      (loop == SLA_LOOP_AUTO && resident_fits(P.n, batch, sizeof(V) == 8 ? SLA_F64 : SLA_F32,
-                                              JAC ? SLA_PRECOND_JACOBI : SLA_PRECOND_NONE, P.maxit)))
+  const int dt = sizeof(V) == 8 ? SLA_F64 : SLA_F32;
+  const int pc = JAC ? SLA_PRECOND_JACOBI : SLA_PRECOND_NONE;
+  if (loop == SLA_LOOP_CLUSTER) return run_cluster<V, I, JAC>(P, batch, stream, info);
+  if (loop == SLA_LOOP_AUTO && cluster_fits(P.n, batch, dt, pc)) {
+    const sla_status st = run_cluster<V, I, JAC>(P, batch, stream, info);
+    if (st != SLA_INVALID_ARG) return st;  // else the cluster could not be placed: next option
+  }
+  if (loop == SLA_LOOP_RESIDENT || (loop == SLA_LOOP_AUTO && resident_fits(P.n, batch, dt, pc, P.maxit)))
     return run_resident<V, I, JAC>(P, stream, info);
   const DeviceInfo di = device_info();
   Launch Lc;

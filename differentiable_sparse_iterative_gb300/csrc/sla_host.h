@@ -29,6 +29,9 @@ size_t workspace_bytes(int64_t n, int64_t batch, int dtype, int precond);
 // True when one system of n unknowns fits the resident (shared-memory) CG kernel on this device.
 bool resident_fits(int64_t n, int64_t batch, int dtype, int precond, int64_t maxit);
 
+// True when every system of a batch fits one thread-block cluster (cluster-resident CG kernel).
+bool cluster_fits(int64_t n, int64_t batch, int dtype, int precond);
+
 // grad_values[s][k] = -lambda_s[row(k)] * x_s[col(k)] for `batch` systems (asynchronous).
 sla_status grad_values_entry(const sla_csr *A, int64_t batch, const void *lambda, const void *x, void *gv,
                              cudaStream_t st);

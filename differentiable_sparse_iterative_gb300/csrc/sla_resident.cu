@@ -15,6 +15,7 @@
 // block adds the G block sums in the same fixed order, so all blocks hold bit-identical
 // scalars and take the same branch.  The launch is cooperative (all blocks co-resident);
 // each barrier wait is bounded and ends the solve with SLA_TIMEOUT if it ever expires.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -509,6 +510,320 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
   }
 }
 
+// ---------------------------------------------------------------- cluster-resident kernel
+//
+// One thread-block cluster of C CTAs (C <= 16) solves one system; a batch is a grid of clusters.
+// CTA j of a cluster keeps x, r, p, q (and 1/diag) of its row chunk in shared memory for the whole
+// solve.  p of rows owned by a partner CTA is read straight from the partner's shared memory
+// (distributed shared memory), so nothing is recomputed and nothing goes through global memory
+// during the iteration except the matrix stream.  The three dependencies of an iteration (p_k of
+// the partners, p.q, r.r) are hardware cluster barriers; each all-reduce adds the C block sums in
+// rank order in every CTA, so all CTAs of a cluster hold bit-identical scalars.
+namespace cgs = cooperative_groups;
+constexpr int kClBlock = 256;
+constexpr int kClMax = 16;
+constexpr size_t kClSmemMax = 110 * 1024;  // dynamic shared memory a cluster CTA may use
+
+// Sum of the C partners' value slot[q] (read through distributed shared memory), for warp 0:
+// lane j reads partner j, then a fixed shuffle tree; every CTA of the cluster obtains the same
+// bits.  Result valid in lane 0.
+template <int NQ>
+__device__ __forceinline__ void cluster_sum(cgs::cluster_group &cl, double *slot, int C, double (&out)[NQ]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    double v = 0.0;
+    if (lane < C) v = cl.map_shared_rank(slot, lane)[q];
+    out[q] = warp_sum(v);
+  }
+}
+
+template <typename V, typename I, bool JAC, int CB>
+__global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, int mcap) {
+  cgs::cluster_group cl = cgs::this_cluster();
+  const int rank = (int)cl.block_rank();
+  const int sys = (int)(blockIdx.x / (unsigned)C);
+  const int tid = threadIdx.x;
+  extern __shared__ __align__(16) unsigned char smem_cl[];
+  V *sx = reinterpret_cast<V *>(smem_cl);
+  V *sr = sx + cap;
+  V *sp = sr + cap;
+  V *sq = sp + cap;
+  V *sd = JAC ? sq + cap : nullptr;
+  // optional copy of the CTA's CSR slice (mcap > 0): row offsets, columns, values
+  int32_t *s_ro = reinterpret_cast<int32_t *>(sq + cap + (JAC ? cap : 0));
+  int32_t *s_ci = s_ro + ((cap + 1 + 3) & ~3);  // padded so the values below stay 16-byte aligned
+  V *s_val = reinterpret_cast<V *>(s_ci + ((mcap + 3) & ~3));
+  __shared__ double s_part[2][5];  // [0]: setup sums, then r.r / r.z; [1]: p.q (partners read these)
+  __shared__ V *s_peer[kClMax];    // partners' p arrays in distributed shared memory
+  __shared__ ResScalars S;
+  __shared__ int s_pending;
+
+  const int64_t n = P.n;
+  auto start_of = [&](int j) { return n * j / C; };
+  const int64_t c0 = start_of(rank), c1 = start_of(rank + 1);
+  const int len = (int)(c1 - c0);
+  const int64_t vo = (int64_t)sys * n;
+  const V *__restrict__ val = P.val + (int64_t)sys * P.val_stride;
+  const I *__restrict__ rp = P.rp;
+  const int32_t *__restrict__ ci = P.ci;
+  const V *b = P.b + vo;
+  const V *x0 = P.x0 ? P.x0 + vo : nullptr;
+  V *xg = P.x + vo;
+  double *hist = P.history ? P.history + (size_t)sys * (size_t)(P.maxit + 1) : nullptr;
+  Ctl *Cs = P.ctl + sys;
+  Glob *glob = P.glob;
+  if (tid < C) s_peer[tid] = cl.map_shared_rank(sp, tid);
+  if (blockIdx.x == 0 && tid == 0) atomicAdd(&glob->kernels, 1ull);
+
+  // ---- setup
+  double acc5[5] = {0.0, 0.0, 0.0, 0.0, 0.0};
+  for (int li = tid; li < len; li += CB) {
+    const int64_t i = c0 + li;
+    int64_t e0, e1;
+    row_range(rp, i, P.nnz, e0, e1, &glob->bad_csr);
+    const V bi = b[i];
+    V ri = bi;
+    if (x0) {
+      V s_ = V(0);
+      for (int64_t e = e0; e < e1; ++e) {
+        const int32_t c = ci[e];
+        if (col_ok(c, (int32_t)n, &glob->bad_csr)) s_ = fmav<V>(val[e], x0[c], s_);
+      }
+      ri = bi - s_;
+      sx[li] = x0[i];
+    } else {
+      sx[li] = V(0);
+    }
+    sr[li] = ri;
+    acc5[0] = fma((double)bi, (double)bi, acc5[0]);
+    acc5[1] = fma((double)ri, (double)ri, acc5[1]);
+    if (JAC) {
+      V d = V(0);
+      for (int64_t e = e0; e < e1; ++e)
+        if (ci[e] == (int32_t)i) d = val[e];
+      if (!isfinite((double)d)) acc5[3] += 1.0;
+      else if (!(d > V(0))) acc5[4] += 1.0;
+      const V di = V(1) / d;
+      sd[li] = di;
+      acc5[2] = fma((double)ri, (double)(di * ri), acc5[2]);
+    }
+  }
+  // the matrix does not change during the solve: keep the CTA's slice on chip when it fits
+  const int64_t m_lo = len > 0 ? (int64_t)rp[c0] : 0, m_hi = len > 0 ? (int64_t)rp[c1] : 0;
+  const bool mstaged = mcap > 0 && m_lo >= 0 && m_hi >= m_lo && m_hi <= P.nnz && (m_hi - m_lo) <= mcap;
+  if (mstaged) {
+    for (int li = tid; li <= len; li += CB) s_ro[li] = (int32_t)((int64_t)rp[c0 + li] - m_lo);
+    for (int64_t e = m_lo + tid; e < m_hi; e += CB) {
+      s_ci[e - m_lo] = ci[e];
+      s_val[e - m_lo] = val[e];
+    }
+  }
+  block_sum_n<5, CB>(acc5);
+  if (tid == 0)
+    for (int q = 0; q < 5; ++q) s_part[0][q] = acc5[q];
+  cl.sync();
+  int status = SLA_NOT_CONVERGED, pending = 0;
+  int64_t k = 0;
+  double rel = 0.0, rr_last = -1.0;
+  double t5[5];
+  if (tid < 32) cluster_sum<5>(cl, &s_part[0][0], C, t5);
+  if (tid == 0) {
+    const double nb = sqrt(t5[0]);
+    int go = 0;
+    double rho = 0.0;
+    if (!isfinite(nb)) {
+      status = SLA_NONFINITE;
+    } else if (nb == 0.0) {
+      status = SLA_OK;
+      pending = 2;
+      if (rank == 0 && hist) hist[0] = 0.0;
+    } else if (JAC && t5[3] > 0.0) {
+      status = SLA_NONFINITE;
+    } else if (JAC && t5[4] > 0.0) {
+      status = SLA_BREAKDOWN;
+    } else {
+      const double rr = t5[1];
+      rel = sqrt(rr) / nb;
+      if (rank == 0 && hist) hist[0] = rel;
+      if (!isfinite(rr)) status = SLA_NONFINITE;
+      else if (sqrt(rr) <= P.rtol * nb) status = SLA_OK;
+      else if (P.maxit == 0) status = SLA_NOT_CONVERGED;
+      else {
+        rho = JAC ? t5[2] : rr;
+        go = 1;
+      }
+    }
+    S.go = go;
+    S.alpha = S.beta = S.alpha_prev = 0.0;
+    S.rho = rho;
+    S.nb = nb;
+    const double tol = P.rtol * nb, e4 = 4.0 * 2.220446049250313e-16;
+    const double t1 = tol * (1.0 - e4), t2 = tol * (1.0 + e4);
+    S.tol = tol;
+    S.rr_lo = t1 * t1;
+    S.rr_hi = t2 * t2;
+  }
+  __syncthreads();
+
+  // ---- iterations
+  SLA_PHASE_INIT();
+  while (S.go) {
+    const bool first = (k == 0);
+    const V vb = (V)S.beta, va_prev = (V)S.alpha_prev;
+    for (int li = tid; li < len; li += CB) {
+      const V rl = sr[li];
+      const V z = JAC ? sd[li] * rl : rl;
+      V pv = z;
+      if (!first) {
+        const V po = sp[li];
+        pv = fmav<V>(vb, po, z);
+        sx[li] = fmav<V>(va_prev, po, sx[li]);
+      }
+      sp[li] = pv;
+    }
+    cl.sync();  // every CTA's p_k is in place
+    SLA_PHASE(0);
+    V part = V(0);
+    double pqd = 0.0;
+    int cnt = 0;
+    for (int li = tid; li < len; li += CB) {
+      const int64_t i = c0 + li;
+      int64_t e0, e1;
+      if (mstaged) {
+        e0 = s_ro[li];
+        e1 = s_ro[li + 1];
+        if (e1 < e0) e1 = e0;
+      } else {
+        row_range(rp, i, P.nnz, e0, e1, &glob->bad_csr);
+      }
+      V acc = V(0);
+      for (int64_t e = e0; e < e1; ++e) {
+        const int32_t c = mstaged ? s_ci[e] : __ldg(ci + e);
+        const V v = mstaged ? s_val[e] : __ldg(val + e);
+        const uint32_t off = (uint32_t)((int64_t)c - c0);
+        V pc;
+        if (off < (uint32_t)len) {
+          pc = sp[off];
+        } else if (col_ok(c, (int32_t)n, &glob->bad_csr)) {
+          int j = (int)((int64_t)c * C / n);
+          if (j + 1 < C && (int64_t)c >= start_of(j + 1)) ++j;
+          pc = s_peer[j][c - start_of(j)];
+        } else {
+          pc = V(0);
+        }
+        acc = fmav<V>(v, pc, acc);
+      }
+      sq[li] = acc;
+      part = fmav<V>(sp[li], acc, part);
+      if constexpr (sizeof(V) == 4) {
+        if (++cnt == 8) {
+          pqd += (double)part;
+          part = V(0);
+          cnt = 0;
+        }
+      }
+    }
+    SLA_PHASE(1);
+    double v1[1] = {pqd + (double)part};
+    block_sum_n<1, CB>(v1);
+    if (tid == 0) s_part[1][0] = v1[0];
+    cl.sync();
+    double pqv[1];
+    if (tid < 32) cluster_sum<1>(cl, &s_part[1][0], C, pqv);
+    if (tid == 0) {
+      const double pq = pqv[0];
+      int go = 1;
+      if (!isfinite(pq)) { status = SLA_NONFINITE; go = 0; }
+      else if (!(pq > 0.0)) { status = SLA_BREAKDOWN; go = 0; }
+      else S.alpha = S.rho / pq;
+      S.go = go;
+    }
+    __syncthreads();
+    SLA_PHASE(2);
+    if (!S.go) break;
+    const V va = (V)S.alpha;
+    double acc2[2] = {0.0, 0.0};
+    V rr_t = V(0), rz_t = V(0);
+    int cnt = 0;
+    for (int li = tid; li < len; li += CB) {
+      const V ri = fmav<V>(-va, sq[li], sr[li]);
+      sr[li] = ri;
+      rr_t = fmav<V>(ri, ri, rr_t);
+      if (JAC) rz_t = fmav<V>(ri, sd[li] * ri, rz_t);
+      if constexpr (sizeof(V) == 4) {
+        if (++cnt == 8) {
+          acc2[0] += (double)rr_t;
+          acc2[1] += (double)rz_t;
+          rr_t = rz_t = V(0);
+          cnt = 0;
+        }
+      }
+    }
+    acc2[0] += (double)rr_t;
+    acc2[1] += (double)rz_t;
+    SLA_PHASE(3);
+    block_sum_n<2, CB>(acc2);
+    if (tid == 0) {
+      s_part[0][0] = acc2[0];
+      s_part[0][1] = acc2[1];
+    }
+    cl.sync();
+    ++k;
+    double t2[2];
+    if (tid < 32) cluster_sum<2>(cl, &s_part[0][0], C, t2);
+    if (tid == 0) {
+      const double rrt = t2[0], rzt = t2[1];
+      rr_last = rrt;
+      if (rank == 0 && hist) hist[k] = rrt;  // turned into ||r|| / ||b|| after the loop
+      int go = 0;
+      pending = 1;
+      if (!isfinite(rrt)) status = SLA_NONFINITE;
+      else if (stop_test(rrt, S)) status = SLA_OK;
+      else if (k >= P.maxit) status = SLA_NOT_CONVERGED;
+      else {
+        const double rho_new = JAC ? rzt : rrt;
+        S.beta = rho_new / S.rho;
+        S.rho = rho_new;
+        S.alpha_prev = S.alpha;
+        pending = 0;
+        go = 1;
+      }
+      S.go = go;
+    }
+    __syncthreads();
+    SLA_PHASE(4);
+  }
+  SLA_PHASE_STORE(k);
+
+  // ---- finish
+  if (tid == 0) s_pending = pending;
+  __syncthreads();
+  const V va = (V)S.alpha;
+  for (int li = tid; li < len; li += CB) {
+    V xv = sx[li];
+    if (s_pending == 1) xv = fmav<V>(va, sp[li], xv);
+    else if (s_pending == 2) xv = V(0);
+    xg[c0 + li] = xv;
+  }
+  if (rank == 0 && hist && S.nb > 0.0) {
+    const double nbs = S.nb;
+    for (int64_t j = 1 + tid; j <= k; j += CB) hist[j] = sqrt(hist[j]) / nbs;
+  }
+  if (rank == 0 && tid == 0) {
+    if (rr_last >= 0.0 || rr_last != rr_last) rel = sqrt(rr_last) / S.nb;
+    Cs->k = k;
+    Cs->status = status;
+    Cs->rel_res = rel;
+    Cs->nb = S.nb;
+    Cs->alpha = S.alpha;
+    Cs->beta = S.beta;
+    Cs->rho = S.rho;
+    Cs->done = 1;
+  }
+  cl.sync();  // no CTA leaves while a partner may still read its shared memory
+}
+
 struct ResidentLimits {
   int sms = 0;
   int max_smem = 0;
@@ -553,6 +868,126 @@ bool resident_fits(int64_t n, int64_t batch, int dtype, int precond, int64_t max
   size_t smem;
   resident_shape(n, dtype == SLA_F64 ? 8 : 4, precond == SLA_PRECOND_JACOBI, limits(), maxit, G, cap, smem);
   return G > 0;
+}
+
+// Cluster shape for `batch` systems of n unknowns: C CTAs per system, rows per CTA (cap), threads
+// per CTA, shared memory, and how many CSR entries a CTA may keep on chip (mcap, 0: none).  Every
+// cluster runs a whole solve, so all of them must be resident at once: candidates are checked
+// with the occupancy API and the first that fits in one wave is taken.
+struct ClusterShape {
+  int C = 0, cap = 0, block = 0, mcap = 0;
+  size_t smem = 0;
+};
+
+template <typename V, typename I, bool JAC>
+ClusterShape cluster_shape_for(int64_t n, int64_t batch, int64_t nnz) {
+  ClusterShape best;
+  const ResidentLimits L = limits();
+  if (n <= 0 || batch < 1 || L.sms <= 0 || batch > 65535) return best;
+  const int nvec = JAC ? 5 : 4;
+  static std::atomic<int> attr_set{0};
+  if (!attr_set.load()) {
+    for (void *f : {(void *)cg_cluster<V, I, JAC, 1024>, (void *)cg_cluster<V, I, JAC, 512>,
+                    (void *)cg_cluster<V, I, JAC, kClBlock>}) {
+      if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClSmemMax) != cudaSuccess ||
+          cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();
+        return best;
+      }
+    }
+    attr_set.store(1);
+  }
+  int c0 = 1;
+  while (c0 < kClMax && (int64_t)c0 * batch < L.sms) c0 *= 2;
+  for (int c = c0; c <= kClMax; c *= 2) {
+    if (c > n) break;
+    const int64_t rows = (n + c - 1) / c;
+    const size_t vec_bytes = (size_t)rows * nvec * sizeof(V);
+    if (vec_bytes > kClSmemMax) continue;
+    // the CSR slice on chip if it fits beside the vectors (average row length plus slack)
+    const int64_t ment = (nnz * rows) / std::max<int64_t>(n, 1) + 64;
+    const size_t mat_bytes = (size_t)((rows + 1 + 3) & ~3) * 4 + (size_t)((ment + 3) & ~3) * 4 + (size_t)ment * sizeof(V);
+    const bool keep_mat = vec_bytes + mat_bytes <= kClSmemMax;
+    const size_t smem = vec_bytes + (keep_mat ? mat_bytes : 0) + 16;
+    for (int block : {rows >= 2048 ? 512 : kClBlock, kClBlock}) {
+      void *fn = block == 512 ? (void *)cg_cluster<V, I, JAC, 512> : (void *)cg_cluster<V, I, JAC, kClBlock>;
+      cudaLaunchConfig_t cfg;
+      memset(&cfg, 0, sizeof(cfg));
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = (unsigned)c;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3((unsigned)(batch * c));
+      cfg.blockDim = dim3(block);
+      cfg.dynamicSmemBytes = smem;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int active = 0;
+      if (cudaOccupancyMaxActiveClusters(&active, fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        continue;
+      }
+      if (active >= batch) {
+        best.C = c;
+        best.cap = (int)rows;
+        best.block = block;
+        best.mcap = keep_mat ? (int)ment : 0;
+        best.smem = smem;
+        return best;
+      }
+    }
+  }
+  return best;
+}
+
+template <typename V, typename I, bool JAC>
+sla_status run_cluster(Prob<V, I> P, int64_t batch, cudaStream_t stream, sla_cg_info *info) {
+  const ClusterShape sh = cluster_shape_for<V, I, JAC>(P.n, batch, P.nnz);
+  if (sh.C == 0) return SLA_INVALID_ARG;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)sh.C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(batch * sh.C));
+  cfg.blockDim = dim3(sh.block);
+  cfg.dynamicSmemBytes = sh.smem;
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaMemsetAsync(P.glob, 0, sizeof(Glob), stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(P.ctl, 0, sizeof(Ctl) * (size_t)batch, stream);
+  if (e != cudaSuccess) return fail(e);
+  if (sh.block == 512)
+    e = cudaLaunchKernelEx(&cfg, cg_cluster<V, I, JAC, 512>, P, sh.C, sh.cap, sh.mcap);
+  else
+    e = cudaLaunchKernelEx(&cfg, cg_cluster<V, I, JAC, kClBlock>, P, sh.C, sh.cap, sh.mcap);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(e);
+  if (!info) return SLA_OK;
+  return read_info(P.ctl, P.glob, batch, stream, info);
+}
+
+#define SLA_INSTANTIATE_CLUSTER(V, I, J) \
+  template sla_status run_cluster<V, I, J>(Prob<V, I>, int64_t, cudaStream_t, sla_cg_info *);
+SLA_INSTANTIATE_CLUSTER(double, int32_t, false)
+SLA_INSTANTIATE_CLUSTER(double, int32_t, true)
+SLA_INSTANTIATE_CLUSTER(double, int64_t, false)
+SLA_INSTANTIATE_CLUSTER(double, int64_t, true)
+SLA_INSTANTIATE_CLUSTER(float, int32_t, false)
+SLA_INSTANTIATE_CLUSTER(float, int32_t, true)
+SLA_INSTANTIATE_CLUSTER(float, int64_t, false)
+SLA_INSTANTIATE_CLUSTER(float, int64_t, true)
+
+bool cluster_fits(int64_t n, int64_t batch, int dtype, int precond) {
+  // cheap necessary condition; run_cluster makes the final (occupancy) decision
+  if (n <= 0 || batch < 1 || batch > 65535) return false;
+  const int64_t rows = (n + kClMax - 1) / kClMax;
+  const size_t vec_bytes = (size_t)rows * (precond == SLA_PRECOND_JACOBI ? 5 : 4) * (dtype == SLA_F64 ? 8 : 4);
+  return vec_bytes <= kClSmemMax;
 }
 
 template <typename V, typename I, bool JAC>

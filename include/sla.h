@@ -91,16 +91,21 @@ typedef struct sla_csr {
 } sla_csr;
 
 typedef enum sla_loop {
-  SLA_LOOP_AUTO = 0,      /* RESIDENT when one system fits on chip, else GRAPH */
+  SLA_LOOP_AUTO = 0,      /* CLUSTER when each system fits one thread-block cluster, else RESIDENT
+                             when one system fits on chip, else GRAPH */
   SLA_LOOP_HOST = 1,      /* the host launches the streaming kernels directly and reads the device
                              status every `unroll` iterations (for profilers that cannot see inside
                              conditional graphs, and for drivers without conditional nodes) */
   SLA_LOOP_GRAPH = 2,     /* streaming kernels in one CUDA graph per solve; the loop is a device-side
                              conditional WHILE node */
-  SLA_LOOP_RESIDENT = 3   /* one persistent cooperative kernel per solve, each SM keeping its rows'
+  SLA_LOOP_RESIDENT = 3,  /* one persistent cooperative kernel per solve, each SM keeping its rows'
                              vectors in shared memory (one system whose 1/#SM share of x, r, p, q
                              [, 1/diag] fits one SM's shared memory: about 1.4M fp64 unknowns on
                              GB300); SLA_INVALID_ARG when it does not fit */
+  SLA_LOOP_CLUSTER = 4    /* one thread-block cluster (up to 16 CTAs) per system, all vectors in
+                             shared memory, partner rows read through distributed shared memory,
+                             hardware cluster barriers; any batch whose systems are small enough
+                             (about 50K fp64 / 100K fp32 unknowns); SLA_INVALID_ARG otherwise */
 } sla_loop;
 
 typedef struct sla_cg_opts {

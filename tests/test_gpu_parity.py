@@ -52,7 +52,7 @@ def test_spmv_exact_integers():
     assert np.array_equal(y, oracle.spmv(A.row_ptr, A.col_idx, A.values, x))
 
 
-LOOPS = {"auto": 0, "graph": 2}  # auto = the resident kernel for systems that fit on chip
+LOOPS = {"auto": 0, "resident": 3, "graph": 2}  # auto = the cluster kernel for these sizes
 
 
 @pytest.mark.parametrize("loop", list(LOOPS))
@@ -136,17 +136,19 @@ def test_batched_f32(m, batch, precond):
 
 
 def test_batched_f64_equals_single_systems():
-    # each system of a batched solve equals the single-system solve of that system
+    # each system of a batched solve equals the single-system solve of that system (same loop driver;
+    # the graph path partitions rows by batch size, so agreement there is to rounding)
     w = config3(m=20, batch=4)
     v64 = w.values_b.astype(np.float64)
     P = to_dev(w.A)
-    xb, infos, _ = sla.sla_cg_solve_batched(P, t(v64), t(w.b.astype(np.float64)), rtol=1e-10, maxit=5000)
-    for s in range(4):
-        As = sla.CSRMatrix(P.row_ptr, P.col_idx, t(v64[s]))
-        xs, info, _ = sla.sla_cg_solve(As, t(w.b[s].astype(np.float64)), rtol=1e-10, maxit=5000,
-                                       loop=sla.SLA_LOOP_GRAPH)
-        assert info.iters == infos[s].iters
-        assert rel(xb[s].cpu().numpy(), xs.cpu().numpy()) <= 1e-12
+    for loop in (sla.SLA_LOOP_GRAPH, sla.SLA_LOOP_CLUSTER):
+        xb, infos, _ = sla.sla_cg_solve_batched(P, t(v64), t(w.b.astype(np.float64)), rtol=1e-10, maxit=5000,
+                                                loop=loop)
+        for s in range(4):
+            As = sla.CSRMatrix(P.row_ptr, P.col_idx, t(v64[s]))
+            xs, info, _ = sla.sla_cg_solve(As, t(w.b[s].astype(np.float64)), rtol=1e-10, maxit=5000, loop=loop)
+            assert info.iters == infos[s].iters
+            assert rel(xb[s].cpu().numpy(), xs.cpu().numpy()) <= 1e-12
 
 
 # ----------------------------------------------------------------------------- edge cases
@@ -362,3 +364,19 @@ def test_tma_spmv_step_equals_plain(tmp_path):
         subprocess.run([sys.executable, str(script), root, str(outp)], check=True, env=env, timeout=600)
         res[mode] = np.load(outp)
     assert rel(res["tma"], res["plain"]) <= 1e-11
+
+
+@pytest.mark.parametrize("precond", [0, 1])
+def test_cluster_matches_graph_batched_f64(precond):
+    w = config3(m=48, batch=9)
+    v64 = t(w.values_b.astype(np.float64))
+    b64 = t(w.b.astype(np.float64))
+    P = to_dev(w.A)
+    xc, ic, _ = sla.sla_cg_solve_batched(P, v64, b64, rtol=1e-10, maxit=5000, precond=precond,
+                                         loop=sla.SLA_LOOP_CLUSTER)
+    xg, ig, _ = sla.sla_cg_solve_batched(P, v64, b64, rtol=1e-10, maxit=5000, precond=precond,
+                                         loop=sla.SLA_LOOP_GRAPH)
+    for s in range(9):
+        assert ic[s].status == ig[s].status == 0 and abs(ic[s].iters - ig[s].iters) <= 1
+        assert rel(xc[s].cpu().numpy(), xg[s].cpu().numpy()) <= X_TOL_F64
+    assert ic[0].kernels == 1  # the whole batched solve is one launch
