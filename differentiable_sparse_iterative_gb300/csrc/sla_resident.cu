@@ -745,7 +745,7 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
     const V va = (V)S.alpha;
     double acc2[2] = {0.0, 0.0};
     V rr_t = V(0), rz_t = V(0);
-    int cnt = 0;
+    cnt = 0;
     for (int li = tid; li < len; li += CB) {
       const V ri = fmav<V>(-va, sq[li], sr[li]);
       sr[li] = ri;
