@@ -56,6 +56,14 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def fp64_peak_tflops(clocks=None):
+    """fp64 FMA peak of GB300: 152 SMs x 2 FMA per clock (1.25 TFLOP/s nominal) at the max SM clock."""
+    mhz = 2070.0
+    if clocks and clocks.get("sm_max_mhz"):
+        mhz = float(clocks["sm_max_mhz"])
+    return 152 * 2 * 2 * mhz * 1e6 / 1e12
+
+
 def csrc_sha256():
     import glob
     import hashlib
@@ -224,6 +232,15 @@ def run_ours(args, rank, world, local_rank):
     achieved = Bi * sum(iters_f) / fwd_s / 1e9
     tr = profiled_traffic(args.config)
     clocks = clk.summary()
+    path = recs[-1][3].path
+    kernel_name = {"resident": "cg_resident (one persistent cooperative kernel per solve)",
+                   "cluster": "cg_cluster (one thread-block cluster per system)",
+                   "graph": "cg_spmv_step + cg_update_step (CUDA graph loop)",
+                   "host": "cg_spmv_step + cg_update_step (host loop)"}.get(path, path)
+    # fp64 issue roofline: algorithmic fp64 flops of one iteration against 152 SMs x 2 FMA/clk
+    flops_it = 2 * nnz + (13 if jac else 10) * n
+    fp64_peak = fp64_peak_tflops(clocks)
+    fp64_ach = flops_it * sum(iters_f) / fwd_s / 1e12
 
     e2e = None
     if not args.no_e2e:
@@ -244,7 +261,11 @@ def run_ours(args, rank, world, local_rank):
         "status": sorted(status),
         "effective_gbs_step": (Bi * tot_iters + Bg * args.steps) / tot_s / 1e9,
         "peak_mem_mb": peak_mem / 2**20,
-        "roofline": {"kernel": "fused CG iteration (cg_spmv_step + cg_update_step)", "bound": "hbm",
+        "path": path,
+        "fp64": {"achieved_tflops": fp64_ach, "peak_tflops": fp64_peak, "frac": fp64_ach / fp64_peak,
+                 "flops_per_iter": flops_it,
+                 "peak_basis": "152 SMs x 2 fp64 FMA/clock x 2 flops x max SM clock"},
+        "roofline": {"kernel": kernel_name, "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind,
                      "bytes_per_iter": Bi,

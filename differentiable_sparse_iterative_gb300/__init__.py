@@ -57,12 +57,16 @@ class SlaError(RuntimeError):
         self.status = status
 
 
+PATHS = {1: "host", 2: "graph", 3: "resident", 4: "cluster"}
+
+
 @dataclass
 class CGInfo:
     iters: int
     rel_res: float
     status: int
     kernels: int
+    path: str = ""
 
     @property
     def status_name(self) -> str:
@@ -201,7 +205,7 @@ def sla_grad_values(A: CSRMatrix, lam: torch.Tensor, x: torch.Tensor,
 
 
 def _info(ci: _abi.sla_cg_info) -> CGInfo:
-    return CGInfo(int(ci.iters), float(ci.rel_res), int(ci.status), int(ci.kernels))
+    return CGInfo(int(ci.iters), float(ci.rel_res), int(ci.status), int(ci.kernels), PATHS.get(int(ci.path), ""))
 
 
 def sla_cg_solve(A: CSRMatrix, b: torch.Tensor, x0: Optional[torch.Tensor] = None, rtol: float = 1e-8,

@@ -35,7 +35,7 @@ class sla_cg_opts(ctypes.Structure):
 
 class sla_cg_info(ctypes.Structure):
     _fields_ = [("iters", ctypes.c_int64), ("rel_res", ctypes.c_double), ("status", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("kernels", ctypes.c_int64)]
+                ("path", ctypes.c_int32), ("kernels", ctypes.c_int64)]
 
 
 def bind(lib):

@@ -30,6 +30,11 @@ sla_status fail(cudaError_t e) {
 
 void count_launches(uint64_t k) { g_launches.fetch_add(k); }
 
+namespace {
+thread_local int t_last_path = 0;
+}
+void set_last_path(int path) { t_last_path = path; }
+
 sla_status read_info(const Ctl *ctl, const Glob *glob, int64_t batch, cudaStream_t stream, sla_cg_info *info) {
   std::vector<Ctl> hc((size_t)batch);
   Glob hg;
@@ -42,7 +47,7 @@ sla_status read_info(const Ctl *ctl, const Glob *glob, int64_t batch, cudaStream
     info[s].iters = hc[s].k;
     info[s].rel_res = hc[s].rel_res;
     info[s].status = hg.bad_csr ? SLA_BAD_CSR : hc[s].status;
-    info[s].reserved = 0;
+    info[s].path = t_last_path;
     info[s].kernels = (int64_t)hg.kernels;
   }
   return SLA_OK;
@@ -223,7 +228,7 @@ void fill_empty(sla_cg_info *info, int64_t batch) {
     info[s].iters = 0;
     info[s].rel_res = 0.0;
     info[s].status = SLA_OK;
-    info[s].reserved = 0;
+    info[s].path = 0;
     info[s].kernels = 0;
   }
 }

@@ -857,13 +857,20 @@ template <typename V, typename I, bool JAC>
 sla_status run_cg(Prob<V, I> P, int unroll, int loop, cudaStream_t stream, sla_cg_info *info, int64_t batch) {
   const int dt = sizeof(V) == 8 ? SLA_F64 : SLA_F32;
   const int pc = JAC ? SLA_PRECOND_JACOBI : SLA_PRECOND_NONE;
-  if (loop == SLA_LOOP_CLUSTER) return run_cluster<V, I, JAC>(P, batch, stream, info);
+  if (loop == SLA_LOOP_CLUSTER) {
+    set_last_path(SLA_LOOP_CLUSTER);
+    return run_cluster<V, I, JAC>(P, batch, stream, info);
+  }
   if (loop == SLA_LOOP_AUTO && cluster_fits(P.n, batch, dt, pc)) {
+    set_last_path(SLA_LOOP_CLUSTER);
     const sla_status st = run_cluster<V, I, JAC>(P, batch, stream, info);
     if (st != SLA_INVALID_ARG) return st;  // else the cluster could not be placed: next option
   }
-  if (loop == SLA_LOOP_RESIDENT || (loop == SLA_LOOP_AUTO && resident_fits(P.n, batch, dt, pc, P.maxit)))
+  if (loop == SLA_LOOP_RESIDENT || (loop == SLA_LOOP_AUTO && resident_fits(P.n, batch, dt, pc, P.maxit))) {
+    set_last_path(SLA_LOOP_RESIDENT);
     return run_resident<V, I, JAC>(P, stream, info);
+  }
+  set_last_path(loop == SLA_LOOP_HOST ? SLA_LOOP_HOST : SLA_LOOP_GRAPH);
   const DeviceInfo di = device_info();
   Launch Lc;
   // TMA-staged SpMV step when every array it copies from is 16-byte aligned (per system too)

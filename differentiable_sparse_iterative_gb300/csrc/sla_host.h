@@ -14,6 +14,9 @@ sla_status fail(cudaError_t e);
 // Adds host-side kernel launches to the process-wide count.
 void count_launches(uint64_t k);
 
+// The sla_loop the last solve on this thread ran (reported in sla_cg_info.path).
+void set_last_path(int path);
+
 // Copies the per-system control blocks back, synchronises the stream and fills info[batch].
 struct Ctl;
 struct Glob;

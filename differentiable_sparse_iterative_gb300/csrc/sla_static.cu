@@ -90,7 +90,7 @@ extern "C" SLA_API sla_status sla_cg_solve_static(const sla_csr *A, const void *
       info->iters = 0;
       info->rel_res = 0.0;
       info->status = SLA_OK;
-      info->reserved = 0;
+      info->path = 0;
       info->kernels = 0;
     }
     return SLA_OK;
@@ -115,7 +115,7 @@ extern "C" SLA_API sla_status sla_cg_solve_static(const sla_csr *A, const void *
   info->iters = hc.k;
   info->rel_res = hc.rel_res;
   info->status = hg.bad_csr ? SLA_BAD_CSR : hc.status;
-  info->reserved = 0;
+  info->path = SLA_LOOP_HOST;
   info->kernels = (int64_t)hg.kernels;
   return SLA_OK;
 }

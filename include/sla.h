@@ -122,7 +122,7 @@ typedef struct sla_cg_info {
   int64_t iters;          /* completed iterations (products A p inside the loop) */
   double rel_res;         /* ||r|| / ||b|| of the recursive residual at exit (0 when b = 0) */
   int32_t status;         /* sla_status of this system */
-  int32_t reserved;
+  int32_t path;           /* the sla_loop that ran: HOST, GRAPH, RESIDENT or CLUSTER */
   int64_t kernels;        /* kernel executions of this call on the GPU, counted on the device */
 } sla_cg_info;
 
