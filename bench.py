@@ -140,6 +140,22 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def aggregate_over_ranks(seconds, iters, world, device=None):
+    """Whole-job numbers of a replicated run: the slowest rank's time and all ranks' iterations.
+
+    Each rank solves its own system (no exchange on the data path); the job's throughput is the
+    sum of iterations over the max time.  With world == 1 this is the identity."""
+    if world <= 1:
+        return float(seconds), float(iters)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(seconds)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    it = torch.tensor([float(iters)], dtype=torch.float64, device=device)
+    dist.all_reduce(it, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(it.item())
+
+
 def flush_l2(buf):
     buf.zero_()  # a write larger than the 129 MB L2 evicts the previous step's lines
 
@@ -215,14 +231,7 @@ def run_ours(args, rank, world, local_rank):
     tot_iters = sum(iters_f) + sum(iters_a)
     peak_mem = torch.cuda.max_memory_allocated(dev) - mem0
 
-    if world > 1:
-        t = torch.tensor([tot_s], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        it = torch.tensor([float(tot_iters)], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(it, op=torch.distributed.ReduceOp.SUM)
-        tot_s_all, tot_iters_all = float(t.item()), float(it.item())
-    else:
-        tot_s_all, tot_iters_all = tot_s, float(tot_iters)
+    tot_s_all, tot_iters_all = aggregate_over_ranks(tot_s, tot_iters, world, dev)
 
     Bi = b_iter(n, nnz, s_v, s_p, jac)
     Bg = b_gradvalues(n, nnz, s_v, s_p)
