@@ -46,6 +46,23 @@ namespace sla {
 
 // ------------------------------------------------------------------------ kernels
 
+// Launch shape of the two streaming kernels (compile-time; measured on GB300).
+#ifndef SLA_SPMV_MIN_BLOCKS
+#define SLA_SPMV_MIN_BLOCKS 4  // resident blocks per SM the SpMV step is compiled for
+#endif
+#ifndef SLA_SPMV_RPT
+#define SLA_SPMV_RPT 4  // rows per thread per tile of the SpMV step
+#endif
+#ifndef SLA_UPD_ROWS
+#define SLA_UPD_ROWS 8  // rows per thread whose loads the update step issues together
+#endif
+#ifndef SLA_UPD_MIN_BLOCKS
+#define SLA_UPD_MIN_BLOCKS 4
+#endif
+#ifndef SLA_UPD_MIN_BLOCKS_JAC64
+#define SLA_UPD_MIN_BLOCKS_JAC64 3  // fp64 with Jacobi: three loaded vectors per row need more registers
+#endif
+
 template <typename V, typename I>
 __global__ void __launch_bounds__(kBlock) cg_init(Prob<V, I> P) {
   // zero the control blocks; every system starts active
@@ -165,7 +182,7 @@ __device__ __forceinline__ V p_of(const V *__restrict__ zs, const V *__restrict_
 }
 
 template <typename V, typename I, bool JAC, int RPT>
-__global__ void __launch_bounds__(kBlock) cg_spmv_step(Prob<V, I> P, int par) {
+__global__ void __launch_bounds__(kBlock, SLA_SPMV_MIN_BLOCKS) cg_spmv_step(Prob<V, I> P, int par) {
   count_kernel(P.glob);
   const int s = blockIdx.y, bx = blockIdx.x;
   Ctl *C = P.ctl + s;
@@ -186,15 +203,18 @@ __global__ void __launch_bounds__(kBlock) cg_spmv_step(Prob<V, I> P, int par) {
   V *__restrict__ x = P.x + vo;
   __shared__ V sp[kBlock * RPT];
 
-  int64_t c0, c1;
-  chunk_of(P.n, P.G, bx, c0, c1);
-  const int64_t chunk = c1 - c0;
-  const int nsub = (int)((chunk + kBlock * RPT - 1) / (kBlock * RPT));
+  // Band sweep: tile t (T consecutive rows) belongs to block t mod G, so the grid walks the
+  // vector as one band of G tiles.  The off-tile columns of a banded matrix (a grid stencil's
+  // rows i +- m) then fall inside the band just read by other blocks and hit in L2, where
+  // contiguous per-block chunks would re-read them from DRAM.  T is capped so that every block
+  // has a tile when n is small.
+  const int64_t per_block = (P.n + P.G - 1) / P.G;
+  const int64_t T = per_block < (int64_t)kBlock * RPT ? per_block : (int64_t)kBlock * RPT;
+  const int64_t ntiles = (P.n + T - 1) / T;
   double pq = 0.0;
-  int64_t s0 = c0;
-  for (int sub = 0; sub < nsub; ++sub) {
-    const int len = (int)((chunk * (sub + 1)) / nsub - (chunk * sub) / nsub);
-    s0 = c0 + (chunk * sub) / nsub;
+  for (int64_t t = bx; t < ntiles; t += P.G) {
+    const int64_t s0 = t * T;
+    const int len = (int)(P.n - s0 < T ? P.n - s0 : T);
     // loads of the tile's rows first (vectors and row pointers), then p_k, the delayed x update
     V zv[RPT], pov[RPT], xv[RPT];
     I rpa[RPT], rpb[RPT];
@@ -538,7 +558,8 @@ __global__ void __launch_bounds__(kTmaBlock, 2) cg_spmv_step_tma(Prob<V, I> P, i
 }
 
 template <typename V, typename I, bool JAC>
-__global__ void __launch_bounds__(kBlock) cg_update_step(Prob<V, I> P, int par) {
+__global__ void __launch_bounds__(kBlock, (JAC && sizeof(V) == 8) ? SLA_UPD_MIN_BLOCKS_JAC64 : SLA_UPD_MIN_BLOCKS)
+    cg_update_step(Prob<V, I> P, int par) {
   count_kernel(P.glob);
   const int s = blockIdx.y, bx = blockIdx.x;
   Ctl *C = P.ctl + s;
@@ -553,7 +574,7 @@ __global__ void __launch_bounds__(kBlock) cg_update_step(Prob<V, I> P, int par) 
   chunk_of(P.n, P.G, bx, c0, c1);
   double acc[2] = {0.0, 0.0};
   // groups of kUpd rows per thread: all loads of a group first, then the arithmetic
-  constexpr int kUpd = 8;
+  constexpr int kUpd = SLA_UPD_ROWS;
   for (int64_t g0 = c0 + threadIdx.x; g0 < c1; g0 += (int64_t)kUpd * kBlock) {
     V qv[kUpd], rv[kUpd], dv[kUpd];
 #pragma unroll
@@ -659,7 +680,7 @@ __global__ void __launch_bounds__(kBlock) cg_finish(Prob<V, I> P) {
 
 namespace {
 
-constexpr int kRPT = 4;       // rows per thread per tile of the SpMV step
+constexpr int kRPT = SLA_SPMV_RPT;
 constexpr int kDefaultUnroll = 8;
 
 struct GraphEntry {

@@ -4,12 +4,13 @@
 // Hestenes-Stiefel CG with optional Jacobi preconditioning; same recurrences, same stopping
 // rule, same status decisions).
 //
-// GB300 design.  When one system fits on chip (x, r, p, q and, with Jacobi, 1/diag for a
-// 1/G share of the rows in one SM's 227 KB of shared memory), one 1024-thread block per SM
-// owns a contiguous row chunk for the whole solve and its vectors never leave the SM.  Per
-// iteration only the matrix is streamed (from L2 when it fits there) and two values per row
-// are published for the neighbouring blocks: r_k and p_k, from which a block recomputes
-// p_k = z + beta p_{k-1} for the few columns outside its chunk.  The two global dependencies
+// GB300 design.  When one system fits on chip (r, p and, with Jacobi, 1/diag for a 1/G
+// share of the rows in one SM's 227 KB of shared memory), one 1024-thread block per SM owns
+// a contiguous row chunk for the whole solve; r and p never leave the SM, while x and q,
+// each touched once per iteration, live in global memory and stay in L2.  Per iteration the
+// matrix is streamed (from L2 when it fits there) and the values the neighbouring blocks
+// need are published: r_k and p_{k-1}, from which a block recomputes p_k = z + beta p_{k-1}
+// for the few columns outside its chunk.  The two global dependencies
 // of an iteration (alpha needs p.Ap, beta needs r.r) are two grid barriers, each carrying
 // a deterministic all-reduce: every block writes its block sum, and after the barrier every
 // block adds the G block sums in the same fixed order, so all blocks hold bit-identical
