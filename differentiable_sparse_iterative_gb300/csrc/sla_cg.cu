@@ -48,10 +48,10 @@ namespace sla {
 
 // Launch shape of the two streaming kernels (compile-time; measured on GB300).
 #ifndef SLA_SPMV_MIN_BLOCKS
-#define SLA_SPMV_MIN_BLOCKS 4  // resident blocks per SM the SpMV step is compiled for
+#define SLA_SPMV_MIN_BLOCKS 8  // resident blocks per SM the SpMV step is compiled for (a full SM)
 #endif
 #ifndef SLA_SPMV_RPT
-#define SLA_SPMV_RPT 4  // rows per thread per tile of the SpMV step
+#define SLA_SPMV_RPT 2  // rows per thread per tile of the SpMV step
 #endif
 #ifndef SLA_UPD_ROWS
 #define SLA_UPD_ROWS 8  // rows per thread whose loads the update step issues together
