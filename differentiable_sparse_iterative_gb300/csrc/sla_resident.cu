@@ -155,10 +155,21 @@ __device__ __forceinline__ double warp_allsum(double v) {
 template <int NV>
 __device__ __forceinline__ void warp_totals(const double *part, int G, double (&tot)[NV]) {
   const int lane = threadIdx.x & 31;
+  // all loads of a 256-block slab first (one L2 round trip instead of one per 32 blocks), then a
+  // fixed pairwise tree per lane: the order depends only on G, so every block gets the same bits
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
+    const double *pj = part + (size_t)j * kMaxBlocksPerSystem;
     double t = 0.0;
-    for (int b = lane; b < G; b += 32) t += __ldcg(part + (size_t)j * kMaxBlocksPerSystem + b);
+    for (int b0 = 0; b0 < G; b0 += 256) {
+      double v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int b = b0 + lane + 32 * u;
+        v[u] = b < G ? __ldcg(pj + b) : 0.0;
+      }
+      t += ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+    }
     tot[j] = warp_allsum(t);
   }
 }
@@ -524,6 +535,17 @@ namespace cgs = cooperative_groups;
 constexpr int kClBlock = 256;
 constexpr int kClMax = 16;
 constexpr size_t kClSmemMax = 110 * 1024;  // dynamic shared memory a cluster CTA may use
+#ifndef SLA_CLUSTER_ROWS
+#define SLA_CLUSTER_ROWS 1
+#endif
+#ifndef SLA_CLUSTER_ENTRIES
+#define SLA_CLUSTER_ENTRIES 5
+#endif
+#ifndef SLA_CLUSTER_STAGE_RO
+#define SLA_CLUSTER_STAGE_RO 1
+#endif
+constexpr int kClR = SLA_CLUSTER_ROWS;     // rows per thread whose entries the streamed SpMV loads together
+constexpr int kClK = SLA_CLUSTER_ENTRIES;  // entries per row loaded up front (the rest one by one)
 
 // Sum of the C partners' value slot[q] (read through distributed shared memory), for warp 0:
 // lane j reads partner j, then a fixed shuffle tree; every CTA of the cluster obtains the same
@@ -540,7 +562,7 @@ __device__ __forceinline__ void cluster_sum(cgs::cluster_group &cl, double *slot
 }
 
 template <typename V, typename I, bool JAC, int CB>
-__global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, int mcap) {
+__global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, int mcap, int ro_on) {
   cgs::cluster_group cl = cgs::this_cluster();
   const int rank = (int)cl.block_rank();
   const int sys = (int)(blockIdx.x / (unsigned)C);
@@ -551,7 +573,8 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
   V *sp = sr + cap;
   V *sq = sp + cap;
   V *sd = JAC ? sq + cap : nullptr;
-  // optional copy of the CTA's CSR slice (mcap > 0): row offsets, columns, values
+  // optional copy of the CTA's CSR slice (mcap > 0): row offsets, columns, values; or of its row
+  // offsets alone (ro_on)
   int32_t *s_ro = reinterpret_cast<int32_t *>(sq + cap + (JAC ? cap : 0));
   int32_t *s_ci = s_ro + ((cap + 1 + 3) & ~3);  // padded so the values below stay 16-byte aligned
   V *s_val = reinterpret_cast<V *>(s_ci + ((mcap + 3) & ~3));
@@ -612,9 +635,23 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
   }
   // the matrix does not change during the solve: keep the CTA's slice on chip when it fits
   const int64_t m_lo = len > 0 ? (int64_t)rp[c0] : 0, m_hi = len > 0 ? (int64_t)rp[c1] : 0;
-  const bool mstaged = mcap > 0 && m_lo >= 0 && m_hi >= m_lo && m_hi <= P.nnz && (m_hi - m_lo) <= mcap;
+  const bool slice_ok = m_lo >= 0 && m_hi >= m_lo && m_hi <= P.nnz && (m_hi - m_lo) < (int64_t)INT32_MAX;
+  const bool mstaged = mcap > 0 && slice_ok && (m_hi - m_lo) <= mcap;
+  const bool rostaged = mstaged || (ro_on && slice_ok);
+  if (rostaged) {
+    // offsets relative to the slice, clamped into it: a malformed row_ptr is reported and can
+    // never index outside the slice
+    const int64_t mlen = m_hi - m_lo;
+    for (int li = tid; li <= len; li += CB) {
+      int64_t o = (int64_t)rp[c0 + li] - m_lo;
+      if (o < 0 || o > mlen) {
+        atomicOr(&glob->bad_csr, 1u);
+        o = o < 0 ? 0 : mlen;
+      }
+      s_ro[li] = (int32_t)o;
+    }
+  }
   if (mstaged) {
-    for (int li = tid; li <= len; li += CB) s_ro[li] = (int32_t)((int64_t)rp[c0 + li] - m_lo);
     for (int64_t e = m_lo + tid; e < m_hi; e += CB) {
       s_ci[e - m_lo] = ci[e];
       s_val[e - m_lo] = val[e];
@@ -688,33 +725,17 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
     V part = V(0);
     double pqd = 0.0;
     int cnt = 0;
-    for (int li = tid; li < len; li += CB) {
-      const int64_t i = c0 + li;
-      int64_t e0, e1;
-      if (mstaged) {
-        e0 = s_ro[li];
-        e1 = s_ro[li + 1];
-        if (e1 < e0) e1 = e0;
-      } else {
-        row_range(rp, i, P.nnz, e0, e1, &glob->bad_csr);
-      }
-      V acc = V(0);
-      for (int64_t e = e0; e < e1; ++e) {
-        const int32_t c = mstaged ? s_ci[e] : __ldg(ci + e);
-        const V v = mstaged ? s_val[e] : __ldg(val + e);
-        const uint32_t off = (uint32_t)((int64_t)c - c0);
-        V pc;
-        if (off < (uint32_t)len) {
-          pc = sp[off];
-        } else if (col_ok(c, (int32_t)n, &glob->bad_csr)) {
-          int j = (int)((int64_t)c * C / n);
-          if (j + 1 < C && (int64_t)c >= start_of(j + 1)) ++j;
-          pc = s_peer[j][c - start_of(j)];
-        } else {
-          pc = V(0);
-        }
-        acc = fmav<V>(v, pc, acc);
-      }
+    // p_k at column c: own rows from shared memory, a partner's from its shared memory (DSMEM)
+    auto p_at = [&](int32_t c) -> V {
+      const uint32_t off = (uint32_t)((int64_t)c - c0);
+      if (off < (uint32_t)len) return sp[off];
+      if (!col_ok(c, (int32_t)n, &glob->bad_csr)) return V(0);
+      int j = (int)((int64_t)c * C / n);
+      if (j + 1 < C && (int64_t)c >= start_of(j + 1)) ++j;
+      return s_peer[j][c - start_of(j)];
+    };
+    // q_i and the row's share of p.q (fp32 data: p.q summed in fp32 over 8 rows, then in fp64)
+    auto row_done = [&](int li, V acc) {
       sq[li] = acc;
       part = fmav<V>(sp[li], acc, part);
       if constexpr (sizeof(V) == 4) {
@@ -723,6 +744,67 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
           part = V(0);
           cnt = 0;
         }
+      }
+    };
+    if (rostaged && !mstaged) {
+      // matrix streamed from L2/HBM: kClR rows per thread at a time, the first kClK entries of
+      // each loaded together (independent loads in flight instead of one row's chain at a time);
+      // every row still adds its entries in order, so the result is the same as row by row
+      const int32_t *__restrict__ cib = ci + m_lo;
+      const V *__restrict__ vab = val + m_lo;
+      for (int j0 = tid; j0 < len; j0 += kClR * CB) {
+        int32_t eb[kClR], ee[kClR];
+#pragma unroll
+        for (int u = 0; u < kClR; ++u) {
+          const int li = j0 + u * CB;
+          eb[u] = li < len ? s_ro[li] : 0;
+          ee[u] = li < len ? s_ro[li + 1] : 0;
+        }
+        int32_t cc[kClR][kClK];
+        V vv[kClR][kClK];
+#pragma unroll
+        for (int t = 0; t < kClK; ++t)
+#pragma unroll
+          for (int u = 0; u < kClR; ++u) {
+            const int32_t e = eb[u] + t;
+            const bool in = e < ee[u];
+            cc[u][t] = in ? __ldg(cib + e) : 0;
+            vv[u][t] = in ? __ldg(vab + e) : V(0);
+          }
+        V acc[kClR];
+#pragma unroll
+        for (int u = 0; u < kClR; ++u) acc[u] = V(0);
+#pragma unroll
+        for (int t = 0; t < kClK; ++t)
+#pragma unroll
+          for (int u = 0; u < kClR; ++u)
+            if (eb[u] + t < ee[u]) acc[u] = fmav<V>(vv[u][t], p_at(cc[u][t]), acc[u]);
+#pragma unroll
+        for (int u = 0; u < kClR; ++u)
+          for (int32_t e = eb[u] + kClK; e < ee[u]; ++e) acc[u] = fmav<V>(__ldg(vab + e), p_at(__ldg(cib + e)), acc[u]);
+#pragma unroll
+        for (int u = 0; u < kClR; ++u) {
+          const int li = j0 + u * CB;
+          if (li < len) row_done(li, acc[u]);
+        }
+      }
+    } else {
+      for (int li = tid; li < len; li += CB) {
+        int64_t e0, e1;
+        if (mstaged) {
+          e0 = s_ro[li];
+          e1 = s_ro[li + 1];
+          if (e1 < e0) e1 = e0;
+        } else {
+          row_range(rp, c0 + li, P.nnz, e0, e1, &glob->bad_csr);
+        }
+        V acc = V(0);
+        for (int64_t e = e0; e < e1; ++e) {
+          const int32_t c = mstaged ? s_ci[e] : __ldg(ci + e);
+          const V v = mstaged ? s_val[e] : __ldg(val + e);
+          acc = fmav<V>(v, p_at(c), acc);
+        }
+        row_done(li, acc);
       }
     }
     SLA_PHASE(1);
@@ -841,6 +923,7 @@ ResidentLimits limits() {
 
 constexpr size_t kResStaticSmem = 4096;  // reduction scratch and flags of the kernel itself
 
+
 // Blocks and rows per block for the resident kernel, or G = 0 if the system does not fit.
 void resident_shape(int64_t n, size_t vbytes, bool jac, const ResidentLimits &L, int64_t maxit, int &G,
                     int &cap, size_t &smem) {
@@ -876,7 +959,7 @@ bool resident_fits(int64_t n, int64_t batch, int dtype, int precond, int64_t max
 // cluster runs a whole solve, so all of them must be resident at once: candidates are checked
 // with the occupancy API and the first that fits in one wave is taken.
 struct ClusterShape {
-  int C = 0, cap = 0, block = 0, mcap = 0;
+  int C = 0, cap = 0, block = 0, mcap = 0, ro = 0;
   size_t smem = 0;
 };
 
@@ -909,7 +992,10 @@ ClusterShape cluster_shape_for(int64_t n, int64_t batch, int64_t nnz) {
     const int64_t ment = (nnz * rows) / std::max<int64_t>(n, 1) + 64;
     const size_t mat_bytes = (size_t)((rows + 1 + 3) & ~3) * 4 + (size_t)((ment + 3) & ~3) * 4 + (size_t)ment * sizeof(V);
     const bool keep_mat = vec_bytes + mat_bytes <= kClSmemMax;
-    const size_t smem = vec_bytes + (keep_mat ? mat_bytes : 0) + 16;
+    // else the row offsets alone, so the streamed SpMV starts from shared memory
+    const size_t ro_bytes = (size_t)((rows + 1 + 3) & ~3) * 4;
+    const bool keep_ro = SLA_CLUSTER_STAGE_RO && !keep_mat && vec_bytes + ro_bytes + 16 <= kClSmemMax;
+    const size_t smem = vec_bytes + (keep_mat ? mat_bytes : 0) + (keep_ro ? ro_bytes : 0) + 16;
     for (int block : {rows >= 2048 ? 512 : kClBlock, kClBlock}) {
       void *fn = block == 512 ? (void *)cg_cluster<V, I, JAC, 512> : (void *)cg_cluster<V, I, JAC, kClBlock>;
       cudaLaunchConfig_t cfg;
@@ -934,6 +1020,7 @@ ClusterShape cluster_shape_for(int64_t n, int64_t batch, int64_t nnz) {
         best.cap = (int)rows;
         best.block = block;
         best.mcap = keep_mat ? (int)ment : 0;
+        best.ro = keep_ro ? 1 : 0;
         best.smem = smem;
         return best;
       }
@@ -963,9 +1050,9 @@ sla_status run_cluster(Prob<V, I> P, int64_t batch, cudaStream_t stream, sla_cg_
   if (e == cudaSuccess) e = cudaMemsetAsync(P.ctl, 0, sizeof(Ctl) * (size_t)batch, stream);
   if (e != cudaSuccess) return fail(e);
   if (sh.block == 512)
-    e = cudaLaunchKernelEx(&cfg, cg_cluster<V, I, JAC, 512>, P, sh.C, sh.cap, sh.mcap);
+    e = cudaLaunchKernelEx(&cfg, cg_cluster<V, I, JAC, 512>, P, sh.C, sh.cap, sh.mcap, sh.ro);
   else
-    e = cudaLaunchKernelEx(&cfg, cg_cluster<V, I, JAC, kClBlock>, P, sh.C, sh.cap, sh.mcap);
+    e = cudaLaunchKernelEx(&cfg, cg_cluster<V, I, JAC, kClBlock>, P, sh.C, sh.cap, sh.mcap, sh.ro);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(e);
   if (!info) return SLA_OK;

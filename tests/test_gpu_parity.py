@@ -380,3 +380,21 @@ def test_cluster_matches_graph_batched_f64(precond):
         assert ic[s].status == ig[s].status == 0 and abs(ic[s].iters - ig[s].iters) <= 1
         assert rel(xc[s].cpu().numpy(), xg[s].cpu().numpy()) <= X_TOL_F64
     assert ic[0].kernels == 1  # the whole batched solve is one launch
+
+
+@pytest.mark.parametrize("loop", [sla.SLA_LOOP_HOST, sla.SLA_LOOP_GRAPH, sla.SLA_LOOP_RESIDENT, sla.SLA_LOOP_CLUSTER])
+@pytest.mark.parametrize("kind", ["beyond_nnz", "decreasing"])
+def test_bad_row_ptr_reported_by_every_engine(loop, kind):
+    # a row pointer inside a block's (or cluster CTA's) row range is corrupted; every engine skips
+    # the rows it cannot trust, reads nothing outside the caller's arrays and reports SLA_BAD_CSR
+    A = poisson_5pt(20)
+    rp = A.row_ptr.copy()
+    j = 203  # inside the rows of one block / CTA, not at a boundary
+    rp[j] = A.nnz + 50 if kind == "beyond_nnz" else rp[j - 5]
+    dA = to_dev(A)
+    bad = sla.CSRMatrix(t(rp), dA.col_idx, dA.values)
+    b = t(np.random.default_rng(3).standard_normal(A.n))
+    x, info, _ = sla.sla_cg_solve(bad, b, rtol=1e-10, maxit=50, loop=loop)
+    assert info.status == sla.SLA_BAD_CSR
+    assert info.path == {sla.SLA_LOOP_HOST: "host", sla.SLA_LOOP_GRAPH: "graph",
+                         sla.SLA_LOOP_RESIDENT: "resident", sla.SLA_LOOP_CLUSTER: "cluster"}[loop]
