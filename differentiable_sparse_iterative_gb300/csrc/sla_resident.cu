@@ -548,17 +548,58 @@ constexpr int kClR = SLA_CLUSTER_ROWS;     // rows per thread whose entries the 
 constexpr int kClK = SLA_CLUSTER_ENTRIES;  // entries per row loaded up front (the rest one by one)
 
 // Sum of the C partners' value slot[q] (read through distributed shared memory), for warp 0:
-// lane j reads partner j, then a fixed shuffle tree; every CTA of the cluster obtains the same
-// bits.  Result valid in lane 0.
+// lane j reads partner j, then a log2(C)-level shuffle tree (C is a power of two); every CTA of
+// the cluster obtains the same bits.  Result valid in lane 0.  Each fp64 add costs a warp 64
+// cycles of its sub-partition's fp64 unit on this GPU, so the tree has no more levels than C needs.
 template <int NQ>
 __device__ __forceinline__ void cluster_sum(cgs::cluster_group &cl, double *slot, int C, double (&out)[NQ]) {
   const int lane = threadIdx.x & 31;
+  double v[NQ];
 #pragma unroll
-  for (int q = 0; q < NQ; ++q) {
-    double v = 0.0;
-    if (lane < C) v = cl.map_shared_rank(slot, lane)[q];
-    out[q] = warp_sum(v);
+  for (int q = 0; q < NQ; ++q) v[q] = 0.0;
+  if (lane < C) {
+    const double *ps = cl.map_shared_rank(slot, lane);
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) v[q] = ps[q];
   }
+  for (int o = C >> 1; o > 0; o >>= 1)
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) v[q] += __shfl_down_sync(0xffffffffu, v[q], o);
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) out[q] = v[q];
+}
+
+// Block sum of NV values per thread, result in thread 0, in a fixed order.  Warps 0-3 (one per SM
+// sub-partition, so their fp64 adds run in parallel) each add CB/4 values: a pairwise tree over
+// the CB/128 values of a lane, then a shuffle tree; thread 0 adds the four warp sums.
+// sb: shared scratch of NV * CB doubles.
+template <int NV, int CB>
+__device__ __forceinline__ void block_sum4(double (&v)[NV], double *sb) {
+  static_assert(CB % 128 == 0 && CB <= 1024, "block of 128..1024 threads");
+  constexpr int PER = CB / 128;
+  __shared__ double s4[NV][4];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) sb[j * CB + tid] = v[j];
+  __syncthreads();
+  if (warp < 4) {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      double a[PER];
+#pragma unroll
+      for (int u = 0; u < PER; ++u) a[u] = sb[j * CB + warp * (CB / 4) + lane + 32 * u];
+#pragma unroll
+      for (int w = 1; w < PER; w <<= 1)
+#pragma unroll
+        for (int u = 0; u + w < PER; u += 2 * w) a[u] += a[u + w];
+      const double t = warp_sum(a[0]);
+      if (lane == 0) s4[j][warp] = t;
+    }
+  }
+  __syncthreads();
+  if (tid == 0)
+#pragma unroll
+    for (int j = 0; j < NV; ++j) v[j] = (s4[j][0] + s4[j][1]) + (s4[j][2] + s4[j][3]);
 }
 
 template <typename V, typename I, bool JAC, int CB>
@@ -579,7 +620,9 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
   int32_t *s_ci = s_ro + ((cap + 1 + 3) & ~3);  // padded so the values below stay 16-byte aligned
   V *s_val = reinterpret_cast<V *>(s_ci + ((mcap + 3) & ~3));
   __shared__ double s_part[2][5];  // [0]: setup sums, then r.r / r.z; [1]: p.q (partners read these)
+  __shared__ double s_red[5 * CB];  // block-sum scratch
   __shared__ V *s_peer[kClMax];    // partners' p arrays in distributed shared memory
+  __shared__ int32_t s_start[kClMax + 1];  // first row of each partner (n for the end)
   __shared__ ResScalars S;
   __shared__ int s_pending;
 
@@ -598,6 +641,8 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
   Ctl *Cs = P.ctl + sys;
   Glob *glob = P.glob;
   if (tid < C) s_peer[tid] = cl.map_shared_rank(sp, tid);
+  if (tid <= C) s_start[tid] = (int32_t)start_of(tid);
+  const float rows_inv = (float)C / (float)n;  // partner estimate of a column, corrected below
   if (blockIdx.x == 0 && tid == 0) atomicAdd(&glob->kernels, 1ull);
 
   // ---- setup
@@ -657,7 +702,7 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
       s_val[e - m_lo] = val[e];
     }
   }
-  block_sum_n<5, CB>(acc5);
+  block_sum4<5, CB>(acc5, s_red);
   if (tid == 0)
     for (int q = 0; q < 5; ++q) s_part[0][q] = acc5[q];
   cl.sync();
@@ -730,9 +775,13 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
       const uint32_t off = (uint32_t)((int64_t)c - c0);
       if (off < (uint32_t)len) return sp[off];
       if (!col_ok(c, (int32_t)n, &glob->bad_csr)) return V(0);
-      int j = (int)((int64_t)c * C / n);
-      if (j + 1 < C && (int64_t)c >= start_of(j + 1)) ++j;
-      return s_peer[j][c - start_of(j)];
+      // the partner owning c: an estimate, corrected against the partners' first rows (the
+      // estimate is off by at most one near a boundary; the loops are bounded by C either way)
+      int j = (int)((float)c * rows_inv);
+      j = j < C - 1 ? (j > 0 ? j : 0) : C - 1;
+      while (j > 0 && c < s_start[j]) --j;
+      while (j + 1 < C && c >= s_start[j + 1]) ++j;
+      return s_peer[j][c - s_start[j]];
     };
     // q_i and the row's share of p.q (fp32 data: p.q summed in fp32 over 8 rows, then in fp64)
     auto row_done = [&](int li, V acc) {
@@ -809,7 +858,7 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
     }
     SLA_PHASE(1);
     double v1[1] = {pqd + (double)part};
-    block_sum_n<1, CB>(v1);
+    block_sum4<1, CB>(v1, s_red);
     if (tid == 0) s_part[1][0] = v1[0];
     cl.sync();
     double pqv[1];
@@ -846,7 +895,7 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
     acc2[0] += (double)rr_t;
     acc2[1] += (double)rz_t;
     SLA_PHASE(3);
-    block_sum_n<2, CB>(acc2);
+    block_sum4<2, CB>(acc2, s_red);
     if (tid == 0) {
       s_part[0][0] = acc2[0];
       s_part[0][1] = acc2[1];
