@@ -173,6 +173,11 @@ def run_ours(args, rank, world, local_rank):
     batched = w.batch > 0
     if batched:
         return run_batched(args, w, dev, rank, world)
+    # the bench's own L2-flush buffer first: the device memory counted below is the step's alone
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    mem_base = torch.cuda.memory_allocated(dev)
     A = sla.CSRMatrix.from_numpy(w.A.row_ptr, w.A.col_idx, w.A.values, dev)
     b = torch.from_numpy(w.b).to(dev)
     g_np = w.g if w.g is not None else np.random.default_rng(1).standard_normal(w.A.n)
@@ -183,7 +188,6 @@ def run_ours(args, rank, world, local_rank):
     x = torch.empty(n, dtype=torch.float64, device=dev)
     gb = torch.empty(n, dtype=torch.float64, device=dev)
     gv = torch.empty(nnz, dtype=torch.float64, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     loop = {"auto": sla.SLA_LOOP_AUTO, "cluster": sla.SLA_LOOP_CLUSTER, "resident": sla.SLA_LOOP_RESIDENT,
             "graph": sla.SLA_LOOP_GRAPH,
@@ -207,8 +211,6 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    torch.cuda.reset_peak_memory_stats(dev)
-    mem0 = torch.cuda.memory_allocated(dev)
     launches0 = sla.sla_launch_count()
     recs = []
     with ClockSampler(local_rank) as clk:
@@ -229,7 +231,9 @@ def run_ours(args, rank, world, local_rank):
     step_ms = [f + a for f, a in zip(fwd_ms, adj_ms)]
     tot_s = sum(step_ms) / 1e3
     tot_iters = sum(iters_f) + sum(iters_a)
-    peak_mem = torch.cuda.max_memory_allocated(dev) - mem0
+    # device memory of forward + adjoint: matrix, b, g, x, grad_b, grad_values and the O(n) workspace
+    peak_mem = torch.cuda.max_memory_allocated(dev) - mem_base
+    ws_mb = ws.numel() / 2**20
 
     tot_s_all, tot_iters_all = aggregate_over_ranks(tot_s, tot_iters, world, dev)
 
@@ -270,6 +274,7 @@ def run_ours(args, rank, world, local_rank):
         "status": sorted(status),
         "effective_gbs_step": (Bi * tot_iters + Bg * args.steps) / tot_s / 1e9,
         "peak_mem_mb": peak_mem / 2**20,
+        "workspace_mb": ws_mb,
         "path": path,
         "fp64": {"achieved_tflops": fp64_ach, "peak_tflops": fp64_peak, "frac": fp64_ach / fp64_peak,
                  "flops_per_iter": flops_it,
@@ -297,6 +302,10 @@ def run_batched(args, w, dev, rank, world):
     import torch
     import differentiable_sparse_iterative_gb300 as sla
     dt = torch.float32 if w.dtype == "f32" else torch.float64
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    mem_base = torch.cuda.memory_allocated(dev)
     P = sla.CSRMatrix.from_numpy(w.A.row_ptr, w.A.col_idx, w.A.values.astype(np.float32 if dt == torch.float32
                                                                               else np.float64), dev)
     vals = torch.from_numpy(w.values_b).to(dev)
@@ -306,7 +315,6 @@ def run_batched(args, w, dev, rank, world):
     loop = {"auto": sla.SLA_LOOP_AUTO, "cluster": sla.SLA_LOOP_CLUSTER, "resident": sla.SLA_LOOP_RESIDENT,
             "graph": sla.SLA_LOOP_GRAPH,
             "host": sla.SLA_LOOP_HOST}[args.loop]
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -331,6 +339,7 @@ def run_batched(args, w, dev, rank, world):
             recs.append(step())
         torch.cuda.synchronize()
     launches = sla.sla_launch_count() - launches0
+    peak_mem = torch.cuda.max_memory_allocated(dev) - mem_base
     fwd_ms = [r[0].elapsed_time(r[1]) for r in recs]
     adj_ms = [r[1].elapsed_time(r[2]) for r in recs]
     it_f = [sum(i.iters for i in r[3]) for r in recs]
@@ -352,7 +361,12 @@ def run_batched(args, w, dev, rank, world):
                    "step": "batched forward CG + batched adjoint"},
         "iters_forward_max": statistics.mean(max_it), "time_to_tolerance_ms": statistics.mean(fwd_ms),
         "adjoint_ms": statistics.mean(adj_ms),
-        "roofline": {"kernel": "batched CG iteration", "bound": "hbm", "achieved": achieved, "peak": peak,
+        "peak_mem_mb": peak_mem / 2**20,
+        "path": recs[-1][3][0].path,
+        "roofline": {"kernel": {"cluster": "cg_cluster (one thread-block cluster per system)",
+                                "graph": "cg_spmv_step + cg_update_step, one grid row per system (CUDA graph loop)",
+                                "host": "cg_spmv_step + cg_update_step, one grid row per system (host loop)"}.get(
+                                    recs[-1][3][0].path, "batched CG iteration"), "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind, "bytes_per_iter": Bi_batch,
                      "traffic": None},
         "gpu_launches": int(launches), "clocks": clk.summary(),
@@ -397,6 +411,8 @@ def run_e2e(args, w, dev, precond, sla, torch):
         flush_l2(flush)
         step()
     torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats(dev)
+    mem_base = torch.cuda.memory_allocated(dev)
     total = 0.0
     for _ in range(args.steps):
         flush_l2(flush)
@@ -406,6 +422,7 @@ def run_e2e(args, w, dev, precond, sla, torch):
         e1.record(stream)
         e1.synchronize()
         total += e0.elapsed_time(e1) / 1e3
+    peak_mem = torch.cuda.max_memory_allocated(dev) - mem_base
     # iterations of the autograd path equal those of the direct calls on the same data
     _, fi, _ = sla.sla_cg_solve(sla.CSRMatrix(h_rp.to(dev), h_ci.to(dev), h_v.to(dev)), h_b.to(dev), rtol=w.rtol,
                                 maxit=w.maxit, precond=precond)
@@ -413,7 +430,8 @@ def run_e2e(args, w, dev, precond, sla, torch):
                                   o_x.to(dev), h_g.to(dev), rtol=w.rtol, maxit=w.maxit, precond=precond)
     per_step_iters = fi.iters + ai.iters
     return {"value": per_step_iters * args.steps / total, "unit": "iters/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "api": "differentiable_sparse_iterative_gb300.solve + backward"}
+            "d2h_bytes_per_step": d2h, "api": "differentiable_sparse_iterative_gb300.solve + backward",
+            "peak_mem_mb": peak_mem / 2**20}
 
 
 def cpu_baseline(w, iters):

@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
   while (S.go) {
     const int par = (int)(k & 1);
     const bool first = (k == 0);
-    const V vb = (V)S.beta, va_prev = (V)S.alpha_prev;
+    const V vb = (V)S.beta;
     V *pn_pub = P.p[par];
     const V *po_pub = P.p[par ^ 1];
     // p_k = z_k + beta p_{k-1} for the own rows; publish p_k
@@ -372,26 +372,7 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
     const double v1[1] = {(double)part};
     SLA_PHASE(1);
     block_publish<1>(v1, sbuf, partA);
-    grid_arrive(arrive, epoch);
-    // while the other blocks arrive: the delayed update x += alpha_{k-1} p_{k-1} (p_{k-1} is this
-    // block's own published copy), which needs neither reduction
-    if (!first) {
-      for (int j0 = tid; j0 < len; j0 += kStage * kResBlock) {
-        V xv[kStage], pv[kStage];
-#pragma unroll
-        for (int u = 0; u < kStage; ++u) {
-          const int li = j0 + u * kResBlock;
-          xv[u] = li < len ? xg[c0 + li] : V(0);
-          pv[u] = li < len ? po_pub[c0 + li] : V(0);
-        }
-#pragma unroll
-        for (int u = 0; u < kStage; ++u) {
-          const int li = j0 + u * kResBlock;
-          if (li < len) xg[c0 + li] = fmav<V>(va_prev, pv[u], xv[u]);
-        }
-      }
-    }
-    const bool ok1 = grid_wait(arrive, timeout, G, epoch);
+    const bool ok1 = grid_barrier(arrive, timeout, G, epoch);
     SLA_PHASE(2);
     if (tid < 32) {
       double t1[1];
@@ -446,7 +427,23 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
       const double v1r[1] = {acc2[0]};
       block_publish<1>(v1r, sbuf, partB);
     }
-    const bool ok2 = grid_barrier(arrive, timeout, G, epoch);
+    grid_arrive(arrive, epoch);
+    // while the other blocks arrive: x_{k+1} = x_k + alpha_k p_k, which needs neither reduction
+    // (p_k is still in shared memory); whatever the r.r test decides, this update is due
+    for (int j0 = tid; j0 < len; j0 += kStage * kResBlock) {
+      V xv[kStage];
+#pragma unroll
+      for (int u = 0; u < kStage; ++u) {
+        const int li = j0 + u * kResBlock;
+        xv[u] = li < len ? xg[c0 + li] : V(0);
+      }
+#pragma unroll
+      for (int u = 0; u < kStage; ++u) {
+        const int li = j0 + u * kResBlock;
+        if (li < len) xg[c0 + li] = fmav<V>(va, sp[li], xv[u]);
+      }
+    }
+    const bool ok2 = grid_wait(arrive, timeout, G, epoch);
     SLA_PHASE(4);
     ++k;
     if (tid < 32) {
@@ -476,9 +473,9 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
         rr_last = rrt;
         int go = 0;
         if (stop_code == 4) status = SLA_TIMEOUT;
-        else if (stop_code == 2) { status = SLA_NONFINITE; pending = 1; }
-        else if (stop_code == 1) { status = SLA_OK; pending = 1; }
-        else if (stop_code == 3) { status = SLA_NOT_CONVERGED; pending = 1; }
+        else if (stop_code == 2) status = SLA_NONFINITE;
+        else if (stop_code == 1) status = SLA_OK;
+        else if (stop_code == 3) status = SLA_NOT_CONVERGED;
         else {
           S.beta = beta_new;
           S.rho = rho_new;
@@ -494,14 +491,11 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
   }
   SLA_PHASE_STORE(k);
 
-  // ---- finish: the last delayed x update (or x = 0 for b = 0)
+  // ---- finish: x = 0 for b = 0 (every other x update was made inside the loop)
   __shared__ int s_pending;
   if (tid == 0) s_pending = pending;
   __syncthreads();
-  const V va = (V)S.alpha;
-  if (s_pending == 1) {
-    for (int li = tid; li < len; li += kResBlock) xg[c0 + li] = fmav<V>(va, sp[li], xg[c0 + li]);
-  } else if (s_pending == 2) {
+  if (s_pending == 2) {
     for (int li = tid; li < len; li += kResBlock) xg[c0 + li] = V(0);
   }
   // history entries 1..k hold r.r: convert them to ||r|| / ||b|| (block 0, all threads)
