@@ -30,7 +30,7 @@ namespace sla {
 
 #ifdef SLA_PHASE_TIMING
 // Profiling build only (compiled out of the library): cycles per phase, summed over iterations,
-// for every block: [p-update, spmv, p.q reduce, r-update, r.r reduce, scalars, -, iterations].
+// for every block: [p-update, spmv, p.q reduce, r-update, r.r reduce, scalars, SM id, iterations].
 __device__ unsigned long long g_phase_cycles[kMaxBlocksPerSystem][8];
 #define SLA_PHASE_INIT() unsigned long long ph_[6] = {0, 0, 0, 0, 0, 0}; long long ph_t = clock64()
 #define SLA_PHASE(q)                \
@@ -42,7 +42,10 @@ __device__ unsigned long long g_phase_cycles[kMaxBlocksPerSystem][8];
 #define SLA_PHASE_STORE(k)                                                    \
   do {                                                                        \
     if (threadIdx.x == 0) {                                                   \
+      unsigned smid_;                                                         \
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid_));                      \
       for (int q_ = 0; q_ < 6; ++q_) g_phase_cycles[blockIdx.x][q_] = ph_[q_]; \
+      g_phase_cycles[blockIdx.x][6] = smid_;                                  \
       g_phase_cycles[blockIdx.x][7] = (unsigned long long)(k);                \
     }                                                                         \
   } while (0)
