@@ -780,17 +780,22 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
       while (j + 1 < C && c >= s_start[j + 1]) ++j;
       return s_peer[j][c - s_start[j]];
     };
-    // q_i and the row's share of p.q (fp32 data: p.q summed in fp32 over 8 rows, then in fp64)
+    // q_i and the row's share of p.q (fp32 data: p.q summed in fp32 over groups of 8 rows, the
+    // groups in fp64; a group is closed only when a ninth row arrives, so a thread with at most
+    // 8 rows converts once and adds nothing in fp64)
+    bool flushed = false;
     auto row_done = [&](int li, V acc) {
       sq[li] = acc;
-      part = fmav<V>(sp[li], acc, part);
       if constexpr (sizeof(V) == 4) {
-        if (++cnt == 8) {
-          pqd += (double)part;
+        if (cnt == 8) {
+          pqd = flushed ? pqd + (double)part : (double)part;
+          flushed = true;
           part = V(0);
           cnt = 0;
         }
+        ++cnt;
       }
+      part = fmav<V>(sp[li], acc, part);
     };
     if (rostaged && !mstaged) {
       // matrix streamed from L2/HBM: kClR rows per thread at a time, the first kClK entries of
@@ -854,7 +859,7 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
       }
     }
     SLA_PHASE(1);
-    double v1[1] = {pqd + (double)part};
+    double v1[1] = {flushed ? pqd + (double)part : (double)part};
     block_sum4<1, CB>(v1, s_red);
     if (tid == 0) s_part[1][0] = v1[0];
     cl.sync();
@@ -875,32 +880,49 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
     double acc2[2] = {0.0, 0.0};
     V rr_t = V(0), rz_t = V(0);
     cnt = 0;
+    bool flushed2 = false;
     for (int li = tid; li < len; li += CB) {
       const V ri = fmav<V>(-va, sq[li], sr[li]);
       sr[li] = ri;
-      rr_t = fmav<V>(ri, ri, rr_t);
-      if (JAC) rz_t = fmav<V>(ri, sd[li] * ri, rz_t);
       if constexpr (sizeof(V) == 4) {
-        if (++cnt == 8) {
-          acc2[0] += (double)rr_t;
-          acc2[1] += (double)rz_t;
+        if (cnt == 8) {  // as for p.q: a group of 8 rows is closed when a ninth arrives
+          acc2[0] = flushed2 ? acc2[0] + (double)rr_t : (double)rr_t;
+          if (JAC) acc2[1] = flushed2 ? acc2[1] + (double)rz_t : (double)rz_t;
+          flushed2 = true;
           rr_t = rz_t = V(0);
           cnt = 0;
         }
+        ++cnt;
       }
+      rr_t = fmav<V>(ri, ri, rr_t);
+      if (JAC) rz_t = fmav<V>(ri, sd[li] * ri, rz_t);
     }
-    acc2[0] += (double)rr_t;
-    acc2[1] += (double)rz_t;
+    acc2[0] = flushed2 ? acc2[0] + (double)rr_t : (double)rr_t;
+    if (JAC) acc2[1] = flushed2 ? acc2[1] + (double)rz_t : (double)rz_t;
     SLA_PHASE(3);
-    block_sum4<2, CB>(acc2, s_red);
+    if (JAC) {
+      block_sum4<2, CB>(acc2, s_red);
+    } else {
+      double a1[1] = {acc2[0]};
+      block_sum4<1, CB>(a1, s_red);
+      acc2[0] = a1[0];
+    }
     if (tid == 0) {
       s_part[0][0] = acc2[0];
       s_part[0][1] = acc2[1];
     }
     cl.sync();
     ++k;
-    double t2[2];
-    if (tid < 32) cluster_sum<2>(cl, &s_part[0][0], C, t2);
+    double t2[2] = {0.0, 0.0};
+    if (tid < 32) {
+      if (JAC) {
+        cluster_sum<2>(cl, &s_part[0][0], C, t2);
+      } else {
+        double t1[1];
+        cluster_sum<1>(cl, &s_part[0][0], C, t1);
+        t2[0] = t1[0];
+      }
+    }
     if (tid == 0) {
       const double rrt = t2[0], rzt = t2[1];
       rr_last = rrt;
