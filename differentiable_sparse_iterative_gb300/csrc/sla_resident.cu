@@ -396,6 +396,10 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
     // summed in float, then added to the fp64 sums.
     const V va = (V)S.alpha;
     double acc2[2] = {0.0, 0.0};
+    // fp64 data: one FMA chain over all of the thread's rows (no extra fp64 adds); fp32 data: a
+    // float sum per stage, the stages added in fp64
+    V rr_t = V(0), rz_t = V(0);
+    bool flushed = false;
     for (int j0 = tid; j0 < len; j0 += kStage * kResBlock) {
       V qv[kStage];
 #pragma unroll
@@ -403,7 +407,6 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
         const int li = j0 + u * kResBlock;
         qv[u] = li < len ? qg[c0 + li] : V(0);
       }
-      V rr_t = V(0), rz_t = V(0);
 #pragma unroll
       for (int u = 0; u < kStage; ++u) {
         const int li = j0 + u * kResBlock;
@@ -415,13 +418,16 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
           if (JAC) rz_t = fmav<V>(ri, sd[li] * ri, rz_t);
         }
       }
-      if constexpr (sizeof(V) == 8) {
-        acc2[0] = (j0 == tid) ? (double)rr_t : acc2[0] + (double)rr_t;
-        if (JAC) acc2[1] = (j0 == tid) ? (double)rz_t : acc2[1] + (double)rz_t;
-      } else {
-        acc2[0] += (double)rr_t;
-        if (JAC) acc2[1] += (double)rz_t;
+      if constexpr (sizeof(V) == 4) {
+        acc2[0] = flushed ? acc2[0] + (double)rr_t : (double)rr_t;
+        if (JAC) acc2[1] = flushed ? acc2[1] + (double)rz_t : (double)rz_t;
+        flushed = true;
+        rr_t = rz_t = V(0);
       }
+    }
+    if constexpr (sizeof(V) == 8) {
+      acc2[0] = rr_t;
+      if (JAC) acc2[1] = rz_t;
     }
     SLA_PHASE(3);
     if (JAC) {
