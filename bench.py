@@ -243,7 +243,7 @@ def run_ours(args, rank, world, local_rank):
     # fused CG iteration (spmv_step + update_step): bytes per iteration / forward time per iteration
     fwd_s = sum(fwd_ms) / 1e3
     achieved = Bi * sum(iters_f) / fwd_s / 1e9
-    tr = profiled_traffic(args.config)
+    tr = None if args.grid_m else profiled_traffic(args.config)  # counters are for the full-size workload
     clocks = clk.summary()
     path = recs[-1][3].path
     kernel_name = {"resident": "cg_resident (one persistent cooperative kernel per solve)",
@@ -284,6 +284,7 @@ def run_ours(args, rank, world, local_rank):
                      "peak_kind": peak_kind,
                      "bytes_per_iter": Bi,
                      "traffic": (tr["dram_bytes_per_iter"] if tr else None),
+                     "traffic_unit": "DRAM bytes per CG iteration (ncu dram__bytes_read + write)",
                      "traffic_source": (tr.get("source") if tr else None)},
         "gpu_launches": int(launches),
         "wall_s": wall,
@@ -349,6 +350,7 @@ def run_batched(args, w, dev, rank, world):
     Bi_sys = nnz * s_v + 9 * n * s_v  # per system-iteration; the shared pattern is read once per iteration
     peak, peak_kind = measured_peaks()
     max_it = [max(i.iters for i in r[3]) for r in recs]
+    tr = None if args.grid_m else profiled_traffic(args.config)  # counters are for the full-size workload
     # bytes of one batched iteration (all systems): B values+vectors, one pattern read
     Bi_batch = B * Bi_sys + nnz * 4 + (n + 1) * 4
     achieved = Bi_batch * sum(max_it) / (sum(fwd_ms) / 1e3) / 1e9
@@ -368,7 +370,9 @@ def run_batched(args, w, dev, rank, world):
                                 "host": "cg_spmv_step + cg_update_step, one grid row per system (host loop)"}.get(
                                     recs[-1][3][0].path, "batched CG iteration"), "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind, "bytes_per_iter": Bi_batch,
-                     "traffic": None},
+                     "traffic": (tr["dram_bytes_per_iter"] if tr else None),
+                     "traffic_unit": "DRAM bytes per batched CG iteration (ncu dram__bytes_read + write)",
+                     "traffic_source": (tr.get("source") if tr else None)},
         "gpu_launches": int(launches), "clocks": clk.summary(),
     }
 
