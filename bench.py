@@ -10,7 +10,10 @@ Metric: CG iterations per second over the whole job (forward + adjoint iteration
 all ranks / the max-over-ranks device time of the timed steps), plus the effective HBM
 GB/s of the fused CG iteration against the measured copy bandwidth, and the adjoint ms.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}] [--config configN]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}] [--config NAME]
+
+NAME: poisson64, poisson1000 (default), diffusion128_batch64, diffusion4096_jacobi,
+poisson13000_int64 (short aliases config1 .. config5).
 
 With N > 1 the script runs under torch.distributed.run; every rank solves its own
 independent system of the same size (the single-system solve has no exchange step:
@@ -73,6 +76,11 @@ def csrc_sha256():
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
+
+
+def canonical_name(name):
+    from workloads import canonical_name as cn
+    return cn(name)
 
 
 def profiled_traffic(config):
@@ -243,7 +251,7 @@ def run_ours(args, rank, world, local_rank):
     # fused CG iteration (spmv_step + update_step): bytes per iteration / forward time per iteration
     fwd_s = sum(fwd_ms) / 1e3
     achieved = Bi * sum(iters_f) / fwd_s / 1e9
-    tr = None if args.grid_m else profiled_traffic(args.config)  # counters are for the full-size workload
+    tr = None if args.grid_m else profiled_traffic(canonical_name(args.config))  # counters are for the full-size workload
     clocks = clk.summary()
     path = recs[-1][3].path
     kernel_name = {"resident": "cg_resident (one persistent cooperative kernel per solve)",
@@ -350,7 +358,7 @@ def run_batched(args, w, dev, rank, world):
     Bi_sys = nnz * s_v + 9 * n * s_v  # per system-iteration; the shared pattern is read once per iteration
     peak, peak_kind = measured_peaks()
     max_it = [max(i.iters for i in r[3]) for r in recs]
-    tr = None if args.grid_m else profiled_traffic(args.config)  # counters are for the full-size workload
+    tr = None if args.grid_m else profiled_traffic(canonical_name(args.config))  # counters are for the full-size workload
     # bytes of one batched iteration (all systems): B values+vectors, one pattern read
     Bi_batch = B * Bi_sys + nnz * 4 + (n + 1) * 4
     achieved = Bi_batch * sum(max_it) / (sum(fwd_ms) / 1e3) / 1e9
@@ -493,7 +501,9 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="config2")
+    ap.add_argument("--config", default="poisson1000",
+                    help="workload: poisson64, poisson1000 (default), diffusion128_batch64, diffusion4096_jacobi, "
+                         "poisson13000_int64 (or config1 .. config5)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-iters", type=int, default=600)

@@ -309,6 +309,20 @@ def small_poisson(m: int, seed: int = 0, rowptr64: bool = False) -> Workload:
                     meta={"m": m})
 
 
+# Descriptive names of the five benchmark systems; config1 .. config5 are short aliases.
+ALIASES = {
+    "poisson64": "config1",             # 64x64 Poisson, fp64, rtol 1e-10
+    "poisson1000": "config2",           # 1000x1000 Poisson, fp64, rtol 1e-8
+    "diffusion128_batch64": "config3",  # 64 x 128x128 interior-edge diffusion, fp32, rtol 1e-5
+    "diffusion4096_jacobi": "config4",  # 4096x4096 Dirichlet diffusion, Jacobi PCG, rtol 1e-8
+    "poisson13000_int64": "config5",    # 13000x13000 Poisson, int64 row_ptr, 1000 iterations
+}
+
+
+def canonical_name(name: str) -> str:
+    return ALIASES.get(name, name)
+
+
 def config_by_name(name: str, **kw) -> Workload:
     return {"config1": config1, "config2": config2, "config3": config3, "config4": config4,
-            "config5": config5}[name](**kw)
+            "config5": config5}[canonical_name(name)](**kw)
