@@ -26,7 +26,7 @@ import torch
 
 from . import _abi
 from ._abi import (SLA_OK, SLA_NOT_CONVERGED, SLA_BREAKDOWN, SLA_INVALID_ARG, SLA_BAD_CSR, SLA_NONFINITE,
-                   SLA_WORKSPACE_TOO_SMALL, SLA_CUDA_ERROR, SLA_PRECOND_NONE, SLA_PRECOND_JACOBI, SLA_LOOP_AUTO,
+                   SLA_WORKSPACE_TOO_SMALL, SLA_TIMEOUT, SLA_CUDA_ERROR, SLA_PRECOND_NONE, SLA_PRECOND_JACOBI, SLA_LOOP_AUTO,
                    SLA_LOOP_HOST, SLA_LOOP_GRAPH, SLA_LOOP_RESIDENT, SLA_LOOP_CLUSTER)
 
 __all__ = [
@@ -34,7 +34,8 @@ __all__ = [
     "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_validate_csr", "sla_cg_workspace_bytes",
     "sla_status_string", "sla_launch_count", "sla_version", "CGSolve", "solve", "matvec",
     "SLA_PRECOND_NONE", "SLA_PRECOND_JACOBI", "SLA_LOOP_AUTO", "SLA_LOOP_HOST", "SLA_LOOP_GRAPH",
-    "SLA_LOOP_RESIDENT", "SLA_LOOP_CLUSTER",
+    "SLA_LOOP_RESIDENT", "SLA_LOOP_CLUSTER", "SLA_OK", "SLA_NOT_CONVERGED", "SLA_BREAKDOWN", "SLA_INVALID_ARG",
+    "SLA_BAD_CSR", "SLA_NONFINITE", "SLA_WORKSPACE_TOO_SMALL", "SLA_TIMEOUT", "SLA_CUDA_ERROR",
 ]
 
 _lib = None

@@ -21,6 +21,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 
 #include "sla_common.cuh"
@@ -67,6 +68,14 @@ constexpr int kResBlock = 1024;
 constexpr int kStage = 8;  // rows per thread whose global loads are issued together
 constexpr long long kSpinLimit = 1ll << 26;  // ~seconds of polling before a barrier gives up
 
+// Bounds of the grid barrier's wait.  `extra` arrivals are expected beyond the G blocks: 0 in
+// use; a test sets 1 (an arrival that never comes) with a short `limit` to drive the timeout path
+// on the GPU and check that the solve returns SLA_TIMEOUT with the context still usable.
+struct WaitCfg {
+  unsigned extra;
+  long long limit;
+};
+
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -84,15 +93,16 @@ __device__ __forceinline__ void grid_arrive(unsigned *arrive, unsigned &epoch) {
   if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(arrive), "r"(1u) : "memory");
 }
 
-__device__ __forceinline__ bool grid_wait(unsigned *arrive, unsigned *timeout, unsigned G, unsigned epoch) {
+__device__ __forceinline__ bool grid_wait(unsigned *arrive, unsigned *timeout, unsigned G, unsigned epoch,
+                                          const WaitCfg &wc) {
   __shared__ int s_ok;
   if (threadIdx.x == 0) {
-    const unsigned target = epoch * G;
+    const unsigned target = epoch * G + wc.extra;
     int ok = 1;
     long long spins = 0;
     while (ld_acquire(arrive) < target) {
       if (*(volatile unsigned *)timeout) { ok = 0; break; }
-      if (++spins > kSpinLimit) {
+      if (++spins > wc.limit) {
         atomicExch(timeout, 1u);
         ok = 0;
         break;
@@ -105,9 +115,10 @@ __device__ __forceinline__ bool grid_wait(unsigned *arrive, unsigned *timeout, u
   return s_ok != 0;
 }
 
-__device__ __forceinline__ bool grid_barrier(unsigned *arrive, unsigned *timeout, unsigned G, unsigned &epoch) {
+__device__ __forceinline__ bool grid_barrier(unsigned *arrive, unsigned *timeout, unsigned G, unsigned &epoch,
+                                             const WaitCfg &wc) {
   grid_arrive(arrive, epoch);
-  return grid_wait(arrive, timeout, G, epoch);
+  return grid_wait(arrive, timeout, G, epoch, wc);
 }
 
 // Deterministic all-reduce across the G blocks, in three steps so that the fp64 work on the
@@ -203,7 +214,7 @@ __device__ __forceinline__ bool stop_test(double rr, const ResScalars &S) {
 }
 
 template <typename V, typename I, bool JAC>
-__global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int cap) {
+__global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int cap, WaitCfg wc) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // shared: reduction buffer (2 x kResBlock doubles), then r, p (and 1/diag) of the block's rows
   double *sbuf = reinterpret_cast<double *>(smem_raw);
@@ -268,7 +279,7 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
   }
   // x = x0 (or 0) after every block has read x0 (x0 may be the same buffer as x)
   block_publish<5>(acc5, sbuf, partB);
-  const bool ok0 = grid_barrier(arrive, timeout, G, epoch);
+  const bool ok0 = grid_barrier(arrive, timeout, G, epoch, wc);
   for (int li = tid; li < len; li += kResBlock) xg[c0 + li] = P.x0 ? P.x0[c0 + li] : V(0);
 
   // thread 0 of every block takes the same decisions from the same totals
@@ -375,7 +386,7 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
     const double v1[1] = {(double)part};
     SLA_PHASE(1);
     block_publish<1>(v1, sbuf, partA);
-    const bool ok1 = grid_barrier(arrive, timeout, G, epoch);
+    const bool ok1 = grid_barrier(arrive, timeout, G, epoch, wc);
     SLA_PHASE(2);
     if (tid < 32) {
       double t1[1];
@@ -452,7 +463,7 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
         if (li < len) xg[c0 + li] = fmav<V>(va, sp[li], xv[u]);
       }
     }
-    const bool ok2 = grid_wait(arrive, timeout, G, epoch);
+    const bool ok2 = grid_wait(arrive, timeout, G, epoch, wc);
     SLA_PHASE(4);
     ++k;
     if (tid < 32) {
@@ -1171,7 +1182,13 @@ sla_status run_resident(Prob<V, I> P, cudaStream_t stream, sla_cg_info *info) {
   cudaError_t e = cudaMemsetAsync(P.glob, 0, sizeof(Glob), stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(P.ctl, 0, sizeof(Ctl), stream);
   if (e != cudaSuccess) return fail(e);
-  void *args[] = {(void *)&P, (void *)&cap};
+  WaitCfg wc{0u, kSpinLimit};
+  if (const char *e = getenv("SLA_TEST_GRID_WAIT_EXTRA")) wc.extra = (unsigned)strtoul(e, nullptr, 10);
+  if (const char *e = getenv("SLA_TEST_SPIN_LIMIT")) {
+    const long long v = strtoll(e, nullptr, 10);
+    if (v > 0 && v < kSpinLimit) wc.limit = v;
+  }
+  void *args[] = {(void *)&P, (void *)&cap, (void *)&wc};
   e = cudaLaunchCooperativeKernel(fn, dim3(G), dim3(kResBlock), args, smem, stream);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(e);

@@ -398,3 +398,25 @@ def test_bad_row_ptr_reported_by_every_engine(loop, kind):
     assert info.status == sla.SLA_BAD_CSR
     assert info.path == {sla.SLA_LOOP_HOST: "host", sla.SLA_LOOP_GRAPH: "graph",
                          sla.SLA_LOOP_RESIDENT: "resident", sla.SLA_LOOP_CLUSTER: "cluster"}[loop]
+
+
+def test_resident_barrier_timeout_returns_status(monkeypatch):
+    # failure detection without a fault: the grid barrier waits for one arrival that never comes,
+    # gives up after a short bounded wait, and the solve returns SLA_TIMEOUT; the context stays
+    # usable and the next solve is exact
+    import time
+    A = poisson_5pt(40)
+    b = t(np.random.default_rng(5).standard_normal(A.n))
+    dA = to_dev(A)
+    monkeypatch.setenv("SLA_TEST_GRID_WAIT_EXTRA", "1")
+    monkeypatch.setenv("SLA_TEST_SPIN_LIMIT", "20000")
+    t0 = time.time()
+    _, info, _ = sla.sla_cg_solve(dA, b, rtol=1e-10, maxit=200, loop=sla.SLA_LOOP_RESIDENT)
+    assert info.status == sla.SLA_TIMEOUT and info.path == "resident"
+    assert time.time() - t0 < 60
+    monkeypatch.delenv("SLA_TEST_GRID_WAIT_EXTRA")
+    monkeypatch.delenv("SLA_TEST_SPIN_LIMIT")
+    x, info2, _ = sla.sla_cg_solve(dA, b, rtol=1e-10, maxit=2000, loop=sla.SLA_LOOP_RESIDENT)
+    xg, infog, _ = sla.sla_cg_solve(dA, b, rtol=1e-10, maxit=2000, loop=sla.SLA_LOOP_GRAPH)
+    assert info2.status == 0 and abs(info2.iters - infog.iters) <= 1
+    assert rel(x.cpu().numpy(), xg.cpu().numpy()) <= X_TOL_F64
