@@ -560,6 +560,7 @@ constexpr size_t kClSmemMax = 110 * 1024;  // dynamic shared memory a cluster CT
 #endif
 constexpr int kClR = SLA_CLUSTER_ROWS;     // rows per thread whose entries the streamed SpMV loads together
 constexpr int kClK = SLA_CLUSTER_ENTRIES;  // entries per row loaded up front (the rest one by one)
+constexpr int kClGroup = 8;  // rows per thread whose p.q and r.r terms are summed in the data type
 
 // Sum of the C partners' value slot[q] (read through distributed shared memory), for warp 0:
 // lane j reads partner j, then a log2(C)-level shuffle tree (C is a power of two); every CTA of
@@ -637,6 +638,9 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
   __shared__ double s_red[5 * CB];  // block-sum scratch
   __shared__ V *s_peer[kClMax];    // partners' p arrays in distributed shared memory
   __shared__ int32_t s_start[kClMax + 1];  // first row of each partner (n for the end)
+  // beta, alpha, alpha_prev in the data type, converted once by thread 0 (a conversion is an fp64
+  // instruction, 64 cycles of a sub-partition's fp64 unit, if every warp made its own)
+  __shared__ V s_vsc[3];
   __shared__ ResScalars S;
   __shared__ int s_pending;
 
@@ -656,7 +660,6 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
   Glob *glob = P.glob;
   if (tid < C) s_peer[tid] = cl.map_shared_rank(sp, tid);
   if (tid <= C) s_start[tid] = (int32_t)start_of(tid);
-  const float rows_inv = (float)C / (float)n;  // partner estimate of a column, corrected below
   if (blockIdx.x == 0 && tid == 0) atomicAdd(&glob->kernels, 1ull);
 
   // ---- setup
@@ -753,6 +756,7 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
     }
     S.go = go;
     S.alpha = S.beta = S.alpha_prev = 0.0;
+    s_vsc[0] = s_vsc[1] = s_vsc[2] = V(0);
     S.rho = rho;
     S.nb = nb;
     const double tol = P.rtol * nb, e4 = 4.0 * 2.220446049250313e-16;
@@ -767,7 +771,7 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
   SLA_PHASE_INIT();
   while (S.go) {
     const bool first = (k == 0);
-    const V vb = (V)S.beta, va_prev = (V)S.alpha_prev;
+    const V vb = s_vsc[0], va_prev = s_vsc[2];
     for (int li = tid; li < len; li += CB) {
       const V rl = sr[li];
       const V z = JAC ? sd[li] * rl : rl;
@@ -781,102 +785,101 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
     }
     cl.sync();  // every CTA's p_k is in place
     SLA_PHASE(0);
-    V part = V(0);
-    double pqd = 0.0;
-    int cnt = 0;
     // p_k at column c: own rows from shared memory, a partner's from its shared memory (DSMEM)
     auto p_at = [&](int32_t c) -> V {
       const uint32_t off = (uint32_t)((int64_t)c - c0);
       if (off < (uint32_t)len) return sp[off];
       if (!col_ok(c, (int32_t)n, &glob->bad_csr)) return V(0);
-      // the partner owning c: an estimate, corrected against the partners' first rows (the
-      // estimate is off by at most one near a boundary; the loops are bounded by C either way)
-      int j = (int)((float)c * rows_inv);
-      j = j < C - 1 ? (j > 0 ? j : 0) : C - 1;
-      while (j > 0 && c < s_start[j]) --j;
-      while (j + 1 < C && c >= s_start[j + 1]) ++j;
+      // the partner owning c: a binary search over the partners' first rows (integer compares
+      // only; C is a power of two <= 16)
+      int j = 0;
+#pragma unroll
+      for (int step = kClMax / 2; step >= 1; step >>= 1)
+        if (j + step < C && c >= s_start[j + step]) j += step;
       return s_peer[j][c - s_start[j]];
     };
-    // q_i and the row's share of p.q (fp32 data: p.q summed in fp32 over groups of 8 rows, the
-    // groups in fp64; a group is closed only when a ninth row arrives, so a thread with at most
-    // 8 rows converts once and adds nothing in fp64)
-    bool flushed = false;
+    // Rows come in groups of kClGroup per thread: p.q is summed in the data type within a group
+    // and the groups in fp64.  The group is an outer loop, so no fp64 instruction sits in the
+    // per-row code (a predicated one would still occupy the fp64 unit on every row).
+    V part = V(0);
     auto row_done = [&](int li, V acc) {
       sq[li] = acc;
-      if constexpr (sizeof(V) == 4) {
-        if (cnt == 8) {
-          pqd = flushed ? pqd + (double)part : (double)part;
-          flushed = true;
-          part = V(0);
-          cnt = 0;
-        }
-        ++cnt;
-      }
       part = fmav<V>(sp[li], acc, part);
     };
-    if (rostaged && !mstaged) {
-      // matrix streamed from L2/HBM: kClR rows per thread at a time, the first kClK entries of
-      // each loaded together (independent loads in flight instead of one row's chain at a time);
-      // every row still adds its entries in order, so the result is the same as row by row
-      const int32_t *__restrict__ cib = ci + m_lo;
-      const V *__restrict__ vab = val + m_lo;
-      for (int j0 = tid; j0 < len; j0 += kClR * CB) {
-        int32_t eb[kClR], ee[kClR];
-#pragma unroll
-        for (int u = 0; u < kClR; ++u) {
-          const int li = j0 + u * CB;
-          eb[u] = li < len ? s_ro[li] : 0;
-          ee[u] = li < len ? s_ro[li + 1] : 0;
-        }
-        int32_t cc[kClR][kClK];
-        V vv[kClR][kClK];
-#pragma unroll
-        for (int t = 0; t < kClK; ++t)
+    auto spmv_rows = [&](int gb, int ge) {
+      if (rostaged && !mstaged) {
+        // matrix streamed from L2/HBM: kClR rows per thread at a time, the first kClK entries of
+        // each loaded together (independent loads in flight instead of one row's chain at a
+        // time); every row still adds its entries in order
+        const int32_t *__restrict__ cib = ci + m_lo;
+        const V *__restrict__ vab = val + m_lo;
+        for (int j0 = gb + tid; j0 < ge; j0 += kClR * CB) {
+          int32_t eb[kClR], ee[kClR];
 #pragma unroll
           for (int u = 0; u < kClR; ++u) {
-            const int32_t e = eb[u] + t;
-            const bool in = e < ee[u];
-            cc[u][t] = in ? __ldg(cib + e) : 0;
-            vv[u][t] = in ? __ldg(vab + e) : V(0);
+            const int li = j0 + u * CB;
+            eb[u] = li < ge ? s_ro[li] : 0;
+            ee[u] = li < ge ? s_ro[li + 1] : 0;
           }
-        V acc[kClR];
+          int32_t cc[kClR][kClK];
+          V vv[kClR][kClK];
 #pragma unroll
-        for (int u = 0; u < kClR; ++u) acc[u] = V(0);
+          for (int t = 0; t < kClK; ++t)
 #pragma unroll
-        for (int t = 0; t < kClK; ++t)
+            for (int u = 0; u < kClR; ++u) {
+              const int32_t e = eb[u] + t;
+              const bool in = e < ee[u];
+              cc[u][t] = in ? __ldg(cib + e) : 0;
+              vv[u][t] = in ? __ldg(vab + e) : V(0);
+            }
+          V acc[kClR];
+#pragma unroll
+          for (int u = 0; u < kClR; ++u) acc[u] = V(0);
+#pragma unroll
+          for (int t = 0; t < kClK; ++t)
+#pragma unroll
+            for (int u = 0; u < kClR; ++u)
+              if (eb[u] + t < ee[u]) acc[u] = fmav<V>(vv[u][t], p_at(cc[u][t]), acc[u]);
 #pragma unroll
           for (int u = 0; u < kClR; ++u)
-            if (eb[u] + t < ee[u]) acc[u] = fmav<V>(vv[u][t], p_at(cc[u][t]), acc[u]);
+            for (int32_t e = eb[u] + kClK; e < ee[u]; ++e)
+              acc[u] = fmav<V>(__ldg(vab + e), p_at(__ldg(cib + e)), acc[u]);
 #pragma unroll
-        for (int u = 0; u < kClR; ++u)
-          for (int32_t e = eb[u] + kClK; e < ee[u]; ++e) acc[u] = fmav<V>(__ldg(vab + e), p_at(__ldg(cib + e)), acc[u]);
-#pragma unroll
-        for (int u = 0; u < kClR; ++u) {
-          const int li = j0 + u * CB;
-          if (li < len) row_done(li, acc[u]);
+          for (int u = 0; u < kClR; ++u) {
+            const int li = j0 + u * CB;
+            if (li < ge) row_done(li, acc[u]);
+          }
+        }
+      } else {
+        for (int li = gb + tid; li < ge; li += CB) {
+          int64_t e0, e1;
+          if (mstaged) {
+            e0 = s_ro[li];
+            e1 = s_ro[li + 1];
+            if (e1 < e0) e1 = e0;
+          } else {
+            row_range(rp, c0 + li, P.nnz, e0, e1, &glob->bad_csr);
+          }
+          V acc = V(0);
+          for (int64_t e = e0; e < e1; ++e) {
+            const int32_t c = mstaged ? s_ci[e] : __ldg(ci + e);
+            const V v = mstaged ? s_val[e] : __ldg(val + e);
+            acc = fmav<V>(v, p_at(c), acc);
+          }
+          row_done(li, acc);
         }
       }
-    } else {
-      for (int li = tid; li < len; li += CB) {
-        int64_t e0, e1;
-        if (mstaged) {
-          e0 = s_ro[li];
-          e1 = s_ro[li + 1];
-          if (e1 < e0) e1 = e0;
-        } else {
-          row_range(rp, c0 + li, P.nnz, e0, e1, &glob->bad_csr);
-        }
-        V acc = V(0);
-        for (int64_t e = e0; e < e1; ++e) {
-          const int32_t c = mstaged ? s_ci[e] : __ldg(ci + e);
-          const V v = mstaged ? s_val[e] : __ldg(val + e);
-          acc = fmav<V>(v, p_at(c), acc);
-        }
-        row_done(li, acc);
-      }
+    };
+    constexpr int kGrpRows = kClGroup * CB;
+    spmv_rows(0, len < kGrpRows ? len : kGrpRows);
+    double pqd = (double)part;
+    for (int gb = kGrpRows; gb < len; gb += kGrpRows) {
+      part = V(0);
+      spmv_rows(gb, len - gb < kGrpRows ? len : gb + kGrpRows);
+      pqd += (double)part;
     }
     SLA_PHASE(1);
-    double v1[1] = {flushed ? pqd + (double)part : (double)part};
+    double v1[1] = {pqd};
     block_sum4<1, CB>(v1, s_red);
     if (tid == 0) s_part[1][0] = v1[0];
     cl.sync();
@@ -887,35 +890,38 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
       int go = 1;
       if (!isfinite(pq)) { status = SLA_NONFINITE; go = 0; }
       else if (!(pq > 0.0)) { status = SLA_BREAKDOWN; go = 0; }
-      else S.alpha = S.rho / pq;
+      else {
+        S.alpha = S.rho / pq;
+        s_vsc[1] = (V)S.alpha;
+      }
       S.go = go;
     }
     __syncthreads();
     SLA_PHASE(2);
     if (!S.go) break;
-    const V va = (V)S.alpha;
+    const V va = s_vsc[1];
     double acc2[2] = {0.0, 0.0};
     V rr_t = V(0), rz_t = V(0);
-    cnt = 0;
-    bool flushed2 = false;
-    for (int li = tid; li < len; li += CB) {
-      const V ri = fmav<V>(-va, sq[li], sr[li]);
-      sr[li] = ri;
-      if constexpr (sizeof(V) == 4) {
-        if (cnt == 8) {  // as for p.q: a group of 8 rows is closed when a ninth arrives
-          acc2[0] = flushed2 ? acc2[0] + (double)rr_t : (double)rr_t;
-          if (JAC) acc2[1] = flushed2 ? acc2[1] + (double)rz_t : (double)rz_t;
-          flushed2 = true;
-          rr_t = rz_t = V(0);
-          cnt = 0;
-        }
-        ++cnt;
+    auto r_rows = [&](int gb, int ge) {
+      for (int li = gb + tid; li < ge; li += CB) {
+        const V ri = fmav<V>(-va, sq[li], sr[li]);
+        sr[li] = ri;
+        rr_t = fmav<V>(ri, ri, rr_t);
+        if (JAC) rz_t = fmav<V>(ri, sd[li] * ri, rz_t);
       }
-      rr_t = fmav<V>(ri, ri, rr_t);
-      if (JAC) rz_t = fmav<V>(ri, sd[li] * ri, rz_t);
+    };
+    {
+      constexpr int kGrpRows = kClGroup * CB;
+      r_rows(0, len < kGrpRows ? len : kGrpRows);  // groups of rows as for p.q
+      acc2[0] = (double)rr_t;
+      if (JAC) acc2[1] = (double)rz_t;
+      for (int gb = kGrpRows; gb < len; gb += kGrpRows) {
+        rr_t = rz_t = V(0);
+        r_rows(gb, len - gb < kGrpRows ? len : gb + kGrpRows);
+        acc2[0] += (double)rr_t;
+        if (JAC) acc2[1] += (double)rz_t;
+      }
     }
-    acc2[0] = flushed2 ? acc2[0] + (double)rr_t : (double)rr_t;
-    if (JAC) acc2[1] = flushed2 ? acc2[1] + (double)rz_t : (double)rz_t;
     SLA_PHASE(3);
     if (JAC) {
       block_sum4<2, CB>(acc2, s_red);
@@ -954,6 +960,8 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
         S.beta = rho_new / S.rho;
         S.rho = rho_new;
         S.alpha_prev = S.alpha;
+        s_vsc[0] = (V)S.beta;
+        s_vsc[2] = (V)S.alpha;
         pending = 0;
         go = 1;
       }
