@@ -362,6 +362,10 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
 #pragma unroll
       for (int u = 0; u < kStage; ++u) {
       const int li = j0 + u * kResBlock;
+      // warps with no row left branch around (fp64 instructions issued with every lane
+      // predicated off would still occupy the fp64 unit); lanes past the outer loop's end are
+      // not active, hence the active mask
+      if (!__any_sync(__activemask(), li < len)) break;
       if (li >= len) continue;
       const int64_t i = c0 + li;
       int64_t e0 = (int64_t)rpa[u], e1 = (int64_t)rpb[u];
@@ -421,6 +425,7 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
 #pragma unroll
       for (int u = 0; u < kStage; ++u) {
         const int li = j0 + u * kResBlock;
+        if (!__any_sync(__activemask(), li < len)) break;  // as in the SpMV
         if (li < len) {
           const V ri = fmav<V>(-va, qv[u], sr[li]);
           sr[li] = ri;
@@ -460,6 +465,7 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
 #pragma unroll
       for (int u = 0; u < kStage; ++u) {
         const int li = j0 + u * kResBlock;
+        if (!__any_sync(__activemask(), li < len)) break;  // as in the SpMV
         if (li < len) xg[c0 + li] = fmav<V>(va, sp[li], xv[u]);
       }
     }
