@@ -420,3 +420,29 @@ def test_resident_barrier_timeout_returns_status(monkeypatch):
     xg, infog, _ = sla.sla_cg_solve(dA, b, rtol=1e-10, maxit=2000, loop=sla.SLA_LOOP_GRAPH)
     assert info2.status == 0 and abs(info2.iters - infog.iters) <= 1
     assert rel(x.cpu().numpy(), xg.cpu().numpy()) <= X_TOL_F64
+
+
+@pytest.mark.parametrize("m", [140, 150])
+def test_batched_f32_several_row_groups(m):
+    # 40 fp32 systems on 4-CTA clusters: m = 140 keeps the row offsets on chip (streamed SpMV with
+    # batched entry loads), m = 150 does not fit them (plain row loop); both give each thread more
+    # than 8 rows, so the fp32 partial sums go through several row groups
+    batch = 40
+    w = config3(m=m, batch=batch)
+    P = to_dev(w.A, np.float32)
+    vals, b, g = t(w.values_b), t(w.b), t(w.g)
+    x, infos, _ = sla.sla_cg_solve_batched(P, vals, b, rtol=w.rtol, maxit=5000)
+    gb, gv, ainfos = sla.sla_cg_adjoint_batched(P, vals, x, g, rtol=w.rtol, maxit=5000)
+    assert infos[0].path == "cluster"
+    xs, gbs, gvs = x.cpu().numpy(), gb.cpu().numpy(), gv.cpu().numpy()
+    for s in (0, 17, batch - 1):
+        v64 = w.values_b[s].astype(np.float64)
+        ref = oracle.cg(w.A.row_ptr, w.A.col_idx, v64, w.b[s].astype(np.float64), rtol=w.rtol, maxit=5000)
+        assert infos[s].status == ref["status"] == 0
+        assert abs(infos[s].iters - ref["iters"]) <= max(1, ITER_SLACK_F32 * ref["iters"])
+        assert rel(xs[s], ref["x"]) <= TOL_F32
+        adj = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, v64, xs[s].astype(np.float64),
+                                w.g[s].astype(np.float64), rtol=w.rtol, maxit=5000)
+        assert ainfos[s].status == 0
+        assert rel(gbs[s], adj["grad_b"]) <= TOL_F32
+        assert rel(gvs[s], adj["grad_values"]) <= TOL_F32
