@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kBlock, SLA_SPMV_MIN_BLOCKS) cg_spmv_step(Prob
   // rows i +- m) then fall inside the band just read by other blocks and hit in L2, where
   // contiguous per-block chunks would re-read them from DRAM.  T is capped so that every block
   // has a tile when n is small.
-  const int64_t per_block = (P.n + P.G - 1) / P.G;
+  const int64_t per_block = ((int64_t)P.n + P.G - 1) / P.G;  // 64-bit: n may be close to 2^31
   const int64_t T = per_block < (int64_t)kBlock * RPT ? per_block : (int64_t)kBlock * RPT;
   const int64_t ntiles = (P.n + T - 1) / T;
   double pq = 0.0;
