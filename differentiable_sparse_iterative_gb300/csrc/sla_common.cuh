@@ -108,6 +108,13 @@ __device__ __forceinline__ void chunk_of(int64_t n, int G, int bx, int64_t &c0, 
   c1 = n * (bx + 1) / G;
 }
 
+// As chunk_of, with every chunk boundary but the end rounded down to a multiple of `align` rows
+// (64-bit throughout), so that only the last block has a ragged tail.
+__device__ __forceinline__ void chunk_aligned(int64_t n, int G, int bx, int64_t align, int64_t &c0, int64_t &c1) {
+  c0 = (n * bx / G) / align * align;
+  c1 = bx + 1 == G ? n : (n * (bx + 1) / G) / align * align;
+}
+
 __device__ __forceinline__ double warp_sum(double v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
