@@ -570,11 +570,14 @@ __global__ void __launch_bounds__(kBlock, (JAC && sizeof(V) == 8) ? SLA_UPD_MIN_
   const V *__restrict__ q = P.q + vo;
   const V *__restrict__ dinv = JAC ? P.dinv + vo : nullptr;
   V *__restrict__ z = JAC ? P.z + vo : nullptr;
-  // groups of kUpd rows per thread: all loads of a group first, then the arithmetic; chunks are
-  // whole groups except the last block's, so no block ends in a partly empty group
+  // groups of kUpd rows per thread: all loads of a group first, then the arithmetic.  When every
+  // block has many groups, chunks are whole groups except the last block's (no block ends in a
+  // partly empty group); with few groups per block that rounding would unbalance the blocks.
   constexpr int kUpd = SLA_UPD_ROWS;
+  constexpr int64_t kGroupRows = (int64_t)kUpd * kBlock;
   int64_t c0, c1;
-  chunk_aligned(P.n, P.G, bx, (int64_t)kUpd * kBlock, c0, c1);
+  if ((int64_t)P.n >= 16 * kGroupRows * (int64_t)P.G) chunk_aligned(P.n, P.G, bx, kGroupRows, c0, c1);
+  else chunk_of(P.n, P.G, bx, c0, c1);
   double acc[2] = {0.0, 0.0};
   for (int64_t g0 = c0 + threadIdx.x; g0 < c1; g0 += (int64_t)kUpd * kBlock) {
     V qv[kUpd], rv[kUpd], dv[kUpd];
