@@ -45,6 +45,12 @@ def b_iter(n, nnz, s_v, s_p, jacobi):
     return nnz * (s_v + 4) + (n + 1) * s_p + V * n * s_v
 
 
+def b_iter_batched(batch, n, nnz, s_v):
+    """Algorithmic bytes of one batched iteration: every system's values and vectors, the shared
+    pattern (col_idx, int32 row_ptr) read once."""
+    return batch * (nnz * s_v + 9 * n * s_v) + nnz * 4 + (n + 1) * 4
+
+
 def b_gradvalues(n, nnz, s_v, s_p):
     """One grad_values pass: col_idx read + gv write, row pointers, lambda and x reads."""
     return nnz * (s_v + 4) + (n + 1) * s_p + 2 * n * s_v
@@ -355,12 +361,10 @@ def run_batched(args, w, dev, rank, world):
     it_a = [sum(i.iters for i in r[4]) for r in recs]
     tot_s = (sum(fwd_ms) + sum(adj_ms)) / 1e3
     s_v = 4 if dt == torch.float32 else 8
-    Bi_sys = nnz * s_v + 9 * n * s_v  # per system-iteration; the shared pattern is read once per iteration
     peak, peak_kind = measured_peaks()
     max_it = [max(i.iters for i in r[3]) for r in recs]
     tr = None if args.grid_m else profiled_traffic(canonical_name(args.config))  # counters are for the full-size workload
-    # bytes of one batched iteration (all systems): B values+vectors, one pattern read
-    Bi_batch = B * Bi_sys + nnz * 4 + (n + 1) * 4
+    Bi_batch = b_iter_batched(B, n, nnz, s_v)
     achieved = Bi_batch * sum(max_it) / (sum(fwd_ms) / 1e3) / 1e9
     return {
         "metric": METRIC, "value": (sum(it_f) + sum(it_a)) / tot_s, "unit": "system-iters/s", "n_gpus": world,

@@ -1,0 +1,57 @@
+"""Host-side pieces of the benchmark that the reported numbers rest on (CPU only)."""
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from workloads import config_by_name, canonical_name  # noqa: E402
+
+
+# algorithmic bytes per CG iteration: nnz (s_v + 4) + (n + 1) s_p + V n s_v, V = 9 (11 with Jacobi)
+@pytest.mark.parametrize("name,n,nnz,s_p,jac,expect", [
+    ("poisson64", 4096, 20224, 4, False, 553_988),
+    ("poisson1000", 1_000_000, 4_996_000, 4, False, 135_952_004),
+    ("diffusion4096_jacobi", 16_777_216, 83_869_696, 4, True, 2_549_940_228),
+])
+def test_bytes_per_iteration(name, n, nnz, s_p, jac, expect):
+    w = config_by_name(name, m=64) if name == "poisson64" else None
+    if w is not None:
+        assert (w.A.n, w.A.nnz) == (n, nnz)
+    assert bench.b_iter(n, nnz, 8, s_p, jac) == expect
+
+
+def test_bytes_per_iteration_int64_rowptr():
+    # 13000 x 13000 Poisson: nnz = 5 m^2 - 4 m, 8-byte row pointers
+    m = 13000
+    n, nnz = m * m, 5 * m * m - 4 * m
+    assert nnz == 844_948_000
+    assert bench.b_iter(n, nnz, 8, 8, False) == 23_659_376_008
+
+
+def test_bytes_per_batched_iteration():
+    w = config_by_name("diffusion128_batch64")
+    assert (w.batch, w.A.n, w.A.nnz) == (64, 16384, 81408)
+    assert bench.b_iter_batched(64, 16384, 81408, 4) == 58_980_356
+
+
+def test_workload_aliases():
+    assert canonical_name("poisson1000") == "config2"
+    assert canonical_name("config4") == "config4"
+    assert config_by_name("poisson64").name == config_by_name("config1").name
+
+
+def test_traffic_record_requires_matching_sources(monkeypatch, tmp_path):
+    rec = {"config2": {"dram_bytes_per_iter": 1, "source": "x", "csrc_sha256": "0" * 64}}
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "csrc_sha256", lambda: "0" * 64)
+    assert bench.profiled_traffic("config2")["dram_bytes_per_iter"] == 1
+    monkeypatch.setattr(bench, "csrc_sha256", lambda: "1" * 64)
+    assert bench.profiled_traffic("config2") is None
+
