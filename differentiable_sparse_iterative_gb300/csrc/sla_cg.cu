@@ -975,10 +975,11 @@ sla_status dispatch_precond(const Prob<V, I> &P, const sla_cg_opts *o, cudaStrea
 
 template <typename V, typename I>
 Prob<V, I> make_prob(const sla_csr *A, int64_t batch, const void *values, int64_t val_stride, const void *b,
-                     const void *x0, const sla_cg_opts *o, void *x, double *history, void *ws, bool jacobi) {
+                     const void *x0, const sla_cg_opts *o, void *x, double *history, void *ws, bool jacobi,
+                     bool halo_ws) {
   Prob<V, I> P;
   memset(&P, 0, sizeof(P));
-  Layout L = make_layout(A->n, batch, sizeof(V), jacobi);
+  Layout L = make_layout(A->n, batch, sizeof(V), jacobi, halo_ws);
   char *w = (char *)ws;
   P.rp = (const I *)A->row_ptr;
   P.ci = A->col_idx;
@@ -995,6 +996,7 @@ Prob<V, I> make_prob(const sla_csr *A, int64_t batch, const void *values, int64_
   P.partials = (double *)(w + L.partials);
   P.ctl = (Ctl *)(w + L.ctl);
   P.glob = (Glob *)(w + L.glob);
+  P.halo = halo_ws ? (uint32_t *)(w + L.halo) : nullptr;
   P.history = history;
   P.val_stride = val_stride;
   P.nnz = A->nnz;
@@ -1009,19 +1011,19 @@ Prob<V, I> make_prob(const sla_csr *A, int64_t batch, const void *values, int64_
 
 sla_status cg_entry(const sla_csr *A, int64_t batch, const void *values, int64_t val_stride, const void *b,
                     const void *x0, const sla_cg_opts *o, void *x, sla_cg_info *info, double *history, void *ws,
-                    cudaStream_t st) {
+                    cudaStream_t st, bool halo_ws) {
   const bool jac = o->precond == SLA_PRECOND_JACOBI;
   if (A->dtype == SLA_F64) {
     if (A->rowptr_type == SLA_I64)
-      return dispatch_precond(make_prob<double, int64_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac),
+      return dispatch_precond(make_prob<double, int64_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac, halo_ws),
                               o, st, info, batch);
-    return dispatch_precond(make_prob<double, int32_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac),
+    return dispatch_precond(make_prob<double, int32_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac, halo_ws),
                             o, st, info, batch);
   }
   if (A->rowptr_type == SLA_I64)
-    return dispatch_precond(make_prob<float, int64_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac),
+    return dispatch_precond(make_prob<float, int64_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac, halo_ws),
                             o, st, info, batch);
-  return dispatch_precond(make_prob<float, int32_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac),
+  return dispatch_precond(make_prob<float, int32_t>(A, batch, values, val_stride, b, x0, o, x, history, ws, jac, halo_ws),
                           o, st, info, batch);
 }
 

@@ -50,10 +50,13 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size
 
 // Workspace layout (offsets in bytes from the workspace base).
 struct Layout {
-  size_t glob, ctl, partials, r, p0, p1, q, dinv, z, total;
+  size_t glob, ctl, partials, r, p0, p1, q, dinv, z, halo, total;
 };
 
-__host__ __device__ inline Layout make_layout(int64_t n, int64_t batch, size_t vbytes, bool jacobi) {
+// halo: one bit per row (shared by the systems of a batch), set for the rows that another block of
+// the resident kernel reads; last, so that a layout without it keeps every other offset.
+__host__ __device__ inline Layout make_layout(int64_t n, int64_t batch, size_t vbytes, bool jacobi,
+                                              bool with_halo = true) {
   Layout L;
   size_t off = 0;
   L.glob = off; off += align256(sizeof(Glob));
@@ -66,6 +69,7 @@ __host__ __device__ inline Layout make_layout(int64_t n, int64_t batch, size_t v
   L.q = off; off += vec;
   L.dinv = off; off += jacobi ? vec : 0;
   L.z = off; off += jacobi ? vec : 0;  // z = M^{-1} r, kept so the SpMV step reads one vector
+  L.halo = off; off += with_halo ? align256(sizeof(uint32_t) * (size_t)((n + 31) / 32)) : 0;
   L.total = off;
   return L;
 }
@@ -92,6 +96,7 @@ struct Prob {
   int64_t nnz;
   int64_t maxit;
   double rtol;
+  uint32_t *halo;        // row bitmap of the resident kernel, or NULL (then every row is published)
   int32_t n;
   int32_t G;             // blocks per system
   int32_t batch;

@@ -25,7 +25,8 @@ sla_status read_info(const Ctl *ctl, const Glob *glob, int64_t batch, cudaStream
 // Device-resident CG for `batch` systems sharing A's pattern (values at values + s*val_stride).
 sla_status cg_entry(const sla_csr *A, int64_t batch, const void *values, int64_t val_stride, const void *b,
                     const void *x0, const sla_cg_opts *o, void *x, sla_cg_info *info, double *history, void *ws,
-                    cudaStream_t st);
+                    cudaStream_t st,
+                    bool halo_ws = true);
 
 size_t workspace_bytes(int64_t n, int64_t batch, int dtype, int precond);
 

@@ -221,6 +221,8 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
   V *sr = reinterpret_cast<V *>(sbuf + 2 * kResBlock);
   V *sp = sr + cap;
   V *sd = JAC ? sp + cap : nullptr;
+  // halo bits of the block's rows (bit i: row i is read by another block), words from c0 / 32
+  uint32_t *s_halo = reinterpret_cast<uint32_t *>((JAC ? sd : sp) + cap);
   __shared__ ResScalars S;
   const unsigned G = gridDim.x;
   const int bid = blockIdx.x, tid = threadIdx.x;
@@ -277,10 +279,32 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
       acc5[2] = fma((double)ri, (double)(di * ri), acc5[2]);
     }
   }
+  // Mark the rows this block reads from other blocks.  Each iteration a block then publishes r
+  // and p for its marked rows only (for a grid stencil about 30 % of them); the others never
+  // leave shared memory.  Without the bitmap (P.halo NULL) every row is published.
+  const bool has_halo = P.halo != nullptr;
+  if (has_halo) {
+    for (int li = tid; li < len; li += kResBlock) {
+      int64_t e0, e1;
+      row_range(rp, c0 + li, P.nnz, e0, e1, &glob->bad_csr);
+      for (int64_t e = e0; e < e1; ++e) {
+        const int32_t c = ci[e];
+        if ((uint32_t)c < (uint32_t)P.n && ((int64_t)c < c0 || (int64_t)c >= c1))
+          atomicOr(P.halo + (c >> 5), 1u << (c & 31));
+      }
+    }
+  }
   // x = x0 (or 0) after every block has read x0 (x0 may be the same buffer as x)
   block_publish<5>(acc5, sbuf, partB);
   const bool ok0 = grid_barrier(arrive, timeout, G, epoch, wc);
   for (int li = tid; li < len; li += kResBlock) xg[c0 + li] = P.x0 ? P.x0[c0 + li] : V(0);
+  const int64_t hw0 = c0 >> 5;  // first bitmap word of the block's rows
+  if (has_halo && len > 0)
+    for (int64_t w = hw0 + tid; w <= ((c1 - 1) >> 5); w += kResBlock) s_halo[w - hw0] = __ldcg(P.halo + w);
+  auto published = [&](int li) -> bool {
+    const int64_t i = c0 + li;
+    return !has_halo || ((s_halo[(i >> 5) - hw0] >> (i & 31)) & 1u);
+  };
 
   // thread 0 of every block takes the same decisions from the same totals
   int status = SLA_NOT_CONVERGED, pending = 0;
@@ -345,7 +369,7 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
       const V z = JAC ? sd[li] * rl : rl;
       const V pv = first ? z : fmav<V>(vb, sp[li], z);
       sp[li] = pv;
-      pn_pub[c0 + li] = pv;
+      if (published(li)) pn_pub[c0 + li] = pv;
     }
     __syncthreads();
     SLA_PHASE(0);
@@ -429,7 +453,7 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
         if (li < len) {
           const V ri = fmav<V>(-va, qv[u], sr[li]);
           sr[li] = ri;
-          rpub[c0 + li] = ri;
+          if (published(li)) rpub[c0 + li] = ri;
           rr_t = fmav<V>(ri, ri, rr_t);
           if (JAC) rz_t = fmav<V>(ri, sd[li] * ri, rz_t);
         }
@@ -1034,7 +1058,9 @@ void resident_shape(int64_t n, size_t vbytes, bool jac, const ResidentLimits &L,
   int g = (int)std::min<int64_t>(L.sms, std::max<int64_t>(1, (n + 255) / 256));
   g = std::min(g, kMaxBlocksPerSystem);
   const int64_t rows = (n + g - 1) / g;
-  const size_t need = (size_t)2 * kResBlock * sizeof(double) + (size_t)rows * nvec * vbytes;
+  // reduction buffer, r, p (1/diag) of the rows, and their halo bitmap words (rows / 32 + 2)
+  const size_t need = (size_t)2 * kResBlock * sizeof(double) + (size_t)rows * nvec * vbytes +
+                      sizeof(uint32_t) * (size_t)(rows / 32 + 2);
   if (need + kResStaticSmem > (size_t)L.max_smem) return;
   // the barrier counter counts 2 barriers per iteration plus setup, G arrivals each
   if ((double)(2 * maxit + 2) * g >= 4.0e9) return;
@@ -1195,6 +1221,8 @@ sla_status run_resident(Prob<V, I> P, cudaStream_t stream, sla_cg_info *info) {
   // fresh loop state: counters, flags and the control block start at zero
   cudaError_t e = cudaMemsetAsync(P.glob, 0, sizeof(Glob), stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(P.ctl, 0, sizeof(Ctl), stream);
+  if (e == cudaSuccess && P.halo)
+    e = cudaMemsetAsync(P.halo, 0, sizeof(uint32_t) * (size_t)((P.n + 31) / 32), stream);
   if (e != cudaSuccess) return fail(e);
   WaitCfg wc{0u, kSpinLimit};
   if (const char *e = getenv("SLA_TEST_GRID_WAIT_EXTRA")) wc.extra = (unsigned)strtoul(e, nullptr, 10);

@@ -83,7 +83,7 @@ extern "C" SLA_API sla_status sla_cg_solve_static(const sla_csr *A, const void *
       !is_aligned(b, vsz) || !is_aligned(x0, vsz) || !is_aligned(x, vsz) || !is_aligned(history, 8))
     return SLA_INVALID_ARG;
   const bool jac = opts->precond == SLA_PRECOND_JACOBI;
-  const Layout L = make_layout(A->n, 1, vsz, jac);
+  const Layout L = make_layout(A->n, 1, vsz, jac, /*with_halo=*/false);  // the host loop needs no row bitmap
   if (L.total > kStaticScratchBytes) return SLA_WORKSPACE_TOO_SMALL;
   if (A->n == 0) {
     if (info) {
@@ -103,7 +103,7 @@ extern "C" SLA_API sla_status sla_cg_solve_static(const sla_csr *A, const void *
   cudaStream_t st = (cudaStream_t)stream;
   // The init kernel of the solve zeroes the control block and the loop state in the scratch, so
   // nothing left by an earlier call is read; vectors are written before they are read.
-  s = cg_entry(A, 1, A->values, 0, b, x0, &o, x, nullptr, history, ws, st);
+  s = cg_entry(A, 1, A->values, 0, b, x0, &o, x, nullptr, history, ws, st, /*halo_ws=*/false);
   if (s != SLA_OK || !info) return s;
   Ctl hc;
   Glob hg;
