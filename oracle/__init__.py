@@ -8,13 +8,15 @@ code with the CUDA path.
 Each function follows "torch-sla: Differentiable Sparse Linear Algebra with
 Adjoint Solvers and Sparse Tensor Parallelism for PyTorch" (Chi, Wen),
 technical summary, Methodology sections 1 (native iterative solver, .matvec /
-.solve) and 2 (adjoint differentiation framework, linear systems); see the C
-source ``sla_oracle.c`` for the readings taken where the pages are silent.
+.solve) and 2 (adjoint differentiation framework: linear systems, and the
+eigenvalue gradient v_i v_j on the pattern); see the C source ``sla_oracle.c``
+for the readings taken where the pages are silent.
 
 Parity pins live in ``tests/test_oracle_*.py``.  Every oracle function is
 pinned there against something other than itself (dense linear algebra on
 tiny grids, closed-form eigenvalues and CG bounds, finite termination, the
-adjoint identity, central finite differences, exact scaling invariants).
+adjoint identity, central finite differences, exact scaling invariants, the
+closed-form fundamental mode of the five-point Laplacian).
 """
 from __future__ import annotations
 
@@ -59,6 +61,8 @@ def _bind(lib):
     lib.orc_cg_adjoint.argtypes = [i64, p, p, p, p, p, ctypes.c_double, i64, ctypes.c_int, p, p,
                                    ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]
     lib.orc_cg_adjoint.restype = ctypes.c_int
+    lib.orc_eig_grad_values.argtypes = [i64, p, p, i64, p, p, p]
+    lib.orc_eig_grad_values.restype = None
     return lib
 
 
@@ -159,3 +163,55 @@ def cg_batched(row_ptr, col_idx, values_b, b_b, rtol, maxit, precond=0, history=
 def cg_adjoint_batched(row_ptr, col_idx, values_b, x_b, g_b, rtol, maxit, precond=0, lib=None) -> list:
     return [cg_adjoint(row_ptr, col_idx, values_b[s], x_b[s], g_b[s], rtol, maxit, precond, lib)
             for s in range(values_b.shape[0])]
+
+
+# --------------------------------------------------------------------------- eigenvalue problems
+#
+# Methodology 2, eigenvalue problems: the gradient of an eigenvalue with respect to the matrix is
+# v_i v_j on the sparsity pattern (Hellmann-Feynman).  The eigenpair itself has a plain
+# definition, so the oracle takes it from a dense symmetric eigensolver (numpy.linalg.eigh) on
+# small matrices; how the GPU reaches it (inverse iteration) does not enter the oracle.
+
+def dense(row_ptr, col_idx, values) -> np.ndarray:
+    """The CSR matrix as a dense fp64 array (small n only)."""
+    rp, ci, v = _csr(row_ptr, col_idx, values)
+    n = rp.shape[0] - 1
+    D = np.zeros((n, n))
+    for i in range(n):
+        for e in range(rp[i], rp[i + 1]):
+            D[i, ci[e]] += v[e]
+    return D
+
+
+def sign_normalise(v: np.ndarray) -> np.ndarray:
+    """The eigenvector's sign: the sum of its entries is made >= 0 (ties: the first nonzero entry > 0)."""
+    s = float(np.sum(v))
+    if s < 0.0 or (s == 0.0 and v[np.flatnonzero(v)[0]] < 0.0):
+        return -v
+    return v
+
+
+def eig_smallest(row_ptr, col_idx, values, k: int = 1):
+    """The k smallest eigenvalues (ascending) and unit eigenvectors [k, n] of symmetric A (dense eigh)."""
+    D = dense(row_ptr, col_idx, values)
+    if not np.array_equal(D, D.T):
+        raise ValueError("eig_smallest needs a symmetric matrix")
+    mu, U = np.linalg.eigh(D)
+    V = np.stack([sign_normalise(U[:, s]) for s in range(k)])
+    return mu[:k].copy(), V
+
+
+def eig_grad_values(row_ptr, col_idx, V, w=None, lib=None) -> np.ndarray:
+    """grad_values[e] = sum_s w_s v_s[i] v_s[j] on A's pattern (V: [k, n]; w: k weights or None = ones)."""
+    lib = lib or load()
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int64)
+    ci = np.ascontiguousarray(col_idx, dtype=np.int32)
+    n = rp.shape[0] - 1
+    V = np.ascontiguousarray(np.atleast_2d(V), dtype=np.float64)
+    k = V.shape[0] if V.size else 0
+    wc = None if w is None else np.ascontiguousarray(w, dtype=np.float64)
+    if wc is not None and wc.shape[0] != k:
+        raise ValueError("one weight per eigenvector")
+    gv = np.empty(ci.shape[0], dtype=np.float64)
+    lib.orc_eig_grad_values(n, _ptr(rp), _ptr(ci), k, _ptr(V), _ptr(wc), _ptr(gv))
+    return gv

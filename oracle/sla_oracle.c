@@ -18,6 +18,8 @@
  *     Ax=b the backward solves A^T lambda = dL/dx once, and the gradient with
  *     respect to the matrix is -lambda_i x_j on the sparsity pattern only;
  *     graph O(1), memory O(n + nnz);
+ *   - Methodology, 2, eigenvalue problems: d mu / d A_ij = v_i v_j
+ *     (Hellmann-Feynman), an outer product on the sparsity pattern only;
  *   - Significance: the native backend uses Jacobi preconditioning.
  * The pages do not spell out the CG variant, the stopping rule or the
  * treatment of breakdown.  Readings taken here (textbook Hestenes-Stiefel CG,
@@ -179,4 +181,27 @@ int orc_cg_adjoint(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, co
   int st = orc_cg(n, row_ptr, col_idx, values, g, NULL, rtol, maxit, precond, grad_b, NULL, iters, rel_res);
   orc_grad_values(n, row_ptr, col_idx, grad_b, x, grad_values);
   return st;
+}
+
+/*
+ * Eigenvalue gradient (Methodology, 2 "Adjoint differentiation framework",
+ * eigenvalue problems): for a symmetric A and a unit eigenvector v of a simple
+ * eigenvalue mu, the Hellmann-Feynman theorem gives d mu / d A_ij = v_i v_j, so
+ * the gradient lives on the stored entries only.  For a weighted sum
+ * L = sum_s w_s mu_s of k eigenvalues (eigenvectors V[s*n .. s*n+n-1]):
+ *   grad_values[e] = sum over s = 0..k-1, in that order, of w_s * (v_s[i] * v_s[j])
+ * for the stored entry e = (i, j).  w == NULL means every w_s = 1.
+ */
+void orc_eig_grad_values(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, int64_t k, const double *V,
+                         const double *w, double *grad_values) {
+  for (int64_t i = 0; i < n; ++i)
+    for (int64_t e = row_ptr[i]; e < row_ptr[i + 1]; ++e) {
+      const int64_t j = col_idx[e];
+      double acc = 0.0;
+      for (int64_t s = 0; s < k; ++s) {
+        const double ws = w ? w[s] : 1.0;
+        acc = acc + ws * (V[s * n + i] * V[s * n + j]);
+      }
+      grad_values[e] = acc;
+    }
 }

@@ -17,13 +17,17 @@ oracle library ``lib`` (see ``oracle.load``) disagrees with:
     not symmetric);
   * the exact scaling invariants sum_k gv_k values_k = -<g, x> and
     <grad_b, b> = <g, x> (from x(tA) = x/t and x(tb) = t x);
+  * for eigenvalue problems: the closed-form fundamental mode of the
+    five-point Laplacian, central differences of eigenvalues of the perturbed
+    (non-symmetric) matrix, and the identity sum_e gv_e A_e = v^T A v = mu;
   * the Jacobi special case: with constant diagonal 4 the preconditioned
     iterates equal the unpreconditioned ones bit for bit (scaling by 1/4 is
     exact in binary floating point), and in general Jacobi PCG iterates equal
     D^{-1/2} times the plain CG iterates of the symmetrically scaled system.
 
 The method is that of "torch-sla" (Chi, Wen), technical summary, Methodology
-section 2 (adjoint differentiation framework, linear systems).
+section 2 (adjoint differentiation framework, linear systems and eigenvalue
+problems).
 """
 from __future__ import annotations
 
@@ -355,6 +359,86 @@ def pin_adjoint_zero_gradient(lib):
     assert not adj["grad_b"].any() and not adj["grad_values"].any()
 
 
+# --------------------------------------------------------------------------- eigenvalue problems
+
+def poisson_fundamental(m: int):
+    """Smallest eigenvalue 4 - 4cos(pi/(m+1)) of the five-point Laplacian and its unit eigenvector,
+    sin(pi (a+1)/(m+1)) sin(pi (b+1)/(m+1)) at grid point (a, b)."""
+    th = np.pi / (m + 1)
+    s = np.sin(th * np.arange(1, m + 1))
+    v = np.outer(s, s).reshape(-1)
+    return 4.0 - 4.0 * np.cos(th), v / np.linalg.norm(v)
+
+
+def _eigs_general(D: np.ndarray) -> np.ndarray:
+    """Eigenvalues of a (possibly non-symmetric) dense matrix, real parts ascending."""
+    return np.sort(np.linalg.eigvals(D).real)
+
+
+def _entry_fd(D, i, j, which, weights, h=1e-6):
+    """Central difference of sum_s w_s mu_s (mu ascending) for a perturbation of the single entry (i, j)."""
+    Dp, Dm = D.copy(), D.copy()
+    Dp[i, j] += h
+    Dm[i, j] -= h
+    ep, em = _eigs_general(Dp), _eigs_general(Dm)
+    return sum(w * (ep[s] - em[s]) for s, w in zip(which, weights)) / (2.0 * h)
+
+
+def pin_eig_smallest_closed_form(lib):
+    for m in [4, 9, 16]:
+        A = poisson_5pt(m)
+        mu, V = oracle.eig_smallest(A.row_ptr, A.col_idx, A.values)
+        mu0, v0 = poisson_fundamental(m)
+        assert abs(mu[0] - mu0) <= 1e-13, (m, mu[0], mu0)
+        assert np.max(np.abs(V[0] - v0)) <= 1e-12, m  # the fundamental mode is positive: no sign flip
+
+
+def pin_eig_grad_fd(lib):
+    # Hellmann-Feynman against central differences of the smallest eigenvalue, one stored entry
+    # perturbed at a time (the perturbed matrix is not symmetric, so its eigenvalues are taken
+    # by the general eigensolver)
+    # (a random graph Laplacian plus a shift would often be disconnected, with a repeated smallest
+    # eigenvalue; the Dirichlet diffusion operator's is simple)
+    A = diffusion_dirichlet(5, np.random.default_rng(1).lognormal(0.0, 0.5, 2 * 5 * 6))
+    D = oracle.dense(A.row_ptr, A.col_idx, A.values)
+    mu, V = oracle.eig_smallest(A.row_ptr, A.col_idx, A.values, 2)
+    assert mu[1] - mu[0] > 0.5  # a simple eigenvalue
+    gv = oracle.eig_grad_values(A.row_ptr, A.col_idx, V[:1], lib=lib)
+    rows = np.repeat(np.arange(A.n), np.diff(A.row_ptr))
+    off = np.flatnonzero(rows != A.col_idx)
+    picks = [0, int(off[0]), int(off[len(off) // 2]), A.nnz - 1, int(np.argmax(np.abs(gv)))]
+    for e in picks:
+        fd = _entry_fd(D, rows[e], A.col_idx[e], [0], [1.0])
+        assert abs(fd - gv[e]) <= 1e-7, (e, fd, gv[e])
+
+
+def pin_eig_grad_weighted_fd(lib):
+    # L = 2 mu_0 - 0.5 mu_1: weights and the second eigenvector enter
+    A = diffusion_dirichlet(5, np.random.default_rng(2).lognormal(0.0, 0.7, 2 * 5 * 6))
+    D = oracle.dense(A.row_ptr, A.col_idx, A.values)
+    mu, V = oracle.eig_smallest(A.row_ptr, A.col_idx, A.values, 3)
+    assert min(mu[1] - mu[0], mu[2] - mu[1]) > 0.2
+    w = [2.0, -0.5]
+    gv = oracle.eig_grad_values(A.row_ptr, A.col_idx, V[:2], w, lib=lib)
+    rows = np.repeat(np.arange(A.n), np.diff(A.row_ptr))
+    for e in [1, A.nnz // 3, int(np.argmax(np.abs(gv))), int(np.argmin(gv))]:
+        fd = _entry_fd(D, rows[e], A.col_idx[e], [0, 1], w)
+        assert abs(fd - gv[e]) <= 1e-7, (e, fd, gv[e])
+
+
+def pin_eig_grad_rayleigh_identity(lib):
+    # sum_e gv_e A_e = sum_s w_s v_s^T A v_s = sum_s w_s mu_s (exact identity up to rounding), and
+    # with no eigenvector the gradient is zero
+    A = diffusion_dirichlet(7, np.random.default_rng(4).lognormal(0.0, 0.5, 2 * 7 * 8))
+    mu, V = oracle.eig_smallest(A.row_ptr, A.col_idx, A.values, 3)
+    w = np.array([1.0, -3.0, 0.25])
+    gv = oracle.eig_grad_values(A.row_ptr, A.col_idx, V, w, lib=lib)
+    assert abs(float(gv @ A.values) - float(w @ mu)) <= 1e-12 * float(np.abs(w) @ np.abs(mu))
+    gv1 = oracle.eig_grad_values(A.row_ptr, A.col_idx, V[:1], lib=lib)
+    assert abs(float(gv1 @ A.values) - mu[0]) <= 1e-13
+    assert not oracle.eig_grad_values(A.row_ptr, A.col_idx, np.zeros((0, A.n)), lib=lib).any()
+
+
 ALL_PINS = [
     pin_spmv_dense, pin_spmv_exact_integers, pin_dot,
     pin_cg_vs_dense, pin_cg_exact_rational, pin_finite_termination, pin_eigen_closed_form_and_bound,
@@ -362,4 +446,5 @@ ALL_PINS = [
     pin_status_codes,
     pin_adjoint_identity, pin_adjoint_fd, pin_adjoint_config1_loss, pin_adjoint_invariants,
     pin_adjoint_zero_gradient,
+    pin_eig_smallest_closed_form, pin_eig_grad_fd, pin_eig_grad_weighted_fd, pin_eig_grad_rayleigh_identity,
 ]
