@@ -13,7 +13,8 @@ GB/s of the fused CG iteration against the measured copy bandwidth, and the adjo
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}] [--config NAME]
 
 NAME: poisson64, poisson1000 (default), diffusion128_batch64, diffusion4096_jacobi,
-poisson13000_int64 (short aliases config1 .. config5).
+poisson13000_int64 (short aliases config1 .. config5); eig_poisson: the smallest eigenpair
+of the 1M-DOF Poisson matrix by inverse iteration on the CG plus its eigenvalue gradient.
 
 With N > 1 the script runs under torch.distributed.run; every rank solves its own
 independent system of the same size (the single-system solve has no exchange step:
@@ -73,13 +74,18 @@ def fp64_peak_tflops(clocks=None):
     return 152 * 2 * 2 * mhz * 1e6 / 1e12
 
 
+# The sources the CG iteration kernels are compiled from: the kernels whose DRAM bytes per
+# iteration profiles/traffic.json records.  Host-side files (argument checks, entry points) and
+# the eigenvalue solver's file hold none of them.
+CG_KERNEL_SOURCES = ("sla_common.cuh", "sla_tma.cuh", "sla_cg.cu", "sla_resident.cu")
+
+
 def csrc_sha256():
-    import glob
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "differentiable_sparse_iterative_gb300", "csrc", "*"))):
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
+    for name in CG_KERNEL_SOURCES:
+        h.update(name.encode())
+        with open(os.path.join(ROOT, "differentiable_sparse_iterative_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
@@ -466,6 +472,119 @@ def cpu_baseline(w, iters):
                       f"pass, {dt:.1f} s on one host core"}
 
 
+EIG_METRIC = "smallest eigenpair (inverse iteration on CG) + eigenvalue gradient, 2D Poisson fp64: CG iters/sec"
+
+
+def b_eig_grad(n, nnz, s_v, s_p):
+    """One eigenvalue-gradient pass (one eigenvector): col_idx read + gv write, row pointers, v read once
+    (the gathers of v[col] assumed served by cache)."""
+    return nnz * (s_v + 4) + (n + 1) * s_p + n * s_v
+
+
+def run_eig(args, rank, world, local_rank):
+    """Eigenvalue workload: the smallest eigenpair of the 2D Poisson matrix by inverse iteration
+    (each step one inner CG solve) and the Hellmann-Feynman gradient v_i v_j on the pattern.  The
+    metric counts the inner CG iterations; the eigen-solve's time includes the host-driven outer
+    loop (one scalar read per step)."""
+    import torch
+    import differentiable_sparse_iterative_gb300 as sla
+    from workloads import poisson_5pt, config_by_name
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    m = args.grid_m or 1000
+    A_np = poisson_5pt(m)
+    n, nnz = A_np.n, A_np.nnz
+    s_v, s_p = 8, A_np.row_ptr.dtype.itemsize
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    A = sla.CSRMatrix.from_numpy(A_np.row_ptr, A_np.col_idx, A_np.values, dev)
+    ws = torch.empty(sla.sla_eig_workspace_bytes(n, torch.float64), dtype=torch.uint8, device=dev)
+    gv = torch.empty(nnz, dtype=torch.float64, device=dev)
+    ones = torch.ones(n, dtype=torch.float64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    tol = 1e-10
+
+    def step():
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        mu, v, info = sla.sla_eig_smallest(A, v0=ones, tol=tol, workspace=ws)
+        e1.record(stream)
+        sla.sla_eig_grad_values(A, v, out=gv)
+        e2.record(stream)
+        return e0, e1, e2, info
+
+    for _ in range(args.warmup):
+        flush_l2(flush)
+        step()
+    torch.cuda.synchronize()
+    launches0 = sla.sla_launch_count()
+    recs = []
+    with ClockSampler(local_rank) as clk:
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            flush_l2(flush)
+            recs.append(step())
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    launches = sla.sla_launch_count() - launches0
+    eig_ms = [r[0].elapsed_time(r[1]) for r in recs]
+    grad_ms = [r[1].elapsed_time(r[2]) for r in recs]
+    # The gradient kernel alone: in a step it starts after the eigen-solve's final synchronisation,
+    # so its interval there includes the host's launch latency.  Here each launch follows an L2
+    # flush that keeps the GPU busy while the host enqueues it (arguments marshalled once).
+    import ctypes
+    cs = sla._csr_struct(A)
+    v_last = sla.sla_eig_smallest(A, v0=ones, tol=tol, workspace=ws)[1]
+    lib, sh = sla.lib(), stream.cuda_stream
+    kern_ms = []
+    for _ in range(20):
+        flush_l2(flush)
+        ka, kb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ka.record(stream)
+        st = lib.sla_eig_grad_values(ctypes.byref(cs), 1, v_last.data_ptr(), None, gv.data_ptr(), sh)
+        kb.record(stream)
+        assert st == 0
+        kern_ms.append((ka, kb))
+    torch.cuda.synchronize()
+    kern_ms = [a.elapsed_time(b) for a, b in kern_ms]
+    infos = [r[3] for r in recs]
+    inner = sum(i.inner_iters for i in infos)
+    tot_s = (sum(eig_ms) + sum(grad_ms)) / 1e3
+    tot_s_all, inner_all = aggregate_over_ranks(tot_s, inner, world, dev)
+    Bi = b_iter(n, nnz, s_v, s_p, False)
+    Bg = b_eig_grad(n, nnz, s_v, s_p)
+    peak, peak_kind = measured_peaks()
+    achieved = Bi * inner / (sum(eig_ms) / 1e3) / 1e9
+    grad_gbs = Bg / (statistics.mean(kern_ms) / 1e3) / 1e9
+    th = np.pi / (m + 1)
+    mu_exact = 4.0 - 4.0 * np.cos(th)
+    out = {
+        "metric": EIG_METRIC, "value": inner_all / tot_s_all, "unit": "iters/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.mean([a + b for a, b in zip(eig_ms, grad_ms)]),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (the five-point Laplacian; start vector all ones)",
+        "config": {"workload": f"eig_poisson{m}", "n": n, "nnz": nnz, "tol": tol, "inner_factor": 0.01,
+                   "step": "smallest eigenpair by inverse iteration + Hellmann-Feynman gradient on the pattern",
+                   "l2": "flushed between steps (256 MB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "outer_steps": statistics.mean(i.iters for i in infos), "inner_iters": inner / len(infos),
+        "time_to_eigenpair_ms": statistics.mean(eig_ms), "eig_grad_ms": statistics.mean(grad_ms),
+        "eig_grad_kernel_ms": statistics.mean(kern_ms),
+        "mu": infos[-1].mu, "mu_rel_err_vs_closed_form": abs(infos[-1].mu - mu_exact) / mu_exact,
+        "status": sorted({i.status for i in infos}),
+        "roofline": {"kernel": "inner CG solves (the engine the solve picks)", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                     "bytes_per_iter": Bi, "traffic": None},
+        "eig_grad_roofline": {"kernel": "eig_grad_kernel", "bound": "hbm", "achieved": grad_gbs, "peak": peak,
+                              "unit": "GB/s", "frac": grad_gbs / peak, "bytes_per_launch": Bg,
+                              "timing": "20 launches, each after a 256 MB L2 flush, CUDA events"},
+        "gpu_launches": int(launches), "wall_s": wall, "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline(config_by_name("poisson1000", m=m), args.cpu_iters)
+    return out
+
+
 def run_reference(args, rank, world):
     """The oracle arm: the fp64 CPU oracle timed on the host, on bounded samples of the workload."""
     from workloads import config_by_name
@@ -531,7 +650,8 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    out = run_ours(args, rank, world, local_rank)
+    out = run_eig(args, rank, world, local_rank) if args.config == "eig_poisson" else \
+        run_ours(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

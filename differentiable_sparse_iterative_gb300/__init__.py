@@ -9,8 +9,8 @@ Method: "torch-sla: Differentiable Sparse Linear Algebra with Adjoint Solvers an
 Sparse Tensor Parallelism for PyTorch" (Chi, Wen), technical summary —
 Methodology 1 (autograd-aware .matvec / .solve; one matrix or a batch sharing a
 pattern), Methodology 2 (adjoint: one A^T lambda = dL/dx solve, grad_b = lambda,
-grad_A = -lambda_i x_j on the pattern, O(1) graph nodes), Significance (Jacobi
-preconditioning).
+grad_A = -lambda_i x_j on the pattern, O(1) graph nodes; eigenvalue problems:
+d mu / d A_ij = v_i v_j on the pattern), Significance (Jacobi preconditioning).
 
     A = CSRMatrix(row_ptr, col_idx, values)          # CUDA tensors
     x = solve(A, b, rtol=1e-8)                       # autograd: grads to values and b
@@ -36,6 +36,8 @@ __all__ = [
     "SLA_PRECOND_NONE", "SLA_PRECOND_JACOBI", "SLA_LOOP_AUTO", "SLA_LOOP_HOST", "SLA_LOOP_GRAPH",
     "SLA_LOOP_RESIDENT", "SLA_LOOP_CLUSTER", "SLA_OK", "SLA_NOT_CONVERGED", "SLA_BREAKDOWN", "SLA_INVALID_ARG",
     "SLA_BAD_CSR", "SLA_NONFINITE", "SLA_WORKSPACE_TOO_SMALL", "SLA_TIMEOUT", "SLA_CUDA_ERROR",
+    "EigInfo", "sla_eig_workspace_bytes", "sla_eig_smallest", "sla_eig_grad_values", "EigSmallest",
+    "eigsh_smallest",
 ]
 
 _lib = None
@@ -344,3 +346,103 @@ def solve(A: CSRMatrix, b: torch.Tensor, rtol: float = 1e-8, maxit: int = 10000,
 def matvec(A: CSRMatrix, x: torch.Tensor) -> torch.Tensor:
     """y = A x through libsla (not differentiable; see solve for the differentiable path)."""
     return sla_spmv(A, x)
+
+
+# --------------------------------------------------------------------------- eigenvalue problems
+
+@dataclass
+class EigInfo:
+    iters: int          # outer steps (inner CG solves)
+    inner_iters: int    # CG iterations over all steps
+    mu: float
+    residual: float     # ||A v - mu v||
+    status: int
+
+    @property
+    def status_name(self) -> str:
+        return sla_status_string(self.status)
+
+
+def sla_eig_workspace_bytes(n: int, dtype: torch.dtype, precond: int = SLA_PRECOND_NONE) -> int:
+    return lib().sla_eig_workspace_bytes(int(n), _DT[dtype], int(precond))
+
+
+def sla_eig_smallest(A: CSRMatrix, v0: Optional[torch.Tensor] = None, tol: Optional[float] = None,
+                     maxit: int = 1000, inner_factor: float = 0.01, inner_maxit: int = 100000,
+                     precond: int = SLA_PRECOND_NONE, loop: int = SLA_LOOP_AUTO,
+                     workspace: Optional[torch.Tensor] = None):
+    """Smallest eigenpair of SPD A by inverse iteration on the CG.  Returns (mu, v, EigInfo).
+
+    v0 defaults to all ones (for a diffusion or Laplace operator it overlaps the positive
+    fundamental mode); tol defaults to 1e-10 for float64 and 1e-5 for float32 data.
+    """
+    dt, dev = A.values.dtype, A.values.device
+    if tol is None:
+        tol = 1e-10 if dt == torch.float64 else 1e-5
+    v = torch.ones(A.n, dtype=dt, device=dev) if v0 is None else v0.detach().clone()
+    need = sla_eig_workspace_bytes(A.n, dt, precond)
+    ws = workspace if workspace is not None and workspace.numel() * workspace.element_size() >= need else \
+        torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    o = _abi.sla_eig_opts()
+    o.tol, o.maxit, o.inner_factor, o.inner_maxit = float(tol), int(maxit), float(inner_factor), int(inner_maxit)
+    o.precond, o.loop = int(precond), int(loop)
+    info = _abi.sla_eig_info()
+    st = lib().sla_eig_smallest(ctypes.byref(_csr_struct(A)), _dev_ptr(v, dt, "v"), ctypes.byref(o),
+                                ctypes.byref(info), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(dev))
+    _check(st, "sla_eig_smallest")
+    ei = EigInfo(int(info.iters), int(info.inner_iters), float(info.mu), float(info.residual), int(info.status))
+    return ei.mu, v, ei
+
+
+def sla_eig_grad_values(A: CSRMatrix, V: torch.Tensor, weights=None,
+                        out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """grad_values[e] = sum_s w_s V[s, row(e)] V[s, col(e)] on A's pattern (V: [k, n] or [n]; asynchronous)."""
+    dt, dev = A.values.dtype, A.values.device
+    V2 = V.reshape(1, -1) if V.dim() == 1 else V
+    k = int(V2.shape[0])
+    if out is None:
+        out = torch.empty(A.nnz, dtype=dt, device=dev)
+    w = None
+    if weights is not None:
+        wl = [float(x) for x in weights]
+        if len(wl) != k:
+            raise ValueError("one weight per eigenvector")
+        w = (ctypes.c_double * max(k, 1))(*wl)
+    _check(lib().sla_eig_grad_values(ctypes.byref(_csr_struct(A)), k, _dev_ptr(V2, dt, "V") if k else None, w,
+                                     _dev_ptr(out, dt, "grad_values"), _stream(dev)), "sla_eig_grad_values")
+    return out
+
+
+class EigSmallest(torch.autograd.Function):
+    """(mu, v) = smallest eigenpair of SPD A; mu is differentiable with respect to A's values.
+
+    Backward (Hellmann-Feynman): d mu / d values[e] = v[row(e)] * v[col(e)] on the pattern, so the
+    node saves v and A only.  v is returned as a constant (no eigenvector gradient).
+    """
+
+    @staticmethod
+    def forward(ctx, row_ptr, col_idx, values, tol, maxit, precond):
+        A = CSRMatrix(row_ptr, col_idx, values)
+        mu, v, info = sla_eig_smallest(A, tol=tol, maxit=maxit, precond=precond)
+        if info.status == SLA_NOT_CONVERGED:
+            warnings.warn(f"EigSmallest.forward: residual {info.residual:.3e} after {info.iters} steps")
+        elif info.status != SLA_OK:
+            raise SlaError(info.status, "EigSmallest.forward")
+        ctx.save_for_backward(row_ptr, col_idx, values, v)
+        ctx.mark_non_differentiable(v)
+        return torch.tensor(mu, dtype=values.dtype, device=values.device), v
+
+    @staticmethod
+    def backward(ctx, g_mu, g_v):
+        row_ptr, col_idx, values, v = ctx.saved_tensors
+        if not ctx.needs_input_grad[2]:
+            return None, None, None, None, None, None
+        A = CSRMatrix(row_ptr, col_idx, values)
+        gv = sla_eig_grad_values(A, v, weights=[float(g_mu)])
+        return None, None, gv, None, None, None
+
+
+def eigsh_smallest(A: CSRMatrix, tol: Optional[float] = None, maxit: int = 1000,
+                   precond: int = SLA_PRECOND_NONE):
+    """Differentiable smallest eigenvalue of SPD A (gradient to A.values) and its eigenvector."""
+    return EigSmallest.apply(A.row_ptr, A.col_idx, A.values, tol, maxit, precond)

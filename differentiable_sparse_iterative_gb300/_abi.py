@@ -18,7 +18,8 @@ SLA_LOOP_AUTO, SLA_LOOP_HOST, SLA_LOOP_GRAPH, SLA_LOOP_RESIDENT, SLA_LOOP_CLUSTE
 EXPORTS = [
     "sla_status_string", "sla_last_cuda_error", "sla_version", "sla_launch_count", "sla_cg_workspace_bytes",
     "sla_validate_csr", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values", "sla_cg_solve_batched",
-    "sla_cg_adjoint_batched", "sla_cg_solve_static",
+    "sla_cg_adjoint_batched", "sla_cg_solve_static", "sla_eig_workspace_bytes", "sla_eig_smallest",
+    "sla_eig_grad_values",
 ]
 
 
@@ -36,6 +37,16 @@ class sla_cg_opts(ctypes.Structure):
 class sla_cg_info(ctypes.Structure):
     _fields_ = [("iters", ctypes.c_int64), ("rel_res", ctypes.c_double), ("status", ctypes.c_int32),
                 ("path", ctypes.c_int32), ("kernels", ctypes.c_int64)]
+
+
+class sla_eig_opts(ctypes.Structure):
+    _fields_ = [("tol", ctypes.c_double), ("maxit", ctypes.c_int64), ("inner_factor", ctypes.c_double),
+                ("inner_maxit", ctypes.c_int64), ("precond", ctypes.c_int32), ("loop", ctypes.c_int32)]
+
+
+class sla_eig_info(ctypes.Structure):
+    _fields_ = [("iters", ctypes.c_int64), ("inner_iters", ctypes.c_int64), ("mu", ctypes.c_double),
+                ("residual", ctypes.c_double), ("status", ctypes.c_int32), ("pad", ctypes.c_int32)]
 
 
 def bind(lib):
@@ -59,8 +70,13 @@ def bind(lib):
     lib.sla_cg_solve_batched.argtypes = [C, i64, P, P, P, O, P, I, P, P, sz, P]
     lib.sla_cg_adjoint_batched.argtypes = [C, i64, P, P, P, O, P, P, I, P, sz, P]
     lib.sla_cg_solve_static.argtypes = [C, P, P, O, P, I, P, P]
+    lib.sla_eig_workspace_bytes.argtypes = [i64, i32, i32]
+    lib.sla_eig_workspace_bytes.restype = sz
+    lib.sla_eig_smallest.argtypes = [C, P, ctypes.POINTER(sla_eig_opts), ctypes.POINTER(sla_eig_info), P, sz, P]
+    lib.sla_eig_grad_values.argtypes = [C, i64, P, ctypes.POINTER(ctypes.c_double), P, P]
     for name in ["sla_validate_csr", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
-                 "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_cg_solve_static"]:
+                 "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_cg_solve_static", "sla_eig_smallest",
+                 "sla_eig_grad_values"]:
         getattr(lib, name).restype = i32
     return lib
 

@@ -177,6 +177,8 @@ int grid_for(int64_t work, int per_block_rows) {
   return (int)want;
 }
 
+}  // namespace
+
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 sla_status check_csr(const sla_csr *A, bool need_values) {
@@ -199,6 +201,8 @@ sla_status check_vec(const void *p, const sla_csr *A, bool allow_null) {
   return aligned(p, A->dtype == SLA_F64 ? 8 : 4) ? SLA_OK : SLA_INVALID_ARG;
 }
 
+namespace {
+
 sla_status check_opts(const sla_cg_opts *o) {
   if (!o) return SLA_INVALID_ARG;
   if (!(o->rtol >= 0.0) || !std::isfinite(o->rtol)) return SLA_INVALID_ARG;
@@ -215,12 +219,6 @@ sla_status check_ws(const sla_csr *A, int64_t batch, const sla_cg_opts *o, void 
   if (ws_bytes < workspace_bytes(A->n, batch, A->dtype, o->precond)) return SLA_WORKSPACE_TOO_SMALL;
   return SLA_OK;
 }
-
-#define SLA_CHECK(expr)            \
-  do {                             \
-    sla_status st_ = (expr);       \
-    if (st_ != SLA_OK) return st_; \
-  } while (0)
 
 void fill_empty(sla_cg_info *info, int64_t batch) {
   if (!info) return;

@@ -36,6 +36,19 @@ bool resident_fits(int64_t n, int64_t batch, int dtype, int precond, int64_t max
 // True when every system of a batch fits one thread-block cluster (cluster-resident CG kernel).
 bool cluster_fits(int64_t n, int64_t batch, int dtype, int precond);
 
+// Argument checks of the entry points (no CUDA call): p aligned to a bytes; a CSR descriptor
+// (sizes, types, non-NULL arrays, alignment; values too when need_values); a vector of A's
+// dtype (NULL allowed when allow_null or n == 0).
+bool aligned(const void *p, size_t a);
+sla_status check_csr(const sla_csr *A, bool need_values);
+sla_status check_vec(const void *p, const sla_csr *A, bool allow_null);
+
+#define SLA_CHECK(expr)            \
+  do {                             \
+    sla_status st_ = (expr);       \
+    if (st_ != SLA_OK) return st_; \
+  } while (0)
+
 // grad_values[s][k] = -lambda_s[row(k)] * x_s[col(k)] for `batch` systems (asynchronous).
 sla_status grad_values_entry(const sla_csr *A, int64_t batch, const void *lambda, const void *x, void *gv,
                              cudaStream_t st);

@@ -232,6 +232,67 @@ SLA_API sla_status sla_cg_adjoint_batched(const sla_csr *pattern, int64_t batch,
                                   const void *g, const sla_cg_opts *opts, void *grad_b, void *grad_values,
                                   sla_cg_info *info, void *workspace, size_t ws_bytes, void *stream);
 
+/* ---------------------------------------------------------------- eigenvalue problems */
+
+/* Options of sla_eig_smallest. */
+typedef struct sla_eig_opts {
+  double tol;           /* stop when ||A v - mu v||_2 <= tol * mu (v of unit norm) */
+  int64_t maxit;        /* outer steps (inner CG solves) at most */
+  double inner_factor;  /* CG rtol of step k = inner_factor * ||A v_k - mu_k v_k|| / mu_k, in (0, 1) */
+  int64_t inner_maxit;  /* CG iterations per solve at most (an unconverged solve still counts as a step) */
+  int32_t precond;      /* sla_precond of the inner CG */
+  int32_t loop;         /* sla_loop of the inner CG */
+} sla_eig_opts;
+
+typedef struct sla_eig_info {
+  int64_t iters;        /* outer steps taken (inner solves) */
+  int64_t inner_iters;  /* CG iterations over all inner solves */
+  double mu;            /* the eigenvalue estimate v^T A v of the returned v */
+  double residual;      /* ||A v - mu v||_2 of the returned v */
+  int32_t status;       /* SLA_OK, SLA_NOT_CONVERGED (maxit steps), SLA_BREAKDOWN (zero start vector, or
+                           v^T A v <= 0: A not positive definite), SLA_NONFINITE, or an inner solve's failure */
+  int32_t pad;
+} sla_eig_info;
+
+/*
+ * Bytes of device workspace sla_eig_smallest needs for n unknowns (0 for invalid arguments):
+ * the inner CG's workspace plus two vectors and the step's reduction scratch.
+ */
+SLA_API size_t sla_eig_workspace_bytes(int64_t n, int32_t dtype, int32_t precond);
+
+/*
+ * Smallest eigenpair (mu, v) of a symmetric positive definite A (TS Methodology 1: the ".eigsh"
+ * API; the summary names no eigensolver).  Inverse iteration on this library's CG: from the
+ * start vector, every step normalises y to v = y / ||y||, forms mu = v^T A v and the residual
+ * ||A v - mu v||, and, until the residual is at most tol * mu, solves A y = v by CG started from
+ * y = v / mu with the rtol opts->inner_factor * residual / mu (an inexact solve whose accuracy
+ * follows the eigen-residual: inexact inverse iteration, Golub and Ye, BIT 40, 2000).
+ * Converges for a start vector not orthogonal to the eigenvector, at the rate mu_1 / mu_2 per step.
+ *   v          device, n entries of A->dtype: the start vector on entry (not all zero), the unit
+ *              eigenvector on return, its sign chosen so that sum_i v_i >= 0.
+ *   info       host, required: steps, CG iterations, mu, residual and status.
+ *   workspace  device, >= sla_eig_workspace_bytes(n, dtype, opts->precond), 256-byte aligned.
+ * The host drives the outer loop (one 40-byte read of the step's scalars per step) and
+ * synchronises the stream; the inner solves run on the device as sla_cg_solve does.
+ * n = 0 returns SLA_INVALID_ARG (no eigenpair).
+ */
+SLA_API sla_status sla_eig_smallest(const sla_csr *A, void *v, const sla_eig_opts *opts, sla_eig_info *info,
+                                    void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Eigenvalue gradient on the sparsity pattern (TS Methodology 2, eigenvalue problems:
+ * d mu / d A_ij = v_i v_j, Hellmann-Feynman).  For L = sum_s w_s mu_s over k eigenpairs with unit
+ * eigenvectors V[s] (s = 0..k-1):
+ *   grad_values[e] = sum over s in order of w_s * (V[s][row(e)] * V[s][col_idx[e]])
+ * evaluated in fp64 without fused multiply-adds, then rounded to A->dtype.
+ *   k          0..16 (k = 0 writes zeros).
+ *   V          device, k x n entries of A->dtype, row-major.
+ *   w          host, k doubles, or NULL for all ones.
+ *   grad_values device, nnz entries (CSR order).  Asynchronous.
+ */
+SLA_API sla_status sla_eig_grad_values(const sla_csr *A, int64_t k, const void *V, const double *w,
+                                       void *grad_values, void *stream);
+
 /* ---------------------------------------------------------------- allocation-free variant */
 
 /*

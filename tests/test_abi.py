@@ -118,3 +118,46 @@ def test_empty_system_needs_no_gpu(lib):
     assert st == 0 and info.status == 0 and info.iters == 0
     assert lib.sla_cg_solve_batched(ctypes.byref(_csr()), 0, 0x10000, 0x10000, None, ctypes.byref(_opts()),
                                     0x10000, None, None, 0x10000, 1 << 20, None) == 0
+
+
+def _eig_opts(tol=1e-10, maxit=10, inner_factor=0.01, inner_maxit=100, precond=0, loop=0):
+    o = _abi.sla_eig_opts()
+    o.tol, o.maxit, o.inner_factor, o.inner_maxit, o.precond, o.loop = tol, maxit, inner_factor, inner_maxit, \
+        precond, loop
+    return o
+
+
+def test_eig_workspace_bytes(lib):
+    f = lib.sla_eig_workspace_bytes
+    assert f(-1, 1, 0) == 0 and f(10, 7, 0) == 0 and f(10, 1, 5) == 0
+    n = 1000
+    assert f(n, 1, 0) >= lib.sla_cg_workspace_bytes(n, 1, 1, 0) + 2 * 8 * n
+    assert f(n, 1, 1) > f(n, 1, 0) > f(n, 0, 0)
+    assert f(n, 1, 0) % 256 == 0
+
+
+def test_eig_argument_rejection_without_gpu(lib):
+    _no_gpu_here()
+    P = 0x10000  # never dereferenced: every case is rejected before any CUDA call
+    ws = 1 << 24
+    info = _abi.sla_eig_info()
+    eig = lib.sla_eig_smallest
+    ok = ctypes.byref(_eig_opts())
+    assert eig(None, P, ok, ctypes.byref(info), P, ws, None) == _abi.SLA_INVALID_ARG
+    assert eig(ctypes.byref(_csr()), P, None, ctypes.byref(info), P, ws, None) == _abi.SLA_INVALID_ARG
+    assert eig(ctypes.byref(_csr()), P, ok, None, P, ws, None) == _abi.SLA_INVALID_ARG
+    for bad in [dict(tol=-1.0), dict(tol=float("nan")), dict(maxit=-1), dict(inner_factor=0.0),
+                dict(inner_factor=1.0), dict(inner_maxit=-1), dict(precond=2), dict(loop=9)]:
+        assert eig(ctypes.byref(_csr()), P, ctypes.byref(_eig_opts(**bad)), ctypes.byref(info), P, ws,
+                   None) == _abi.SLA_INVALID_ARG, bad
+    assert eig(ctypes.byref(_csr(n=0, nnz=0)), P, ok, ctypes.byref(info), P, ws, None) == _abi.SLA_INVALID_ARG
+    assert eig(ctypes.byref(_csr()), None, ok, ctypes.byref(info), P, ws, None) == _abi.SLA_INVALID_ARG
+    assert eig(ctypes.byref(_csr()), P + 4, ok, ctypes.byref(info), P, ws, None) == _abi.SLA_INVALID_ARG
+    assert eig(ctypes.byref(_csr()), P, ok, ctypes.byref(info), P + 16, ws, None) == _abi.SLA_INVALID_ARG
+    assert eig(ctypes.byref(_csr()), P, ok, ctypes.byref(info), P, 64, None) == _abi.SLA_WORKSPACE_TOO_SMALL
+    grad = lib.sla_eig_grad_values
+    assert grad(ctypes.byref(_csr()), -1, P, None, P, None) == _abi.SLA_INVALID_ARG
+    assert grad(ctypes.byref(_csr()), 17, P, None, P, None) == _abi.SLA_INVALID_ARG
+    assert grad(ctypes.byref(_csr()), 1, None, None, P, None) == _abi.SLA_INVALID_ARG
+    assert grad(ctypes.byref(_csr()), 1, P, None, None, None) == _abi.SLA_INVALID_ARG
+    assert grad(ctypes.byref(_csr(nnz=0)), 1, P, None, None, None) == _abi.SLA_OK  # nothing to write

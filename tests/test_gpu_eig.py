@@ -1,0 +1,168 @@
+"""Eigenvalue problems on the GPU against the fp64 oracle.
+
+The gradient kernel (d mu / d A_ij = v_i v_j on the pattern, weighted over k eigenvectors) is
+compared bit for bit with the oracle on arbitrary vectors: both sides evaluate the same fp64
+expression with separately rounded operations.  The eigenpair from inverse iteration is compared
+with the oracle's dense symmetric eigensolver and with the five-point Laplacian's closed form, to
+tolerances derived from the stopping test: a unit vector with ||A v - mu v|| <= tol * mu is within
+tol * mu / gap of the eigenvector (sin theta bound), and its Rayleigh quotient within
+(tol * mu)^2 / gap of the eigenvalue, plus rounding.
+"""
+import numpy as np
+import pytest
+
+from gpu_helpers import sla, oracle, torch, rel, to_dev, t
+from oracle_pins import poisson_fundamental
+from workloads import poisson_5pt, diffusion_dirichlet, random_spd
+
+pytestmark = pytest.mark.gpu
+
+EPS64 = np.finfo(np.float64).eps
+
+
+def _vec_bound(tol, mu, gap, n, eps=EPS64):
+    return 10.0 * tol * mu / gap + 100.0 * np.sqrt(n) * eps
+
+
+# --------------------------------------------------------------------------- gradient kernel
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+@pytest.mark.parametrize("k", [1, 3, 16])
+def test_eig_grad_values_bit_exact(dtype, k):
+    A = random_spd(777, 5.0, 3, long_rows=2)
+    rng = np.random.default_rng(40 + k)
+    V = rng.standard_normal((k, A.n)).astype(dtype)
+    w = rng.standard_normal(k)
+    gv = sla.sla_eig_grad_values(to_dev(A, dtype), t(V), weights=w).cpu().numpy()
+    ref = oracle.eig_grad_values(A.row_ptr, A.col_idx, V.astype(np.float64), w).astype(dtype)
+    assert np.array_equal(gv, ref)
+    # unit weights by default; k = 0 gives zeros
+    gv1 = sla.sla_eig_grad_values(to_dev(A, dtype), t(V[:1])).cpu().numpy()
+    assert np.array_equal(gv1, oracle.eig_grad_values(A.row_ptr, A.col_idx, V[:1].astype(np.float64)).astype(dtype))
+    z = sla.sla_eig_grad_values(to_dev(A, dtype), t(np.zeros((0, A.n), dtype))).cpu().numpy()
+    assert not z.any()
+
+
+def test_eig_grad_values_ragged_rows_int64():
+    # rows of length 0..40 and an int64 row_ptr, several warps' worth of row groups with a ragged tail
+    rng = np.random.default_rng(9)
+    n = 32 * 37 + 5
+    lens = rng.integers(0, 41, n)
+    rp = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    ci = np.concatenate([np.sort(rng.choice(n, L, replace=False)) for L in lens]).astype(np.int32)
+    vals = rng.standard_normal(rp[-1])
+    dA = sla.CSRMatrix.from_numpy(rp, ci, vals, "cuda:0")
+    V = rng.standard_normal((2, n))
+    gv = sla.sla_eig_grad_values(dA, t(V), weights=[0.5, -2.0]).cpu().numpy()
+    assert np.array_equal(gv, oracle.eig_grad_values(rp, ci, V, [0.5, -2.0]))
+
+
+# --------------------------------------------------------------------------- eigenpair
+
+@pytest.mark.parametrize("m", [16, 32])
+def test_eig_smallest_poisson_closed_form(m):
+    A = poisson_5pt(m)
+    mu, v, info = sla.sla_eig_smallest(to_dev(A), tol=1e-10)
+    mu0, v0 = poisson_fundamental(m)
+    th = np.pi / (m + 1)
+    gap = 2.0 * (np.cos(th) - np.cos(2 * th))
+    assert info.status == sla.SLA_OK and info.iters > 0
+    assert info.residual <= 1e-10 * info.mu
+    assert abs(mu - mu0) <= 1e-12 * mu0 + 20 * EPS64 * 8.0
+    assert np.linalg.norm(v.cpu().numpy() - v0) <= _vec_bound(1e-10, mu0, gap, A.n)
+
+
+@pytest.mark.parametrize("precond", [0, 1])
+@pytest.mark.parametrize("loop", [sla.SLA_LOOP_AUTO, sla.SLA_LOOP_GRAPH, sla.SLA_LOOP_RESIDENT])
+def test_eig_smallest_matches_dense_oracle(loop, precond):
+    m = 30
+    A = diffusion_dirichlet(m, np.random.default_rng(17).lognormal(0.0, 0.5, 2 * m * (m + 1)))
+    mu_o, V_o = oracle.eig_smallest(A.row_ptr, A.col_idx, A.values, 2)
+    gap = mu_o[1] - mu_o[0]
+    tol = 1e-10
+    mu, v, info = sla.sla_eig_smallest(to_dev(A), tol=tol, precond=precond, loop=loop)
+    assert info.status == sla.SLA_OK, info
+    assert abs(mu - mu_o[0]) <= 1e-11 * mu_o[0]
+    vg = v.cpu().numpy()
+    assert abs(np.linalg.norm(vg) - 1.0) <= 1e-13
+    assert vg.sum() >= 0.0  # sign convention, as the oracle's
+    assert np.linalg.norm(vg - V_o[0]) <= _vec_bound(tol, mu_o[0], gap, A.n)
+
+
+def test_eig_smallest_float32():
+    m = 24
+    A = poisson_5pt(m)
+    mu, v, info = sla.sla_eig_smallest(to_dev(A, np.float32), tol=1e-5)
+    mu0, v0 = poisson_fundamental(m)
+    assert info.status == sla.SLA_OK, info
+    assert abs(mu - mu0) <= 1e-4 * mu0
+    assert rel(v.cpu().numpy(), v0) <= 1e-3
+
+
+def test_eig_smallest_status_cases():
+    A = poisson_5pt(10)
+    dA = to_dev(A)
+    # a zero start vector: no direction to iterate on
+    _, _, info = sla.sla_eig_smallest(dA, v0=torch.zeros(A.n, dtype=torch.float64, device="cuda:0"))
+    assert info.status == sla.SLA_BREAKDOWN and info.iters == 0
+    # negative definite: the first Rayleigh quotient is negative, before any solve
+    neg = sla.CSRMatrix.from_numpy(A.row_ptr, A.col_idx, -A.values, "cuda:0")
+    _, _, info = sla.sla_eig_smallest(neg)
+    assert info.status == sla.SLA_BREAKDOWN and info.iters == 0 and info.inner_iters == 0
+    # maxit = 0: the start vector, normalised, with its Rayleigh quotient and residual
+    v0 = np.random.default_rng(2).standard_normal(A.n)
+    mu, v, info = sla.sla_eig_smallest(dA, v0=t(v0), maxit=0)
+    assert info.status == sla.SLA_NOT_CONVERGED and info.iters == 0
+    u = v0 / np.linalg.norm(v0)
+    u = u if u.sum() >= 0 else -u
+    assert np.allclose(v.cpu().numpy(), u, rtol=0, atol=1e-15)
+    Au = oracle.spmv(A.row_ptr, A.col_idx, A.values, u)
+    assert abs(mu - u @ Au) <= 1e-13 * abs(u @ Au)
+    assert abs(info.residual - np.linalg.norm(Au - (u @ Au) * u)) <= 1e-12 * np.linalg.norm(Au)
+    # an invalid option is rejected before any launch
+    with pytest.raises(sla.SlaError):
+        sla.sla_eig_smallest(dA, inner_factor=1.5)
+
+
+# --------------------------------------------------------------------------- autograd
+
+def test_eigsh_smallest_gradient():
+    m = 20
+    A = diffusion_dirichlet(m, np.random.default_rng(5).lognormal(0.0, 0.5, 2 * m * (m + 1)))
+    vals = t(A.values).requires_grad_(True)
+    dA = sla.CSRMatrix(t(A.row_ptr), t(A.col_idx), vals)
+    mu, v = sla.eigsh_smallest(dA, tol=1e-11)
+    assert not v.requires_grad
+    (3.0 * mu).backward()
+    mu_o, V_o = oracle.eig_smallest(A.row_ptr, A.col_idx, A.values, 2)
+    assert abs(float(mu) - mu_o[0]) <= 1e-11 * mu_o[0]
+    ref = 3.0 * oracle.eig_grad_values(A.row_ptr, A.col_idx, V_o[:1])
+    assert rel(vals.grad.cpu().numpy(), ref) <= 1e-8
+
+
+# --------------------------------------------------------------------------- full size
+
+@pytest.mark.slow
+def test_eig_smallest_poisson1000_sampled():
+    # 1M unknowns: the eigenpair against the closed form, the eigenvector on a sample of entries
+    m = 1000
+    A = poisson_5pt(m)
+    tol = 1e-10
+    mu, v, info = sla.sla_eig_smallest(to_dev(A), tol=tol)
+    th = np.pi / (m + 1)
+    mu0 = 4.0 - 4.0 * np.cos(th)
+    gap = 2.0 * (np.cos(th) - np.cos(2 * th))
+    assert info.status == sla.SLA_OK, info
+    assert abs(mu - mu0) <= 1e-9 * mu0
+    idx = np.random.default_rng(3).choice(A.n, 2000, replace=False)
+    a, b = idx // m, idx % m
+    s = np.sin(th * np.arange(1, m + 1))
+    v0 = s[a] * s[b] / float(np.sum(s * s))
+    vg = v.cpu().numpy()[idx]
+    assert np.max(np.abs(vg - v0)) <= _vec_bound(tol, mu0, gap, A.n)
+    # its gradient through autograd equals v_i v_j on a sample of stored entries
+    gv = sla.sla_eig_grad_values(to_dev(A), v).cpu().numpy()
+    rows = np.repeat(np.arange(A.n), np.diff(A.row_ptr.astype(np.int64)))
+    vv = v.cpu().numpy()
+    e = np.random.default_rng(4).choice(A.nnz, 2000, replace=False)
+    assert np.array_equal(gv[e], vv[rows[e]] * vv[A.col_idx[e]])
