@@ -149,21 +149,36 @@ __global__ void __launch_bounds__(kBlock) eig_negate(int64_t n, V *__restrict__ 
 
 // ------------------------------------------------------------------------ gradient kernel
 
-// gv[e] = sum_s w_s * (V_s[row(e)] * V_s[col(e)]), summed over s in order in fp64 with separately
-// rounded products and adds, then rounded once to V.  One warp covers 32 consecutive rows: the
-// lanes hold the 33 row starts and walk the rows' entries with lane-strided (coalesced) loads and
-// stores; an entry's row is the last lane whose start is <= the entry (binary search by shuffles).
+// gv[e] = sum_s (w_s * V_s[row(e)]) * V_s[col(e)], summed over s in order from the s = 0 term, in
+// fp64 with separately rounded operations, then rounded once to V.  One warp covers 32 consecutive
+// rows: each lane forms w_0 * V_0[row] for its row (one product per row, none when w_0 = 1, which
+// is exact), the lanes walk the rows' entries with lane-strided (coalesced) loads and stores, and an
+// entry's row is the last lane whose start is <= the entry (binary search by shuffles).  For k = 1
+// an entry costs one fp64 multiply.  The loop over further eigenvectors has a dynamic trip count:
+// an unrolled loop with predicated-off iterations would still occupy the fp64 unit.
 template <typename V, typename I>
-__global__ void __launch_bounds__(kBlock) eig_grad_kernel(int64_t n, int64_t nnz, const I *__restrict__ rp,
+__global__ void __launch_bounds__(kBlock, 4) eig_grad_kernel(int64_t n, int64_t nnz, const I *__restrict__ rp,
                                                           const int32_t *__restrict__ ci, int k,
                                                           const V *__restrict__ vec, EigWeights W,
                                                           V *__restrict__ gv) {
+  __shared__ double sw[kEigMaxVecs];
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < kEigMaxVecs; ++s) sw[s] = W.w[s];  // static indices: no local-memory copy
+  }
+  __syncthreads();
+  const double w0 = sw[0];
   const int lane = threadIdx.x & 31;
   const int64_t warps_total = (int64_t)gridDim.x * kWarps;
   for (int64_t wi = blockIdx.x * (int64_t)kWarps + (threadIdx.x >> 5); wi * 32 < n; wi += warps_total) {
     const int64_t r0 = wi * 32;
     const int64_t rl = r0 + lane;
     const int64_t my_start = rl <= n ? (int64_t)rp[rl] : (int64_t)rp[n];
+    double my_wv = 0.0;
+    if (rl < n) {
+      const double a = (double)vec[rl];
+      my_wv = w0 == 1.0 ? a : __dmul_rn(w0, a);
+    }
     const int64_t rend = r0 + 32 <= n ? r0 + 32 : n;
     int64_t e_begin = __shfl_sync(0xffffffffu, my_start, 0);
     int64_t e_end = (int64_t)rp[rend];
@@ -176,19 +191,19 @@ __global__ void __launch_bounds__(kBlock) eig_grad_kernel(int64_t n, int64_t nnz
         const int64_t st = __shfl_sync(0xffffffffu, my_start, lo + step);
         if (st <= e) lo += step;
       }
+      const double wv0 = __shfl_sync(0xffffffffu, my_wv, lo);
       if (e < e_end) {
         const int32_t c = ci[e];
         const int64_t row = r0 + lo;
         double acc = 0.0;
         if ((uint32_t)c < (uint32_t)n && row < n) {
-          // unrolled to the fixed maximum so that the weights stay in the parameter bank
-#pragma unroll
-          for (int s = 0; s < kEigMaxVecs; ++s) {
-            if (s < k) {
-              const double a = (double)vec[(int64_t)s * n + row];
-              const double b = (double)vec[(int64_t)s * n + c];
-              acc = __dadd_rn(acc, __dmul_rn(W.w[s], __dmul_rn(a, b)));
-            }
+          acc = __dmul_rn(wv0, (double)vec[c]);
+#pragma unroll 1
+          for (int s = 1; s < k; ++s) {
+            const double ws = sw[s];
+            const double a = (double)vec[(int64_t)s * n + row];
+            const double wa = ws == 1.0 ? a : __dmul_rn(ws, a);
+            acc = __dadd_rn(acc, __dmul_rn(wa, (double)vec[(int64_t)s * n + c]));
           }
         }
         gv[e] = (V)acc;

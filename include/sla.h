@@ -283,8 +283,9 @@ SLA_API sla_status sla_eig_smallest(const sla_csr *A, void *v, const sla_eig_opt
  * Eigenvalue gradient on the sparsity pattern (TS Methodology 2, eigenvalue problems:
  * d mu / d A_ij = v_i v_j, Hellmann-Feynman).  For L = sum_s w_s mu_s over k eigenpairs with unit
  * eigenvectors V[s] (s = 0..k-1):
- *   grad_values[e] = sum over s in order of w_s * (V[s][row(e)] * V[s][col_idx[e]])
- * evaluated in fp64 without fused multiply-adds, then rounded to A->dtype.
+ *   grad_values[e] = sum over s in order of (w_s * V[s][row(e)]) * V[s][col_idx[e]]
+ * (the sum starting from the s = 0 term) evaluated in fp64 without fused multiply-adds, then
+ * rounded to A->dtype.
  *   k          0..16 (k = 0 writes zeros).
  *   V          device, k x n entries of A->dtype, row-major.
  *   w          host, k doubles, or NULL for all ones.

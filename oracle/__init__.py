@@ -202,7 +202,7 @@ def eig_smallest(row_ptr, col_idx, values, k: int = 1):
 
 
 def eig_grad_values(row_ptr, col_idx, V, w=None, lib=None) -> np.ndarray:
-    """grad_values[e] = sum_s w_s v_s[i] v_s[j] on A's pattern (V: [k, n]; w: k weights or None = ones)."""
+    """grad_values[e] = sum_s (w_s v_s[i]) v_s[j] on A's pattern (V: [k, n]; w: k weights or None = ones)."""
     lib = lib or load()
     rp = np.ascontiguousarray(row_ptr, dtype=np.int64)
     ci = np.ascontiguousarray(col_idx, dtype=np.int32)

@@ -189,8 +189,9 @@ int orc_cg_adjoint(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, co
  * eigenvalue mu, the Hellmann-Feynman theorem gives d mu / d A_ij = v_i v_j, so
  * the gradient lives on the stored entries only.  For a weighted sum
  * L = sum_s w_s mu_s of k eigenvalues (eigenvectors V[s*n .. s*n+n-1]):
- *   grad_values[e] = sum over s = 0..k-1, in that order, of w_s * (v_s[i] * v_s[j])
- * for the stored entry e = (i, j).  w == NULL means every w_s = 1.
+ *   grad_values[e] = sum over s = 0..k-1, in that order, of (w_s * v_s[i]) * v_s[j]
+ * for the stored entry e = (i, j), the sum starting from the s = 0 term.  w == NULL
+ * means every w_s = 1.
  */
 void orc_eig_grad_values(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, int64_t k, const double *V,
                          const double *w, double *grad_values) {
@@ -200,7 +201,8 @@ void orc_eig_grad_values(int64_t n, const int64_t *row_ptr, const int32_t *col_i
       double acc = 0.0;
       for (int64_t s = 0; s < k; ++s) {
         const double ws = w ? w[s] : 1.0;
-        acc = acc + ws * (V[s * n + i] * V[s * n + j]);
+        const double term = (ws * V[s * n + i]) * V[s * n + j];
+        acc = (s == 0) ? term : acc + term;
       }
       grad_values[e] = acc;
     }

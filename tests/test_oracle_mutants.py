@@ -36,14 +36,13 @@ MUTANTS = [
     ("adjoint_wrong_rhs", "orc_cg(n, row_ptr, col_idx, values, g, NULL,", "orc_cg(n, row_ptr, col_idx, values, x, NULL,"),
     ("x0_residual_sign", "r[i] = b[i] - q[i];", "r[i] = b[i] + q[i];"),
     ("breakdown_test_dropped", "if (!(pq > 0.0)) { status = ORC_BREAKDOWN; goto done; }", ""),
-    ("eig_grad_sign", "acc = acc + ws * (V[s * n + i] * V[s * n + j]);",
-     "acc = acc - ws * (V[s * n + i] * V[s * n + j]);"),
+    ("eig_grad_sign", "acc = (s == 0) ? term : acc + term;", "acc = (s == 0) ? -term : acc - term;"),
     ("eig_grad_drops_weight", "const double ws = w ? w[s] : 1.0;", "const double ws = 1.0;"),
-    ("eig_grad_first_vector_only", "for (int64_t s = 0; s < k; ++s) {", "for (int64_t s = 0; s < 1 && s < k; ++s) {"),
-    ("eig_grad_row_for_column", "acc = acc + ws * (V[s * n + i] * V[s * n + j]);",
-     "acc = acc + ws * (V[s * n + i] * V[s * n + i]);"),
-    ("eig_grad_wrong_vector", "acc = acc + ws * (V[s * n + i] * V[s * n + j]);",
-     "acc = acc + ws * (V[i] * V[j]);"),
+    ("eig_grad_first_vector_only", "acc = (s == 0) ? term : acc + term;", "acc = (s == 0) ? term : acc;"),
+    ("eig_grad_row_for_column", "const double term = (ws * V[s * n + i]) * V[s * n + j];",
+     "const double term = (ws * V[s * n + i]) * V[s * n + i];"),
+    ("eig_grad_wrong_vector", "const double term = (ws * V[s * n + i]) * V[s * n + j];",
+     "const double term = (ws * V[i]) * V[j];"),
 ]
 
 
