@@ -55,3 +55,27 @@ def test_traffic_record_requires_matching_sources(monkeypatch, tmp_path):
     monkeypatch.setattr(bench, "csrc_sha256", lambda: "1" * 64)
     assert bench.profiled_traffic("config2") is None
 
+
+
+def test_eig_gradient_bytes():
+    # col_idx + gradient (nnz (s_v + 4)), row pointers, one eigenvector read once
+    assert bench.b_eig_grad(1_000_000, 4_996_000, 8, 4) == 4_996_000 * 12 + 1_000_001 * 4 + 8_000_000
+
+
+def test_traffic_hash_covers_the_cg_kernel_sources_only(monkeypatch, tmp_path):
+    # the record stays valid across changes to files holding no CG kernel, and not otherwise
+    csrc = tmp_path / "differentiable_sparse_iterative_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for name in bench.CG_KERNEL_SOURCES + ("sla_eig.cu", "sla_api.cu"):
+        (csrc / name).write_text(name)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.csrc_sha256()
+    (csrc / "sla_eig.cu").write_text("changed")
+    (csrc / "sla_api.cu").write_text("changed")
+    assert bench.csrc_sha256() == h0
+    for name in bench.CG_KERNEL_SOURCES:
+        (csrc / name).write_text(name + " changed")
+        assert bench.csrc_sha256() != h0
+        (csrc / name).write_text(name)
+    assert bench.csrc_sha256() == h0
+

@@ -89,6 +89,22 @@ def test_eig_smallest_matches_dense_oracle(loop, precond):
     assert np.linalg.norm(vg - V_o[0]) <= _vec_bound(tol, mu_o[0], gap, A.n)
 
 
+def test_eig_smallest_int64_rowptr_and_ragged_grid():
+    # int64 row pointers; a 45 x 45 grid (2025 rows: several blocks with a ragged tail)
+    m = 45
+    A = poisson_5pt(m, rowptr64=True)
+    assert A.row_ptr.dtype == np.int64
+    mu, v, info = sla.sla_eig_smallest(to_dev(A), tol=1e-10)
+    mu0, v0 = poisson_fundamental(m)
+    th = np.pi / (m + 1)
+    gap = 2.0 * (np.cos(th) - np.cos(2 * th))
+    assert info.status == sla.SLA_OK, info
+    assert abs(mu - mu0) <= 1e-11 * mu0
+    assert np.linalg.norm(v.cpu().numpy() - v0) <= _vec_bound(1e-10, mu0, gap, A.n)
+    gv = sla.sla_eig_grad_values(to_dev(A), v, weights=[-1.5]).cpu().numpy()
+    assert np.array_equal(gv, oracle.eig_grad_values(A.row_ptr, A.col_idx, v.cpu().numpy(), [-1.5]))
+
+
 def test_eig_smallest_float32():
     m = 24
     A = poisson_5pt(m)
