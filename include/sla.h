@@ -13,6 +13,8 @@
  *     gradient with respect to the matrix is -lambda_i x_j on the sparsity
  *     pattern only, so the autograd graph is O(1) and its memory O(n + nnz),
  *     independent of the iteration count;
+ *   - TS Methodology 2, eigenvalue problems: the eigenvalue gradient is the
+ *     outer product v_i v_j on the sparsity pattern (Hellmann-Feynman);
  *   - TS Significance: the native iterative backend is Jacobi preconditioned.
  * Where the summary leaves a step open the library takes the textbook reading:
  * Hestenes-Stiefel CG, stopping when ||r_k||_2 <= rtol * ||b||_2 on the
