@@ -274,7 +274,7 @@ SLA_API size_t sla_eig_workspace_bytes(int64_t n, int32_t dtype, int32_t precond
  *              eigenvector on return, its sign chosen so that sum_i v_i >= 0.
  *   info       host, required: steps, CG iterations, mu, residual and status.
  *   workspace  device, >= sla_eig_workspace_bytes(n, dtype, opts->precond), 256-byte aligned.
- * The host drives the outer loop (one 40-byte read of the step's scalars per step) and
+ * The host drives the outer loop (one 48-byte read of the step's scalars per step) and
  * synchronises the stream; the inner solves run on the device as sla_cg_solve does.
  * n = 0 returns SLA_INVALID_ARG (no eigenpair).
  */
