@@ -30,19 +30,31 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "sla_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_LIB_OMP_PATH = os.path.join(_HERE, "liboracle_omp.so")
 _lib = None
+_lib_omp = None
 
 STATUS = {0: "OK", 1: "NOT_CONVERGED", 2: "BREAKDOWN", 5: "NONFINITE"}
 
 
-def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
-    """Compile the oracle with gcc (-O2 -ffp-contract=off: no fused multiply-add)."""
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH, openmp: bool = False) -> str:
+    """Compile the oracle with gcc (-O2 -ffp-contract=off: no fused multiply-add).
+
+    openmp=True makes the multi-core build of the same file (chunked dot products whose result
+    does not depend on the thread count; see the C source's header)."""
     if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
         tmp = out + f".tmp{os.getpid()}"
-        subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+        flags = ["-fopenmp"] if openmp else []
+        subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", *flags,
                         "-o", tmp, src, "-lm"], check=True)
         os.replace(tmp, out)
     return out
+
+
+def build_all(force: bool = False) -> None:
+    """Both builds: the plain one-thread library and the multi-core one."""
+    build(force)
+    build(force, out=_LIB_OMP_PATH, openmp=True)
 
 
 def _bind(lib):
@@ -63,17 +75,39 @@ def _bind(lib):
     lib.orc_cg_adjoint.restype = ctypes.c_int
     lib.orc_eig_grad_values.argtypes = [i64, p, p, i64, p, p, p]
     lib.orc_eig_grad_values.restype = None
+    lib.orc_threads.argtypes = [ctypes.c_int]
+    lib.orc_threads.restype = ctypes.c_int
     return lib
 
 
 def load(path: Optional[str] = None):
-    """Load (building if needed) the oracle shared library."""
+    """Load (building if needed) the plain one-thread oracle library."""
     global _lib
     if path is not None:
         return _bind(ctypes.CDLL(path))
     if _lib is None:
         _lib = _bind(ctypes.CDLL(build()))
     return _lib
+
+
+def host_cores() -> int:
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover - not Linux
+        return os.cpu_count() or 1
+
+
+def load_parallel(threads: Optional[int] = None):
+    """Load (building if needed) the multi-core oracle library; threads defaults to every host core.
+
+    Its results do not depend on the thread count; they differ from the plain build's only by
+    the dot products' summation order (fixed chunks)."""
+    global _lib_omp
+    if _lib_omp is None:
+        _lib_omp = _bind(ctypes.CDLL(build(out=_LIB_OMP_PATH, openmp=True)))
+    _lib_omp.orc_threads(int(threads) if threads else host_cores())
+    return _lib_omp
 
 
 def _ptr(a: Optional[np.ndarray]):

@@ -4,10 +4,19 @@
  * TEST INFRASTRUCTURE ONLY.  This file is the checker, not the product: only
  * the test suite, the smoke check and the benchmark's CPU-baseline leg load it.
  * It shares no code, header or constant with the CUDA library.  It is written
- * to be read against the method's description, not to be fast: one thread,
- * sequential sums in index order, no blocking, no fusion.  Build with
- * -ffp-contract=off so that a*b+c is always a rounded multiply then a rounded
- * add on every host (x86_64 and aarch64 give identical results).
+ * to be read against the method's description, not to be fast: sequential
+ * sums in index order, no blocking, no fusion.  Build with -ffp-contract=off so
+ * that a*b+c is always a rounded multiply then a rounded add on every host
+ * (x86_64 and aarch64 give identical results).
+ *
+ * Two builds of this one file:
+ *   - plain (no OpenMP): one thread; a dot product is one sum in index order;
+ *   - multi-core (-fopenmp): every loop over rows or vector entries is split
+ *     across threads (each entry's arithmetic is unchanged), and a dot product
+ *     is summed in fixed chunks of ORC_CHUNK entries, each chunk in index order,
+ *     then the chunk sums in chunk order.  The chunk boundaries do not depend on
+ *     the thread count, so this build gives the same bits on 1, 2 or N threads;
+ *     it differs from the plain build only by the dot products' summation order.
  *
  * Source of the method: "torch-sla: Differentiable Sparse Linear Algebra with
  * Adjoint Solvers and Sparse Tensor Parallelism for PyTorch" (Chi, Wen),
@@ -43,14 +52,36 @@
 #include <stdlib.h>
 #include <string.h>
 
+#ifdef _OPENMP
+#include <omp.h>
+#define ORC_PARALLEL_FOR _Pragma("omp parallel for schedule(static)")
+#else
+#define ORC_PARALLEL_FOR
+#endif
+
+/* entries per dot-product chunk in the multi-core build */
+#define ORC_CHUNK 4096
+
 #define ORC_OK 0
 #define ORC_NOT_CONVERGED 1
 #define ORC_BREAKDOWN 2
 #define ORC_NONFINITE 5
 
+/* Threads used by the multi-core build (nthreads > 0 sets it); 1 for the plain build. */
+int orc_threads(int nthreads) {
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+  return omp_get_max_threads();
+#else
+  (void)nthreads;
+  return 1;
+#endif
+}
+
 /* y = A x: for every row, the sum over its stored entries in storage order. */
 void orc_spmv(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const double *values,
               const double *x, double *y) {
+  ORC_PARALLEL_FOR
   for (int64_t i = 0; i < n; ++i) {
     double s = 0.0;
     for (int64_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k) s += values[k] * x[col_idx[k]];
@@ -58,16 +89,37 @@ void orc_spmv(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const d
   }
 }
 
+#ifndef _OPENMP
 /* a . b, summed in index order. */
 double orc_dot(int64_t n, const double *a, const double *b) {
   double s = 0.0;
   for (int64_t i = 0; i < n; ++i) s += a[i] * b[i];
   return s;
 }
+#else
+/* a . b: chunk c holds entries [c*ORC_CHUNK, (c+1)*ORC_CHUNK), summed in index order; the chunk
+ * sums are then added in chunk order. */
+double orc_dot(int64_t n, const double *a, const double *b) {
+  const int64_t nc = (n + ORC_CHUNK - 1) / ORC_CHUNK;
+  double *cs = (double *)malloc(sizeof(double) * (size_t)(nc > 0 ? nc : 1));
+  ORC_PARALLEL_FOR
+  for (int64_t c = 0; c < nc; ++c) {
+    const int64_t i1 = (c + 1) * ORC_CHUNK < n ? (c + 1) * ORC_CHUNK : n;
+    double s = 0.0;
+    for (int64_t i = c * ORC_CHUNK; i < i1; ++i) s += a[i] * b[i];
+    cs[c] = s;
+  }
+  double s = 0.0;
+  for (int64_t c = 0; c < nc; ++c) s += cs[c];
+  free(cs);
+  return s;
+}
+#endif
 
 /* diag[i] = A_ii (0 when row i stores no diagonal entry). */
 void orc_diagonal(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const double *values,
                   double *diag) {
+  ORC_PARALLEL_FOR
   for (int64_t i = 0; i < n; ++i) {
     diag[i] = 0.0;
     for (int64_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k)
@@ -102,7 +154,7 @@ int orc_cg(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const doub
 
   double nb = sqrt(orc_dot(n, b, b));
   if (x0) memcpy(x, x0, sizeof(double) * (size_t)n);
-  else for (int64_t i = 0; i < n; ++i) x[i] = 0.0;
+  else memset(x, 0, sizeof(double) * (size_t)n);
   if (!isfinite(nb)) { status = ORC_NONFINITE; goto done; }
   if (nb == 0.0) {
     for (int64_t i = 0; i < n; ++i) x[i] = 0.0;
@@ -120,9 +172,10 @@ int orc_cg(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const doub
 
   if (x0) {
     orc_spmv(n, row_ptr, col_idx, values, x, q);
+    ORC_PARALLEL_FOR
     for (int64_t i = 0; i < n; ++i) r[i] = b[i] - q[i];
   } else {
-    for (int64_t i = 0; i < n; ++i) r[i] = b[i];
+    memcpy(r, b, sizeof(double) * (size_t)n);
   }
   double rr = orc_dot(n, r, r);
   *rel_res = sqrt(rr) / nb;
@@ -130,8 +183,9 @@ int orc_cg(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const doub
   if (!isfinite(rr)) { status = ORC_NONFINITE; goto done; }
   if (sqrt(rr) <= rtol * nb) { status = ORC_OK; goto done; }
 
+  ORC_PARALLEL_FOR
   for (int64_t i = 0; i < n; ++i) z[i] = (precond == 1) ? r[i] / d[i] : r[i];
-  for (int64_t i = 0; i < n; ++i) p[i] = z[i];
+  memcpy(p, z, sizeof(double) * (size_t)n);
   double rho = orc_dot(n, r, z);
 
   for (int64_t k = 0; k < maxit; ++k) {
@@ -140,7 +194,9 @@ int orc_cg(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const doub
     if (!isfinite(pq)) { status = ORC_NONFINITE; goto done; }
     if (!(pq > 0.0)) { status = ORC_BREAKDOWN; goto done; }
     double alpha = rho / pq;
+    ORC_PARALLEL_FOR
     for (int64_t i = 0; i < n; ++i) x[i] = x[i] + alpha * p[i];
+    ORC_PARALLEL_FOR
     for (int64_t i = 0; i < n; ++i) r[i] = r[i] - alpha * q[i];
     rr = orc_dot(n, r, r);
     *iters = k + 1;
@@ -148,9 +204,11 @@ int orc_cg(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const doub
     if (history) history[k + 1] = *rel_res;
     if (!isfinite(rr)) { status = ORC_NONFINITE; goto done; }
     if (sqrt(rr) <= rtol * nb) { status = ORC_OK; goto done; }
+    ORC_PARALLEL_FOR
     for (int64_t i = 0; i < n; ++i) z[i] = (precond == 1) ? r[i] / d[i] : r[i];
     double rho_new = orc_dot(n, r, z);
     double beta = rho_new / rho;
+    ORC_PARALLEL_FOR
     for (int64_t i = 0; i < n; ++i) p[i] = z[i] + beta * p[i];
     rho = rho_new;
   }
@@ -164,6 +222,7 @@ done:
 /* grad_values[k] = -lambda[row(k)] * x[col(k)] for every stored entry, in CSR order. */
 void orc_grad_values(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const double *lambda,
                      const double *x, double *grad_values) {
+  ORC_PARALLEL_FOR
   for (int64_t i = 0; i < n; ++i)
     for (int64_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k) grad_values[k] = -(lambda[i] * x[col_idx[k]]);
 }
@@ -189,20 +248,20 @@ int orc_cg_adjoint(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, co
  * eigenvalue mu, the Hellmann-Feynman theorem gives d mu / d A_ij = v_i v_j, so
  * the gradient lives on the stored entries only.  For a weighted sum
  * L = sum_s w_s mu_s of k eigenvalues (eigenvectors V[s*n .. s*n+n-1]):
- *   grad_values[e] = sum over s = 0..k-1, in that order, of (w_s * v_s[i]) * v_s[j]
- * for the stored entry e = (i, j), the sum starting from the s = 0 term.  w == NULL
- * means every w_s = 1.
+ *   grad_values[e] = sum over s = 0..k-1 of w_s * (v_s[i] * v_s[j])
+ * for the stored entry e = (i, j): the products v_i v_j of the theorem, weighted and
+ * added from zero in index order.  w == NULL means every w_s = 1.
  */
 void orc_eig_grad_values(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, int64_t k, const double *V,
                          const double *w, double *grad_values) {
+  ORC_PARALLEL_FOR
   for (int64_t i = 0; i < n; ++i)
     for (int64_t e = row_ptr[i]; e < row_ptr[i + 1]; ++e) {
       const int64_t j = col_idx[e];
       double acc = 0.0;
       for (int64_t s = 0; s < k; ++s) {
         const double ws = w ? w[s] : 1.0;
-        const double term = (ws * V[s * n + i]) * V[s * n + j];
-        acc = (s == 0) ? term : acc + term;
+        acc = acc + ws * (V[s * n + i] * V[s * n + j]);
       }
       grad_values[e] = acc;
     }

@@ -86,12 +86,37 @@ def pin_spmv_exact_integers(lib):
 
 def pin_dot(lib):
     rng = np.random.default_rng(7)
-    for n in [0, 1, 5, 1000]:
+    # lengths around and across the multi-core build's 4096-entry chunks
+    for n in [0, 1, 5, 1000, 4095, 4096, 4097, 3 * 4096 + 17, 20000]:
         a, b = rng.standard_normal(n), rng.standard_normal(n)
         exact = math.fsum((a * b).tolist()) if n else 0.0
         got = oracle.dot(a, b, lib=lib)
         assert abs(got - exact) <= n * EPS * float(np.abs(a) @ np.abs(b)) + 1e-300
     assert oracle.dot(np.array([3.0, 4.0]), np.array([5.0, -2.0]), lib=lib) == 7.0
+    # small integers: every partial sum is exact whatever the order, so the result is exact
+    for n in [4097, 2 * 4096, 10000]:
+        a = rng.integers(-20, 21, n).astype(np.float64)
+        b = rng.integers(-20, 21, n).astype(np.float64)
+        assert oracle.dot(a, b, lib=lib) == float(int(a.astype(np.int64) @ b.astype(np.int64)))
+
+
+def pin_cg_several_chunks_true_residual(lib):
+    # a system longer than two dot-product chunks (n = 4900): the returned iterate's true residual,
+    # computed with scipy's sparse product (not the oracle's), meets the stopping rule up to the
+    # usual drift of the recursive residual, and the solution agrees with a sparse direct solve
+    sp = __import__("pytest").importorskip("scipy.sparse")
+    spla = __import__("pytest").importorskip("scipy.sparse.linalg")
+    m = 70
+    A = diffusion_dirichlet(m, np.random.default_rng(61).lognormal(0, 0.5, 2 * m * (m + 1)))
+    S = sp.csr_matrix((A.values, A.col_idx, A.row_ptr.astype(np.int64)), shape=(A.n, A.n))
+    b = np.random.default_rng(62).standard_normal(A.n)
+    for precond in (0, 1):
+        r = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-10, maxit=5000, precond=precond, lib=lib)
+        assert r["status"] == 0
+        true_rel = np.linalg.norm(b - S @ r["x"]) / np.linalg.norm(b)
+        assert true_rel <= 1.5e-10, (precond, true_rel)
+        xd = spla.spsolve(S.tocsc(), b)
+        assert np.linalg.norm(r["x"] - xd) <= 1e-10 * 1e4 * np.linalg.norm(xd)
 
 
 # --------------------------------------------------------------------------- forward CG
@@ -441,7 +466,7 @@ def pin_eig_grad_rayleigh_identity(lib):
 
 ALL_PINS = [
     pin_spmv_dense, pin_spmv_exact_integers, pin_dot,
-    pin_cg_vs_dense, pin_cg_exact_rational, pin_finite_termination, pin_eigen_closed_form_and_bound,
+    pin_cg_vs_dense, pin_cg_several_chunks_true_residual, pin_cg_exact_rational, pin_finite_termination, pin_eigen_closed_form_and_bound,
     pin_history_matches_true_residual, pin_x0_restart, pin_jacobi_constant_diagonal, pin_jacobi_equals_scaled_cg,
     pin_status_codes,
     pin_adjoint_identity, pin_adjoint_fd, pin_adjoint_config1_loss, pin_adjoint_invariants,

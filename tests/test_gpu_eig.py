@@ -1,8 +1,10 @@
 """Eigenvalue problems on the GPU against the fp64 oracle.
 
 The gradient kernel (d mu / d A_ij = v_i v_j on the pattern, weighted over k eigenvectors) is
-compared bit for bit with the oracle on arbitrary vectors: both sides evaluate the same fp64
-expression with separately rounded operations.  The eigenpair from inverse iteration is compared
+compared with the oracle on arbitrary vectors entry by entry, within the rounding bound of the
+sum: each side forms k products of three factors and k - 1 additions in fp64, so each is within
+(k + 1) u sum_s |w_s v_s[i] v_s[j]| of the exact value (u = 2^-53) and the two within twice that;
+for float data one float ulp of the result is added (each side rounds its fp64 value once).  The eigenpair from inverse iteration is compared
 with the oracle's dense symmetric eigensolver and with the five-point Laplacian's closed form, to
 tolerances derived from the stopping test: a unit vector with ||A v - mu v|| <= tol * mu is within
 tol * mu / gap of the eigenvector (sin theta bound), and its Rayleigh quotient within
@@ -18,6 +20,24 @@ from workloads import poisson_5pt, diffusion_dirichlet, random_spd
 pytestmark = pytest.mark.gpu
 
 EPS64 = np.finfo(np.float64).eps
+EPS32 = float(np.finfo(np.float32).eps)
+
+
+def assert_eig_grad_close(gv, rp, ci, V, w, dtype):
+    """gv against the oracle's sum_s w_s (v_s[i] v_s[j]), entry by entry, within the rounding bound."""
+    V64 = np.atleast_2d(np.asarray(V, dtype=np.float64))
+    k = V64.shape[0]
+    ref = oracle.eig_grad_values(rp, ci, V64, w)
+    rows = np.repeat(np.arange(len(rp) - 1), np.diff(np.asarray(rp, dtype=np.int64)))
+    wv = np.ones(k) if w is None else np.asarray(w, dtype=np.float64)
+    terms = np.zeros(len(ci))
+    for s in range(k):
+        terms += np.abs(wv[s] * V64[s, rows] * V64[s, ci])
+    bound = (k + 1) * EPS64 * terms + 1e-300
+    if dtype == np.float32:
+        bound = bound + EPS32 * np.abs(ref)
+    diff = np.abs(np.asarray(gv, dtype=np.float64) - ref)
+    assert np.all(diff <= bound), f"max excess {np.max(diff / bound):.3g} of the rounding bound"
 
 
 def _vec_bound(tol, mu, gap, n, eps=EPS64):
@@ -28,17 +48,17 @@ def _vec_bound(tol, mu, gap, n, eps=EPS64):
 
 @pytest.mark.parametrize("dtype", [np.float64, np.float32])
 @pytest.mark.parametrize("k", [1, 3, 16])
-def test_eig_grad_values_bit_exact(dtype, k):
+def test_eig_grad_values_within_rounding(dtype, k):
     A = random_spd(777, 5.0, 3, long_rows=2)
     rng = np.random.default_rng(40 + k)
     V = rng.standard_normal((k, A.n)).astype(dtype)
     w = rng.standard_normal(k)
     gv = sla.sla_eig_grad_values(to_dev(A, dtype), t(V), weights=w).cpu().numpy()
-    ref = oracle.eig_grad_values(A.row_ptr, A.col_idx, V.astype(np.float64), w).astype(dtype)
-    assert np.array_equal(gv, ref)
+    assert gv.dtype == dtype
+    assert_eig_grad_close(gv, A.row_ptr, A.col_idx, V, w, dtype)
     # unit weights by default; k = 0 gives zeros
     gv1 = sla.sla_eig_grad_values(to_dev(A, dtype), t(V[:1])).cpu().numpy()
-    assert np.array_equal(gv1, oracle.eig_grad_values(A.row_ptr, A.col_idx, V[:1].astype(np.float64)).astype(dtype))
+    assert_eig_grad_close(gv1, A.row_ptr, A.col_idx, V[:1], None, dtype)
     z = sla.sla_eig_grad_values(to_dev(A, dtype), t(np.zeros((0, A.n), dtype))).cpu().numpy()
     assert not z.any()
 
@@ -54,7 +74,7 @@ def test_eig_grad_values_ragged_rows_int64():
     dA = sla.CSRMatrix.from_numpy(rp, ci, vals, "cuda:0")
     V = rng.standard_normal((2, n))
     gv = sla.sla_eig_grad_values(dA, t(V), weights=[0.5, -2.0]).cpu().numpy()
-    assert np.array_equal(gv, oracle.eig_grad_values(rp, ci, V, [0.5, -2.0]))
+    assert_eig_grad_close(gv, rp, ci, V, [0.5, -2.0], np.float64)
 
 
 # --------------------------------------------------------------------------- eigenpair
@@ -102,7 +122,7 @@ def test_eig_smallest_int64_rowptr_and_ragged_grid():
     assert abs(mu - mu0) <= 1e-11 * mu0
     assert np.linalg.norm(v.cpu().numpy() - v0) <= _vec_bound(1e-10, mu0, gap, A.n)
     gv = sla.sla_eig_grad_values(to_dev(A), v, weights=[-1.5]).cpu().numpy()
-    assert np.array_equal(gv, oracle.eig_grad_values(A.row_ptr, A.col_idx, v.cpu().numpy(), [-1.5]))
+    assert_eig_grad_close(gv, A.row_ptr, A.col_idx, v.cpu().numpy(), [-1.5], np.float64)
 
 
 def test_eig_smallest_float32():
@@ -181,4 +201,5 @@ def test_eig_smallest_poisson1000_sampled():
     rows = np.repeat(np.arange(A.n), np.diff(A.row_ptr.astype(np.int64)))
     vv = v.cpu().numpy()
     e = np.random.default_rng(4).choice(A.nnz, 2000, replace=False)
+    # one eigenvector with unit weight: a single rounded product v_i * v_j on both sides, so exact
     assert np.array_equal(gv[e], vv[rows[e]] * vv[A.col_idx[e]])

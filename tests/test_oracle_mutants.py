@@ -18,7 +18,8 @@ MUTANTS = [
     ("spmv_wrong_index", "s += values[k] * x[col_idx[k]];", "s += values[k] * x[i];"),
     ("spmv_dropped_term", "for (int64_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k) s += values[k]",
      "for (int64_t k = row_ptr[i] + 1; k < row_ptr[i + 1]; ++k) s += values[k]"),
-    ("dot_wrong_operand", "s += a[i] * b[i];", "s += a[i] * a[i];"),
+    ("dot_wrong_operand", "for (int64_t i = 0; i < n; ++i) s += a[i] * b[i];",
+     "for (int64_t i = 0; i < n; ++i) s += a[i] * a[i];"),
     ("x_update_sign", "x[i] = x[i] + alpha * p[i];", "x[i] = x[i] - alpha * p[i];"),
     ("r_update_operand", "r[i] = r[i] - alpha * q[i];", "r[i] = r[i] - alpha * p[i];"),
     ("alpha_transposed", "double alpha = rho / pq;", "double alpha = pq / rho;"),
@@ -26,8 +27,8 @@ MUTANTS = [
     ("p_update_uses_r", "p[i] = z[i] + beta * p[i];", "p[i] = r[i] + beta * p[i];"),
     ("jacobi_multiplies", "z[i] = (precond == 1) ? r[i] / d[i] : r[i];\n    double rho_new",
      "z[i] = (precond == 1) ? r[i] * d[i] : r[i];\n    double rho_new"),
-    ("stop_rule_no_sqrt", "if (sqrt(rr) <= rtol * nb) { status = ORC_OK; goto done; }\n    for",
-     "if (rr <= rtol * nb) { status = ORC_OK; goto done; }\n    for"),
+    ("stop_rule_no_sqrt", "if (sqrt(rr) <= rtol * nb) { status = ORC_OK; goto done; }\n    ORC_PARALLEL_FOR",
+     "if (rr <= rtol * nb) { status = ORC_OK; goto done; }\n    ORC_PARALLEL_FOR"),
     ("history_off_by_one", "if (history) history[k + 1] = *rel_res;", "if (history) history[k] = *rel_res;"),
     ("grad_values_transposed", "grad_values[k] = -(lambda[i] * x[col_idx[k]]);",
      "grad_values[k] = -(lambda[col_idx[k]] * x[i]);"),
@@ -36,13 +37,15 @@ MUTANTS = [
     ("adjoint_wrong_rhs", "orc_cg(n, row_ptr, col_idx, values, g, NULL,", "orc_cg(n, row_ptr, col_idx, values, x, NULL,"),
     ("x0_residual_sign", "r[i] = b[i] - q[i];", "r[i] = b[i] + q[i];"),
     ("breakdown_test_dropped", "if (!(pq > 0.0)) { status = ORC_BREAKDOWN; goto done; }", ""),
-    ("eig_grad_sign", "acc = (s == 0) ? term : acc + term;", "acc = (s == 0) ? -term : acc - term;"),
+    ("eig_grad_sign", "acc = acc + ws * (V[s * n + i] * V[s * n + j]);",
+     "acc = acc - ws * (V[s * n + i] * V[s * n + j]);"),
     ("eig_grad_drops_weight", "const double ws = w ? w[s] : 1.0;", "const double ws = 1.0;"),
-    ("eig_grad_first_vector_only", "acc = (s == 0) ? term : acc + term;", "acc = (s == 0) ? term : acc;"),
-    ("eig_grad_row_for_column", "const double term = (ws * V[s * n + i]) * V[s * n + j];",
-     "const double term = (ws * V[s * n + i]) * V[s * n + i];"),
-    ("eig_grad_wrong_vector", "const double term = (ws * V[s * n + i]) * V[s * n + j];",
-     "const double term = (ws * V[i]) * V[j];"),
+    ("eig_grad_first_vector_only", "for (int64_t s = 0; s < k; ++s) {\n        const double ws",
+     "for (int64_t s = 0; s < (k > 0 ? 1 : 0); ++s) {\n        const double ws"),
+    ("eig_grad_row_for_column", "acc = acc + ws * (V[s * n + i] * V[s * n + j]);",
+     "acc = acc + ws * (V[s * n + i] * V[s * n + i]);"),
+    ("eig_grad_wrong_vector", "acc = acc + ws * (V[s * n + i] * V[s * n + j]);",
+     "acc = acc + ws * (V[i] * V[j]);"),
 ]
 
 
