@@ -37,8 +37,9 @@ __all__ = [
     "SLA_LOOP_RESIDENT", "SLA_LOOP_CLUSTER", "SLA_OK", "SLA_NOT_CONVERGED", "SLA_BREAKDOWN", "SLA_INVALID_ARG",
     "SLA_BAD_CSR", "SLA_NONFINITE", "SLA_WORKSPACE_TOO_SMALL", "SLA_TIMEOUT", "SLA_CUDA_ERROR",
     "EigInfo", "sla_eig_workspace_bytes", "sla_eig_smallest", "sla_eig_grad_values", "EigSmallest",
-    "eigsh_smallest",
+    "eigsh_smallest", "sla_set_spmv_variant", "sla_test_set_barrier_wait", "SLA_SPMV_PLAIN", "SLA_SPMV_TMA",
 ]
+from ._abi import SLA_SPMV_PLAIN, SLA_SPMV_TMA  # noqa: E402
 
 _lib = None
 
@@ -159,6 +160,16 @@ def sla_status_string(status: int) -> str:
 
 def sla_version() -> int:
     return lib().sla_version()
+
+
+def sla_set_spmv_variant(variant: int) -> None:
+    """Process-wide SpMV step of the GRAPH and HOST loops: SLA_SPMV_PLAIN (default) or SLA_SPMV_TMA."""
+    _check(lib().sla_set_spmv_variant(int(variant)), "sla_set_spmv_variant")
+
+
+def sla_test_set_barrier_wait(extra: int, spin_limit: int) -> None:
+    """Test hook: the resident grid barrier waits for `extra` more arrivals, at most `spin_limit` polls."""
+    _check(lib().sla_test_set_barrier_wait(int(extra), int(spin_limit)), "sla_test_set_barrier_wait")
 
 
 def sla_launch_count() -> int:

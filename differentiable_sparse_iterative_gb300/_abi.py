@@ -19,8 +19,9 @@ EXPORTS = [
     "sla_status_string", "sla_last_cuda_error", "sla_version", "sla_launch_count", "sla_cg_workspace_bytes",
     "sla_validate_csr", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values", "sla_cg_solve_batched",
     "sla_cg_adjoint_batched", "sla_cg_solve_static", "sla_eig_workspace_bytes", "sla_eig_smallest",
-    "sla_eig_grad_values",
+    "sla_eig_grad_values", "sla_set_spmv_variant", "sla_test_set_barrier_wait",
 ]
+SLA_SPMV_PLAIN, SLA_SPMV_TMA = 0, 1
 
 
 class sla_csr(ctypes.Structure):
@@ -74,7 +75,9 @@ def bind(lib):
     lib.sla_eig_workspace_bytes.restype = sz
     lib.sla_eig_smallest.argtypes = [C, P, ctypes.POINTER(sla_eig_opts), ctypes.POINTER(sla_eig_info), P, sz, P]
     lib.sla_eig_grad_values.argtypes = [C, i64, P, ctypes.POINTER(ctypes.c_double), P, P]
-    for name in ["sla_validate_csr", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
+    lib.sla_set_spmv_variant.argtypes = [i32]
+    lib.sla_test_set_barrier_wait.argtypes = [ctypes.c_uint32, i64]
+    for name in ["sla_set_spmv_variant", "sla_test_set_barrier_wait", "sla_validate_csr", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
                  "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_cg_solve_static", "sla_eig_smallest",
                  "sla_eig_grad_values"]:
         getattr(lib, name).restype = i32

@@ -201,8 +201,6 @@ sla_status check_vec(const void *p, const sla_csr *A, bool allow_null) {
   return aligned(p, A->dtype == SLA_F64 ? 8 : 4) ? SLA_OK : SLA_INVALID_ARG;
 }
 
-namespace {
-
 sla_status check_opts(const sla_cg_opts *o) {
   if (!o) return SLA_INVALID_ARG;
   if (!(o->rtol >= 0.0) || !std::isfinite(o->rtol)) return SLA_INVALID_ARG;
@@ -213,6 +211,8 @@ sla_status check_opts(const sla_cg_opts *o) {
   if (o->reserved != 0) return SLA_INVALID_ARG;
   return SLA_OK;
 }
+
+namespace {
 
 sla_status check_ws(const sla_csr *A, int64_t batch, const sla_cg_opts *o, void *ws, size_t ws_bytes) {
   if (!ws || !aligned(ws, 256)) return SLA_INVALID_ARG;

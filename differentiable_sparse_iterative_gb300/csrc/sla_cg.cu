@@ -791,16 +791,12 @@ cudaError_t build_graph(const Prob<V, I> &P0, const Launch &Lc, int unroll, cuda
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-// The TMA-staged SpMV step is opt-in (SLA_SPMV=tma in the environment): measured on GB300 it is
-// slower than the plain step on the five-point workloads (its per-entry staging bookkeeping
-// makes it instruction-bound), so the plain step is the default.  Both compute the same rows.
-bool tma_enabled() {
-  static const int on = [] {
-    const char *e = getenv("SLA_SPMV");
-    return (e && strcmp(e, "tma") == 0) ? 1 : 0;
-  }();
-  return on != 0;
-}
+// The TMA-staged SpMV step is opt-in (sla_set_spmv_variant): measured on GB300 it is slower than
+// the plain step on the five-point workloads (its per-entry staging bookkeeping makes it
+// instruction-bound), so the plain step is the default.  Both compute the same rows.
+std::atomic<int> g_spmv_variant{SLA_SPMV_PLAIN};
+
+bool tma_enabled() { return g_spmv_variant.load() == SLA_SPMV_TMA; }
 
 int occupancy_blocks(const void *fn) {
   int nb = 0;
@@ -1032,3 +1028,9 @@ size_t workspace_bytes(int64_t n, int64_t batch, int dtype, int precond) {
 }
 
 }  // namespace sla
+
+extern "C" sla_status sla_set_spmv_variant(int32_t variant) {
+  if (variant != SLA_SPMV_PLAIN && variant != SLA_SPMV_TMA) return SLA_INVALID_ARG;
+  sla::g_spmv_variant.store(variant);
+  return SLA_OK;
+}

@@ -46,7 +46,7 @@ struct Glob {
   uint32_t timeout;               // 1 if a bounded grid-barrier wait expired
 };
 
-__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+__host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Workspace layout (offsets in bytes from the workspace base).
 struct Layout {
@@ -55,9 +55,9 @@ struct Layout {
 
 // halo: one bit per row (shared by the systems of a batch), set for the rows that another block of
 // the resident kernel reads; last, so that a layout without it keeps every other offset.
-__host__ __device__ inline Layout make_layout(int64_t n, int64_t batch, size_t vbytes, bool jacobi,
-                                              bool with_halo = true) {
-  Layout L;
+__host__ __device__ constexpr Layout make_layout(int64_t n, int64_t batch, size_t vbytes, bool jacobi,
+                                                 bool with_halo = true) {
+  Layout L{};
   size_t off = 0;
   L.glob = off; off += align256(sizeof(Glob));
   L.ctl = off; off += align256(sizeof(Ctl) * (size_t)batch);

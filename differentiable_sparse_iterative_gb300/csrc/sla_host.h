@@ -42,6 +42,7 @@ bool cluster_fits(int64_t n, int64_t batch, int dtype, int precond);
 bool aligned(const void *p, size_t a);
 sla_status check_csr(const sla_csr *A, bool need_values);
 sla_status check_vec(const void *p, const sla_csr *A, bool allow_null);
+sla_status check_opts(const sla_cg_opts *o);
 
 #define SLA_CHECK(expr)            \
   do {                             \

@@ -68,6 +68,10 @@ constexpr int kResBlock = 1024;
 constexpr int kStage = 8;  // rows per thread whose global loads are issued together
 constexpr long long kSpinLimit = 1ll << 26;  // ~seconds of polling before a barrier gives up
 
+// Grid-barrier wait bounds of the next launches (sla_test_set_barrier_wait; normally 0 and kSpinLimit).
+std::atomic<unsigned> g_wait_extra{0u};
+std::atomic<long long> g_wait_limit{kSpinLimit};
+
 // Bounds of the grid barrier's wait.  `extra` arrivals are expected beyond the G blocks: 0 in
 // use; a test sets 1 (an arrival that never comes) with a short `limit` to drive the timeout path
 // on the GPU and check that the solve returns SLA_TIMEOUT with the context still usable.
@@ -1224,12 +1228,7 @@ sla_status run_resident(Prob<V, I> P, cudaStream_t stream, sla_cg_info *info) {
   if (e == cudaSuccess && P.halo)
     e = cudaMemsetAsync(P.halo, 0, sizeof(uint32_t) * (size_t)((P.n + 31) / 32), stream);
   if (e != cudaSuccess) return fail(e);
-  WaitCfg wc{0u, kSpinLimit};
-  if (const char *e = getenv("SLA_TEST_GRID_WAIT_EXTRA")) wc.extra = (unsigned)strtoul(e, nullptr, 10);
-  if (const char *e = getenv("SLA_TEST_SPIN_LIMIT")) {
-    const long long v = strtoll(e, nullptr, 10);
-    if (v > 0 && v < kSpinLimit) wc.limit = v;
-  }
+  WaitCfg wc{g_wait_extra.load(), g_wait_limit.load()};
   void *args[] = {(void *)&P, (void *)&cap, (void *)&wc};
   e = cudaLaunchCooperativeKernel(fn, dim3(G), dim3(kResBlock), args, smem, stream);
   if (e == cudaSuccess) e = cudaGetLastError();
@@ -1257,3 +1256,10 @@ extern "C" SLA_API int sla_phase_cycles(unsigned long long *host, int nblocks) {
   return (int)cudaMemcpyFromSymbol(host, sla::g_phase_cycles, sizeof(unsigned long long) * 8 * (size_t)nblocks);
 }
 #endif
+
+extern "C" sla_status sla_test_set_barrier_wait(uint32_t extra, int64_t spin_limit) {
+  if (extra > 1u || spin_limit < 0 || spin_limit > sla::kSpinLimit) return SLA_INVALID_ARG;
+  sla::g_wait_extra.store(extra);
+  sla::g_wait_limit.store(spin_limit == 0 ? sla::kSpinLimit : spin_limit);
+  return SLA_OK;
+}

@@ -5,8 +5,10 @@
 // code on latency-critical paths where an allocation (and the device synchronisation
 // it can imply) is not allowed, and thin bindings that have no device allocator at
 // all.  For them this entry point keeps its scratch in a fixed array in the library's
-// own device memory, reserved when the library is loaded on a GPU and held until the
-// process exits.  The caller still passes the matrix, b, x0 and x.
+// own device memory.  The array is reserved on a GPU when this file's device code is
+// loaded there, which (under CUDA's lazy module loading) is the first call on that GPU,
+// and it is held until the process exits.  The caller still passes the matrix, b, x0
+// and x.
 //
 // Limits: one system (no batch) of at most kStaticMaxN = 65,536 unknowns, fp32 or fp64,
 // with or without Jacobi; larger systems are rejected with SLA_WORKSPACE_TOO_SMALL
@@ -24,10 +26,12 @@ namespace sla {
 namespace {
 
 constexpr int64_t kStaticMaxN = 65536;
-// Workspace layout for n = 65,536, one system, fp64 values, Jacobi: Glob (256 B) + Ctl (256 B)
-// + partial sums (6 x 2048 doubles = 98,304 B) + 6 vectors of 65,536 doubles (524,288 B each:
-// r, p0, p1, q, 1/diag, z).
-constexpr size_t kStaticScratchBytes = 256 + 256 + 98304 + 6 * 524288;  // 3,244,544 bytes
+// The workspace layout of the largest case: n = 65,536, one system, fp64 values, Jacobi, no row
+// bitmap (the host-driven loop never runs the resident kernel): Glob (256 B) + Ctl (256 B) +
+// partial sums (6 x 2048 doubles = 98,304 B) + 6 vectors of 65,536 doubles (524,288 B each:
+// r, p0, p1, q, 1/diag, z).  Every smaller or fp32 case needs less.
+constexpr size_t kStaticScratchBytes = make_layout(kStaticMaxN, 1, sizeof(double), true, false).total;
+static_assert(kStaticScratchBytes == 3244544, "the documented size of the static scratch");
 constexpr int kMaxDevices = 64;
 
 // The shared scratch.  In host code this name is only a stand-in for the device symbol:
@@ -55,8 +59,6 @@ sla_status static_scratch(void **out) {
   return SLA_OK;
 }
 
-bool is_aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
-
 }  // namespace
 
 }  // namespace sla
@@ -66,22 +68,18 @@ using namespace sla;
 extern "C" SLA_API sla_status sla_cg_solve_static(const sla_csr *A, const void *b, const void *x0,
                                                   const sla_cg_opts *opts, void *x, sla_cg_info *info,
                                                   double *history, void *stream) {
-  // argument checks first: they need no GPU
-  if (!A || !opts) return SLA_INVALID_ARG;
-  if (A->n < 0 || A->nnz < 0) return SLA_INVALID_ARG;
+  // argument checks first (the same as sla_cg_solve's): they need no GPU
+  SLA_CHECK(check_csr(A, true));
+  SLA_CHECK(check_vec(b, A, false));
+  SLA_CHECK(check_vec(x0, A, true));
+  SLA_CHECK(check_vec(x, A, false));
+  if (!aligned(history, 8)) return SLA_INVALID_ARG;
+  if (!opts) return SLA_INVALID_ARG;
+  sla_cg_opts o = *opts;
+  o.loop = SLA_LOOP_HOST;  // the only loop that needs no graph (instantiating one may allocate)
+  SLA_CHECK(check_opts(&o));
   if (A->n > kStaticMaxN) return SLA_WORKSPACE_TOO_SMALL;  // beyond the static scratch
-  if (A->dtype != SLA_F32 && A->dtype != SLA_F64) return SLA_INVALID_ARG;
-  if (A->rowptr_type != SLA_I32 && A->rowptr_type != SLA_I64) return SLA_INVALID_ARG;
-  if (opts->precond != SLA_PRECOND_NONE && opts->precond != SLA_PRECOND_JACOBI) return SLA_INVALID_ARG;
-  if (!(opts->rtol >= 0.0) || opts->rtol > 1e300 || opts->maxit < 0 || opts->maxit > ((int64_t)1 << 40))
-    return SLA_INVALID_ARG;
-  if (opts->unroll < 0 || opts->unroll > 64 || opts->reserved != 0) return SLA_INVALID_ARG;
-  const size_t vsz = A->dtype == SLA_F64 ? 8 : 4, isz = A->rowptr_type == SLA_I64 ? 8 : 4;
-  if (A->n > 0 && (!A->row_ptr || !b || !x)) return SLA_INVALID_ARG;
-  if (A->nnz > 0 && (!A->col_idx || !A->values)) return SLA_INVALID_ARG;
-  if (!is_aligned(A->row_ptr, isz) || !is_aligned(A->col_idx, 4) || !is_aligned(A->values, vsz) ||
-      !is_aligned(b, vsz) || !is_aligned(x0, vsz) || !is_aligned(x, vsz) || !is_aligned(history, 8))
-    return SLA_INVALID_ARG;
+  const size_t vsz = A->dtype == SLA_F64 ? 8 : 4;
   const bool jac = opts->precond == SLA_PRECOND_JACOBI;
   const Layout L = make_layout(A->n, 1, vsz, jac, /*with_halo=*/false);  // the host loop needs no row bitmap
   if (L.total > kStaticScratchBytes) return SLA_WORKSPACE_TOO_SMALL;
@@ -98,8 +96,6 @@ extern "C" SLA_API sla_status sla_cg_solve_static(const sla_csr *A, const void *
   void *ws = nullptr;
   sla_status s = static_scratch(&ws);
   if (s != SLA_OK) return s;
-  sla_cg_opts o = *opts;
-  o.loop = SLA_LOOP_HOST;
   cudaStream_t st = (cudaStream_t)stream;
   // The init kernel of the solve zeroes the control block and the loop state in the scratch, so
   // nothing left by an earlier call is read; vectors are written before they are read.

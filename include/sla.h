@@ -303,10 +303,13 @@ SLA_API sla_status sla_eig_grad_values(const sla_csr *A, int64_t k, const void *
  * (plugins inside a host application that owns all device memory, latency-critical paths where
  * an allocation is not allowed, bindings with no device allocator).  The paper has no
  * counterpart: this is a library convenience, not part of the method.
- *   Scratch: a fixed 3,244,544-byte array in the library's own device memory, reserved on every
- *   GPU that loads the library and held until the process exits.  Systems of up to 65,536
- *   unknowns (one system, fp32 or fp64, with or without Jacobi) fit; larger n returns
- *   SLA_WORKSPACE_TOO_SMALL before anything is launched.
+ *   Scratch: a fixed 3,244,544-byte array in the library's own device memory.  CUDA reserves it
+ *   on a GPU when it loads the library's device code for this entry point there, which under
+ *   CUDA's default lazy module loading is this entry point's first call on that GPU; it is held
+ *   until the process exits.  That first call can therefore fail with SLA_CUDA_ERROR when the
+ *   GPU has no 3.2 MB left: make it once at start-up.  Systems of up to 65,536 unknowns (one
+ *   system, fp32 or fp64, with or without Jacobi) fit; larger n returns SLA_WORKSPACE_TOO_SMALL
+ *   before anything is launched.
  *   Set-up: the first call on a device looks up the array's device address on the current
  *   device (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
  *   Sharing: every call uses the same array.  Each call resets the state it needs, but calls
@@ -318,6 +321,33 @@ SLA_API sla_status sla_eig_grad_values(const sla_csr *A, int64_t k, const void *
  */
 SLA_API sla_status sla_cg_solve_static(const sla_csr *A, const void *b, const void *x0, const sla_cg_opts *opts,
                                        void *x, sla_cg_info *info, double *history, void *stream);
+
+/* ---------------------------------------------------------------- tuning and testing */
+
+typedef enum sla_spmv_variant {
+  SLA_SPMV_PLAIN = 0,  /* default: each thread loads its rows' entries directly */
+  SLA_SPMV_TMA = 1     /* the CSR entries of a tile are staged in shared memory by cp.async.bulk with
+                          mbarrier double buffering (same per-row arithmetic and results) */
+} sla_spmv_variant;
+
+/*
+ * Process-wide choice of the SpMV step that the GRAPH and HOST loops launch (not an operation of
+ * the method: a tuning switch).  The TMA variant is used only when every array it copies is
+ * 16-byte aligned; its mbarrier waits are bounded and fall back to plain loads.  On five-point
+ * matrices it measured slower than the plain step, hence the default.  Takes effect at the next
+ * solve.  Returns SLA_INVALID_ARG for an unknown variant.
+ */
+SLA_API sla_status sla_set_spmv_variant(int32_t variant);
+
+/*
+ * Test hook for failure detection (not an operation of the method).  Process-wide bounds of the
+ * RESIDENT kernel's grid-barrier wait for the next launches: the barrier waits for `extra`
+ * (0 or 1) arrivals beyond its blocks and gives up after `spin_limit` polls (0 = the library
+ * default, several seconds; at most 2^26).  With extra = 1 no barrier can complete, so a solve
+ * returns SLA_TIMEOUT after spin_limit polls with the CUDA context intact.
+ * sla_test_set_barrier_wait(0, 0) restores normal operation.  SLA_INVALID_ARG otherwise.
+ */
+SLA_API sla_status sla_test_set_barrier_wait(uint32_t extra, int64_t spin_limit);
 
 #ifdef __cplusplus
 }

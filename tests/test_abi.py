@@ -161,3 +161,21 @@ def test_eig_argument_rejection_without_gpu(lib):
     assert grad(ctypes.byref(_csr()), 1, None, None, P, None) == _abi.SLA_INVALID_ARG
     assert grad(ctypes.byref(_csr()), 1, P, None, None, None) == _abi.SLA_INVALID_ARG
     assert grad(ctypes.byref(_csr(nnz=0)), 1, P, None, None, None) == _abi.SLA_OK  # nothing to write
+
+
+def test_tuning_and_test_hooks_reject_bad_values(lib):
+    # process-wide switches: no GPU needed to refuse an unknown value
+    assert lib.sla_set_spmv_variant(2) == _abi.SLA_INVALID_ARG
+    assert lib.sla_set_spmv_variant(-1) == _abi.SLA_INVALID_ARG
+    assert lib.sla_set_spmv_variant(_abi.SLA_SPMV_PLAIN) == _abi.SLA_OK
+    assert lib.sla_test_set_barrier_wait(2, 0) == _abi.SLA_INVALID_ARG
+    assert lib.sla_test_set_barrier_wait(0, -5) == _abi.SLA_INVALID_ARG
+    assert lib.sla_test_set_barrier_wait(0, (1 << 26) + 1) == _abi.SLA_INVALID_ARG
+    assert lib.sla_test_set_barrier_wait(0, 0) == _abi.SLA_OK
+
+
+def test_library_reads_no_environment_variables():
+    # the solver's behaviour is set through the C ABI only: no getenv in the library sources
+    csrc = os.path.join(ROOT, "differentiable_sparse_iterative_gb300", "csrc")
+    for f in os.listdir(csrc):
+        assert "getenv" not in open(os.path.join(csrc, f)).read(), f

@@ -128,7 +128,8 @@ def test_batched_f32(m, batch, precond):
         assert abs(infos[s].iters - ref["iters"]) <= max(1, ITER_SLACK_F32 * ref["iters"])
         assert rel(xs[s], ref["x"]) <= TOL_F32
         check_history(hs[s], ref["history"], k=10, tol=1e-4)
-        adj = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, v64, xs[s].astype(np.float64),
+        # the oracle's adjoint chains from its own forward solution, as in the fp64 tests
+        adj = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, v64, ref["x"],
                                 w.g[s].astype(np.float64), rtol=w.rtol, maxit=5000, precond=precond)
         assert ainfos[s].status == 0
         assert rel(gbs[s], adj["grad_b"]) <= TOL_F32
@@ -329,41 +330,25 @@ def test_resident_rejects_what_does_not_fit():
         sla.sla_cg_solve_batched(P, t(w.values_b), t(w.b), rtol=1e-5, maxit=100, loop=sla.SLA_LOOP_RESIDENT)
 
 
-_SPMV_SCRIPT = r"""
-import sys, numpy as np, torch
-sys.path.insert(0, sys.argv[1])
-import differentiable_sparse_iterative_gb300 as sla
-from workloads import diffusion_dirichlet, random_spd
-out = []
-for A, pc in [(diffusion_dirichlet(300, np.random.default_rng(3).lognormal(0, 1, 2 * 300 * 301)), 1),
-              (random_spd(5000, 6.0, 4, long_rows=5), 0)]:
-    dA = sla.CSRMatrix.from_numpy(A.row_ptr, A.col_idx, A.values, "cuda")
-    b = torch.from_numpy(np.random.default_rng(5).standard_normal(A.n)).cuda()
-    x, info, _ = sla.sla_cg_solve(dA, b, rtol=1e-9, maxit=4000, precond=pc, loop=sla.SLA_LOOP_GRAPH)
-    out.append(x.cpu().numpy())
-np.save(sys.argv[2], np.concatenate(out))
-"""
-
-
-def test_tma_spmv_step_equals_plain(tmp_path):
+def test_tma_spmv_step_equals_plain():
     # the TMA-staged SpMV step and the plain one do the same per-row arithmetic; they run at
     # different occupancy, so the blocks (and the order of the p.q block sums) differ
-    import os
-    import subprocess
-    import sys
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    script = tmp_path / "spmv_variant.py"
-    script.write_text(_SPMV_SCRIPT)
     res = {}
-    for mode in ("tma", "plain"):
-        env = dict(os.environ)
-        env.pop("SLA_SPMV", None)
-        if mode == "tma":
-            env["SLA_SPMV"] = "tma"
-        outp = tmp_path / f"{mode}.npy"
-        subprocess.run([sys.executable, str(script), root, str(outp)], check=True, env=env, timeout=600)
-        res[mode] = np.load(outp)
-    assert rel(res["tma"], res["plain"]) <= 1e-11
+    try:
+        for variant in (sla.SLA_SPMV_TMA, sla.SLA_SPMV_PLAIN):
+            sla.sla_set_spmv_variant(variant)
+            out = []
+            for A, pc in [(diffusion_dirichlet(300, np.random.default_rng(3).lognormal(0, 1, 2 * 300 * 301)), 1),
+                          (random_spd(5000, 6.0, 4, long_rows=5), 0)]:
+                dA = to_dev(A)
+                b = t(np.random.default_rng(5).standard_normal(A.n))
+                x, info, _ = sla.sla_cg_solve(dA, b, rtol=1e-9, maxit=4000, precond=pc, loop=sla.SLA_LOOP_GRAPH)
+                assert info.status == 0
+                out.append(x.cpu().numpy())
+            res[variant] = np.concatenate(out)
+    finally:
+        sla.sla_set_spmv_variant(sla.SLA_SPMV_PLAIN)
+    assert rel(res[sla.SLA_SPMV_TMA], res[sla.SLA_SPMV_PLAIN]) <= 1e-11
 
 
 @pytest.mark.parametrize("precond", [0, 1])
@@ -400,7 +385,7 @@ def test_bad_row_ptr_reported_by_every_engine(loop, kind):
                          sla.SLA_LOOP_RESIDENT: "resident", sla.SLA_LOOP_CLUSTER: "cluster"}[loop]
 
 
-def test_resident_barrier_timeout_returns_status(monkeypatch):
+def test_resident_barrier_timeout_returns_status():
     # failure detection without a fault: the grid barrier waits for one arrival that never comes,
     # gives up after a short bounded wait, and the solve returns SLA_TIMEOUT; the context stays
     # usable and the next solve is exact
@@ -408,14 +393,14 @@ def test_resident_barrier_timeout_returns_status(monkeypatch):
     A = poisson_5pt(40)
     b = t(np.random.default_rng(5).standard_normal(A.n))
     dA = to_dev(A)
-    monkeypatch.setenv("SLA_TEST_GRID_WAIT_EXTRA", "1")
-    monkeypatch.setenv("SLA_TEST_SPIN_LIMIT", "20000")
-    t0 = time.time()
-    _, info, _ = sla.sla_cg_solve(dA, b, rtol=1e-10, maxit=200, loop=sla.SLA_LOOP_RESIDENT)
+    sla.sla_test_set_barrier_wait(1, 20000)
+    try:
+        t0 = time.time()
+        _, info, _ = sla.sla_cg_solve(dA, b, rtol=1e-10, maxit=200, loop=sla.SLA_LOOP_RESIDENT)
+    finally:
+        sla.sla_test_set_barrier_wait(0, 0)
     assert info.status == sla.SLA_TIMEOUT and info.path == "resident"
     assert time.time() - t0 < 60
-    monkeypatch.delenv("SLA_TEST_GRID_WAIT_EXTRA")
-    monkeypatch.delenv("SLA_TEST_SPIN_LIMIT")
     x, info2, _ = sla.sla_cg_solve(dA, b, rtol=1e-10, maxit=2000, loop=sla.SLA_LOOP_RESIDENT)
     xg, infog, _ = sla.sla_cg_solve(dA, b, rtol=1e-10, maxit=2000, loop=sla.SLA_LOOP_GRAPH)
     assert info2.status == 0 and abs(info2.iters - infog.iters) <= 1
@@ -441,7 +426,7 @@ def test_batched_f32_several_row_groups(m):
         assert infos[s].status == ref["status"] == 0
         assert abs(infos[s].iters - ref["iters"]) <= max(1, ITER_SLACK_F32 * ref["iters"])
         assert rel(xs[s], ref["x"]) <= TOL_F32
-        adj = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, v64, xs[s].astype(np.float64),
+        adj = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, v64, ref["x"],
                                 w.g[s].astype(np.float64), rtol=w.rtol, maxit=5000)
         assert ainfos[s].status == 0
         assert rel(gbs[s], adj["grad_b"]) <= TOL_F32
