@@ -1,15 +1,16 @@
-"""Full-size workloads through the C ABI, in the launch configuration the benchmark times.
+"""Full-size workloads through the C ABI, in the launch configuration the benchmark times,
+compared element by element with the oracle.
 
-config 2 (1M-DOF Poisson, fp64, rtol 1e-8): full oracle comparison of the converged
-  solution, the first 50 residual-history entries and the adjoint gradients.
-config 4 (16.8M-DOF variable-coefficient diffusion, Jacobi, rtol 1e-8) and config 5
-  (169M-DOF Poisson, int64 row_ptr, 1000 fixed iterations): the oracle cannot afford the
-  whole solve, so the checks are (a) the first iterations element by element against the
-  oracle run for the same few iterations, (b) the true residual b - A x of the GPU's
-  final iterate computed by the oracle's SpMV, (c) grad_values bit for bit against the
-  oracle's -lambda_i x_j on the GPU's own lambda and x, (d) A lambda = g to tolerance.
+The two large systems use the oracle's multi-core build (same arithmetic as the plain build;
+dot products summed in fixed chunks, so its results do not depend on the thread count):
+config 2 (1M-DOF Poisson, fp64, rtol 1e-8), config 4 (16.8M-DOF variable-coefficient
+diffusion, Jacobi PCG, rtol 1e-8) and config 5 (169M-DOF Poisson, int64 row_ptr, 1000 fixed
+iterations) each compare the solution (1e-9), the first 50 residual-history entries (1e-8) and
+the adjoint gradients grad_b and grad_values (1e-7), the oracle's adjoint chaining from its own
+forward solution.  Wall time on the GPU machine's host cores is dominated by the oracle: see the
+timing printed with -s.
 """
-import os
+import time
 
 import numpy as np
 import pytest
@@ -49,54 +50,57 @@ def test_config2_full_oracle():
     assert rel(gv.cpu().numpy(), adj["grad_values"]) <= GRAD_TOL_F64
 
 
-def _large_checks(w, dA, x, gb, gv, info, hist, k_match, precond):
-    b, g = w.b, w.g
-    # (a) the first k_match iterations, element by element
-    xk, ik, hk = sla.sla_cg_solve(dA, t(b), rtol=0.0, maxit=k_match, precond=precond, history=True)
-    ref = oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, b, rtol=0.0, maxit=k_match, precond=precond, history=True)
-    assert ik.iters == ref["iters"] == k_match
-    assert rel(xk.cpu().numpy(), ref["x"]) <= X_TOL_F64
-    check_history(hk.cpu().numpy(), ref["history"], k=k_match)
-    check_history(hist.cpu().numpy(), ref["history"], k=k_match)
-    del xk, hk
-    # (b) true residual of the final iterate vs the recursive one
-    xs = x.cpu().numpy()
-    res = b - oracle.spmv(w.A.row_ptr, w.A.col_idx, w.A.values, xs)
-    true_rel = float(np.linalg.norm(res) / np.linalg.norm(b))
-    # (c) grad_values = -lambda_i x_j exactly, on the GPU's own lambda and x
-    lam = gb.cpu().numpy()
-    gvo = oracle.grad_values(w.A.row_ptr, w.A.col_idx, lam, xs)
-    assert np.array_equal(gv.cpu().numpy(), gvo)
-    return lam, xs, true_rel
+def _gpu_forward_adjoint(w, rtol, precond):
+    """Forward solve with history and adjoint on the GPU; results copied to the host, device freed."""
+    dA = to_dev(w.A)
+    x, info, hist = sla.sla_cg_solve(dA, t(w.b), rtol=rtol, maxit=w.maxit, precond=precond, history=True)
+    gb, gv, ainfo = sla.sla_cg_adjoint(dA, x, t(w.g), rtol=rtol, maxit=w.maxit, precond=precond)
+    out = (x.cpu().numpy(), hist.cpu().numpy(), gb.cpu().numpy(), gv.cpu().numpy(), info, ainfo)
+    del dA, x, hist, gb, gv
+    torch.cuda.empty_cache()
+    return out
 
 
-def test_config4_jacobi_sampled():
+def _oracle_forward_adjoint(w, rtol, precond):
+    lib = oracle.load_parallel()
+    t0 = time.time()
+    ref = oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=rtol, maxit=w.maxit, precond=precond,
+                    history=True, lib=lib)
+    t1 = time.time()
+    adj = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, w.A.values, ref["x"], w.g, rtol=rtol, maxit=w.maxit,
+                            precond=precond, lib=lib)
+    t2 = time.time()
+    print(f"\n{w.name}: oracle on {lib.orc_threads(0)} host threads: forward {ref['iters']} iterations "
+          f"{t1 - t0:.1f} s, adjoint {adj['iters']} iterations {t2 - t1:.1f} s")
+    return ref, adj
+
+
+def test_config4_jacobi_full_oracle():
     w = config4()
-    dA = to_dev(w.A)
-    x, info, hist = sla.sla_cg_solve(dA, t(w.b), rtol=w.rtol, maxit=w.maxit, precond=1, history=True)
-    assert info.status == 0, info
-    gb, gv, ainfo = sla.sla_cg_adjoint(dA, x, t(w.g), rtol=w.rtol, maxit=w.maxit, precond=1)
-    assert ainfo.status == 0, ainfo
-    lam, xs, true_rel = _large_checks(w, dA, x, gb, gv, info, hist, 50, 1)
-    assert true_rel <= 10 * w.rtol, (true_rel, info.rel_res)
-    # (d) A lambda = g
-    lres = float(np.linalg.norm(w.g - oracle.spmv(w.A.row_ptr, w.A.col_idx, w.A.values, lam)) / np.linalg.norm(w.g))
-    assert lres <= 10 * w.rtol
-    # exact invariants of the solution map, to solve tolerance
-    gx = float(w.g @ xs)
-    assert abs(float(gv.cpu().numpy() @ w.A.values) + gx) <= 1e-4 * abs(gx)
-    assert abs(float(lam @ w.b) - gx) <= 1e-4 * abs(gx)
+    xs, hs, gbs, gvs, info, ainfo = _gpu_forward_adjoint(w, w.rtol, 1)
+    assert info.status == 0 and ainfo.status == 0, (info, ainfo)
+    ref, adj = _oracle_forward_adjoint(w, w.rtol, 1)
+    assert ref["status"] == adj["status"] == 0
+    assert abs(info.iters - ref["iters"]) <= ITER_SLACK_F64
+    assert abs(ainfo.iters - adj["iters"]) <= ITER_SLACK_F64
+    assert rel(xs, ref["x"]) <= X_TOL_F64
+    check_history(hs, ref["history"], k=50)
+    assert gvs.shape == (w.A.nnz,)  # one gradient per stored entry, in CSR order: the pattern of A
+    assert rel(gbs, adj["grad_b"]) <= GRAD_TOL_F64
+    assert rel(gvs, adj["grad_values"]) <= GRAD_TOL_F64
 
 
-@pytest.mark.skipif(_free_host_gb() < 64, reason="needs ~64 GB of host memory for the 169M-DOF oracle checks")
-def test_config5_fixed_iterations_sampled():
+@pytest.mark.skipif(_free_host_gb() < 64, reason="needs ~64 GB of host memory for the 169M-DOF oracle")
+def test_config5_fixed_iterations_full_oracle():
     w = config5()
-    dA = to_dev(w.A)
-    assert dA.row_ptr.dtype == torch.int64
-    x, info, hist = sla.sla_cg_solve(dA, t(w.b), rtol=0.0, maxit=w.maxit, history=True)
-    assert info.status == 1 and info.iters == w.maxit
-    gb, gv, ainfo = sla.sla_cg_adjoint(dA, x, t(w.g), rtol=0.0, maxit=w.maxit)
+    assert w.A.row_ptr.dtype == np.int64
+    xs, hs, gbs, gvs, info, ainfo = _gpu_forward_adjoint(w, 0.0, 0)
+    assert info.status == sla.SLA_NOT_CONVERGED and info.iters == w.maxit
     assert ainfo.iters == w.maxit
-    # after 1000 iterations the recursive and true residuals still agree closely
-    _, _, true_rel = _large_checks(w, dA, x, gb, gv, info, hist, 3, 0)
-    assert abs(true_rel - info.rel_res) <= 1e-6 * info.rel_res, (true_rel, info.rel_res)
+    ref, adj = _oracle_forward_adjoint(w, 0.0, 0)
+    assert ref["iters"] == adj["iters"] == w.maxit
+    assert rel(xs, ref["x"]) <= X_TOL_F64
+    check_history(hs, ref["history"], k=50)
+    assert gvs.shape == (w.A.nnz,)
+    assert rel(gbs, adj["grad_b"]) <= GRAD_TOL_F64
+    assert rel(gvs, adj["grad_values"]) <= GRAD_TOL_F64

@@ -3,8 +3,11 @@
 This module is shared by the oracle's tests, the GPU parity tests and the
 benchmark.  It holds the random draws and the assembly of the test matrices
 (2D five-point Poisson and variable-coefficient diffusion on a grid), and none
-of the solver's arithmetic: no matrix-vector product, no dot product, no
-conjugate-gradient step.
+of the solver's arithmetic: no dot product and no conjugate-gradient step.  The
+one product with a matrix it evaluates is input generation, the same on both
+sides: the manufactured right-hand side b = A x* of the 64 x 64 Poisson
+workload, taken on the grid by the five-point stencil (``_stencil_apply``)
+rather than through a CSR product.
 
 Workloads follow the experiments of "torch-sla: Differentiable Sparse Linear
 Algebra with Adjoint Solvers and Sparse Tensor Parallelism for PyTorch"
