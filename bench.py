@@ -457,19 +457,26 @@ def run_e2e(args, w, dev, precond, sla, torch):
 
 
 def cpu_baseline(w, iters):
-    """The fp64 oracle as it stands (one host thread) on a bounded sample: `iters` forward CG
-    iterations plus `iters` adjoint iterations on the same system."""
+    """The fp64 oracle as it stands, multi-core build on every host core, on a bounded sample:
+    `iters` forward CG iterations plus `iters` adjoint iterations on the same system (iters = 0:
+    sized from a short probe to about 15 s of host time)."""
     import oracle
-    oracle.load()
-    t0 = time.perf_counter()
-    f = oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=0.0, maxit=iters, precond=w.precond)
+    lib = oracle.load_parallel()
+    cores = lib.orc_threads(0)
     g = w.g if w.g is not None else np.random.default_rng(1).standard_normal(w.A.n)
+    if iters <= 0:
+        t0 = time.perf_counter()
+        oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=0.0, maxit=20, precond=w.precond, lib=lib)
+        per_it = (time.perf_counter() - t0) / 20
+        iters = int(min(20000, max(100, 7.5 / max(per_it, 1e-6))))
+    t0 = time.perf_counter()
+    f = oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=0.0, maxit=iters, precond=w.precond, lib=lib)
     a = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, w.A.values, f["x"], g, rtol=0.0, maxit=iters,
-                          precond=w.precond)
+                          precond=w.precond, lib=lib)
     dt = time.perf_counter() - t0
-    return {"value": (f["iters"] + a["iters"]) / dt, "unit": "iters/s", "cores": 1, "kind": "oracle",
+    return {"value": (f["iters"] + a["iters"]) / dt, "unit": "iters/s", "cores": cores, "kind": "oracle",
             "sample": f"{w.name}: {iters} forward + {iters} adjoint CG iterations (rtol 0) and one grad_values "
-                      f"pass, {dt:.1f} s on one host core"}
+                      f"pass, {dt:.1f} s on {cores} host cores (the oracle's multi-core build)"}
 
 
 EIG_METRIC = "smallest eigenpair (inverse iteration on CG) + eigenvalue gradient, 2D Poisson fp64: CG iters/sec"
@@ -600,14 +607,15 @@ def run_reference(args, rank, world):
     # on the same matrix is its baseline (a dense eigensolver does not scale to 1M unknowns)
     eig = args.config == "eig_poisson"
     w = config_by_name("poisson1000", m=args.grid_m or 1000) if eig else config_by_name(args.config)
-    oracle.load()
+    lib = oracle.load_parallel()
+    cores = lib.orc_threads(0)
     g = w.g if w.g is not None else np.random.default_rng(1).standard_normal(w.A.n)
     k = args.ref_iters
 
     def step():
-        f = oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=0.0, maxit=k, precond=w.precond)
+        f = oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=0.0, maxit=k, precond=w.precond, lib=lib)
         a = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, w.A.values, f["x"], g, rtol=0.0, maxit=k,
-                              precond=w.precond)
+                              precond=w.precond, lib=lib)
         return f["iters"] + a["iters"]
 
     for _ in range(args.warmup):
@@ -616,14 +624,15 @@ def run_reference(args, rank, world):
     its = sum(step() for _ in range(args.steps))
     dt = time.perf_counter() - t0
     v = its / dt
-    sample = f"{w.name}: each step {k} forward + {k} adjoint CG iterations (rtol 0) + grad_values, one host core"
+    sample = (f"{w.name}: each step {k} forward + {k} adjoint CG iterations (rtol 0) + grad_values, on {cores} "
+              f"host cores (the oracle's multi-core build)")
     return {"impl": "reference", "metric": EIG_METRIC if eig else METRIC, "value": v, "unit": "iters/s",
             "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generators)",
             "config": {"workload": w.name, "n": w.A.n, "nnz": w.A.nnz, "rtol": w.rtol},
-            "cpu_baseline": {"value": v, "unit": "iters/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "iters/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "iters/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -638,8 +647,8 @@ def main():
                          "poisson13000_int64 (or config1 .. config5)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-iters", type=int, default=600)
-    ap.add_argument("--ref-iters", type=int, default=100)
+    ap.add_argument("--cpu-iters", type=int, default=0, help="oracle sample size (0: about 15 s of host time)")
+    ap.add_argument("--ref-iters", type=int, default=200)
     ap.add_argument("--grid-m", type=int, default=0,
                     help="override the grid side m of the chosen workload (smaller cases for profiling)")
     ap.add_argument("--loop", choices=["auto", "cluster", "resident", "graph", "host"], default="auto",
