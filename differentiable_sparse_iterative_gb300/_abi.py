@@ -19,7 +19,9 @@ EXPORTS = [
     "sla_status_string", "sla_last_cuda_error", "sla_version", "sla_launch_count", "sla_cg_workspace_bytes",
     "sla_validate_csr", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values", "sla_cg_solve_batched",
     "sla_cg_adjoint_batched", "sla_cg_solve_static", "sla_eig_workspace_bytes", "sla_eig_smallest",
-    "sla_eig_grad_values", "sla_set_spmv_variant", "sla_test_set_barrier_wait",
+    "sla_eig_grad_values", "sla_set_spmv_variant", "sla_test_set_barrier_wait", "sla_dist_state_bytes",
+    "sla_dist_cg_begin", "sla_dist_cg_start", "sla_dist_cg_spmv", "sla_dist_cg_update", "sla_dist_cg_direction",
+    "sla_dist_pack", "sla_dist_cg_info",
 ]
 SLA_SPMV_PLAIN, SLA_SPMV_TMA = 0, 1
 
@@ -75,9 +77,20 @@ def bind(lib):
     lib.sla_eig_workspace_bytes.restype = sz
     lib.sla_eig_smallest.argtypes = [C, P, ctypes.POINTER(sla_eig_opts), ctypes.POINTER(sla_eig_info), P, sz, P]
     lib.sla_eig_grad_values.argtypes = [C, i64, P, ctypes.POINTER(ctypes.c_double), P, P]
+    lib.sla_dist_state_bytes.argtypes = []
+    lib.sla_dist_state_bytes.restype = sz
+    lib.sla_dist_cg_begin.argtypes = [C, i64, P, O, P, P, P, P, P, P, P, P]
+    lib.sla_dist_cg_start.argtypes = [P, i32, P, P, P]
+    lib.sla_dist_cg_spmv.argtypes = [C, i64, P, P, P, P, P]
+    lib.sla_dist_cg_update.argtypes = [i64, i32, i32, P, i32, P, P, P, P, P, P, P, P, P]
+    lib.sla_dist_cg_direction.argtypes = [i64, i32, P, i32, P, P, P, P, P]
+    lib.sla_dist_pack.argtypes = [i64, i32, P, P, i64, P, P]
+    lib.sla_dist_cg_info.argtypes = [P, I, ctypes.POINTER(i32), P]
     lib.sla_set_spmv_variant.argtypes = [i32]
     lib.sla_test_set_barrier_wait.argtypes = [ctypes.c_uint32, i64]
-    for name in ["sla_set_spmv_variant", "sla_test_set_barrier_wait", "sla_validate_csr", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
+    for name in ["sla_dist_cg_begin", "sla_dist_cg_start", "sla_dist_cg_spmv", "sla_dist_cg_update",
+                 "sla_dist_cg_direction", "sla_dist_pack", "sla_dist_cg_info",
+                 "sla_set_spmv_variant", "sla_test_set_barrier_wait", "sla_validate_csr", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
                  "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_cg_solve_static", "sla_eig_smallest",
                  "sla_eig_grad_values"]:
         getattr(lib, name).restype = i32

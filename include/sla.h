@@ -296,6 +296,76 @@ SLA_API sla_status sla_eig_smallest(const sla_csr *A, void *v, const sla_eig_opt
 SLA_API sla_status sla_eig_grad_values(const sla_csr *A, int64_t k, const void *V, const double *w,
                                        void *grad_values, void *stream);
 
+/* ---------------------------------------------------------------- distributed row-block CG */
+
+/*
+ * One rank's share of a CG solve whose matrix is split into contiguous row blocks, one per rank
+ * (TS Methodology 3, "distributed layer with halo exchange": each rank owns a row block, and
+ * before its local SpMV receives the values of the vector at the columns it references but does
+ * not own).  These calls run one rank's part of each step on its GPU; between them the caller
+ * moves halo values between ranks and gathers every rank's partial sums (torch.distributed in the
+ * Python layer).  Every rank adds the gathered partials in rank order, so all ranks hold
+ * bit-identical scalars and stop at the same iteration.
+ *
+ * Local block A_ext: the rank's n_own rows with columns renumbered, owned columns 0..n_own-1 first
+ * and then the halo columns n_own..n_ext-1 (n_ext = A_ext->n), given as a square CSR of order
+ * n_ext whose rows n_own..n_ext-1 are empty.  "own" vectors are device arrays of n_own entries of
+ * A_ext->dtype, "ext" vectors n_ext entries (owned values first, then the halo).
+ * State: a device buffer of sla_dist_state_bytes() bytes, 256-byte aligned, owned by the caller.
+ * Gathered partials: device arrays holding every rank's partials, rank-major ([ranks][k]).
+ * Iteration (each call is a no-op once the state's done flag is set, so a caller may enqueue
+ * several iterations between two reads of it):
+ *   sla_dist_cg_spmv      -> gather 1 partial (p.q)
+ *   sla_dist_cg_update    -> gather 2 partials (r.r, r.z)
+ *   sla_dist_cg_direction
+ *   sla_dist_pack + halo exchange of p
+ * The recurrences, stopping rule and status decisions are those of sla_cg_solve; x0 = 0.
+ * All calls are asynchronous except sla_dist_cg_info.
+ */
+SLA_API size_t sla_dist_state_bytes(void);
+
+/*
+ * Start of a solve: x = 0, r = b, p = z = M^{-1} r on the owned rows ((Jacobi) dinv = 1 / A_ii);
+ * writes this rank's 5 partials (b.b, r.r, r.z, count of non-finite and of non-positive diagonal
+ * entries) to `partials` (device, 5 doubles) and resets the state with opts (rtol, maxit, precond;
+ * opts->loop and unroll are ignored).  x, r: own vectors; p_ext: ext vector (its halo part is
+ * filled by the caller's exchange); z, dinv: own vectors, used only with Jacobi (else may be NULL).
+ */
+SLA_API sla_status sla_dist_cg_begin(const sla_csr *A_ext, int64_t n_own, const void *b, const sla_cg_opts *opts,
+                                     void *x, void *r, void *z, void *p_ext, void *dinv, double *partials,
+                                     void *state, void *stream);
+
+/* From the gathered begin partials ([ranks][5]): ||b||, the initial stopping test and status, rho;
+ * history (device, maxit+1 doubles, or NULL) receives ||r_0|| / ||b||. */
+SLA_API sla_status sla_dist_cg_start(const double *gathered, int32_t ranks, void *state, double *history,
+                                     void *stream);
+
+/* q = A_ext p_ext on the owned rows (q: own vector); this rank's partial of p.q into *partial. */
+SLA_API sla_status sla_dist_cg_spmv(const sla_csr *A_ext, int64_t n_own, const void *p_ext, void *q, double *partial,
+                                    void *state, void *stream);
+
+/* alpha = rho / (p.q summed over the gathered [ranks] partials); x += alpha p; r -= alpha q;
+ * z = dinv r (Jacobi); this rank's partials of r.r and r.z into partials[0..1].  p.q <= 0 stops
+ * with SLA_BREAKDOWN, a non-finite p.q with SLA_NONFINITE (x left at the last iterate). */
+SLA_API sla_status sla_dist_cg_update(int64_t n_own, int32_t dtype, int32_t precond, const double *gathered,
+                                      int32_t ranks, void *x, void *r, const void *p_ext, const void *q,
+                                      const void *dinv, void *z, double *partials, void *state, void *stream);
+
+/* r.r and r.z summed over the gathered [ranks][2] partials; history[k]; the stopping test
+ * (||r|| <= rtol ||b||, maxit, non-finite); else beta = r.z / rho and p = zr + beta p on the owned
+ * rows (zr: z with Jacobi, r without). */
+SLA_API sla_status sla_dist_cg_direction(int64_t n_own, int32_t dtype, const double *gathered, int32_t ranks,
+                                         const void *zr, void *p_ext, double *history, void *state, void *stream);
+
+/* buf[t] = v[idx[t]] for t < m (the owned values a neighbour reads; idx: device int64, entries
+ * outside [0, n) give 0).  Asynchronous. */
+SLA_API sla_status sla_dist_pack(int64_t n, int32_t dtype, const void *v, const int64_t *idx, int64_t m, void *buf,
+                                 void *stream);
+
+/* Reads the state (synchronises the stream): iterations, ||r|| / ||b||, status into info (host,
+ * may be NULL) and the done flag into *done (host, may be NULL). */
+SLA_API sla_status sla_dist_cg_info(const void *state, sla_cg_info *info, int32_t *done, void *stream);
+
 /* ---------------------------------------------------------------- allocation-free variant */
 
 /*
