@@ -15,6 +15,7 @@
 
 #include "sla_common.cuh"
 #include "sla_host.h"
+#include "sla_pattern.cuh"
 
 namespace sla {
 
@@ -72,46 +73,24 @@ __global__ void __launch_bounds__(kBlock) spmv_kernel(int64_t n, int64_t nnz, co
   }
 }
 
-// gv[s][k] = -lambda_s[row(k)] * x_s[col(k)]: one warp covers 32 consecutive rows and writes
-// their stored entries with lane-strided (coalesced) stores; the row of entry k comes from a
-// search over the 33 row starts held in registers.
+// gv[s][k] = -lambda_s[row(k)] * x_s[col(k)]: one streaming pass over the pattern (sla_pattern.cuh),
+// lambda staged per row tile in shared memory, x gathered per entry; blockIdx.y = system.
 template <typename V, typename I>
-__global__ void __launch_bounds__(kBlock) grad_values_kernel(int64_t n, int64_t nnz, const I *__restrict__ rp,
-                                                             const int32_t *__restrict__ ci,
-                                                             const V *__restrict__ lam, const V *__restrict__ x,
-                                                             V *__restrict__ gv) {
+__global__ void __launch_bounds__(kPatBlock, kPatMinBlocks) grad_values_kernel(int64_t n, int64_t nnz, const I *__restrict__ rp,
+                                                                const int32_t *__restrict__ ci,
+                                                                const V *__restrict__ lam, const V *__restrict__ x,
+                                                                V *__restrict__ gv) {
+  __shared__ PatSmem<V> sm;
   const int s = blockIdx.y;
   lam += (int64_t)s * n;
   x += (int64_t)s * n;
   gv += (int64_t)s * nnz;
-  const int lane = threadIdx.x & 31;
-  const int64_t warps_total = (int64_t)gridDim.x * kWarps;
-  for (int64_t w = blockIdx.x * (int64_t)kWarps + (threadIdx.x >> 5); w * 32 < n; w += warps_total) {
-    const int64_t r0 = w * 32;
-    const int64_t rl = r0 + lane;
-    const int64_t my_start = rl <= n ? (int64_t)rp[rl] : (int64_t)rp[n];
-    const V my_lam = rl < n ? lam[rl] : V(0);
-    const int64_t rend = r0 + 32 <= n ? r0 + 32 : n;
-    int64_t e_begin = __shfl_sync(0xffffffffu, my_start, 0);
-    int64_t e_end = (int64_t)rp[rend];
-    if (e_begin < 0 || e_end > nnz || e_end < e_begin) e_begin = e_end = 0;  // malformed row_ptr: skip
-    // warp-uniform trip count: every lane takes part in every shuffle
-    for (int64_t base = e_begin; base < e_end; base += 32) {
-      const int64_t e = base + lane;
-      // row of e: the last lane j with start_j <= e (binary search via shuffles)
-      int lo = 0;
-#pragma unroll
-      for (int step = 16; step > 0; step >>= 1) {
-        const int64_t st = __shfl_sync(0xffffffffu, my_start, lo + step);
-        if (st <= e) lo += step;
-      }
-      const V li = __shfl_sync(0xffffffffu, my_lam, lo);
-      if (e < e_end) {
-        const int32_t c = ci[e];
-        gv[e] = (uint32_t)c < (uint32_t)n ? -(li * x[c]) : V(0);
-      }
-    }
-  }
+  pattern_pass<V, I>(
+      n, nnz, rp, ci, sm, [&](int64_t i) { return __ldcs(lam + i); }, [](V l) { return l; },
+      [&](int32_t c) { return __ldg(x + c); },
+      [&](int64_t e, int64_t, V li, int32_t c, V xc) {
+        __stcs(gv + e, (uint32_t)c < (uint32_t)n ? -(li * xc) : V(0));
+      });
 }
 
 // Structural CSR check; records the smallest offending row.
@@ -165,6 +144,19 @@ __global__ void __launch_bounds__(kBlock) validate_kernel(int64_t n, int64_t nnz
 // ------------------------------------------------------------------------ helpers
 
 namespace {
+
+// Blocks of a pattern pass: one per row tile, at most as many as are resident on the device at once
+// (the remaining tiles are taken round-robin).
+int pattern_grid(int64_t n) {
+  int dev = 0, sms = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t want = (n + kPatRows - 1) / kPatRows;
+  const int64_t cap = (int64_t)sms * kPatMinBlocks;
+  if (want > cap) want = cap;
+  if (want < 1) want = 1;
+  return (int)want;
+}
 
 int grid_for(int64_t work, int per_block_rows) {
   int dev = 0, sms = 1;
@@ -240,8 +232,8 @@ void launch_spmv(const sla_csr *A, const void *x, void *y, cudaStream_t st) {
 
 template <typename V, typename I>
 void launch_grad(const sla_csr *A, int64_t batch, const void *lam, const void *x, void *gv, cudaStream_t st) {
-  dim3 grid(grid_for(A->n, kBlock * 4), (unsigned)batch);
-  grad_values_kernel<V, I><<<grid, kBlock, 0, st>>>(A->n, A->nnz, (const I *)A->row_ptr, A->col_idx,
+  dim3 grid(pattern_grid(A->n), (unsigned)batch);
+  grad_values_kernel<V, I><<<grid, kPatBlock, 0, st>>>(A->n, A->nnz, (const I *)A->row_ptr, A->col_idx,
                                                     (const V *)lam, (const V *)x, (V *)gv);
 }
 

@@ -15,6 +15,7 @@
 
 #include "sla_common.cuh"
 #include "sla_host.h"
+#include "sla_pattern.cuh"
 
 namespace sla {
 namespace {
@@ -150,17 +151,17 @@ __global__ void __launch_bounds__(kBlock) eig_negate(int64_t n, V *__restrict__ 
 // ------------------------------------------------------------------------ gradient kernel
 
 // gv[e] = sum_s (w_s * V_s[row(e)]) * V_s[col(e)], summed over s in order from the s = 0 term, in
-// fp64 with separately rounded operations, then rounded once to V.  One warp covers 32 consecutive
-// rows: each lane forms w_0 * V_0[row] for its row (one product per row, none when w_0 = 1, which
-// is exact), the lanes walk the rows' entries with lane-strided (coalesced) loads and stores, and an
-// entry's row is the last lane whose start is <= the entry (binary search by shuffles).  For k = 1
-// an entry costs one fp64 multiply.  The loop over further eigenvectors has a dynamic trip count:
-// an unrolled loop with predicated-off iterations would still occupy the fp64 unit.
+// fp64 with separately rounded operations, then rounded once to V: one streaming pass over the
+// pattern (sla_pattern.cuh) whose row factor w_0 * V_0[row] is formed once per row (none when
+// w_0 = 1, which is exact), so that for k = 1 an entry costs one fp64 multiply.  The loop over
+// further eigenvectors has a dynamic trip count: an unrolled loop with predicated-off iterations
+// would still occupy the fp64 unit.
 template <typename V, typename I>
-__global__ void __launch_bounds__(kBlock, 4) eig_grad_kernel(int64_t n, int64_t nnz, const I *__restrict__ rp,
-                                                          const int32_t *__restrict__ ci, int k,
-                                                          const V *__restrict__ vec, EigWeights W,
-                                                          V *__restrict__ gv) {
+__global__ void __launch_bounds__(kPatBlock, kPatMinBlocks) eig_grad_kernel(int64_t n, int64_t nnz, const I *__restrict__ rp,
+                                                             const int32_t *__restrict__ ci, int k,
+                                                             const V *__restrict__ vec, EigWeights W,
+                                                             V *__restrict__ gv) {
+  __shared__ PatSmem<double> sm;
   __shared__ double sw[kEigMaxVecs];
   if (threadIdx.x == 0) {
 #pragma unroll
@@ -168,36 +169,17 @@ __global__ void __launch_bounds__(kBlock, 4) eig_grad_kernel(int64_t n, int64_t 
   }
   __syncthreads();
   const double w0 = sw[0];
-  const int lane = threadIdx.x & 31;
-  const int64_t warps_total = (int64_t)gridDim.x * kWarps;
-  for (int64_t wi = blockIdx.x * (int64_t)kWarps + (threadIdx.x >> 5); wi * 32 < n; wi += warps_total) {
-    const int64_t r0 = wi * 32;
-    const int64_t rl = r0 + lane;
-    const int64_t my_start = rl <= n ? (int64_t)rp[rl] : (int64_t)rp[n];
-    double my_wv = 0.0;
-    if (rl < n) {
-      const double a = (double)vec[rl];
-      my_wv = w0 == 1.0 ? a : __dmul_rn(w0, a);
-    }
-    const int64_t rend = r0 + 32 <= n ? r0 + 32 : n;
-    int64_t e_begin = __shfl_sync(0xffffffffu, my_start, 0);
-    int64_t e_end = (int64_t)rp[rend];
-    if (e_begin < 0 || e_end > nnz || e_end < e_begin) e_begin = e_end = 0;  // malformed row_ptr: skip
-    for (int64_t base = e_begin; base < e_end; base += 32) {  // warp-uniform trip count
-      const int64_t e = base + lane;
-      int lo = 0;
-#pragma unroll
-      for (int step = 16; step > 0; step >>= 1) {
-        const int64_t st = __shfl_sync(0xffffffffu, my_start, lo + step);
-        if (st <= e) lo += step;
-      }
-      const double wv0 = __shfl_sync(0xffffffffu, my_wv, lo);
-      if (e < e_end) {
-        const int32_t c = ci[e];
-        const int64_t row = r0 + lo;
+  pattern_pass<double, I>(
+      n, nnz, rp, ci, sm, [&](int64_t i) { return vec[i]; },
+      [&](V raw) {
+        const double a = (double)raw;
+        return w0 == 1.0 ? a : __dmul_rn(w0, a);
+      },
+      [&](int32_t c) { return __ldg(vec + c); },
+      [&](int64_t e, int64_t row, double wv0, int32_t c, V vc) {
         double acc = 0.0;
-        if ((uint32_t)c < (uint32_t)n && row < n) {
-          acc = __dmul_rn(wv0, (double)vec[c]);
+        if ((uint32_t)c < (uint32_t)n) {
+          acc = __dmul_rn(wv0, (double)vc);
 #pragma unroll 1
           for (int s = 1; s < k; ++s) {
             const double ws = sw[s];
@@ -206,10 +188,8 @@ __global__ void __launch_bounds__(kBlock, 4) eig_grad_kernel(int64_t n, int64_t 
             acc = __dadd_rn(acc, __dmul_rn(wa, (double)vec[(int64_t)s * n + c]));
           }
         }
-        gv[e] = (V)acc;
-      }
-    }
-  }
+        __stcs(gv + e, (V)acc);
+      });
 }
 
 // ------------------------------------------------------------------------ host side
@@ -287,10 +267,10 @@ sla_status eig_grad_launch(const sla_csr *A, int k, const void *vec, const EigWe
   int dev = 0, sms = 1;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  int64_t g = (A->n + kBlock - 1) / kBlock;  // one warp per 32 rows
-  if (g > (int64_t)sms * 16) g = (int64_t)sms * 16;
+  int64_t g = (A->n + kPatRows - 1) / kPatRows;  // one block per row tile, at most one wave of blocks
+  if (g > (int64_t)sms * kPatMinBlocks) g = (int64_t)sms * kPatMinBlocks;
   if (g < 1) g = 1;
-  eig_grad_kernel<V, I><<<(unsigned)g, kBlock, 0, st>>>(A->n, A->nnz, (const I *)A->row_ptr, A->col_idx, k,
+  eig_grad_kernel<V, I><<<(unsigned)g, kPatBlock, 0, st>>>(A->n, A->nnz, (const I *)A->row_ptr, A->col_idx, k,
                                                         (const V *)vec, W, (V *)gv);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(e);

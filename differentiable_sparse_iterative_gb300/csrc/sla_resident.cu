@@ -574,11 +574,15 @@ __global__ void __launch_bounds__(kResBlock, 1) cg_resident(Prob<V, I> P, int ca
 //
 // One thread-block cluster of C CTAs (C <= 16) solves one system; a batch is a grid of clusters.
 // CTA j of a cluster keeps x, r, p, q (and 1/diag) of its row chunk in shared memory for the whole
-// solve.  p of rows owned by a partner CTA is read straight from the partner's shared memory
-// (distributed shared memory), so nothing is recomputed and nothing goes through global memory
-// during the iteration except the matrix stream.  The three dependencies of an iteration (p_k of
-// the partners, p.q, r.r) are hardware cluster barriers; each all-reduce adds the C block sums in
-// rank order in every CTA, so all CTAs of a cluster hold bit-identical scalars.
+// solve; nothing goes through global memory during the iteration except the matrix stream.  When
+// shared memory has room for a second p buffer (two_p), p_k is written to buffer k & 1 while the
+// partners still read p_{k-1} from the other, and p_k of a row owned by a partner CTA is formed
+// from the partner's r_k (1/diag) and p_{k-1}, read from its shared memory (distributed shared
+// memory) with the partner's own expression, so the same bits: the two dependencies of an
+// iteration (p.q and r.r) are then the only hardware cluster barriers.  Otherwise p of a
+// partner's row is read from the partner's shared memory once a third barrier has made every
+// CTA's p_k visible.  Each all-reduce adds the C block sums in rank order in every CTA, so all
+// CTAs of a cluster hold bit-identical scalars.
 namespace cgs = cooperative_groups;
 constexpr int kClBlock = 256;
 constexpr int kClMax = 16;
@@ -652,17 +656,20 @@ __device__ __forceinline__ void block_sum4(double (&v)[NV], double *sb) {
 }
 
 template <typename V, typename I, bool JAC, int CB>
-__global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, int mcap, int ro_on) {
+__global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, int mcap, int ro_on, int two_p) {
   cgs::cluster_group cl = cgs::this_cluster();
   const int rank = (int)cl.block_rank();
   const int sys = (int)(blockIdx.x / (unsigned)C);
   const int tid = threadIdx.x;
   extern __shared__ __align__(16) unsigned char smem_cl[];
+  // x, r, p (two buffers with two_p), q (and 1/diag), cap rows each, in this order in every CTA
   V *sx = reinterpret_cast<V *>(smem_cl);
   V *sr = sx + cap;
-  V *sp = sr + cap;
-  V *sq = sp + cap;
+  V *sp0 = sr + cap;
+  V *sp1 = two_p ? sp0 + cap : sp0;
+  V *sq = sp1 + cap;
   V *sd = JAC ? sq + cap : nullptr;
+  const int64_t sq_off = (int64_t)(two_p ? 4 : 3) * cap;  // offsets of q and 1/diag in every CTA's layout
   // optional copy of the CTA's CSR slice (mcap > 0): row offsets, columns, values; or of its row
   // offsets alone (ro_on)
   int32_t *s_ro = reinterpret_cast<int32_t *>(sq + cap + (JAC ? cap : 0));
@@ -670,7 +677,7 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
   V *s_val = reinterpret_cast<V *>(s_ci + ((mcap + 3) & ~3));
   __shared__ double s_part[2][5];  // [0]: setup sums, then r.r / r.z; [1]: p.q (partners read these)
   __shared__ double s_red[5 * CB];  // block-sum scratch
-  __shared__ V *s_peer[kClMax];    // partners' p arrays in distributed shared memory
+  __shared__ V *s_peer[kClMax];    // partners' vectors (the address of their x) in distributed shared memory
   __shared__ int32_t s_start[kClMax + 1];  // first row of each partner (n for the end)
   // beta, alpha, alpha_prev in the data type, converted once by thread 0 (a conversion is an fp64
   // instruction, 64 cycles of a sub-partition's fp64 unit, if every warp made its own)
@@ -692,7 +699,7 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
   double *hist = P.history ? P.history + (size_t)sys * (size_t)(P.maxit + 1) : nullptr;
   Ctl *Cs = P.ctl + sys;
   Glob *glob = P.glob;
-  if (tid < C) s_peer[tid] = cl.map_shared_rank(sp, tid);
+  if (tid < C) s_peer[tid] = cl.map_shared_rank(sx, tid);
   if (tid <= C) s_start[tid] = (int32_t)start_of(tid);
   if (blockIdx.x == 0 && tid == 0) atomicAdd(&glob->kernels, 1ull);
 
@@ -806,20 +813,25 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
   while (S.go) {
     const bool first = (k == 0);
     const V vb = s_vsc[0], va_prev = s_vsc[2];
+    V *sp = (k & 1) ? sp1 : sp0;         // p_k (one buffer without two_p)
+    const V *spo = (k & 1) ? sp0 : sp1;  // p_{k-1}
+    // p_k (one buffer) or p_{k-1} (two_p) in a partner's layout
+    const int64_t pp_off = (int64_t)cap * (two_p ? ((k & 1) ? 2 : 3) : 2);
     for (int li = tid; li < len; li += CB) {
       const V rl = sr[li];
       const V z = JAC ? sd[li] * rl : rl;
       V pv = z;
       if (!first) {
-        const V po = sp[li];
+        const V po = spo[li];
         pv = fmav<V>(vb, po, z);
         sx[li] = fmav<V>(va_prev, po, sx[li]);
       }
       sp[li] = pv;
     }
-    cl.sync();  // every CTA's p_k is in place
+    if (two_p) __syncthreads();  // this CTA's p_k is in place; the partners' is formed below
+    else cl.sync();              // every CTA's p_k is in place
     SLA_PHASE(0);
-    // p_k at column c: own rows from shared memory, a partner's from its shared memory (DSMEM)
+    // p_k at column c: own rows from shared memory, a partner's through distributed shared memory
     auto p_at = [&](int32_t c) -> V {
       const uint32_t off = (uint32_t)((int64_t)c - c0);
       if (off < (uint32_t)len) return sp[off];
@@ -830,7 +842,13 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
 #pragma unroll
       for (int step = kClMax / 2; step >= 1; step >>= 1)
         if (j + step < C && c >= s_start[j + step]) j += step;
-      return s_peer[j][c - s_start[j]];
+      const V *px = s_peer[j];
+      const int64_t o = (int64_t)c - s_start[j];
+      if (!two_p) return px[pp_off + o];
+      // the partner's own p_k expression from its r_k (1/diag) and p_{k-1}: the same bits
+      const V rc = px[cap + o];
+      const V zc = JAC ? px[sq_off + cap + o] * rc : rc;
+      return first ? zc : fmav<V>(vb, px[pp_off + o], zc);
     };
     // Rows come in groups of kClGroup per thread: p.q is summed in the data type within a group
     // and the groups in fp64.  The group is an outer loop, so no fp64 instruction sits in the
@@ -1010,9 +1028,10 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
   if (tid == 0) s_pending = pending;
   __syncthreads();
   const V va = (V)S.alpha;
+  const V *sp_last = ((k - 1) & 1) ? sp1 : sp0;  // p of the last iteration
   for (int li = tid; li < len; li += CB) {
     V xv = sx[li];
-    if (s_pending == 1) xv = fmav<V>(va, sp[li], xv);
+    if (s_pending == 1) xv = fmav<V>(va, sp_last[li], xv);
     else if (s_pending == 2) xv = V(0);
     xg[c0 + li] = xv;
   }
@@ -1088,7 +1107,7 @@ bool resident_fits(int64_t n, int64_t batch, int dtype, int precond, int64_t max
 // cluster runs a whole solve, so all of them must be resident at once: candidates are checked
 // with the occupancy API and the first that fits in one wave is taken.
 struct ClusterShape {
-  int C = 0, cap = 0, block = 0, mcap = 0, ro = 0;
+  int C = 0, cap = 0, block = 0, mcap = 0, ro = 0, two_p = 0;
   size_t smem = 0;
 };
 
@@ -1115,43 +1134,51 @@ ClusterShape cluster_shape_for(int64_t n, int64_t batch, int64_t nnz) {
   for (int c = c0; c <= kClMax; c *= 2) {
     if (c > n) break;
     const int64_t rows = (n + c - 1) / c;
-    const size_t vec_bytes = (size_t)rows * nvec * sizeof(V);
-    if (vec_bytes > kClSmemMax) continue;
-    // the CSR slice on chip if it fits beside the vectors (average row length plus slack)
+    // on-chip staging of the CSR slice, decided with one p buffer: the slice on chip if it fits
+    // beside the vectors (average row length plus slack), else the row offsets alone, so the
+    // streamed SpMV starts from shared memory
     const int64_t ment = (nnz * rows) / std::max<int64_t>(n, 1) + 64;
     const size_t mat_bytes = (size_t)((rows + 1 + 3) & ~3) * 4 + (size_t)((ment + 3) & ~3) * 4 + (size_t)ment * sizeof(V);
-    const bool keep_mat = vec_bytes + mat_bytes <= kClSmemMax;
-    // else the row offsets alone, so the streamed SpMV starts from shared memory
     const size_t ro_bytes = (size_t)((rows + 1 + 3) & ~3) * 4;
-    const bool keep_ro = SLA_CLUSTER_STAGE_RO && !keep_mat && vec_bytes + ro_bytes + 16 <= kClSmemMax;
-    const size_t smem = vec_bytes + (keep_mat ? mat_bytes : 0) + (keep_ro ? ro_bytes : 0) + 16;
+    const size_t vec1 = (size_t)rows * nvec * sizeof(V);
+    if (vec1 > kClSmemMax) continue;
+    const bool keep_mat = vec1 + mat_bytes <= kClSmemMax;
+    const bool keep_ro = SLA_CLUSTER_STAGE_RO && !keep_mat && vec1 + ro_bytes + 16 <= kClSmemMax;
+    // block sizes in order of preference; for each, a second p buffer (one cluster barrier fewer
+    // per iteration) when it fits with the same staging, else one
     for (int block : {rows >= 2048 ? 512 : kClBlock, kClBlock}) {
-      void *fn = block == 512 ? (void *)cg_cluster<V, I, JAC, 512> : (void *)cg_cluster<V, I, JAC, kClBlock>;
-      cudaLaunchConfig_t cfg;
-      memset(&cfg, 0, sizeof(cfg));
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeClusterDimension;
-      at[0].val.clusterDim.x = (unsigned)c;
-      at[0].val.clusterDim.y = 1;
-      at[0].val.clusterDim.z = 1;
-      cfg.gridDim = dim3((unsigned)(batch * c));
-      cfg.blockDim = dim3(block);
-      cfg.dynamicSmemBytes = smem;
-      cfg.attrs = at;
-      cfg.numAttrs = 1;
-      int active = 0;
-      if (cudaOccupancyMaxActiveClusters(&active, fn, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        continue;
-      }
-      if (active >= batch) {
-        best.C = c;
-        best.cap = (int)rows;
-        best.block = block;
-        best.mcap = keep_mat ? (int)ment : 0;
-        best.ro = keep_ro ? 1 : 0;
-        best.smem = smem;
-        return best;
+      for (int two_p = 1; two_p >= 0; --two_p) {
+        const size_t vec_bytes = vec1 + (two_p ? (size_t)rows * sizeof(V) : 0);
+        const size_t smem = vec_bytes + (keep_mat ? mat_bytes : 0) + (keep_ro ? ro_bytes : 0) + 16;
+        if (smem > kClSmemMax) continue;
+        void *fn = block == 512 ? (void *)cg_cluster<V, I, JAC, 512> : (void *)cg_cluster<V, I, JAC, kClBlock>;
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof(cfg));
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = (unsigned)c;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3((unsigned)(batch * c));
+        cfg.blockDim = dim3(block);
+        cfg.dynamicSmemBytes = smem;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, fn, &cfg) != cudaSuccess) {
+          cudaGetLastError();
+          continue;
+        }
+        if (active >= batch) {
+          best.C = c;
+          best.cap = (int)rows;
+          best.block = block;
+          best.mcap = keep_mat ? (int)ment : 0;
+          best.ro = keep_ro ? 1 : 0;
+          best.two_p = two_p;
+          best.smem = smem;
+          return best;
+        }
       }
     }
   }
@@ -1179,9 +1206,9 @@ sla_status run_cluster(Prob<V, I> P, int64_t batch, cudaStream_t stream, sla_cg_
   if (e == cudaSuccess) e = cudaMemsetAsync(P.ctl, 0, sizeof(Ctl) * (size_t)batch, stream);
   if (e != cudaSuccess) return fail(e);
   if (sh.block == 512)
-    e = cudaLaunchKernelEx(&cfg, cg_cluster<V, I, JAC, 512>, P, sh.C, sh.cap, sh.mcap, sh.ro);
+    e = cudaLaunchKernelEx(&cfg, cg_cluster<V, I, JAC, 512>, P, sh.C, sh.cap, sh.mcap, sh.ro, sh.two_p);
   else
-    e = cudaLaunchKernelEx(&cfg, cg_cluster<V, I, JAC, kClBlock>, P, sh.C, sh.cap, sh.mcap, sh.ro);
+    e = cudaLaunchKernelEx(&cfg, cg_cluster<V, I, JAC, kClBlock>, P, sh.C, sh.cap, sh.mcap, sh.ro, sh.two_p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(e);
   if (!info) return SLA_OK;

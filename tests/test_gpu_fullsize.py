@@ -38,12 +38,13 @@ def test_config2_full_oracle():
     b, g = t(w.b), t(w.g)
     x, info, hist = sla.sla_cg_solve(dA, b, rtol=w.rtol, maxit=w.maxit, history=True)
     gb, gv, ainfo = sla.sla_cg_adjoint(dA, x, g, rtol=w.rtol, maxit=w.maxit)
-    ref = oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=w.rtol, maxit=w.maxit, history=True)
+    lib = oracle.load_parallel()
+    ref = oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=w.rtol, maxit=w.maxit, history=True, lib=lib)
     assert info.status == ref["status"] == 0
     assert abs(info.iters - ref["iters"]) <= ITER_SLACK_F64
     assert rel(x.cpu().numpy(), ref["x"]) <= X_TOL_F64
     check_history(hist.cpu().numpy(), ref["history"], k=50)
-    adj = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, w.A.values, ref["x"], w.g, rtol=w.rtol, maxit=w.maxit)
+    adj = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, w.A.values, ref["x"], w.g, rtol=w.rtol, maxit=w.maxit, lib=lib)
     assert ainfo.status == adj["status"] == 0
     assert abs(ainfo.iters - adj["iters"]) <= ITER_SLACK_F64
     assert rel(gb.cpu().numpy(), adj["grad_b"]) <= GRAD_TOL_F64

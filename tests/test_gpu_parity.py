@@ -94,6 +94,40 @@ def test_grad_values_exact_on_given_vectors():
     assert np.array_equal(gv, oracle.grad_values(A.row_ptr, A.col_idx, lam, x))
 
 
+def _ragged_pattern(n, seed, long_lens=(), empty_every=7, rowptr64=False, empty_span=None):
+    """Rows of 0..12 entries (every empty_every-th row empty, and all rows of empty_span), plus rows of
+    the given long lengths."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(0, 13, n)
+    lens[::empty_every] = 0
+    if empty_span:
+        lens[empty_span[0]:empty_span[1]] = 0
+    for j, L in enumerate(long_lens):
+        lens[(j * 997 + 11) % n] = min(L, n)
+    rp = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64 if rowptr64 else np.int32)
+    ci = np.concatenate([np.sort(rng.choice(n, L, replace=False)) for L in lens]).astype(np.int32)
+    return rp, ci
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+@pytest.mark.parametrize("rowptr64", [False, True])
+def test_grad_values_tiles_chunks_long_and_empty_rows(dtype, rowptr64):
+    # several 1024-row tiles with a ragged last one; rows longer than an 8192-entry chunk (split
+    # across chunks), exactly one chunk long, and empty rows; one rounded product per entry, so
+    # the result is exact (for float data the oracle's fp64 product of two floats is exact and
+    # rounds once, as the kernel's float product does)
+    n = 9 * 1024 + 77
+    rp, ci = _ragged_pattern(n, 11, long_lens=(9000, 8192, 8193, 3000), rowptr64=rowptr64, empty_span=(2048, 2900))
+    assert np.diff(rp.astype(np.int64)).max() > 8192 and (np.diff(rp) == 0).any()
+    rng = np.random.default_rng(12)
+    lam, x = rng.standard_normal(n).astype(dtype), rng.standard_normal(n).astype(dtype)
+    vals = np.ones(ci.shape[0], dtype)
+    dA = sla.CSRMatrix.from_numpy(rp, ci, vals, "cuda:0")
+    gv = sla.sla_grad_values(dA, t(lam), t(x)).cpu().numpy()
+    ref = oracle.grad_values(rp, ci, lam.astype(np.float64), x.astype(np.float64)).astype(dtype)
+    assert gv.dtype == dtype and np.array_equal(gv, ref)
+
+
 def test_config1_manufactured_and_loss_adjoint():
     w = config1()
     dA = to_dev(w.A)
@@ -431,3 +465,31 @@ def test_batched_f32_several_row_groups(m):
         assert ainfos[s].status == 0
         assert rel(gbs[s], adj["grad_b"]) <= TOL_F32
         assert rel(gvs[s], adj["grad_values"]) <= TOL_F32
+
+
+@pytest.mark.parametrize("case", ["poisson179", "dirichlet150_jacobi"])
+def test_cluster_two_p_buffers_streamed_matrix(case):
+    # one fp64 system on a 16-CTA cluster whose CSR slice does not fit on chip (the SpMV streams it,
+    # row offsets staged) while two p buffers do: partner rows' p_k formed from the partner's r_k
+    # (1/diag) and p_{k-1}, two cluster barriers per iteration; against the oracle
+    if case == "poisson179":
+        A, precond = poisson_5pt(179), 0
+    else:
+        m = 150
+        A, precond = diffusion_dirichlet(m, np.random.default_rng(8).lognormal(0, 1.0, 2 * m * (m + 1))), 1
+    b = np.random.default_rng(9).standard_normal(A.n)
+    g = np.random.default_rng(10).standard_normal(A.n)
+    dA = to_dev(A)
+    x, info, hist = sla.sla_cg_solve(dA, t(b), rtol=1e-10, maxit=20000, precond=precond, history=True,
+                                     loop=sla.SLA_LOOP_CLUSTER)
+    gb, gv, ainfo = sla.sla_cg_adjoint(dA, x, t(g), rtol=1e-10, maxit=20000, precond=precond,
+                                       loop=sla.SLA_LOOP_CLUSTER)
+    assert info.path == "cluster" and info.kernels == 1
+    ref = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-10, maxit=20000, precond=precond, history=True)
+    adj = oracle.cg_adjoint(A.row_ptr, A.col_idx, A.values, ref["x"], g, rtol=1e-10, maxit=20000, precond=precond)
+    assert info.status == ref["status"] == 0 and abs(info.iters - ref["iters"]) <= ITER_SLACK_F64
+    assert rel(x.cpu().numpy(), ref["x"]) <= X_TOL_F64
+    check_history(hist.cpu().numpy(), ref["history"])
+    assert ainfo.status == 0 and abs(ainfo.iters - adj["iters"]) <= ITER_SLACK_F64
+    assert rel(gb.cpu().numpy(), adj["grad_b"]) <= GRAD_TOL_F64
+    assert rel(gv.cpu().numpy(), adj["grad_values"]) <= GRAD_TOL_F64
