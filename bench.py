@@ -17,8 +17,8 @@ poisson13000_int64 (short aliases config1 .. config5); eig_poisson: the smallest
 of the 1M-DOF Poisson matrix by inverse iteration on the CG plus its eigenvalue gradient.
 
 With N > 1 the script runs under torch.distributed.run; every rank solves its own
-independent system of the same size (the single-system solve has no exchange step:
-replicas, weak scaling).  --impl reference times the fp64 CPU oracle on a bounded
+independent system of the same size (replicas, weak scaling).  --dist splits one system
+across the ranks instead (row blocks with halo exchange, strong scaling).  --impl reference times the fp64 CPU oracle on a bounded
 sample of the same workload.
 """
 from __future__ import annotations
@@ -315,6 +315,86 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(w, args.cpu_iters)
     return out
+
+
+def run_dist(args, rank, world, local_rank):
+    """One system split across the ranks (row blocks of whole grid rows, halo exchange, sums over ranks:
+    the distributed layer): forward solve + adjoint per step, timed on every rank, max over ranks.
+    Strong scaling: the system is the same for every N."""
+    import torch
+    import torch.distributed as dist
+    from differentiable_sparse_iterative_gb300 import distributed as D
+    from workloads import config_by_name
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = config_by_name(args.config, **({"m": args.grid_m} if args.grid_m else {}))
+    if w.batch > 0:
+        raise SystemExit("--dist takes a single-system workload")
+    m = int(w.meta.get("m", 1))
+    bounds = D.partition_rows(w.A.row_ptr, world, m)
+    blk = D.local_block(w.A.row_ptr, w.A.col_idx, w.A.values, bounds, rank)
+    solver = D.DistCG(blk, D.TorchComm(), device=dev)
+    g_np = w.g if w.g is not None else np.random.default_rng(1).standard_normal(w.A.n)
+    b = torch.from_numpy(w.b[blk.lo:blk.hi].copy()).to(dev)
+    g = torch.from_numpy(g_np[blk.lo:blk.hi].copy()).to(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        x, fi, _ = solver.solve(b, rtol=w.rtol, maxit=w.maxit, precond=w.precond)
+        e1.record(stream)
+        _, _, ai = solver.adjoint(x, g, rtol=w.rtol, maxit=w.maxit, precond=w.precond)
+        e2.record(stream)
+        return e0, e1, e2, fi, ai
+
+    for _ in range(args.warmup):
+        flush_l2(flush)
+        step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    recs = []
+    with ClockSampler(local_rank) as clk:
+        for _ in range(args.steps):
+            flush_l2(flush)
+            recs.append(step())
+        torch.cuda.synchronize()
+    dist.barrier()
+    fwd_ms = [r[0].elapsed_time(r[1]) for r in recs]
+    adj_ms = [r[1].elapsed_time(r[2]) for r in recs]
+    its = sum(r[3].iters + r[4].iters for r in recs)
+    t = torch.tensor([sum(fwd_ms) + sum(adj_ms)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    tot_s = float(t.item()) / 1e3
+    n, nnz = w.A.n, w.A.nnz
+    Bi = b_iter(n, nnz, 8, w.A.row_ptr.dtype.itemsize, w.precond == 1)
+    peak, peak_kind = measured_peaks()
+    achieved = Bi * sum(r[3].iters for r in recs) / (sum(fwd_ms) / 1e3) / 1e9
+    return {
+        "metric": METRIC, "value": its / tot_s, "unit": "iters/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_s * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generators; no dataset on the pages)",
+        "config": {"workload": w.name, "n": n, "nnz": nnz, "rtol": w.rtol,
+                   "precond": "jacobi" if w.precond == 1 else "none",
+                   "step": "forward CG solve + adjoint (grad_b, grad_values), one system over all ranks",
+                   "l2": "flushed between steps (256 MB write)",
+                   "parallelism": f"row blocks x{world} (halo exchange, all-gathered partial sums)"},
+        "iters_forward": statistics.mean(r[3].iters for r in recs),
+        "iters_adjoint": statistics.mean(r[4].iters for r in recs),
+        "time_to_tolerance_ms": statistics.mean(fwd_ms), "adjoint_ms": statistics.mean(adj_ms),
+        "status": sorted({r[3].status for r in recs} | {r[4].status for r in recs}),
+        "path": "distributed",
+        "roofline": {"kernel": "sla_dist_* steps (job-wide algorithmic bytes over the job's peak)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak * world, "unit": "GB/s",
+                     "frac": achieved / (peak * world), "peak_kind": peak_kind, "bytes_per_iter": Bi,
+                     "traffic": None},
+        "rows_per_rank": [int(bounds[q + 1] - bounds[q]) for q in range(world)],
+        "clocks": clk.summary(),
+    }
 
 
 def run_batched(args, w, dev, rank, world):
@@ -651,6 +731,8 @@ def main():
     ap.add_argument("--ref-iters", type=int, default=200)
     ap.add_argument("--grid-m", type=int, default=0,
                     help="override the grid side m of the chosen workload (smaller cases for profiling)")
+    ap.add_argument("--dist", action="store_true",
+                    help="one system split across the ranks (row blocks, halo exchange) instead of replicas")
     ap.add_argument("--loop", choices=["auto", "cluster", "resident", "graph", "host"], default="auto",
                     help="auto (default): resident kernel when the system fits on chip, else graph; "
                          "host: host-driven loop, e.g. for per-kernel ncu")
@@ -663,16 +745,26 @@ def main():
         if out is not None:
             print(json.dumps(out), flush=True)
         return
-    if world > 1:
+    if world > 1 or args.dist:
         import torch
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
+        if "MASTER_ADDR" not in os.environ:  # a single process without torch.distributed.run
+            import socket
+            with socket.socket() as sk:
+                sk.bind(("127.0.0.1", 0))
+                os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(sk.getsockname()[1]), RANK="0",
+                                  WORLD_SIZE="1")
         dist.init_process_group("nccl")
-    out = run_eig(args, rank, world, local_rank) if args.config == "eig_poisson" else \
-        run_ours(args, rank, world, local_rank)
+    if args.dist:
+        out = run_dist(args, rank, world, local_rank)
+    elif args.config == "eig_poisson":
+        out = run_eig(args, rank, world, local_rank)
+    else:
+        out = run_ours(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(out), flush=True)
-    if world > 1:
+    if world > 1 or args.dist:
         import torch.distributed as dist
         dist.destroy_process_group()
 
