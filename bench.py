@@ -74,16 +74,22 @@ def fp64_peak_tflops(clocks=None):
     return 152 * 2 * 2 * mhz * 1e6 / 1e12
 
 
-# The sources the CG iteration kernels are compiled from: the kernels whose DRAM bytes per
-# iteration profiles/traffic.json records.  Host-side files (argument checks, entry points) and
-# the eigenvalue solver's file hold none of them.
-CG_KERNEL_SOURCES = ("sla_common.cuh", "sla_tma.cuh", "sla_cg.cu", "sla_resident.cu")
+# The sources each engine's CG kernels are compiled from: a traffic record in profiles/traffic.json
+# stays valid while these files are unchanged.  Host-side files (argument checks, entry points),
+# the gradient and eigenvalue kernels and the other engines' files hold none of them.
+KERNEL_SOURCES = {
+    "cluster": ("sla_common.cuh", "sla_onchip.cuh", "sla_cluster.cu"),
+    "resident": ("sla_common.cuh", "sla_onchip.cuh", "sla_resident.cu"),
+    "streaming": ("sla_common.cuh", "sla_tma.cuh", "sla_cg.cu"),
+}
+ENGINE_OF = {"config1": "cluster", "config3": "cluster", "config2": "resident", "config4": "streaming",
+             "config5": "streaming"}
 
 
-def csrc_sha256():
+def csrc_sha256(engine):
     import hashlib
     h = hashlib.sha256()
-    for name in CG_KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[engine]:
         h.update(name.encode())
         with open(os.path.join(ROOT, "differentiable_sparse_iterative_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
@@ -103,7 +109,7 @@ def profiled_traffic(config):
             rec = json.load(f).get(config)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("csrc_sha256") != csrc_sha256():
+    if not rec or config not in ENGINE_OF or rec.get("csrc_sha256") != csrc_sha256(ENGINE_OF[config]):
         return None
     return rec
 

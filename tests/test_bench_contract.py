@@ -50,9 +50,9 @@ def test_traffic_record_requires_matching_sources(monkeypatch, tmp_path):
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "csrc_sha256", lambda: "0" * 64)
+    monkeypatch.setattr(bench, "csrc_sha256", lambda engine: "0" * 64)
     assert bench.profiled_traffic("config2")["dram_bytes_per_iter"] == 1
-    monkeypatch.setattr(bench, "csrc_sha256", lambda: "1" * 64)
+    monkeypatch.setattr(bench, "csrc_sha256", lambda engine: "1" * 64)
     assert bench.profiled_traffic("config2") is None
 
 
@@ -62,20 +62,19 @@ def test_eig_gradient_bytes():
     assert bench.b_eig_grad(1_000_000, 4_996_000, 8, 4) == 4_996_000 * 12 + 1_000_001 * 4 + 8_000_000
 
 
-def test_traffic_hash_covers_the_cg_kernel_sources_only(monkeypatch, tmp_path):
-    # the record stays valid across changes to files holding no CG kernel, and not otherwise
+def test_traffic_hash_covers_each_engines_kernel_sources_only(monkeypatch, tmp_path):
+    # an engine's record stays valid across changes to files holding none of its kernels, and not otherwise
     csrc = tmp_path / "differentiable_sparse_iterative_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    for name in bench.CG_KERNEL_SOURCES + ("sla_eig.cu", "sla_api.cu"):
+    names = sorted({f for fs in bench.KERNEL_SOURCES.values() for f in fs} | {"sla_eig.cu", "sla_api.cu"})
+    for name in names:
         (csrc / name).write_text(name)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    h0 = bench.csrc_sha256()
-    (csrc / "sla_eig.cu").write_text("changed")
-    (csrc / "sla_api.cu").write_text("changed")
-    assert bench.csrc_sha256() == h0
-    for name in bench.CG_KERNEL_SOURCES:
-        (csrc / name).write_text(name + " changed")
-        assert bench.csrc_sha256() != h0
-        (csrc / name).write_text(name)
-    assert bench.csrc_sha256() == h0
-
+    for engine, files in bench.KERNEL_SOURCES.items():
+        h0 = bench.csrc_sha256(engine)
+        for name in names:
+            (csrc / name).write_text(name + " changed")
+            assert (bench.csrc_sha256(engine) != h0) == (name in files), (engine, name)
+            (csrc / name).write_text(name)
+        assert bench.csrc_sha256(engine) == h0
+    assert set(bench.ENGINE_OF) == {"config1", "config2", "config3", "config4", "config5"}
