@@ -37,7 +37,7 @@ __all__ = [
     "SLA_LOOP_RESIDENT", "SLA_LOOP_CLUSTER", "SLA_OK", "SLA_NOT_CONVERGED", "SLA_BREAKDOWN", "SLA_INVALID_ARG",
     "SLA_BAD_CSR", "SLA_NONFINITE", "SLA_WORKSPACE_TOO_SMALL", "SLA_TIMEOUT", "SLA_CUDA_ERROR",
     "EigInfo", "sla_eig_workspace_bytes", "sla_eig_smallest", "sla_eig_grad_values", "EigSmallest",
-    "eigsh_smallest", "sla_set_spmv_variant", "sla_test_set_barrier_wait", "SLA_SPMV_PLAIN", "SLA_SPMV_TMA",
+    "eigsh_smallest", "sla_spmv_transpose", "sla_matvec_grad_values", "MatVec", "sla_set_spmv_variant", "sla_test_set_barrier_wait", "SLA_SPMV_PLAIN", "SLA_SPMV_TMA",
 ]
 from ._abi import SLA_SPMV_PLAIN, SLA_SPMV_TMA  # noqa: E402
 
@@ -354,9 +354,55 @@ def solve(A: CSRMatrix, b: torch.Tensor, rtol: float = 1e-8, maxit: int = 10000,
     return CGSolve.apply(A.row_ptr, A.col_idx, A.values, b, rtol, maxit, precond)
 
 
+def sla_spmv_transpose(A: CSRMatrix, x: torch.Tensor, y: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """y = A^T x for a structurally symmetric pattern (values may differ); raises SlaError(SLA_BAD_CSR)
+    when a stored entry has no stored partner (synchronises the stream to check)."""
+    dt, dev = A.values.dtype, A.values.device
+    if y is None:
+        y = torch.empty(A.n, dtype=dt, device=dev)
+    bad = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(lib().sla_spmv_transpose(ctypes.byref(_csr_struct(A)), _dev_ptr(x, dt, "x"), _dev_ptr(y, dt, "y"),
+                                    _dev_ptr(bad, name="bad"), _stream(dev)), "sla_spmv_transpose")
+    if int(bad.item()) != 0:
+        raise SlaError(SLA_BAD_CSR, "sla_spmv_transpose (the pattern is not structurally symmetric)")
+    return y
+
+
+def sla_matvec_grad_values(A: CSRMatrix, gy: torch.Tensor, x: torch.Tensor,
+                           out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """grad_values[k] = gy[row(k)] * x[col(k)]: the gradient of L(A x) w.r.t. the stored values (asynchronous)."""
+    dt, dev = A.values.dtype, A.values.device
+    if out is None:
+        out = torch.empty(A.nnz, dtype=dt, device=dev)
+    _check(lib().sla_matvec_grad_values(ctypes.byref(_csr_struct(A)), _dev_ptr(gy, dt, "gy"), _dev_ptr(x, dt, "x"),
+                                        _dev_ptr(out, dt, "grad_values"), _stream(dev)), "sla_matvec_grad_values")
+    return out
+
+
+class MatVec(torch.autograd.Function):
+    """y = A x with gradients to the stored values (gy_i x_j on the pattern) and to x (A^T gy)."""
+
+    @staticmethod
+    def forward(ctx, row_ptr, col_idx, values, x):
+        A = CSRMatrix(row_ptr, col_idx, values)
+        y = sla_spmv(A, x.contiguous())
+        ctx.save_for_backward(row_ptr, col_idx, values, x)
+        return y
+
+    @staticmethod
+    def backward(ctx, gy):
+        row_ptr, col_idx, values, x = ctx.saved_tensors
+        A = CSRMatrix(row_ptr, col_idx, values)
+        gy = gy.contiguous()
+        gv = sla_matvec_grad_values(A, gy, x.contiguous()) if ctx.needs_input_grad[2] else None
+        gx = sla_spmv_transpose(A, gy) if ctx.needs_input_grad[3] else None
+        return None, None, gv, gx
+
+
 def matvec(A: CSRMatrix, x: torch.Tensor) -> torch.Tensor:
-    """y = A x through libsla (not differentiable; see solve for the differentiable path)."""
-    return sla_spmv(A, x)
+    """Differentiable y = A x (gradients flow to A.values and x; the x gradient A^T dL/dy needs a
+    structurally symmetric pattern)."""
+    return MatVec.apply(A.row_ptr, A.col_idx, A.values, x)
 
 
 # --------------------------------------------------------------------------- eigenvalue problems

@@ -21,7 +21,7 @@ EXPORTS = [
     "sla_cg_adjoint_batched", "sla_cg_solve_static", "sla_eig_workspace_bytes", "sla_eig_smallest",
     "sla_eig_grad_values", "sla_set_spmv_variant", "sla_test_set_barrier_wait", "sla_dist_state_bytes",
     "sla_dist_cg_begin", "sla_dist_cg_start", "sla_dist_cg_spmv", "sla_dist_cg_update", "sla_dist_cg_direction",
-    "sla_dist_pack", "sla_dist_cg_info",
+    "sla_dist_pack", "sla_dist_cg_info", "sla_spmv_transpose", "sla_matvec_grad_values", "sla_dist_scatter_add",
 ]
 SLA_SPMV_PLAIN, SLA_SPMV_TMA = 0, 1
 
@@ -77,6 +77,9 @@ def bind(lib):
     lib.sla_eig_workspace_bytes.restype = sz
     lib.sla_eig_smallest.argtypes = [C, P, ctypes.POINTER(sla_eig_opts), ctypes.POINTER(sla_eig_info), P, sz, P]
     lib.sla_eig_grad_values.argtypes = [C, i64, P, ctypes.POINTER(ctypes.c_double), P, P]
+    lib.sla_spmv_transpose.argtypes = [C, P, P, P, P]
+    lib.sla_matvec_grad_values.argtypes = [C, P, P, P, P]
+    lib.sla_dist_scatter_add.argtypes = [i64, i32, P, P, i64, P, P]
     lib.sla_dist_state_bytes.argtypes = []
     lib.sla_dist_state_bytes.restype = sz
     lib.sla_dist_cg_begin.argtypes = [C, i64, P, O, P, P, P, P, P, P, P, P]
@@ -88,7 +91,7 @@ def bind(lib):
     lib.sla_dist_cg_info.argtypes = [P, I, ctypes.POINTER(i32), P]
     lib.sla_set_spmv_variant.argtypes = [i32]
     lib.sla_test_set_barrier_wait.argtypes = [ctypes.c_uint32, i64]
-    for name in ["sla_dist_cg_begin", "sla_dist_cg_start", "sla_dist_cg_spmv", "sla_dist_cg_update",
+    for name in ["sla_spmv_transpose", "sla_matvec_grad_values", "sla_dist_scatter_add", "sla_dist_cg_begin", "sla_dist_cg_start", "sla_dist_cg_spmv", "sla_dist_cg_update",
                  "sla_dist_cg_direction", "sla_dist_pack", "sla_dist_cg_info",
                  "sla_set_spmv_variant", "sla_test_set_barrier_wait", "sla_validate_csr", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
                  "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_cg_solve_static", "sla_eig_smallest",

@@ -93,6 +93,61 @@ __global__ void __launch_bounds__(kPatBlock, kPatMinBlocks) grad_values_kernel(i
       });
 }
 
+// gv[e] = gy[row(e)] * x[col(e)]: the gradient of L(A x) with respect to the stored values, for
+// gy = dL/dy (one rounded product per entry), by the same streaming pass.
+template <typename V, typename I>
+__global__ void __launch_bounds__(kPatBlock, kPatMinBlocks) matvec_grad_kernel(int64_t n, int64_t nnz,
+                                                                               const I *__restrict__ rp,
+                                                                               const int32_t *__restrict__ ci,
+                                                                               const V *__restrict__ gy,
+                                                                               const V *__restrict__ x,
+                                                                               V *__restrict__ gv) {
+  __shared__ PatSmem<V> sm;
+  pattern_pass<V, I>(
+      n, nnz, rp, ci, sm, [&](int64_t i) { return __ldcs(gy + i); }, [](V a) { return a; },
+      [&](int32_t c) { return __ldg(x + c); },
+      [&](int64_t e, int64_t, V gi, int32_t c, V xc) {
+        __stcs(gv + e, (uint32_t)c < (uint32_t)n ? gi * xc : V(0));
+      });
+}
+
+// y = A^T x for a structurally symmetric pattern (every stored (j, i) has a stored (i, j)): row j
+// gathers a_ij x_i over the columns i of its own row, in their (increasing) order, each a_ij found
+// by a binary search in row i.  One thread per row; deterministic.  A missing partner entry is
+// skipped and raises *bad (when given).
+template <typename V, typename I>
+__global__ void __launch_bounds__(kBlock) spmv_t_kernel(int64_t n, int64_t nnz, const I *__restrict__ rp,
+                                                        const int32_t *__restrict__ ci,
+                                                        const V *__restrict__ val, const V *__restrict__ x,
+                                                        V *__restrict__ y, uint32_t *bad) {
+  for (int64_t j = blockIdx.x * (int64_t)kBlock + threadIdx.x; j < n; j += (int64_t)gridDim.x * kBlock) {
+    int64_t e0, e1;
+    row_range(rp, j, nnz, e0, e1, bad);
+    V acc = V(0);
+    for (int64_t e = e0; e < e1; ++e) {
+      const int32_t i = ci[e];
+      if (!col_ok(i, (int32_t)n, bad)) continue;
+      int64_t lo, hi;
+      row_range(rp, i, nnz, lo, hi, bad);
+      --hi;
+      bool found = false;
+      while (lo <= hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        const int32_t cm = ci[mid];
+        if (cm == (int32_t)j) {
+          acc = fmav<V>(val[mid], x[i], acc);
+          found = true;
+          break;
+        }
+        if (cm < (int32_t)j) lo = mid + 1;
+        else hi = mid - 1;
+      }
+      if (!found && bad) atomicOr(bad, 1u);
+    }
+    y[j] = acc;
+  }
+}
+
 // Structural CSR check; records the smallest offending row.
 template <typename I>
 __global__ void __launch_bounds__(kBlock) validate_kernel(int64_t n, int64_t nnz, const I *__restrict__ rp,
@@ -341,6 +396,74 @@ sla_status sla_grad_values(const sla_csr *A, const void *lambda, const void *x, 
   if (A->nnz > 0 && !grad_values) return SLA_INVALID_ARG;
   SLA_CHECK(check_vec(grad_values, A, true));
   return grad_values_entry(A, 1, lambda, x, grad_values, (cudaStream_t)stream);
+}
+
+sla_status sla_matvec_grad_values(const sla_csr *A, const void *gy, const void *x, void *grad_values,
+                                  void *stream) {
+  SLA_CHECK(check_csr(A, false));
+  SLA_CHECK(check_vec(gy, A, false));
+  SLA_CHECK(check_vec(x, A, false));
+  if (A->nnz > 0 && !grad_values) return SLA_INVALID_ARG;
+  SLA_CHECK(check_vec(grad_values, A, true));
+  if (A->n == 0 || A->nnz == 0) return SLA_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int g = pattern_grid(A->n);
+  if (A->dtype == SLA_F64) {
+    if (A->rowptr_type == SLA_I64)
+      matvec_grad_kernel<double, int64_t><<<g, kPatBlock, 0, st>>>(A->n, A->nnz, (const int64_t *)A->row_ptr,
+                                                                    A->col_idx, (const double *)gy,
+                                                                    (const double *)x, (double *)grad_values);
+    else
+      matvec_grad_kernel<double, int32_t><<<g, kPatBlock, 0, st>>>(A->n, A->nnz, (const int32_t *)A->row_ptr,
+                                                                    A->col_idx, (const double *)gy,
+                                                                    (const double *)x, (double *)grad_values);
+  } else {
+    if (A->rowptr_type == SLA_I64)
+      matvec_grad_kernel<float, int64_t><<<g, kPatBlock, 0, st>>>(A->n, A->nnz, (const int64_t *)A->row_ptr,
+                                                                   A->col_idx, (const float *)gy, (const float *)x,
+                                                                   (float *)grad_values);
+    else
+      matvec_grad_kernel<float, int32_t><<<g, kPatBlock, 0, st>>>(A->n, A->nnz, (const int32_t *)A->row_ptr,
+                                                                   A->col_idx, (const float *)gy, (const float *)x,
+                                                                   (float *)grad_values);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(e);
+  count_launches(1);
+  return SLA_OK;
+}
+
+sla_status sla_spmv_transpose(const sla_csr *A, const void *x, void *y, uint32_t *bad, void *stream) {
+  SLA_CHECK(check_csr(A, true));
+  SLA_CHECK(check_vec(x, A, false));
+  SLA_CHECK(check_vec(y, A, false));
+  if (!aligned(bad, 4)) return SLA_INVALID_ARG;
+  if (A->n == 0) return SLA_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int g = grid_for(A->n, kBlock * 4);
+  if (A->dtype == SLA_F64) {
+    if (A->rowptr_type == SLA_I64)
+      spmv_t_kernel<double, int64_t><<<g, kBlock, 0, st>>>(A->n, A->nnz, (const int64_t *)A->row_ptr, A->col_idx,
+                                                            (const double *)A->values, (const double *)x,
+                                                            (double *)y, bad);
+    else
+      spmv_t_kernel<double, int32_t><<<g, kBlock, 0, st>>>(A->n, A->nnz, (const int32_t *)A->row_ptr, A->col_idx,
+                                                            (const double *)A->values, (const double *)x,
+                                                            (double *)y, bad);
+  } else {
+    if (A->rowptr_type == SLA_I64)
+      spmv_t_kernel<float, int64_t><<<g, kBlock, 0, st>>>(A->n, A->nnz, (const int64_t *)A->row_ptr, A->col_idx,
+                                                           (const float *)A->values, (const float *)x, (float *)y,
+                                                           bad);
+    else
+      spmv_t_kernel<float, int32_t><<<g, kBlock, 0, st>>>(A->n, A->nnz, (const int32_t *)A->row_ptr, A->col_idx,
+                                                           (const float *)A->values, (const float *)x, (float *)y,
+                                                           bad);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(e);
+  count_launches(1);
+  return SLA_OK;
 }
 
 sla_status sla_cg_solve(const sla_csr *A, const void *b, const void *x0, const sla_cg_opts *opts, void *x,

@@ -306,6 +306,18 @@ __global__ void __launch_bounds__(kBlock) dist_pack_kernel(int64_t n, const V *_
   }
 }
 
+// v[idx[t]] += buf[t] (the contributions a neighbour computed for this rank's owned entries; the
+// indices of one call are distinct, so the adds do not race).
+template <typename V>
+__global__ void __launch_bounds__(kBlock) dist_scatter_add_kernel(int64_t n, V *__restrict__ v,
+                                                                  const int64_t *__restrict__ idx, int64_t m,
+                                                                  const V *__restrict__ buf) {
+  for (int64_t t = blockIdx.x * (int64_t)kBlock + threadIdx.x; t < m; t += (int64_t)gridDim.x * kBlock) {
+    const int64_t i = idx[t];
+    if ((uint64_t)i < (uint64_t)n) v[i] += buf[t];
+  }
+}
+
 sla_status launched() {
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(e);
@@ -489,6 +501,22 @@ sla_status sla_dist_pack(int64_t n, int32_t dtype, const void *v, const int64_t 
     dist_pack_kernel<double><<<G, kBlock, 0, (cudaStream_t)stream>>>(n, (const double *)v, idx, m, (double *)buf);
   else
     dist_pack_kernel<float><<<G, kBlock, 0, (cudaStream_t)stream>>>(n, (const float *)v, idx, m, (float *)buf);
+  return launched();
+}
+
+sla_status sla_dist_scatter_add(int64_t n, int32_t dtype, void *v, const int64_t *idx, int64_t m, const void *buf,
+                                void *stream) {
+  if (n < 0 || m < 0 || (dtype != SLA_F32 && dtype != SLA_F64)) return SLA_INVALID_ARG;
+  if (m == 0) return SLA_OK;
+  const size_t vs = dtype == SLA_F64 ? 8 : 4;
+  if (!v || !idx || !buf || !aligned(v, vs) || !aligned(idx, 8) || !aligned(buf, vs)) return SLA_INVALID_ARG;
+  const int G = dist_grid(m);
+  if (dtype == SLA_F64)
+    dist_scatter_add_kernel<double><<<G, kBlock, 0, (cudaStream_t)stream>>>(n, (double *)v, idx, m,
+                                                                            (const double *)buf);
+  else
+    dist_scatter_add_kernel<float><<<G, kBlock, 0, (cudaStream_t)stream>>>(n, (float *)v, idx, m,
+                                                                           (const float *)buf);
   return launched();
 }
 

@@ -35,7 +35,8 @@ from typing import Dict, List, Optional, Tuple
 import numpy as np
 import torch
 
-__all__ = ["partition_rows", "LocalBlock", "local_block", "TorchComm", "LibslaOps", "DistCG"]
+__all__ = ["partition_rows", "LocalBlock", "local_block", "TorchComm", "LibslaOps", "DistCG", "DistMatVec",
+           "dist_matvec"]
 
 
 # --------------------------------------------------------------------------- partitioning (host)
@@ -83,6 +84,11 @@ class LocalBlock:
     halo_global: np.ndarray
     recv: Dict[int, Tuple[int, int]]
     send: Dict[int, np.ndarray] = field(default_factory=dict)
+    # the local block's transpose (square of order n_ext: row j lists the owned rows i with a stored
+    # (i, j)), for the backward of a distributed product; its values are values[t_perm]
+    t_row_ptr: Optional[np.ndarray] = None
+    t_col_idx: Optional[np.ndarray] = None
+    t_perm: Optional[np.ndarray] = None
 
     @property
     def n_own(self) -> int:
@@ -119,8 +125,14 @@ def local_block(row_ptr, col_idx, values, bounds, rank: int) -> LocalBlock:
     for peer in np.unique(owner):
         idx = np.nonzero(owner == peer)[0]
         recv[int(peer)] = (int(idx[0]), int(idx.shape[0]))
+    # transpose of the local block: entries sorted by column, stably (so by row within a column)
+    n_ext = n_own + halo.shape[0]
+    rows = np.repeat(np.arange(n_own, dtype=np.int64), np.diff(rp[lo:hi + 1]))
+    t_perm = np.argsort(loc, kind="stable").astype(np.int64)
+    t_rp = np.concatenate([[0], np.cumsum(np.bincount(loc, minlength=n_ext))]).astype(rp_loc.dtype)
     return LocalBlock(rank, world, lo, hi, bounds, rp_loc, loc.astype(np.int32),
-                      np.ascontiguousarray(np.asarray(values)[e0:e1]), halo, recv)
+                      np.ascontiguousarray(np.asarray(values)[e0:e1]), halo, recv,
+                      t_row_ptr=t_rp, t_col_idx=rows[t_perm].astype(np.int32), t_perm=t_perm)
 
 
 def plan_exchange(block: LocalBlock, comm) -> None:
@@ -245,6 +257,19 @@ class LibslaOps:
                     "sla_dist_cg_info")
         return ci, int(done.value)
 
+    def product(self, A, x, y, stream):
+        from . import _csr_struct
+        self._check(self.lib.sla_spmv(ctypes.byref(_csr_struct(A)), self._p(x), self._p(y), stream), "sla_spmv")
+
+    def scatter_add(self, n, dtype, v, idx, buf, stream):
+        self._check(self.lib.sla_dist_scatter_add(n, dtype, self._p(v), self._p(idx), int(idx.numel()), self._p(buf),
+                                                  stream), "sla_dist_scatter_add")
+
+    def matvec_grad(self, A, gy, x, gv, stream):
+        from . import _csr_struct
+        self._check(self.lib.sla_matvec_grad_values(ctypes.byref(_csr_struct(A)), self._p(gy), self._p(x),
+                                                    self._p(gv), stream), "sla_matvec_grad_values")
+
     def grad_values(self, A, lam_ext, x_ext, gv, stream):
         from . import _csr_struct
         self._check(self.lib.sla_grad_values(ctypes.byref(_csr_struct(A)), self._p(lam_ext), self._p(x_ext),
@@ -274,6 +299,9 @@ class DistCG:
                            torch.from_numpy(np.ascontiguousarray(block.col_idx)).to(dev),
                            torch.from_numpy(np.ascontiguousarray(block.values)).to(dev))
         self.vdtype = self.A.values.dtype
+        self.t_row_ptr = torch.from_numpy(np.ascontiguousarray(block.t_row_ptr)).to(dev)
+        self.t_col_idx = torch.from_numpy(np.ascontiguousarray(block.t_col_idx)).to(dev)
+        self.t_perm = torch.from_numpy(np.ascontiguousarray(block.t_perm)).to(dev)
         self.send_idx = {p: torch.from_numpy(idx).to(dev) for p, idx in block.send.items()}
         self.send_buf = {p: torch.empty(idx.shape[0], dtype=self.vdtype, device=dev)
                          for p, idx in block.send.items()}
@@ -340,6 +368,52 @@ class DistCG:
             hist = hist[: info.iters + 1]
         return x, info, hist
 
+    # ------------------------------------------------------------------ distributed product
+
+    def matvec(self, x_own: torch.Tensor, values: Optional[torch.Tensor] = None):
+        """y = A x for this rank's rows: the halo of x is exchanged first (forward halo exchange).
+        Returns (y_own, x_ext); values (optional) replaces the local block's values."""
+        from . import CSRMatrix
+        blk = self.block
+        A = self.A if values is None else CSRMatrix(self.A.row_ptr, self.A.col_idx, values)
+        xe = torch.zeros(blk.n_ext, dtype=self.vdtype, device=self.device)
+        xe[: blk.n_own] = x_own.to(device=self.device, dtype=self.vdtype)
+        self.exchange(xe)
+        y = torch.empty(blk.n_ext, dtype=self.vdtype, device=self.device)
+        self.ops.product(A, xe, y, self._stream())
+        return y[: blk.n_own], xe
+
+    def matvec_backward(self, gy_own: torch.Tensor, x_ext: torch.Tensor, values: Optional[torch.Tensor] = None):
+        """Backward of y = A x for this rank's rows (Methodology 3's transposed halo exchange).
+
+        The rank forms A_loc^T gy over every column its rows touch; the halo part belongs to the
+        neighbours and is sent to them, and the contributions they computed for this rank's owned
+        entries are received and added in (rank order).  Returns (grad_x_own, grad_values_local)
+        with grad_values[e] = gy_i x_j on the rank's entries."""
+        from . import CSRMatrix
+        blk, ops, st, code = self.block, self.ops, self._stream(), self._dtype_code()
+        vals = self.A.values if values is None else values
+        A = CSRMatrix(self.A.row_ptr, self.A.col_idx, vals)
+        gye = torch.zeros(blk.n_ext, dtype=self.vdtype, device=self.device)
+        gye[: blk.n_own] = gy_own.to(device=self.device, dtype=self.vdtype)
+        vt = torch.empty(blk.nnz, dtype=self.vdtype, device=self.device)
+        if blk.nnz:
+            ops.pack(blk.nnz, code, vals, self.t_perm, vt, st)  # values in the transpose's order
+        At = CSRMatrix(self.t_row_ptr, self.t_col_idx, vt)
+        gxe = torch.empty(blk.n_ext, dtype=self.vdtype, device=self.device)
+        ops.product(At, gye, gxe, st)
+        sends = {p: gxe[blk.n_own + s:blk.n_own + s + c] for p, (s, c) in blk.recv.items()}
+        recvs = {p: torch.empty(idx.numel(), dtype=self.vdtype, device=self.device)
+                 for p, idx in self.send_idx.items()}
+        self.comm.exchange(sends, recvs)
+        gx = gxe[: blk.n_own]
+        for p in sorted(recvs):
+            ops.scatter_add(blk.n_own, code, gx, self.send_idx[p], recvs[p], st)
+        gv = torch.empty(blk.nnz, dtype=self.vdtype, device=self.device)
+        if blk.nnz:
+            ops.matvec_grad(A, gye, x_ext, gv, st)
+        return gx, gv
+
     def adjoint(self, x: torch.Tensor, g_own: torch.Tensor, rtol: float = 1e-8, maxit: int = 10000,
                 precond: int = 0, unroll: int = 8):
         """Adjoint of x = A^{-1} b (Methodology 2) for this rank's rows.
@@ -356,3 +430,26 @@ class DistCG:
         if self.block.nnz:
             self.ops.grad_values(self.A, lam, xe, gv, self._stream())
         return lam[: self.block.n_own], gv, info
+
+
+class DistMatVec(torch.autograd.Function):
+    """Differentiable distributed y = A x for one rank's rows (forward halo exchange; transposed
+    halo exchange in backward).  Gradients flow to the rank's stored values and owned x."""
+
+    @staticmethod
+    def forward(ctx, values, x_own, solver):
+        y, xe = solver.matvec(x_own, values)
+        ctx.solver = solver
+        ctx.save_for_backward(values, xe)
+        return y.clone()
+
+    @staticmethod
+    def backward(ctx, gy):
+        values, xe = ctx.saved_tensors
+        gx, gv = ctx.solver.matvec_backward(gy.contiguous(), xe, values)
+        return gv, gx, None
+
+
+def dist_matvec(solver: DistCG, values: torch.Tensor, x_own: torch.Tensor) -> torch.Tensor:
+    """y_own = (A x)_own, differentiable with respect to the rank's values and owned x."""
+    return DistMatVec.apply(values, x_own, solver)

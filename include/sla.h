@@ -171,6 +171,25 @@ SLA_API sla_status sla_validate_csr(const sla_csr *A, int32_t check_symmetric, i
 SLA_API sla_status sla_spmv(const sla_csr *A, const void *x, void *y, void *stream);
 
 /*
+ * y = A^T x (TS Methodology 1: the backward of an autograd-aware ".matvec" with respect to x).
+ * The pattern must be structurally symmetric (every stored (i, j) has a stored (j, i)); values
+ * need not be.  Row j of y adds a_ij x_i over the columns i of row j in their order, each a_ij
+ * found by a binary search in row i; deterministic.  bad: device uint32 or NULL; a missing partner
+ * entry (a pattern that is not structurally symmetric) or an out-of-range index is skipped and
+ * sets *bad to 1 (never cleared by the call).  x, y: device, n entries, not overlapping.
+ * Asynchronous.
+ */
+SLA_API sla_status sla_spmv_transpose(const sla_csr *A, const void *x, void *y, uint32_t *bad, void *stream);
+
+/*
+ * grad_values[k] = gy[row(k)] * x[col_idx[k]] for every stored entry (TS Methodology 1-2: the
+ * gradient of L(A x) with respect to the stored values, for gy = dL/dy, on the pattern only).
+ * gy, x: device, n entries; grad_values: device, nnz entries.  Asynchronous.
+ */
+SLA_API sla_status sla_matvec_grad_values(const sla_csr *A, const void *gy, const void *x, void *grad_values,
+                                          void *stream);
+
+/*
  * Solve A x = b by conjugate gradient (TS Methodology 1: the GPU iterative backend; Jacobi
  * preconditioning per TS Significance when opts->precond = SLA_PRECOND_JACOBI).
  *   b        device, n entries.
@@ -361,6 +380,12 @@ SLA_API sla_status sla_dist_cg_direction(int64_t n_own, int32_t dtype, const dou
  * outside [0, n) give 0).  Asynchronous. */
 SLA_API sla_status sla_dist_pack(int64_t n, int32_t dtype, const void *v, const int64_t *idx, int64_t m, void *buf,
                                  void *stream);
+
+/* v[idx[t]] += buf[t] for t < m (TS Methodology 3: the transposed halo exchange of a backward
+ * pass, where the values a neighbour computed for this rank's owned entries are added in; idx:
+ * device int64, distinct within a call, entries outside [0, n) skipped).  Asynchronous. */
+SLA_API sla_status sla_dist_scatter_add(int64_t n, int32_t dtype, void *v, const int64_t *idx, int64_t m,
+                                        const void *buf, void *stream);
 
 /* Reads the state (synchronises the stream): iterations, ||r|| / ||b||, status into info (host,
  * may be NULL) and the done flag into *done (host, may be NULL). */

@@ -75,6 +75,10 @@ def _bind(lib):
     lib.orc_cg_adjoint.restype = ctypes.c_int
     lib.orc_eig_grad_values.argtypes = [i64, p, p, i64, p, p, p]
     lib.orc_eig_grad_values.restype = None
+    lib.orc_spmv_transpose.argtypes = [i64, p, p, p, p, p]
+    lib.orc_spmv_transpose.restype = None
+    lib.orc_matvec_grad_values.argtypes = [i64, p, p, p, p, p]
+    lib.orc_matvec_grad_values.restype = None
     lib.orc_threads.argtypes = [ctypes.c_int]
     lib.orc_threads.restype = ctypes.c_int
     return lib
@@ -129,6 +133,30 @@ def spmv(row_ptr, col_idx, values, x, lib=None) -> np.ndarray:
     y = np.empty(n, dtype=np.float64)
     lib.orc_spmv(n, _ptr(rp), _ptr(ci), _ptr(v), _ptr(x), _ptr(y))
     return y
+
+
+def spmv_transpose(row_ptr, col_idx, values, x, lib=None) -> np.ndarray:
+    """y = A^T x (square A)."""
+    lib = lib or load()
+    rp, ci, v = _csr(row_ptr, col_idx, values)
+    n = rp.shape[0] - 1
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty(n, dtype=np.float64)
+    lib.orc_spmv_transpose(n, _ptr(rp), _ptr(ci), _ptr(v), _ptr(x), _ptr(y))
+    return y
+
+
+def matvec_grad_values(row_ptr, col_idx, gy, x, lib=None) -> np.ndarray:
+    """grad_values[k] = gy[row(k)] * x[col(k)]: the gradient of L(A x) with respect to the stored values."""
+    lib = lib or load()
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int64)
+    ci = np.ascontiguousarray(col_idx, dtype=np.int32)
+    n = rp.shape[0] - 1
+    gy = np.ascontiguousarray(gy, dtype=np.float64)
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    gv = np.empty(ci.shape[0], dtype=np.float64)
+    lib.orc_matvec_grad_values(n, _ptr(rp), _ptr(ci), _ptr(gy), _ptr(x), _ptr(gv))
+    return gv
 
 
 def dot(a, b, lib=None) -> float:

@@ -89,6 +89,24 @@ void orc_spmv(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const d
   }
 }
 
+/* y = A^T x: y_j = sum over stored entries (i, j) of a_ij x_i, the entries taken row by row in
+ * storage order (so each y_j adds its terms in increasing i).  n rows and n columns. */
+void orc_spmv_transpose(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const double *values,
+                        const double *x, double *y) {
+  for (int64_t j = 0; j < n; ++j) y[j] = 0.0;
+  for (int64_t i = 0; i < n; ++i)
+    for (int64_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k) y[col_idx[k]] = y[col_idx[k]] + values[k] * x[i];
+}
+
+/* Gradient of L(y) with y = A x with respect to the stored values, for gy = dL/dy:
+ * grad_values[k] = gy[row(k)] * x[col(k)] for every stored entry, in CSR order. */
+void orc_matvec_grad_values(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const double *gy,
+                            const double *x, double *grad_values) {
+  ORC_PARALLEL_FOR
+  for (int64_t i = 0; i < n; ++i)
+    for (int64_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k) grad_values[k] = gy[i] * x[col_idx[k]];
+}
+
 #ifndef _OPENMP
 /* a . b, summed in index order. */
 double orc_dot(int64_t n, const double *a, const double *b) {

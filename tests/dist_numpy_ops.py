@@ -157,6 +157,21 @@ class NumpyOps:
     def info(self, S, stream):
         return SimpleNamespace(iters=S["k"], rel_res=S["rel_res"], status=S["status"]), S["done"]
 
+    def product(self, A, x, y, stream):
+        n = A.row_ptr.shape[0] - 1
+        _a(y)[:] = _local_spmv(A, n, _a(x))
+
+    def scatter_add(self, n, dtype, v, idx, buf, stream):
+        va, ia, ba = _a(v), _a(idx), _a(buf)
+        for t in range(ia.shape[0]):
+            if 0 <= ia[t] < n:
+                va[ia[t]] += ba[t]
+
+    def matvec_grad(self, A, gy, x, gv, stream):
+        rp, ci = A.row_ptr.numpy().astype(np.int64), A.col_idx.numpy()
+        rows = np.repeat(np.arange(A.row_ptr.shape[0] - 1), np.diff(rp))
+        _a(gv)[:] = _a(gy)[rows] * _a(x)[ci]
+
     def grad_values(self, A, lam_ext, x_ext, gv, stream):
         rp, ci = A.row_ptr.numpy().astype(np.int64), A.col_idx.numpy()
         rows = np.repeat(np.arange(A.row_ptr.shape[0] - 1), np.diff(rp))

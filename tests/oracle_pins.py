@@ -119,6 +119,73 @@ def pin_cg_several_chunks_true_residual(lib):
         assert np.linalg.norm(r["x"] - xd) <= 1e-10 * 1e4 * np.linalg.norm(xd)
 
 
+def _random_csr(n, per_row, seed):
+    """A structurally non-symmetric random CSR matrix (sorted, unique columns per row)."""
+    rng = np.random.default_rng(seed)
+    rows, cols = [], []
+    for i in range(n):
+        k = int(rng.integers(0, per_row + 1)) if n else 0
+        c = np.sort(rng.choice(n, min(k, n), replace=False))
+        rows.append(np.full(c.shape[0], i))
+        cols.append(c)
+    cols = np.concatenate(cols).astype(np.int32) if n else np.zeros(0, np.int32)
+    lens = np.array([c.shape[0] for c in rows]) if n else np.zeros(0, np.int64)
+    rp = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    vals = rng.standard_normal(cols.shape[0])
+    return rp, cols, vals
+
+
+def _dense(rp, ci, v, n):
+    D = np.zeros((n, n))
+    for i in range(n):
+        for e in range(rp[i], rp[i + 1]):
+            D[i, ci[e]] += v[e]
+    return D
+
+
+def pin_spmv_transpose_dense(lib):
+    for n, per_row, seed in [(1, 1, 0), (7, 3, 1), (40, 6, 2), (300, 9, 3)]:
+        rp, ci, v = _random_csr(n, per_row, seed)
+        D = _dense(rp, ci, v, n)
+        assert not np.array_equal(D, D.T) or n == 1  # a genuinely non-symmetric case
+        x = np.random.default_rng(seed + 50).standard_normal(n)
+        y = oracle.spmv_transpose(rp, ci, v, x, lib=lib)
+        bound = 4 * max(per_row, 1) * EPS * (np.abs(D.T) @ np.abs(x)) + 1e-300
+        assert np.all(np.abs(y - D.T @ x) <= bound * n), n
+    # small integers: exact
+    rp, ci, v = _random_csr(60, 5, 9)
+    v = np.round(v * 10)
+    x = np.random.default_rng(8).integers(-9, 10, 60).astype(np.float64)
+    assert np.array_equal(oracle.spmv_transpose(rp, ci, v, x, lib=lib), _dense(rp, ci, v, 60).T @ x)
+    # the adjoint identity <g, A x> = <A^T g, x>
+    rp, ci, v = _random_csr(200, 7, 4)
+    g, x = np.random.default_rng(5).standard_normal(200), np.random.default_rng(6).standard_normal(200)
+    lhs = float(g @ oracle.spmv(rp, ci, v, x, lib=lib))
+    rhs = float(oracle.spmv_transpose(rp, ci, v, g, lib=lib) @ x)
+    assert abs(lhs - rhs) <= 1e-12 * (np.abs(g) @ np.abs(_dense(rp, ci, v, 200)) @ np.abs(x))
+
+
+def pin_matvec_grad_values(lib):
+    # L = <g, A x> is linear in each stored value: dL/dv_k = g_row x_col exactly, and
+    # sum_k gv_k v_k = <g, A x>; a central difference reproduces an entry to rounding
+    n = 50
+    rp, ci, v = _random_csr(n, 6, 11)
+    rng = np.random.default_rng(12)
+    g, x = rng.standard_normal(n), rng.standard_normal(n)
+    gv = oracle.matvec_grad_values(rp, ci, g, x, lib=lib)
+    rows = np.repeat(np.arange(n), np.diff(rp))
+    assert np.array_equal(gv, g[rows] * x[ci])
+    L = float(g @ (_dense(rp, ci, v, n) @ x))
+    assert abs(float(gv @ v) - L) <= 1e-12 * (np.abs(g) @ np.abs(_dense(rp, ci, v, n)) @ np.abs(x))
+    for k in (0, int(ci.shape[0]) // 2, int(ci.shape[0]) - 1):
+        h = 1e-3
+        vp, vm = v.copy(), v.copy()
+        vp[k] += h
+        vm[k] -= h
+        fd = (float(g @ (_dense(rp, ci, vp, n) @ x)) - float(g @ (_dense(rp, ci, vm, n) @ x))) / (2 * h)
+        assert abs(fd - gv[k]) <= 1e-9 * max(1.0, abs(gv[k]))
+
+
 # --------------------------------------------------------------------------- forward CG
 
 def pin_cg_vs_dense(lib):
@@ -465,7 +532,7 @@ def pin_eig_grad_rayleigh_identity(lib):
 
 
 ALL_PINS = [
-    pin_spmv_dense, pin_spmv_exact_integers, pin_dot,
+    pin_spmv_dense, pin_spmv_exact_integers, pin_dot, pin_spmv_transpose_dense, pin_matvec_grad_values,
     pin_cg_vs_dense, pin_cg_several_chunks_true_residual, pin_cg_exact_rational, pin_finite_termination, pin_eigen_closed_form_and_bound,
     pin_history_matches_true_residual, pin_x0_restart, pin_jacobi_constant_diagonal, pin_jacobi_equals_scaled_cg,
     pin_status_codes,

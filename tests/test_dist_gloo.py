@@ -152,3 +152,57 @@ def test_distributed_cg_and_adjoint_match_the_oracle(name, world, tmp_path):
     assert _rel(res["gb"], adj["grad_b"]) <= 1e-7
     assert res["gv"].shape == (A.nnz,)  # the ranks' entries, in global CSR order
     assert _rel(res["gv"], adj["grad_values"]) <= 1e-7
+
+
+# --------------------------------------------------------------------------- distributed product
+
+def _nonsym_csr(n, per_row, seed):
+    """A structurally non-symmetric random CSR matrix with a stored diagonal."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for i in range(n):
+        c = set(rng.choice(n, int(rng.integers(0, per_row + 1)), replace=False).tolist()) | {i}
+        rows.append(np.array(sorted(c), dtype=np.int32))
+    rp = np.concatenate([[0], np.cumsum([r.shape[0] for r in rows])]).astype(np.int32)
+    return rp, np.concatenate(rows), rng.standard_normal(int(rp[-1]))
+
+
+def _matvec_rank(rank, world, port, out_dir):
+    sys.path[:0] = [ROOT, TESTS]
+    import torch.distributed as dist
+    from dist_numpy_ops import NumpyOps
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        rp, ci, v = _nonsym_csr(400, 6, 21)
+        rng = np.random.default_rng(22)
+        x, gy = rng.standard_normal(400), rng.standard_normal(400)
+        bounds = D.partition_rows(rp, world, 1)
+        blk = D.local_block(rp, ci, v, bounds, rank)
+        solver = D.DistCG(blk, D.TorchComm(), device="cpu", ops=NumpyOps())
+        vals = torch.from_numpy(blk.values.copy()).requires_grad_(True)
+        xo = torch.from_numpy(x[blk.lo:blk.hi].copy()).requires_grad_(True)
+        y = D.dist_matvec(solver, vals, xo)
+        y.backward(torch.from_numpy(gy[blk.lo:blk.hi].copy()))
+        mine = (y.detach().numpy().copy(), xo.grad.numpy().copy(), vals.grad.numpy().copy())
+        everyone = solver.comm.all_gather_object(mine)
+        if rank == 0:
+            np.savez(os.path.join(out_dir, f"mv_{world}.npz"), y=np.concatenate([e[0] for e in everyone]),
+                     gx=np.concatenate([e[1] for e in everyone]), gv=np.concatenate([e[2] for e in everyone]))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_distributed_matvec_and_transposed_exchange(world, tmp_path):
+    # a structurally non-symmetric matrix: grad_x = A^T gy needs the contributions other ranks
+    # computed for this rank's entries (the transposed halo exchange)
+    import torch.multiprocessing as mp
+    mp.spawn(_matvec_rank, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    res = np.load(tmp_path / f"mv_{world}.npz")
+    rp, ci, v = _nonsym_csr(400, 6, 21)
+    rng = np.random.default_rng(22)
+    x, gy = rng.standard_normal(400), rng.standard_normal(400)
+    assert _rel(res["y"], oracle.spmv(rp, ci, v, x)) <= 1e-14
+    assert _rel(res["gx"], oracle.spmv_transpose(rp, ci, v, gy)) <= 1e-14
+    assert np.array_equal(res["gv"], oracle.matvec_grad_values(rp, ci, gy, x))

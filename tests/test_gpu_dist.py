@@ -91,3 +91,46 @@ def test_distributed_cg_and_adjoint_on_gpu(world, name, tmp_path):
     assert rel(res["gb"], adj["grad_b"]) <= 1e-7
     assert res["gv"].shape == (A.nnz,)
     assert rel(res["gv"], adj["grad_values"]) <= 1e-7
+
+
+def _matvec_rank(rank, world, port, out_dir):
+    sys.path[:0] = [ROOT, TESTS]
+    import torch.distributed as dist
+    from differentiable_sparse_iterative_gb300 import distributed as D
+    from test_dist_gloo import _nonsym_csr
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    torch.cuda.set_device(0)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        rp, ci, v = _nonsym_csr(3000, 6, 31)
+        rng = np.random.default_rng(32)
+        x, gy = rng.standard_normal(3000), rng.standard_normal(3000)
+        bounds = D.partition_rows(rp, world, 1)
+        blk = D.local_block(rp, ci, v, bounds, rank)
+        solver = D.DistCG(blk, D.TorchComm(), device="cuda:0")
+        vals = torch.from_numpy(blk.values.copy()).cuda().requires_grad_(True)
+        xo = torch.from_numpy(x[blk.lo:blk.hi].copy()).cuda().requires_grad_(True)
+        y = D.dist_matvec(solver, vals, xo)
+        y.backward(torch.from_numpy(gy[blk.lo:blk.hi].copy()).cuda())
+        torch.cuda.synchronize()
+        mine = (y.detach().cpu().numpy(), xo.grad.cpu().numpy(), vals.grad.cpu().numpy())
+        everyone = solver.comm.all_gather_object(mine)
+        if rank == 0:
+            np.savez(os.path.join(out_dir, "mv.npz"), y=np.concatenate([e[0] for e in everyone]),
+                     gx=np.concatenate([e[1] for e in everyone]), gv=np.concatenate([e[2] for e in everyone]))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [1, 2, 3])
+def test_distributed_matvec_transposed_exchange_on_gpu(world, tmp_path):
+    import torch.multiprocessing as mp
+    mp.spawn(_matvec_rank, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    res = np.load(tmp_path / "mv.npz")
+    from test_dist_gloo import _nonsym_csr
+    rp, ci, v = _nonsym_csr(3000, 6, 31)
+    rng = np.random.default_rng(32)
+    x, gy = rng.standard_normal(3000), rng.standard_normal(3000)
+    assert rel(res["y"], oracle.spmv(rp, ci, v, x)) <= 1e-14
+    assert rel(res["gx"], oracle.spmv_transpose(rp, ci, v, gy)) <= 1e-14
+    assert np.array_equal(res["gv"], oracle.matvec_grad_values(rp, ci, gy, x))

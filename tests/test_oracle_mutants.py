@@ -37,6 +37,12 @@ MUTANTS = [
     ("adjoint_wrong_rhs", "orc_cg(n, row_ptr, col_idx, values, g, NULL,", "orc_cg(n, row_ptr, col_idx, values, x, NULL,"),
     ("x0_residual_sign", "r[i] = b[i] - q[i];", "r[i] = b[i] + q[i];"),
     ("breakdown_test_dropped", "if (!(pq > 0.0)) { status = ORC_BREAKDOWN; goto done; }", ""),
+    ("spmv_transpose_row_for_column", "y[col_idx[k]] = y[col_idx[k]] + values[k] * x[i];",
+     "y[col_idx[k]] = y[col_idx[k]] + values[k] * x[col_idx[k]];"),
+    ("spmv_transpose_not_transposed", "y[col_idx[k]] = y[col_idx[k]] + values[k] * x[i];",
+     "y[i] = y[i] + values[k] * x[col_idx[k]];"),
+    ("matvec_grad_transposed", "grad_values[k] = gy[i] * x[col_idx[k]];", "grad_values[k] = gy[col_idx[k]] * x[i];"),
+    ("matvec_grad_sign", "grad_values[k] = gy[i] * x[col_idx[k]];", "grad_values[k] = -(gy[i] * x[col_idx[k]]);"),
     ("eig_grad_sign", "acc = acc + ws * (V[s * n + i] * V[s * n + j]);",
      "acc = acc - ws * (V[s * n + i] * V[s * n + j]);"),
     ("eig_grad_drops_weight", "const double ws = w ? w[s] : 1.0;", "const double ws = 1.0;"),
