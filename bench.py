@@ -281,6 +281,8 @@ def run_ours(args, rank, world, local_rank):
     fp64_peak = fp64_peak_tflops(clocks)
     fp64_ach = flops_it * sum(iters_f) / fwd_s / 1e12
 
+    grad_k = grad_kernel_timing(A, gb, x, gv, flush, stream, sla, torch, peak, Bg)
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, w, dev, precond, sla, torch)
@@ -312,6 +314,7 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": (tr["dram_bytes_per_iter"] if tr else None),
                      "traffic_unit": "DRAM bytes per CG iteration (ncu dram__bytes_read + write)",
                      "traffic_source": (tr.get("source") if tr else None)},
+        "grad_values_roofline": grad_k,
         "gpu_launches": int(launches),
         "wall_s": wall,
         "clocks": clocks,
@@ -321,6 +324,68 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(w, args.cpu_iters)
     return out
+
+
+def grad_kernel_timing(A, lam, x, gv, flush, stream, sla, torch, peak, Bg, reps=20):
+    """grad_values_kernel alone, each launch after an L2 flush (a 256 MB write): per-launch CUDA
+    events (the flush keeps the GPU busy while the launch is enqueued), and the difference between
+    reps x (flush + kernel) and reps x flush.  Beside it, for scale, PyTorch's index_select over the
+    same col_idx (x gathered per entry, one value written per entry: the kernel's access pattern
+    without the row factor) timed the same way: what a plain library gather reaches at this size."""
+    ci = A.col_idx
+    try:
+        torch.index_select(x, 0, ci[:1])
+    except (RuntimeError, TypeError):  # a PyTorch without 32-bit indices: 64-bit ones, counted as such
+        ci = ci.long()
+    sel = torch.empty(A.nnz, dtype=x.dtype, device=x.device)
+
+    def timed(fn):
+        per = []
+        for _ in range(reps):
+            flush_l2(flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            per.append((a, b))
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        for _ in range(reps):
+            flush_l2(flush)
+            fn()
+        e[1].record(stream)
+        for _ in range(reps):
+            flush_l2(flush)
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        ev_ms = statistics.mean(a.elapsed_time(b) for a, b in per)
+        diff_ms = (e[0].elapsed_time(e[1]) - e[1].elapsed_time(e[2])) / reps
+        return ev_ms, diff_ms
+
+    import ctypes
+    cs = sla._csr_struct(A)  # arguments marshalled once: each launch is one C call
+    lib, sh = sla.lib(), stream.cuda_stream
+    lp, xp, gp = lam.data_ptr(), x.data_ptr(), gv.data_ptr()
+
+    def kernel():
+        assert lib.sla_grad_values(ctypes.byref(cs), lp, xp, gp, sh) == 0
+
+    for _ in range(3):  # warm-up
+        kernel()
+        torch.index_select(x, 0, ci, out=sel)
+    k_ev, k_diff = timed(kernel)
+    g_ev, g_diff = timed(lambda: torch.index_select(x, 0, ci, out=sel))
+    Bsel = A.nnz * (ci.element_size() + x.element_size()) + A.n * x.element_size()  # col_idx, values written, x
+    return {"kernel": "grad_values_kernel", "bound": "hbm", "unit": "GB/s", "peak": peak,
+            "bytes_per_launch": Bg,
+            "achieved": Bg / (k_ev / 1e3) / 1e9, "frac": Bg / (k_ev / 1e3) / 1e9 / peak, "us_events": k_ev * 1e3,
+            "achieved_flush_subtracted": Bg / (k_diff / 1e3) / 1e9,
+            "frac_flush_subtracted": Bg / (k_diff / 1e3) / 1e9 / peak, "us_flush_subtracted": k_diff * 1e3,
+            "gather_floor": {"op": "torch.index_select(x, 0, col_idx)", "bytes_per_launch": Bsel,
+                             "us_events": g_ev * 1e3, "frac": Bsel / (g_ev / 1e3) / 1e9 / peak,
+                             "us_flush_subtracted": g_diff * 1e3,
+                             "frac_flush_subtracted": Bsel / (g_diff / 1e3) / 1e9 / peak},
+            "timing": f"{reps} launches, each after a 256 MB L2 flush, CUDA events"}
 
 
 def run_dist(args, rank, world, local_rank):
