@@ -20,7 +20,7 @@ from __future__ import annotations
 import ctypes
 import warnings
 from dataclasses import dataclass
-from typing import Optional
+from typing import Optional, Tuple
 
 import torch
 
@@ -37,7 +37,7 @@ __all__ = [
     "SLA_LOOP_RESIDENT", "SLA_LOOP_CLUSTER", "SLA_OK", "SLA_NOT_CONVERGED", "SLA_BREAKDOWN", "SLA_INVALID_ARG",
     "SLA_BAD_CSR", "SLA_NONFINITE", "SLA_WORKSPACE_TOO_SMALL", "SLA_TIMEOUT", "SLA_CUDA_ERROR",
     "EigInfo", "sla_eig_workspace_bytes", "sla_eig_smallest", "sla_eig_grad_values", "EigSmallest",
-    "eigsh_smallest", "sla_spmv_transpose", "sla_matvec_grad_values", "MatVec", "sla_set_spmv_variant", "sla_test_set_barrier_wait", "SLA_SPMV_PLAIN", "SLA_SPMV_TMA",
+    "eigsh_smallest", "sla_spmv_transpose", "sla_matvec_grad_values", "MatVec", "sla_set_spmv_variant", "sla_graph_cache_stats", "sla_test_set_barrier_wait", "SLA_SPMV_PLAIN", "SLA_SPMV_TMA",
 ]
 from ._abi import SLA_SPMV_PLAIN, SLA_SPMV_TMA  # noqa: E402
 
@@ -165,6 +165,13 @@ def sla_version() -> int:
 def sla_set_spmv_variant(variant: int) -> None:
     """Process-wide SpMV step of the GRAPH and HOST loops: SLA_SPMV_PLAIN (default) or SLA_SPMV_TMA."""
     _check(lib().sla_set_spmv_variant(int(variant)), "sla_set_spmv_variant")
+
+
+def sla_graph_cache_stats() -> Tuple[int, int, int]:
+    """(cached graph loops, graphs instantiated, in-place argument replacements) of this process."""
+    e, b, u = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().sla_graph_cache_stats(ctypes.byref(e), ctypes.byref(b), ctypes.byref(u)), "sla_graph_cache_stats")
+    return int(e.value), int(b.value), int(u.value)
 
 
 def sla_test_set_barrier_wait(extra: int, spin_limit: int) -> None:

@@ -22,6 +22,7 @@ EXPORTS = [
     "sla_eig_grad_values", "sla_set_spmv_variant", "sla_test_set_barrier_wait", "sla_dist_state_bytes",
     "sla_dist_cg_begin", "sla_dist_cg_start", "sla_dist_cg_spmv", "sla_dist_cg_update", "sla_dist_cg_direction",
     "sla_dist_pack", "sla_dist_cg_info", "sla_spmv_transpose", "sla_matvec_grad_values", "sla_dist_scatter_add",
+    "sla_graph_cache_stats",
 ]
 SLA_SPMV_PLAIN, SLA_SPMV_TMA = 0, 1
 
@@ -90,10 +91,11 @@ def bind(lib):
     lib.sla_dist_pack.argtypes = [i64, i32, P, P, i64, P, P]
     lib.sla_dist_cg_info.argtypes = [P, I, ctypes.POINTER(i32), P]
     lib.sla_set_spmv_variant.argtypes = [i32]
+    lib.sla_graph_cache_stats.argtypes = [ctypes.POINTER(i64)] * 3
     lib.sla_test_set_barrier_wait.argtypes = [ctypes.c_uint32, i64]
     for name in ["sla_spmv_transpose", "sla_matvec_grad_values", "sla_dist_scatter_add", "sla_dist_cg_begin", "sla_dist_cg_start", "sla_dist_cg_spmv", "sla_dist_cg_update",
                  "sla_dist_cg_direction", "sla_dist_pack", "sla_dist_cg_info",
-                 "sla_set_spmv_variant", "sla_test_set_barrier_wait", "sla_validate_csr", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
+                 "sla_set_spmv_variant", "sla_graph_cache_stats", "sla_test_set_barrier_wait", "sla_validate_csr", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
                  "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_cg_solve_static", "sla_eig_smallest",
                  "sla_eig_grad_values"]:
         getattr(lib, name).restype = i32

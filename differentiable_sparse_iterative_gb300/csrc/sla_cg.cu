@@ -687,16 +687,24 @@ namespace {
 constexpr int kRPT = SLA_SPMV_RPT;
 constexpr int kDefaultUnroll = 8;
 
+// A cached graph loop.  Its key is the graph's shape (types, launch shape, unroll, device); the
+// buffers and scalars of a call are kernel arguments, so a call of the same shape with other
+// buffers reuses the instantiated graph after its nodes' arguments are replaced (`nodes` in the
+// order of graph_node_params; `args` the problem they were last set for).
 struct GraphEntry {
   std::vector<char> key;
+  std::vector<char> args;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
+  cudaGraphConditionalHandle handle = 0;
+  std::vector<cudaGraphNode_t> nodes;
   uint64_t stamp = 0;
 };
 
 std::mutex g_mu;
 std::vector<GraphEntry> g_cache;
 uint64_t g_stamp = 0;
+uint64_t g_builds = 0, g_updates = 0;  // graphs instantiated; cached graphs pointed at a new problem
 constexpr size_t kCacheCap = 32;
 
 template <typename V, typename I, bool JAC>
@@ -709,19 +717,6 @@ struct Kernels {
   static void *finish() { return (void *)cg_finish<V, I>; }
 };
 
-cudaError_t add_kernel(cudaGraphNode_t *node, cudaGraph_t g, const cudaGraphNode_t *dep, size_t ndep, void *fn,
-                       dim3 grid, dim3 block, void **args, unsigned smem = 0) {
-  cudaKernelNodeParams kp;
-  memset(&kp, 0, sizeof(kp));
-  kp.func = fn;
-  kp.gridDim = grid;
-  kp.blockDim = block;
-  kp.sharedMemBytes = smem;
-  kp.kernelParams = args;
-  kp.extra = nullptr;
-  return cudaGraphAddKernelNode(node, g, dep, ndep, &kp);
-}
-
 // Launch shape of the streaming path: blocks per system for the SpMV step and for the other
 // kernels, and whether the SpMV step is the TMA-staged one (with its dynamic shared memory).
 struct Launch {
@@ -731,61 +726,138 @@ struct Launch {
   unsigned tma_smem = 0;
 };
 
+// Arguments of the graph loop's kernel nodes for one problem (the arrays point into this object,
+// which therefore stays where it was built).  Nodes, in order: init, setup, then per unrolled
+// iteration u the SpMV step and the update step (parity u & 1), the loop control, finish.
+template <typename V, typename I>
+struct GraphArgs {
+  Prob<V, I> P, Ps;
+  int par[2] = {0, 1};
+  Glob *gp;
+  cudaGraphConditionalHandle h;
+  uint32_t max_bodies;
+  void *args_p[1];
+  void *args_pp[2][2];
+  void *args_ps[2][2];
+  void *args_c[3];
+  GraphArgs(const Prob<V, I> &P0, const Launch &Lc, int unroll, cudaGraphConditionalHandle h_) : P(P0), Ps(P0) {
+    P.G = Lc.G_main;
+    Ps.G = Lc.G_spmv;
+    gp = P.glob;
+    h = h_;
+    max_bodies = (uint32_t)std::min<int64_t>((P.maxit + unroll - 1) / unroll + 2, 0x7fffffff);
+    args_p[0] = &P;
+    for (int q = 0; q < 2; ++q) {
+      args_pp[q][0] = &P;
+      args_pp[q][1] = &par[q];
+      args_ps[q][0] = &Ps;
+      args_ps[q][1] = &par[q];
+    }
+    args_c[0] = &gp;
+    args_c[1] = &h;
+    args_c[2] = &max_bodies;
+  }
+  GraphArgs(const GraphArgs &) = delete;
+  GraphArgs &operator=(const GraphArgs &) = delete;
+};
+
 template <typename V, typename I, bool JAC>
-cudaError_t build_graph(const Prob<V, I> &P0, const Launch &Lc, int unroll, cudaGraph_t *out_graph,
-                        cudaGraphExec_t *out_exec) {
+cudaKernelNodeParams graph_node_params(GraphArgs<V, I> &A, const Launch &Lc, int unroll, int idx) {
   using K = Kernels<V, I, JAC>;
-  Prob<V, I> P = P0;
-  Prob<V, I> Ps = P0;
-  P.G = Lc.G_main;
-  Ps.G = Lc.G_spmv;
-  const dim3 grid_s(Ps.G, P.batch);
-  void *fn_s = Lc.tma ? K::spmv_step_tma() : K::spmv_step();
-  const unsigned smem_s = Lc.tma ? Lc.tma_smem : 0u;
+  cudaKernelNodeParams kp;
+  memset(&kp, 0, sizeof(kp));
+  const dim3 grid(A.P.G, A.P.batch), block(kBlock);
+  const int nbody = 2 * unroll;
+  if (idx == 0) {
+    kp.func = K::init();
+    kp.gridDim = dim3(1);
+    kp.blockDim = block;
+    kp.kernelParams = A.args_p;
+  } else if (idx == 1) {
+    kp.func = K::setup();
+    kp.gridDim = grid;
+    kp.blockDim = block;
+    kp.kernelParams = A.args_p;
+  } else if (idx < 2 + nbody) {
+    const int u = (idx - 2) / 2;
+    if (((idx - 2) & 1) == 0) {
+      kp.func = Lc.tma ? K::spmv_step_tma() : K::spmv_step();
+      kp.gridDim = dim3(A.Ps.G, A.P.batch);
+      kp.blockDim = dim3(Lc.tma ? kTmaBlock : kBlock);
+      kp.sharedMemBytes = Lc.tma ? Lc.tma_smem : 0u;
+      kp.kernelParams = A.args_ps[u & 1];
+    } else {
+      kp.func = K::update_step();
+      kp.gridDim = grid;
+      kp.blockDim = block;
+      kp.kernelParams = A.args_pp[u & 1];
+    }
+  } else if (idx == 2 + nbody) {
+    kp.func = (void *)cg_loop_control;
+    kp.gridDim = dim3(1);
+    kp.blockDim = dim3(32);
+    kp.kernelParams = A.args_c;
+  } else {
+    kp.func = K::finish();
+    kp.gridDim = grid;
+    kp.blockDim = block;
+    kp.kernelParams = A.args_p;
+  }
+  return kp;
+}
+
+// The graph loop: init, setup, a conditional WHILE node whose body runs `unroll` iterations and
+// the loop control, then finish.
+template <typename V, typename I, bool JAC>
+cudaError_t build_graph(const Prob<V, I> &P0, const Launch &Lc, int unroll, GraphEntry &en) {
   cudaGraph_t g = nullptr;
   cudaError_t e = cudaGraphCreate(&g, 0);
   if (e != cudaSuccess) return e;
   cudaGraphConditionalHandle h;
-  dim3 grid(P.G, P.batch), block(kBlock);
-  cudaGraphNode_t n_init, n_setup, n_while, n_fin, prev = nullptr;
-  void *args_p[] = {(void *)&P};
-  int par[2] = {0, 1};
-  void *args_pp[2][2] = {{(void *)&P, (void *)&par[0]}, {(void *)&P, (void *)&par[1]}};
-  void *args_ps[2][2] = {{(void *)&Ps, (void *)&par[0]}, {(void *)&Ps, (void *)&par[1]}};
-  const uint32_t max_bodies = (uint32_t)std::min<int64_t>((P.maxit + unroll - 1) / unroll + 2, 0x7fffffff);
+  const int nbody = 2 * unroll;
+  std::vector<cudaGraphNode_t> nodes((size_t)nbody + 4);
   cudaGraphNodeParams cp = {cudaGraphNodeTypeConditional};
   do {
     if ((e = cudaGraphConditionalHandleCreate(&h, g, 1u, cudaGraphCondAssignDefault)) != cudaSuccess) break;
-    if ((e = add_kernel(&n_init, g, nullptr, 0, K::init(), dim3(1), block, args_p)) != cudaSuccess) break;
-    if ((e = add_kernel(&n_setup, g, &n_init, 1, K::setup(), grid, block, args_p)) != cudaSuccess) break;
+    GraphArgs<V, I> A(P0, Lc, unroll, h);
+    auto add = [&](int idx, cudaGraph_t gr, const cudaGraphNode_t *dep) {
+      const cudaKernelNodeParams kp = graph_node_params<V, I, JAC>(A, Lc, unroll, idx);
+      return cudaGraphAddKernelNode(&nodes[(size_t)idx], gr, dep, dep ? 1 : 0, &kp);
+    };
+    if ((e = add(0, g, nullptr)) != cudaSuccess) break;
+    if ((e = add(1, g, &nodes[0])) != cudaSuccess) break;
+    cudaGraphNode_t n_while;
     cp.type = cudaGraphNodeTypeConditional;
     cp.conditional.handle = h;
     cp.conditional.type = cudaGraphCondTypeWhile;
     cp.conditional.size = 1;
-    if ((e = cudaGraphAddNode(&n_while, g, &n_setup, nullptr, 1, &cp)) != cudaSuccess) break;
+    if ((e = cudaGraphAddNode(&n_while, g, &nodes[1], nullptr, 1, &cp)) != cudaSuccess) break;
     cudaGraph_t body = cp.conditional.phGraph_out[0];
-    for (int u = 0; u < unroll && e == cudaSuccess; ++u) {
-      cudaGraphNode_t na, nb;
-      e = add_kernel(&na, body, prev ? &prev : nullptr, prev ? 1 : 0, fn_s, grid_s, dim3(Lc.tma ? kTmaBlock : kBlock),
-                     args_ps[u & 1], smem_s);
-      if (e != cudaSuccess) break;
-      e = add_kernel(&nb, body, &na, 1, K::update_step(), grid, block, args_pp[u & 1]);
-      prev = nb;
-    }
+    for (int idx = 2; idx <= 2 + nbody && e == cudaSuccess; ++idx)
+      e = add(idx, body, idx > 2 ? &nodes[(size_t)idx - 1] : nullptr);
     if (e != cudaSuccess) break;
-    Glob *gp = P.glob;
-    void *args_c[] = {(void *)&gp, (void *)&h, (void *)&max_bodies};
-    cudaGraphNode_t nc;
-    if ((e = add_kernel(&nc, body, &prev, 1, (void *)cg_loop_control, dim3(1), dim3(32), args_c)) != cudaSuccess)
-      break;
-    if ((e = add_kernel(&n_fin, g, &n_while, 1, K::finish(), grid, block, args_p)) != cudaSuccess) break;
-    e = cudaGraphInstantiate(out_exec, g, 0);
+    if ((e = add(3 + nbody, g, &n_while)) != cudaSuccess) break;
+    e = cudaGraphInstantiate(&en.exec, g, 0);
   } while (0);
   if (e != cudaSuccess) {
     cudaGraphDestroy(g);
     return e;
   }
-  *out_graph = g;
+  en.graph = g;
+  en.handle = h;
+  en.nodes = std::move(nodes);
+  return cudaSuccess;
+}
+
+// Points the nodes of a cached graph at another problem of the same shape (later launches only).
+template <typename V, typename I, bool JAC>
+cudaError_t update_graph(const Prob<V, I> &P0, const Launch &Lc, int unroll, GraphEntry &en) {
+  GraphArgs<V, I> A(P0, Lc, unroll, en.handle);
+  for (size_t idx = 0; idx < en.nodes.size(); ++idx) {
+    const cudaKernelNodeParams kp = graph_node_params<V, I, JAC>(A, Lc, unroll, (int)idx);
+    const cudaError_t e = cudaGraphExecKernelNodeSetParams(en.exec, en.nodes[idx], &kp);
+    if (e != cudaSuccess) return e;
+  }
   return cudaSuccess;
 }
 
@@ -923,27 +995,41 @@ sla_status run_cg(Prob<V, I> P, int unroll, int loop, cudaStream_t stream, sla_c
   if (unroll & 1) unroll += 1;  // the ping-pong parity of the body must repeat
   if (loop == SLA_LOOP_HOST) return run_cg_host_loop<V, I, JAC>(P, Lc, unroll, stream, info, batch);
 
-  std::vector<char> key(sizeof(P) + 4 * sizeof(int));
-  int tag[4] = {(int)sizeof(V), (int)sizeof(I), (int)JAC + 2 * (int)Lc.tma + 4 * Lc.G_spmv, unroll};
-  memcpy(key.data(), &P, sizeof(P));
-  memcpy(key.data() + sizeof(P), tag, sizeof(tag));
+  // the graph's shape; the problem itself goes in as node arguments
+  const int shape[8] = {(int)sizeof(V), (int)sizeof(I), (int)JAC, (int)Lc.tma, Lc.G_main, Lc.G_spmv,
+                        (int)std::min<int64_t>(P.batch, INT32_MAX), unroll};
+  std::vector<char> key((const char *)shape, (const char *)shape + sizeof(shape));
   int dev = di.dev;
   key.insert(key.end(), (char *)&dev, (char *)&dev + sizeof(dev));
+  std::vector<char> pargs((const char *)&P, (const char *)&P + sizeof(P));
 
-  cudaGraphExec_t exec = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
+    GraphEntry *hit = nullptr;
     for (auto &en : g_cache)
       if (en.key == key) {
-        en.stamp = ++g_stamp;
-        exec = en.exec;
+        hit = &en;
         break;
       }
-    if (!exec) {
+    if (hit && hit->args != pargs) {
+      if (update_graph<V, I, JAC>(P, Lc, unroll, *hit) == cudaSuccess) {
+        hit->args = pargs;
+        ++g_updates;
+      } else {  // arguments not replaceable here: rebuild this entry
+        cudaGetLastError();
+        cudaGraphExecDestroy(hit->exec);
+        cudaGraphDestroy(hit->graph);
+        g_cache.erase(g_cache.begin() + (hit - g_cache.data()));
+        hit = nullptr;
+      }
+    }
+    if (!hit) {
       GraphEntry en;
       en.key = key;
-      cudaError_t e = build_graph<V, I, JAC>(P, Lc, unroll, &en.graph, &en.exec);
+      en.args = pargs;
+      cudaError_t e = build_graph<V, I, JAC>(P, Lc, unroll, en);
       if (e != cudaSuccess) return fail(e);
+      ++g_builds;
       if (g_cache.size() >= kCacheCap) {
         auto it = std::min_element(g_cache.begin(), g_cache.end(),
                                    [](const GraphEntry &a, const GraphEntry &b) { return a.stamp < b.stamp; });
@@ -951,11 +1037,11 @@ sla_status run_cg(Prob<V, I> P, int unroll, int loop, cudaStream_t stream, sla_c
         cudaGraphDestroy(it->graph);
         g_cache.erase(it);
       }
-      en.stamp = ++g_stamp;
-      exec = en.exec;
       g_cache.push_back(std::move(en));
+      hit = &g_cache.back();
     }
-    cudaError_t e = cudaGraphLaunch(exec, stream);
+    hit->stamp = ++g_stamp;
+    cudaError_t e = cudaGraphLaunch(hit->exec, stream);
     if (e != cudaSuccess) return fail(e);
   }
   if (!info) return SLA_OK;
@@ -1028,6 +1114,14 @@ size_t workspace_bytes(int64_t n, int64_t batch, int dtype, int precond) {
 }
 
 }  // namespace sla
+
+extern "C" sla_status sla_graph_cache_stats(int64_t *entries, int64_t *builds, int64_t *updates) {
+  std::lock_guard<std::mutex> lk(sla::g_mu);
+  if (entries) *entries = (int64_t)sla::g_cache.size();
+  if (builds) *builds = (int64_t)sla::g_builds;
+  if (updates) *updates = (int64_t)sla::g_updates;
+  return SLA_OK;
+}
 
 extern "C" sla_status sla_set_spmv_variant(int32_t variant) {
   if (variant != SLA_SPMV_PLAIN && variant != SLA_SPMV_TMA) return SLA_INVALID_ARG;

@@ -435,6 +435,17 @@ typedef enum sla_spmv_variant {
 SLA_API sla_status sla_set_spmv_variant(int32_t variant);
 
 /*
+ * Introspection of the GRAPH loop's cache (not an operation of the method).  The library keeps up
+ * to 32 instantiated graph loops per process, keyed by their shape (value and index types, Jacobi,
+ * SpMV variant, launch grid, batch, unroll, device).  A solve of the same shape with other buffers
+ * or scalars reuses the cached graph after replacing its kernel nodes' arguments in place; if the
+ * runtime refuses that, the entry is rebuilt.  Writes the number of cached graphs, of graphs
+ * instantiated and of in-place argument replacements since the process started, to each host
+ * pointer that is not NULL.  Always SLA_OK.
+ */
+SLA_API sla_status sla_graph_cache_stats(int64_t *entries, int64_t *builds, int64_t *updates);
+
+/*
  * Test hook for failure detection (not an operation of the method).  Process-wide bounds of the
  * RESIDENT kernel's grid-barrier wait for the next launches: the barrier waits for `extra`
  * (0 or 1) arrivals beyond its blocks and gives up after `spin_limit` polls (0 = the library

@@ -165,6 +165,10 @@ def test_eig_argument_rejection_without_gpu(lib):
 
 def test_tuning_and_test_hooks_reject_bad_values(lib):
     # process-wide switches: no GPU needed to refuse an unknown value
+    e, b_, u = (ctypes.c_int64(-1) for _ in range(3))  # no CUDA call: counters of this process
+    assert lib.sla_graph_cache_stats(ctypes.byref(e), ctypes.byref(b_), ctypes.byref(u)) == _abi.SLA_OK
+    assert 0 <= e.value <= 32 and e.value <= b_.value and u.value >= 0
+    assert lib.sla_graph_cache_stats(None, None, None) == _abi.SLA_OK
     assert lib.sla_set_spmv_variant(2) == _abi.SLA_INVALID_ARG
     assert lib.sla_set_spmv_variant(-1) == _abi.SLA_INVALID_ARG
     assert lib.sla_set_spmv_variant(_abi.SLA_SPMV_PLAIN) == _abi.SLA_OK

@@ -337,6 +337,32 @@ def test_host_loop_equals_graph_loop(precond):
 
 
 @pytest.mark.parametrize("precond", [0, 1])
+def test_graph_loop_reused_with_other_buffers(precond):
+    # the graph loop is cached by shape: later solves of the same shape with other buffers (matrix,
+    # right-hand side, workspace, x) and scalars (rtol, maxit) replace the cached graph's kernel
+    # arguments in place.  Each result must be the host loop's, bit for bit, and the oracle's.
+    A = diffusion_dirichlet(37, np.random.default_rng(31).lognormal(0, 0.5, 2 * 37 * 38))
+    _, builds0, updates0 = sla.sla_graph_cache_stats()
+    keep = []  # the earlier calls' buffers stay allocated, so later calls get other addresses
+    for rep, rtol in enumerate((1e-8, 1e-10, 1e-9)):
+        b = np.random.default_rng(60 + rep).standard_normal(A.n)
+        dA, db = to_dev(A), t(b)
+        ws = torch.empty(sla.sla_cg_workspace_bytes(A.n, 1, torch.float64, precond), dtype=torch.uint8,
+                         device="cuda")
+        maxit = 3000 + rep
+        xg, ig, _ = sla.sla_cg_solve(dA, db, rtol=rtol, maxit=maxit, precond=precond, workspace=ws,
+                                     loop=sla.SLA_LOOP_GRAPH)
+        xh, ih, _ = sla.sla_cg_solve(dA, db, rtol=rtol, maxit=maxit, precond=precond, loop=sla.SLA_LOOP_HOST)
+        assert ig.status == ih.status == 0 and ig.iters == ih.iters and torch.equal(xg, xh)
+        ref = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=rtol, maxit=maxit, precond=precond)
+        assert abs(ig.iters - ref["iters"]) <= ITER_SLACK_F64
+        assert rel(xg.cpu().numpy(), ref["x"]) <= X_TOL_F64
+        keep.append((dA, db, ws, xg))
+    _, builds1, updates1 = sla.sla_graph_cache_stats()
+    assert builds1 - builds0 <= 1 and updates1 - updates0 >= 2
+
+
+@pytest.mark.parametrize("precond", [0, 1])
 @pytest.mark.parametrize("dtype", [np.float64, np.float32])
 def test_resident_matches_graph(precond, dtype):
     # the resident kernel and the streaming kernels partition rows differently (so dot products
