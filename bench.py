@@ -80,7 +80,7 @@ def fp64_peak_tflops(clocks=None):
 KERNEL_SOURCES = {
     "cluster": ("sla_common.cuh", "sla_onchip.cuh", "sla_cluster.cu"),
     "resident": ("sla_common.cuh", "sla_onchip.cuh", "sla_resident.cu"),
-    "streaming": ("sla_common.cuh", "sla_tma.cuh", "sla_cg.cu"),
+    "streaming": ("sla_common.cuh", "sla_tma.cuh", "sla_stream.cuh"),
 }
 ENGINE_OF = {"config1": "cluster", "config3": "cluster", "config2": "resident", "config4": "streaming",
              "config5": "streaming"}
