@@ -7,8 +7,10 @@ config 2 (1M-DOF Poisson, fp64, rtol 1e-8), config 4 (16.8M-DOF variable-coeffic
 diffusion, Jacobi PCG, rtol 1e-8) and config 5 (169M-DOF Poisson, int64 row_ptr, 1000 fixed
 iterations) each compare the solution (1e-9), the first 50 residual-history entries (1e-8) and
 the adjoint gradients grad_b and grad_values (1e-7), the oracle's adjoint chaining from its own
-forward solution.  Wall time on the GPU machine's host cores is dominated by the oracle: see the
-timing printed with -s.
+forward solution.  A fourth case crosses the 32-bit entry-offset boundary: a banded SPD
+pattern with 2.18e9 stored entries and int64 row_ptr, five iterations forward and adjoint against
+the oracle, grad_values on sampled rows past entry 2^31.  Wall time on the GPU machine's host cores is
+dominated by the oracle: see the timing printed with -s.
 """
 import time
 
@@ -105,3 +107,38 @@ def test_config5_fixed_iterations_full_oracle():
     assert gvs.shape == (w.A.nnz,)
     assert rel(gbs, adj["grad_b"]) <= GRAD_TOL_F64
     assert rel(gvs, adj["grad_values"]) <= GRAD_TOL_F64
+
+
+@pytest.mark.skipif(_free_host_gb() < 64, reason="needs ~40 GB of host memory for a 2.18e9-entry pattern")
+def test_rowptr64_past_2_pow_31_entries():
+    # 64-bit row offsets where they matter: 2,097,152 rows of up to 1,041 entries, 2.18e9 stored
+    # entries (past 2^31), int64 row_ptr, through the engine AUTO picks (the graph loop at this
+    # size).  Five CG iterations forward and adjoint (both stop at maxit), against the oracle's;
+    # grad_values on sampled rows, among them the rows whose entries straddle and follow 2^31.
+    from workloads import banded_dominant
+    A = banded_dominant(1 << 21, 520)
+    assert A.nnz > 2 ** 31 and A.row_ptr.dtype == np.int64
+    rng = np.random.default_rng(71)
+    b, g = rng.standard_normal(A.n), rng.standard_normal(A.n)
+    rtol, maxit = 1e-12, 5
+    dA = sla.CSRMatrix.from_numpy(A.row_ptr, A.col_idx, A.values, "cuda:0")
+    x, info, hist = sla.sla_cg_solve(dA, t(b), rtol=rtol, maxit=maxit, history=True)
+    gb, gv, ainfo = sla.sla_cg_adjoint(dA, x, t(g), rtol=rtol, maxit=maxit)
+    lib = oracle.load_parallel()
+    ref = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=rtol, maxit=maxit, history=True, lib=lib)
+    assert info.status == ref["status"] == 1 and info.iters == ref["iters"] == maxit
+    assert rel(x.cpu().numpy(), ref["x"]) <= X_TOL_F64
+    check_history(hist.cpu().numpy(), ref["history"], k=maxit)
+    # the adjoint of the symmetric solve: A lambda = g by the same CG from zero
+    lam = oracle.cg(A.row_ptr, A.col_idx, A.values, g, rtol=rtol, maxit=maxit, lib=lib)["x"]
+    assert ainfo.status == 1 and ainfo.iters == maxit
+    assert rel(gb.cpu().numpy(), lam) <= GRAD_TOL_F64
+    # grad_values[e] = -lambda_row(e) * x_col(e) on sampled rows
+    r31 = int(np.searchsorted(A.row_ptr, 2 ** 31, side="right")) - 1  # the row holding entry 2^31
+    rows = np.unique(np.concatenate([rng.choice(A.n, 300, replace=False), np.arange(r31 - 2, r31 + 3),
+                                     np.arange(A.n - 3, A.n), [0, 1]]))
+    ents = np.concatenate([np.arange(A.row_ptr[i], A.row_ptr[i + 1]) for i in rows])
+    assert ents.max() > 2 ** 31
+    want = np.concatenate([-lam[i] * ref["x"][A.col_idx[A.row_ptr[i]:A.row_ptr[i + 1]]] for i in rows])
+    got = gv[torch.from_numpy(ents).to(gv.device)].cpu().numpy()
+    assert rel(got, want) <= GRAD_TOL_F64

@@ -165,6 +165,31 @@ def diffusion_dirichlet(m: int, k: np.ndarray, rowptr64: bool = False) -> CSR:
     return CSR(m * m, rp, ci, _edge_values(m, slot, rp, kN, kW, kE, kS, 0.0))
 
 
+def banded_dominant(n: int, half_band: int, chunk_rows: int = 1 << 16) -> CSR:
+    """Symmetric banded matrix with int64 row_ptr: row i stores columns max(0, i - h) .. min(n - 1,
+    i + h) in increasing order, -1 off the diagonal and (number of off-diagonal entries + 1) on it,
+    so it is strictly diagonally dominant, hence SPD.  Built in row chunks straight into the final
+    arrays, so that a pattern with more than 2^31 entries (the 64-bit row-offset case) costs its
+    own size in host memory and little more."""
+    h = int(half_band)
+    i = np.arange(n, dtype=np.int64)
+    lens = np.minimum(i, h) + np.minimum(n - 1 - i, h) + 1
+    rp = np.zeros(n + 1, dtype=np.int64)
+    np.cumsum(lens, out=rp[1:])
+    nnz = int(rp[-1])
+    ci = np.empty(nnz, dtype=np.int32)
+    vals = np.full(nnz, -1.0)
+    offs = np.arange(-h, h + 1, dtype=np.int64)
+    for r0 in range(0, n, chunk_rows):
+        r1 = min(n, r0 + chunk_rows)
+        cols = np.arange(r0, r1, dtype=np.int64)[:, None] + offs[None, :]
+        keep = (cols >= 0) & (cols < n)
+        ci[rp[r0]:rp[r1]] = cols[keep].astype(np.int32)
+        diag = rp[r0:r1] + np.minimum(np.arange(r0, r1), h)  # position of (i, i) in row i
+        vals[diag] = lens[r0:r1].astype(np.float64)  # off-diagonal count + 1
+    return CSR(n, rp, ci, vals)
+
+
 def random_spd(n: int, avg_offdiag: float, seed: int, long_rows: int = 0, shift: float = 1.0) -> CSR:
     """Random symmetric strictly diagonally dominant (hence SPD) CSR matrix.
 
