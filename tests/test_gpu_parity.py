@@ -383,6 +383,36 @@ def test_resident_matches_graph(precond, dtype):
     assert ir.kernels == 1  # the whole solve is one launch
 
 
+def _largest_resident_m(precond, lo, hi):
+    # the largest m whose m x m five-point Poisson system AUTO still solves with the resident
+    # kernel (one-iteration probes; the answer depends on the device's SM count and shared memory)
+    b1 = None
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        A = poisson_5pt(mid)
+        b1 = t(np.ones(A.n))
+        _, info, _ = sla.sla_cg_solve(to_dev(A), b1, rtol=1e-30, maxit=1, precond=precond)
+        lo, hi = (mid, hi) if info.path == "resident" else (lo, mid)
+    return lo
+
+
+@pytest.mark.parametrize("precond", [0, 1])
+def test_resident_at_capacity(precond):
+    # r, p (and 1/diag) of a block's rows and their halo bitmap fill the SM's shared memory at
+    # the largest resident size; one grid row more goes to the graph loop.  Both against the oracle.
+    m = _largest_resident_m(precond, 900, 1700) if precond == 0 else _largest_resident_m(precond, 700, 1400)
+    lib = oracle.load_parallel()
+    for mm, path in ((m, "resident"), (m + 1, "graph")):
+        A = poisson_5pt(mm)
+        b = np.random.default_rng(mm).standard_normal(A.n)
+        x, info, hist = sla.sla_cg_solve(to_dev(A), t(b), rtol=1e-30, maxit=40, precond=precond, history=True)
+        ref = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-30, maxit=40, precond=precond, history=True,
+                        lib=lib)
+        assert info.path == path and info.status == ref["status"] == 1 and info.iters == ref["iters"] == 40
+        assert rel(x.cpu().numpy(), ref["x"]) <= X_TOL_F64
+        check_history(hist.cpu().numpy(), ref["history"], k=40)
+
+
 def test_resident_rejects_what_does_not_fit():
     w = config3(m=8, batch=2)
     P = to_dev(w.A, np.float32)
