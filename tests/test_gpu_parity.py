@@ -383,34 +383,43 @@ def test_resident_matches_graph(precond, dtype):
     assert ir.kernels == 1  # the whole solve is one launch
 
 
-def _largest_resident_m(precond, lo, hi):
-    # the largest m whose m x m five-point Poisson system AUTO still solves with the resident
-    # kernel (one-iteration probes; the answer depends on the device's SM count and shared memory)
-    b1 = None
+def _largest_m(path, precond, lo, hi):
+    # the largest m whose m x m five-point Poisson system AUTO still solves on `path` (one-iteration
+    # probes; the answer depends on the device's SM count and shared memory)
     while hi - lo > 1:
         mid = (lo + hi) // 2
         A = poisson_5pt(mid)
-        b1 = t(np.ones(A.n))
-        _, info, _ = sla.sla_cg_solve(to_dev(A), b1, rtol=1e-30, maxit=1, precond=precond)
-        lo, hi = (mid, hi) if info.path == "resident" else (lo, mid)
+        _, info, _ = sla.sla_cg_solve(to_dev(A), t(np.ones(A.n)), rtol=1e-30, maxit=1, precond=precond)
+        lo, hi = (mid, hi) if info.path == path else (lo, mid)
     return lo
+
+
+def _check_fixed_iterations(A, precond, path, k=40):
+    b = np.random.default_rng(A.n).standard_normal(A.n)
+    x, info, hist = sla.sla_cg_solve(to_dev(A), t(b), rtol=1e-30, maxit=k, precond=precond, history=True)
+    ref = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-30, maxit=k, precond=precond, history=True,
+                    lib=oracle.load_parallel())
+    assert info.path == path and info.status == ref["status"] == 1 and info.iters == ref["iters"] == k
+    assert rel(x.cpu().numpy(), ref["x"]) <= X_TOL_F64
+    check_history(hist.cpu().numpy(), ref["history"], k=k)
+
+
+@pytest.mark.parametrize("precond", [0, 1])
+def test_cluster_at_capacity(precond):
+    # the largest system one cluster holds in shared memory (its vectors, and the CSR slice or its
+    # row offsets as they fit); one grid row more goes to the resident kernel
+    m = _largest_m("cluster", precond, 60, 400)
+    _check_fixed_iterations(poisson_5pt(m), precond, "cluster")
+    _check_fixed_iterations(poisson_5pt(m + 1), precond, "resident")
 
 
 @pytest.mark.parametrize("precond", [0, 1])
 def test_resident_at_capacity(precond):
     # r, p (and 1/diag) of a block's rows and their halo bitmap fill the SM's shared memory at
     # the largest resident size; one grid row more goes to the graph loop.  Both against the oracle.
-    m = _largest_resident_m(precond, 900, 1700) if precond == 0 else _largest_resident_m(precond, 700, 1400)
-    lib = oracle.load_parallel()
+    m = _largest_m("resident", precond, 900, 1700) if precond == 0 else _largest_m("resident", precond, 700, 1400)
     for mm, path in ((m, "resident"), (m + 1, "graph")):
-        A = poisson_5pt(mm)
-        b = np.random.default_rng(mm).standard_normal(A.n)
-        x, info, hist = sla.sla_cg_solve(to_dev(A), t(b), rtol=1e-30, maxit=40, precond=precond, history=True)
-        ref = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-30, maxit=40, precond=precond, history=True,
-                        lib=lib)
-        assert info.path == path and info.status == ref["status"] == 1 and info.iters == ref["iters"] == 40
-        assert rel(x.cpu().numpy(), ref["x"]) <= X_TOL_F64
-        check_history(hist.cpu().numpy(), ref["history"], k=40)
+        _check_fixed_iterations(poisson_5pt(mm), precond, path)
 
 
 def test_resident_rejects_what_does_not_fit():
