@@ -833,11 +833,14 @@ def main():
         out = run_eig(args, rank, world, local_rank)
     else:
         out = run_ours(args, rank, world, local_rank)
-    if rank == 0:
-        print(json.dumps(out), flush=True)
     if world > 1 or args.dist:
+        # before the line is printed: the communicator's teardown may write to stdout, and the
+        # JSON line is the last thing on it
         import torch.distributed as dist
         dist.destroy_process_group()
+    if rank == 0:
+        sys.stdout.flush()
+        print(json.dumps(out), flush=True)
 
 
 if __name__ == "__main__":
