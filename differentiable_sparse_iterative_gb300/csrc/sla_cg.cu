@@ -326,9 +326,14 @@ sla_status run_cg(Prob<V, I> P, int unroll, int loop, cudaStream_t stream, sla_c
     const sla_status st = run_cluster<V, I, JAC>(P, batch, stream, info);
     if (st != SLA_INVALID_ARG) return st;  // else the cluster could not be placed: next option
   }
-  if (loop == SLA_LOOP_RESIDENT || (loop == SLA_LOOP_AUTO && resident_fits(P.n, batch, dt, pc, P.maxit))) {
+  if (loop == SLA_LOOP_RESIDENT) {
     set_last_path(SLA_LOOP_RESIDENT);
     return run_resident<V, I, JAC>(P, stream, info);
+  }
+  if (loop == SLA_LOOP_AUTO && resident_fits(P.n, batch, dt, pc, P.maxit)) {
+    set_last_path(SLA_LOOP_RESIDENT);
+    const sla_status st = run_resident<V, I, JAC>(P, stream, info);
+    if (st != SLA_INVALID_ARG) return st;  // else its blocks could not all be resident: next option
   }
   set_last_path(loop == SLA_LOOP_HOST ? SLA_LOOP_HOST : SLA_LOOP_GRAPH);
   const DeviceInfo di = device_info();

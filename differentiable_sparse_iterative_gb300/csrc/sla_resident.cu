@@ -579,6 +579,13 @@ sla_status run_resident(Prob<V, I> P, cudaStream_t stream, sla_cg_info *info) {
   WaitCfg wc{g_wait_extra.load(), g_wait_limit.load()};
   void *args[] = {(void *)&P, (void *)&cap, (void *)&wc};
   e = cudaLaunchCooperativeKernel(fn, dim3(G), dim3(kResBlock), args, smem, stream);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    // not every block can be resident at once here (e.g. a GPU shared by SM partitioning): the
+    // launch is refused before anything runs and the context is unaffected; SLA_INVALID_ARG lets
+    // the automatic engine choice move on to the graph loop
+    cudaGetLastError();
+    return SLA_INVALID_ARG;
+  }
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(e);
   if (!info) return SLA_OK;
