@@ -124,7 +124,10 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
   int32_t *s_ci = s_ro + ((cap + 1 + 3) & ~3);  // padded so the values below stay 16-byte aligned
   V *s_val = reinterpret_cast<V *>(s_ci + ((mcap + 3) & ~3));
   __shared__ double s_part[2][5];  // [0]: setup sums, then r.r / r.z; [1]: p.q (partners read these)
-  __shared__ double s_red[5 * CB];  // block-sum scratch
+  // block-sum scratch for two values per thread: the iterations sum at most two; the five setup
+  // sums go through it in three passes.  (Five values' worth, 20 KB at 512 threads, kept two
+  // CTAs with a second p buffer from sharing an SM.)
+  __shared__ double s_red[2 * CB];
   __shared__ V *s_peer[kClMax];    // partners' vectors (the address of their x) in distributed shared memory
   __shared__ int32_t s_start[kClMax + 1];  // first row of each partner (n for the end)
   // beta, alpha, alpha_prev in the data type, converted once by thread 0 (a conversion is an fp64
@@ -208,7 +211,17 @@ __global__ void __launch_bounds__(CB) cg_cluster(Prob<V, I> P, int C, int cap, i
       s_val[e - m_lo] = val[e];
     }
   }
-  block_sum4<5, CB>(acc5, s_red);
+  {
+    double a01[2] = {acc5[0], acc5[1]}, a23[2] = {acc5[2], acc5[3]}, a4[1] = {acc5[4]};
+    block_sum4<2, CB>(a01, s_red);
+    block_sum4<2, CB>(a23, s_red);
+    block_sum4<1, CB>(a4, s_red);
+    acc5[0] = a01[0];
+    acc5[1] = a01[1];
+    acc5[2] = a23[0];
+    acc5[3] = a23[1];
+    acc5[4] = a4[0];
+  }
   if (tid == 0)
     for (int q = 0; q < 5; ++q) s_part[0][q] = acc5[q];
   cl.sync();
