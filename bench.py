@@ -543,7 +543,49 @@ def run_batched(args, w, dev, rank, world):
                      "traffic_unit": "DRAM bytes per batched CG iteration (ncu dram__bytes_read + write)",
                      "traffic_source": (tr.get("source") if tr else None)},
         "gpu_launches": int(launches), "clocks": clk.summary(),
+        **({} if args.no_e2e else {"e2e": run_e2e_batched(args, w, dev, sla, torch, it_f[-1] + it_a[-1])}),
     }
+
+
+def run_e2e_batched(args, w, dev, sla, torch, sys_iters_per_step):
+    """The batched step through the public autograd API (solve_batched + backward): pattern, values
+    [S, nnz], b and g from pinned host memory, x and both gradients read back, every step."""
+    h = {k: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+         for k, a in (("rp", w.A.row_ptr), ("ci", w.A.col_idx), ("v", w.values_b), ("b", w.b), ("g", w.g))}
+    o_x = torch.empty(w.b.shape, dtype=h["b"].dtype).pin_memory()
+    o_gb = torch.empty(w.b.shape, dtype=h["b"].dtype).pin_memory()
+    o_gv = torch.empty(w.values_b.shape, dtype=h["v"].dtype).pin_memory()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = sum(t.numel() * t.element_size() for t in (o_x, o_gb, o_gv))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        rp, ci = h["rp"].to(dev, non_blocking=True), h["ci"].to(dev, non_blocking=True)
+        v = h["v"].to(dev, non_blocking=True).requires_grad_(True)
+        b = h["b"].to(dev, non_blocking=True).requires_grad_(True)
+        g = h["g"].to(dev, non_blocking=True)
+        x = sla.solve_batched(rp, ci, v, b, rtol=w.rtol, maxit=w.maxit, precond=w.precond)
+        x.backward(g)
+        o_x.copy_(x.detach(), non_blocking=True)
+        o_gb.copy_(b.grad, non_blocking=True)
+        o_gv.copy_(v.grad, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        flush_l2(flush)
+        step()
+    torch.cuda.synchronize()
+    total = 0.0
+    for _ in range(args.steps):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        total += e0.elapsed_time(e1) / 1e3
+    return {"value": sys_iters_per_step * args.steps / total, "unit": "system-iters/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "api": "differentiable_sparse_iterative_gb300.solve_batched + backward"}
 
 
 def local_rank_of(dev):

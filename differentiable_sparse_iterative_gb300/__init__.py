@@ -32,7 +32,8 @@ from ._abi import (SLA_OK, SLA_NOT_CONVERGED, SLA_BREAKDOWN, SLA_INVALID_ARG, SL
 __all__ = [
     "CSRMatrix", "SlaError", "CGInfo", "lib", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
     "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_validate_csr", "sla_cg_workspace_bytes",
-    "sla_status_string", "sla_launch_count", "sla_version", "CGSolve", "solve", "matvec",
+    "sla_status_string", "sla_launch_count", "sla_version", "CGSolve", "solve", "CGSolveBatched", "solve_batched",
+    "matvec",
     "SLA_PRECOND_NONE", "SLA_PRECOND_JACOBI", "SLA_LOOP_AUTO", "SLA_LOOP_HOST", "SLA_LOOP_GRAPH",
     "SLA_LOOP_RESIDENT", "SLA_LOOP_CLUSTER", "SLA_OK", "SLA_NOT_CONVERGED", "SLA_BREAKDOWN", "SLA_INVALID_ARG",
     "SLA_BAD_CSR", "SLA_NONFINITE", "SLA_WORKSPACE_TOO_SMALL", "SLA_TIMEOUT", "SLA_CUDA_ERROR",
@@ -359,6 +360,43 @@ def solve(A: CSRMatrix, b: torch.Tensor, rtol: float = 1e-8, maxit: int = 10000,
           precond: int = SLA_PRECOND_NONE) -> torch.Tensor:
     """Differentiable x = A^{-1} b (gradients flow to A.values and b)."""
     return CGSolve.apply(A.row_ptr, A.col_idx, A.values, b, rtol, maxit, precond)
+
+
+class CGSolveBatched(torch.autograd.Function):
+    """X[s] = A_s^{-1} B[s] for a batch of systems sharing one pattern (values [S, nnz], B [S, n]),
+    with the batched adjoint backward: grad_values[s] = -lambda_s[i] x_s[j] on the pattern and
+    grad_B[s] = lambda_s, lambda_s solving A_s lambda_s = dL/dX[s] with the same rtol, maxit and
+    preconditioner.  Saved for backward: the pattern, the values and X (O(S (n + nnz)))."""
+
+    @staticmethod
+    def forward(ctx, row_ptr, col_idx, values, b, rtol, maxit, precond):
+        P = CSRMatrix(row_ptr, col_idx, values[0])
+        x, infos, _ = sla_cg_solve_batched(P, values.contiguous(), b.contiguous(), rtol=rtol, maxit=maxit,
+                                           precond=precond)
+        for s, info in enumerate(infos):
+            _raise_on_failure(info, f"CGSolveBatched.forward (system {s})")
+        ctx.save_for_backward(row_ptr, col_idx, values, x)
+        ctx.opts = (rtol, maxit, precond)
+        return x
+
+    @staticmethod
+    def backward(ctx, g):
+        row_ptr, col_idx, values, x = ctx.saved_tensors
+        rtol, maxit, precond = ctx.opts
+        P = CSRMatrix(row_ptr, col_idx, values[0])
+        need_v, need_b = ctx.needs_input_grad[2], ctx.needs_input_grad[3]
+        grad_b, grad_v, infos = sla_cg_adjoint_batched(P, values.contiguous(), x, g.contiguous(), rtol=rtol,
+                                                       maxit=maxit, precond=precond, want_grad_values=need_v)
+        for s, info in enumerate(infos):
+            _raise_on_failure(info, f"CGSolveBatched.backward (system {s})")
+        return None, None, (grad_v if need_v else None), (grad_b if need_b else None), None, None, None
+
+
+def solve_batched(row_ptr: torch.Tensor, col_idx: torch.Tensor, values: torch.Tensor, b: torch.Tensor,
+                  rtol: float = 1e-5, maxit: int = 10000, precond: int = SLA_PRECOND_NONE) -> torch.Tensor:
+    """Differentiable batched solve over one shared pattern: values [S, nnz], b [S, n] -> x [S, n]
+    (gradients flow to values and b)."""
+    return CGSolveBatched.apply(row_ptr, col_idx, values, b, rtol, maxit, precond)
 
 
 def sla_spmv_transpose(A: CSRMatrix, x: torch.Tensor, y: Optional[torch.Tensor] = None) -> torch.Tensor:

@@ -79,3 +79,34 @@ def test_graph_is_one_node_and_memory_independent_of_iterations():
     assert peaks[0] == peaks[1], peaks
     # O(n + nnz): well under 16 vectors of n doubles plus two value arrays
     assert peaks[1] <= 16 * A.n * 8 + 2 * A.nnz * 8 + (1 << 20)
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_solve_batched_backward(dtype):
+    # the batched autograd node: forward and backward are the batched solve and adjoint, bit for bit,
+    # and each system matches the oracle (its adjoint chained from the oracle's own x)
+    from workloads import config3
+    from gpu_helpers import TOL_F32, X_TOL_F64
+    w = config3(m=24, batch=5)
+    rtol = 1e-10 if dtype == np.float64 else w.rtol
+    rp = torch.from_numpy(w.A.row_ptr).cuda()
+    ci = torch.from_numpy(w.A.col_idx).cuda()
+    vals = torch.from_numpy(w.values_b.astype(dtype)).cuda().requires_grad_(True)
+    b = torch.from_numpy(w.b.astype(dtype)).cuda().requires_grad_(True)
+    g = torch.from_numpy(w.g.astype(dtype)).cuda()
+    x = sla.solve_batched(rp, ci, vals, b, rtol=rtol, maxit=5000)
+    x.backward(g)
+    P = sla.CSRMatrix(rp, ci, vals.detach()[0])
+    xd, _, _ = sla.sla_cg_solve_batched(P, vals.detach(), b.detach(), rtol=rtol, maxit=5000)
+    gbd, gvd, _ = sla.sla_cg_adjoint_batched(P, vals.detach(), xd, g, rtol=rtol, maxit=5000)
+    assert torch.equal(x.detach(), xd) and torch.equal(b.grad, gbd) and torch.equal(vals.grad, gvd)
+    tol_x = X_TOL_F64 if dtype == np.float64 else TOL_F32
+    tol_g = GRAD_TOL_F64 if dtype == np.float64 else TOL_F32
+    for s in range(w.batch):
+        v64 = w.values_b[s].astype(dtype).astype(np.float64)
+        b64, g64 = w.b[s].astype(dtype).astype(np.float64), w.g[s].astype(dtype).astype(np.float64)
+        ref = oracle.cg(w.A.row_ptr, w.A.col_idx, v64, b64, rtol=rtol, maxit=5000)
+        adj = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, v64, ref["x"], g64, rtol=rtol, maxit=5000)
+        assert rel(x[s].detach().cpu().numpy(), ref["x"]) <= tol_x
+        assert rel(b.grad[s].cpu().numpy(), adj["grad_b"]) <= tol_g
+        assert rel(vals.grad[s].cpu().numpy(), adj["grad_values"]) <= tol_g
