@@ -101,6 +101,21 @@ class CSRMatrix:
     def with_values(self, values: torch.Tensor) -> "CSRMatrix":
         return CSRMatrix(self.row_ptr, self.col_idx, values)
 
+    # The method-style interface of the pages' sparse tensor (A.solve(f), A.matvec(x), A.eigsh()),
+    # each the differentiable module function of the same name.
+    def solve(self, b: torch.Tensor, rtol: float = 1e-8, maxit: int = 10000, precond: int = 0) -> torch.Tensor:
+        """Differentiable x = A^{-1} b (see solve)."""
+        return solve(self, b, rtol=rtol, maxit=maxit, precond=precond)
+
+    def matvec(self, x: torch.Tensor) -> torch.Tensor:
+        """Differentiable y = A x (see matvec)."""
+        return matvec(self, x)
+
+    def eigsh(self, **kw):
+        """The smallest eigenpair (mu, v), mu differentiable with respect to the values (see
+        eigsh_smallest, which takes the same keyword arguments)."""
+        return eigsh_smallest(self, **kw)
+
 
 _DT = {torch.float32: _abi.SLA_F32, torch.float64: _abi.SLA_F64}
 _IT = {torch.int32: _abi.SLA_I32, torch.int64: _abi.SLA_I64}

@@ -110,3 +110,20 @@ def test_solve_batched_backward(dtype):
         assert rel(x[s].detach().cpu().numpy(), ref["x"]) <= tol_x
         assert rel(b.grad[s].cpu().numpy(), adj["grad_b"]) <= tol_g
         assert rel(vals.grad[s].cpu().numpy(), adj["grad_values"]) <= tol_g
+
+
+def test_method_style_interface():
+    # A.solve(b), A.matvec(x), A.eigsh(): the module functions, with their gradients
+    A, b, g = _problem(m=16, seed=5)
+    dA = to_dev(A)
+    v1 = dA.values.clone().requires_grad_(True)
+    v2 = dA.values.clone().requires_grad_(True)
+    x1 = dA.with_values(v1).solve(t(b), rtol=1e-12)
+    x2 = sla.solve(dA.with_values(v2), t(b), rtol=1e-12)
+    (x1 * t(g)).sum().backward()
+    (x2 * t(g)).sum().backward()
+    assert torch.equal(x1.detach(), x2.detach()) and torch.equal(v1.grad, v2.grad)
+    assert torch.equal(dA.matvec(t(b)), sla.matvec(dA, t(b)))
+    mu1, _ = dA.eigsh()
+    mu2, _ = sla.eigsh_smallest(dA)
+    assert float(mu1.detach()) == float(mu2.detach())
