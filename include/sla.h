@@ -94,16 +94,18 @@ typedef struct sla_csr {
 
 typedef enum sla_loop {
   SLA_LOOP_AUTO = 0,      /* CLUSTER when each system fits one thread-block cluster, else RESIDENT
-                             when one system fits on chip, else GRAPH */
+                             when one system fits on chip, else GRAPH; an engine that cannot be
+                             placed (its blocks not all resident at once) passes to the next */
   SLA_LOOP_HOST = 1,      /* the host launches the streaming kernels directly and reads the device
                              status every `unroll` iterations (for profilers that cannot see inside
                              conditional graphs, and for drivers without conditional nodes) */
   SLA_LOOP_GRAPH = 2,     /* streaming kernels in one CUDA graph per solve; the loop is a device-side
                              conditional WHILE node */
-  SLA_LOOP_RESIDENT = 3,  /* one persistent cooperative kernel per solve, each SM keeping its rows'
-                             vectors in shared memory (one system whose 1/#SM share of x, r, p, q
-                             [, 1/diag] fits one SM's shared memory: about 1.4M fp64 unknowns on
-                             GB300); SLA_INVALID_ARG when it does not fit */
+  SLA_LOOP_RESIDENT = 3,  /* one persistent cooperative kernel per solve, each SM keeping r and p
+                             [and 1/diag] of its rows in shared memory, x and q in L2 (one system
+                             whose 1/#SM share fits one SM's shared memory: about 2.0M fp64
+                             unknowns on GB300, 1.3M with Jacobi); SLA_INVALID_ARG when it does not
+                             fit or its blocks cannot all be resident at once */
   SLA_LOOP_CLUSTER = 4    /* one thread-block cluster (up to 16 CTAs) per system, all vectors in
                              shared memory, partner rows read through distributed shared memory,
                              hardware cluster barriers; any batch whose systems are small enough
