@@ -32,7 +32,7 @@ from ._abi import (SLA_OK, SLA_NOT_CONVERGED, SLA_BREAKDOWN, SLA_INVALID_ARG, SL
 __all__ = [
     "CSRMatrix", "SlaError", "CGInfo", "lib", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
     "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_validate_csr", "sla_cg_workspace_bytes",
-    "sla_status_string", "sla_launch_count", "sla_version", "CGSolve", "solve", "CGSolveBatched", "solve_batched",
+    "sla_status_string", "sla_launch_count", "sla_version", "CGSolve", "solve", "CGSolveBatched", "solve_batched", "sla_eigsh", "sla_eigsh_workspace_bytes", "Eigsh", "eigsh",
     "matvec",
     "SLA_PRECOND_NONE", "SLA_PRECOND_JACOBI", "SLA_LOOP_AUTO", "SLA_LOOP_HOST", "SLA_LOOP_GRAPH",
     "SLA_LOOP_RESIDENT", "SLA_LOOP_CLUSTER", "SLA_OK", "SLA_NOT_CONVERGED", "SLA_BREAKDOWN", "SLA_INVALID_ARG",
@@ -111,10 +111,11 @@ class CSRMatrix:
         """Differentiable y = A x (see matvec)."""
         return matvec(self, x)
 
-    def eigsh(self, **kw):
-        """The smallest eigenpair (mu, v), mu differentiable with respect to the values (see
-        eigsh_smallest, which takes the same keyword arguments)."""
-        return eigsh_smallest(self, **kw)
+    def eigsh(self, k: Optional[int] = None, **kw):
+        """Without k: the smallest eigenpair (mu, v) (see eigsh_smallest).  With k: the k smallest
+        (mu [k], V [k, n]) (see eigsh).  mu is differentiable with respect to the values; the
+        keyword arguments are those of the function called."""
+        return eigsh_smallest(self, **kw) if k is None else eigsh(self, k, **kw)
 
 
 _DT = {torch.float32: _abi.SLA_F32, torch.float64: _abi.SLA_F64}
@@ -563,3 +564,79 @@ def eigsh_smallest(A: CSRMatrix, tol: Optional[float] = None, maxit: int = 1000,
                    precond: int = SLA_PRECOND_NONE):
     """Differentiable smallest eigenvalue of SPD A (gradient to A.values) and its eigenvector."""
     return EigSmallest.apply(A.row_ptr, A.col_idx, A.values, tol, maxit, precond)
+
+
+def sla_eigsh_workspace_bytes(n: int, k: int, dtype: torch.dtype, precond: int = SLA_PRECOND_NONE) -> int:
+    return lib().sla_eigsh_workspace_bytes(int(n), int(k), _DT[dtype], int(precond))
+
+
+def sla_eigsh(A: CSRMatrix, k: int, V0: Optional[torch.Tensor] = None, tol: Optional[float] = None,
+              maxit: int = 2000, inner_factor: float = 0.01, inner_maxit: int = 100000,
+              precond: int = SLA_PRECOND_NONE, loop: int = SLA_LOOP_AUTO, seed: int = 0,
+              workspace: Optional[torch.Tensor] = None):
+    """The k smallest eigenpairs of SPD A (1 <= k <= 16) by block inverse iteration with a
+    Rayleigh-Ritz step.  Returns (mu [k] ascending, V [k, n] orthonormal rows, EigInfo).
+
+    V0 ([k, n]) defaults to a block of standard normal entries drawn on the device from a generator
+    seeded with `seed`; tol defaults to 1e-10 for float64 and 1e-5 for float32 data.
+    """
+    dt, dev = A.values.dtype, A.values.device
+    if tol is None:
+        tol = 1e-10 if dt == torch.float64 else 1e-5
+    if V0 is None:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(int(seed))
+        V = torch.randn(int(k), A.n, dtype=dt, device=dev, generator=gen)
+    else:
+        V = V0.detach().to(dtype=dt).contiguous().clone()
+    if V.dim() != 2 or V.shape[0] != int(k) or V.shape[1] != A.n:
+        raise ValueError("V0 must have shape [k, n]")
+    need = sla_eigsh_workspace_bytes(A.n, k, dt, precond)
+    ws = workspace if workspace is not None and workspace.numel() * workspace.element_size() >= need else \
+        torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    o = _abi.sla_eig_opts()
+    o.tol, o.maxit, o.inner_factor, o.inner_maxit = float(tol), int(maxit), float(inner_factor), int(inner_maxit)
+    o.precond, o.loop = int(precond), int(loop)
+    info = _abi.sla_eig_info()
+    mu = (ctypes.c_double * int(k))()
+    st = lib().sla_eigsh(ctypes.byref(_csr_struct(A)), int(k), _dev_ptr(V, dt, "V"), mu, ctypes.byref(o),
+                         ctypes.byref(info), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(dev))
+    _check(st, "sla_eigsh")
+    ei = EigInfo(int(info.iters), int(info.inner_iters), float(info.mu), float(info.residual), int(info.status))
+    return torch.tensor(list(mu), dtype=torch.float64), V, ei
+
+
+class Eigsh(torch.autograd.Function):
+    """(mu, V) = the k smallest eigenpairs of SPD A; mu ([k]) is differentiable with respect to A's
+    values.  Backward (Hellmann-Feynman, summed over the pairs): d L / d values[e] =
+    sum_s (dL/dmu_s) V[s, row(e)] V[s, col(e)] on the pattern.  Within a multiple eigenvalue only
+    sums of gradients over the eigenspace are defined (L symmetric in its eigenvalues).  V is
+    returned as a constant."""
+
+    @staticmethod
+    def forward(ctx, row_ptr, col_idx, values, k, tol, maxit, precond):
+        A = CSRMatrix(row_ptr, col_idx, values)
+        mu, V, info = sla_eigsh(A, k, tol=tol, maxit=maxit, precond=precond)
+        if info.status == SLA_NOT_CONVERGED:
+            warnings.warn(f"Eigsh.forward: largest residual {info.residual:.3e} after {info.iters} steps")
+        elif info.status != SLA_OK:
+            raise SlaError(info.status, "Eigsh.forward")
+        ctx.save_for_backward(row_ptr, col_idx, values, V)
+        ctx.mark_non_differentiable(V)
+        return mu.to(dtype=values.dtype, device=values.device), V
+
+    @staticmethod
+    def backward(ctx, g_mu, g_V):
+        row_ptr, col_idx, values, V = ctx.saved_tensors
+        if not ctx.needs_input_grad[2]:
+            return None, None, None, None, None, None, None
+        A = CSRMatrix(row_ptr, col_idx, values)
+        gv = sla_eig_grad_values(A, V, weights=[float(x) for x in g_mu.detach().cpu()])
+        return None, None, gv, None, None, None, None
+
+
+def eigsh(A: CSRMatrix, k: int = 1, tol: Optional[float] = None, maxit: int = 2000,
+          precond: int = SLA_PRECOND_NONE):
+    """Differentiable k smallest eigenvalues of SPD A ([k], ascending; gradient to A.values) and the
+    eigenvectors ([k, n])."""
+    return Eigsh.apply(A.row_ptr, A.col_idx, A.values, int(k), tol, maxit, precond)

@@ -303,6 +303,37 @@ SLA_API sla_status sla_eig_smallest(const sla_csr *A, void *v, const sla_eig_opt
                                     void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Bytes of device workspace sla_eigsh needs for k eigenpairs of n unknowns (0 for invalid
+ * arguments, k outside 1..16): the inner batched CG's workspace for k systems, three blocks of k
+ * vectors and the reductions' scratch.
+ */
+SLA_API size_t sla_eigsh_workspace_bytes(int64_t n, int64_t k, int32_t dtype, int32_t precond);
+
+/*
+ * The k smallest eigenpairs of a symmetric positive definite A, 1 <= k <= min(16, n) (TS
+ * Methodology 1: the ".eigsh" API; the summary names no eigensolver).  Block inverse iteration
+ * with a Rayleigh-Ritz step (subspace iteration on A^{-1}): the start block is orthonormalised
+ * (Cholesky QR, twice); every step forms W = A X and H = X^T W, takes H's eigenvectors Q
+ * (theta ascending) to the Ritz vectors X Q and their images W Q, and, until every residual
+ * ||A x_s - theta_s x_s|| is at most tol * theta_s, solves A Y = X for the k vectors at once by
+ * CG from Y = X diag(1 / theta) with the rtol inner_factor * max_s residual_s / theta_s, then
+ * orthonormalises Y into the next X.  The vector s converges at the rate theta_s / theta_{k+1}
+ * per step, so a block somewhat larger than the eigenpairs needed converges faster.  Within a
+ * multiple eigenvalue the vectors are some orthonormal basis of its eigenspace.
+ *   V      device, k x n entries of A->dtype, row-major: the start block on entry (linearly
+ *          independent), the unit eigenvectors on return (orthonormal to rounding), each with its
+ *          sign chosen so that sum_i v_i >= 0.
+ *   mu     host, k doubles: the eigenvalues, ascending (written for SLA_OK and SLA_NOT_CONVERGED).
+ *   info   host, required: steps, CG iterations over all vectors, mu = the smallest eigenvalue,
+ *          residual = the largest residual, status (SLA_BREAKDOWN also for a rank-deficient block).
+ *   workspace device, >= sla_eigsh_workspace_bytes(n, k, dtype, opts->precond), 256-byte aligned.
+ * The k x k eigenproblem and Cholesky factor of each step are solved by the host (fp64); the
+ * host reads a few k x k results per step and synchronises the stream.
+ */
+SLA_API sla_status sla_eigsh(const sla_csr *A, int64_t k, void *V, double *mu, const sla_eig_opts *opts,
+                             sla_eig_info *info, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Eigenvalue gradient on the sparsity pattern (TS Methodology 2, eigenvalue problems:
  * d mu / d A_ij = v_i v_j, Hellmann-Feynman).  For L = sum_s w_s mu_s over k eigenpairs with unit
  * eigenvectors V[s] (s = 0..k-1):

@@ -171,7 +171,7 @@ def test_eigsh_smallest_gradient():
     assert not v.requires_grad
     (3.0 * mu).backward()
     mu_o, V_o = oracle.eig_smallest(A.row_ptr, A.col_idx, A.values, 2)
-    assert abs(float(mu) - mu_o[0]) <= 1e-11 * mu_o[0]
+    assert abs(float(mu.detach()) - mu_o[0]) <= 1e-11 * mu_o[0]
     ref = 3.0 * oracle.eig_grad_values(A.row_ptr, A.col_idx, V_o[:1])
     assert rel(vals.grad.cpu().numpy(), ref) <= 1e-8
 
@@ -203,3 +203,108 @@ def test_eig_smallest_poisson1000_sampled():
     e = np.random.default_rng(4).choice(A.nnz, 2000, replace=False)
     # one eigenvector with unit weight: a single rounded product v_i * v_j on both sides, so exact
     assert np.array_equal(gv[e], vv[rows[e]] * vv[A.col_idx[e]])
+
+
+# --------------------------------------------------------------------------- k smallest eigenpairs
+
+def _diffusion(m, seed):
+    return diffusion_dirichlet(m, np.random.default_rng(seed).lognormal(0.0, 0.5, 2 * m * (m + 1)))
+
+
+@pytest.mark.parametrize("precond", [0, 1])
+@pytest.mark.parametrize("k", [1, 3, 6])
+def test_eigsh_k_matches_dense_oracle(k, precond):
+    # distinct eigenvalues: each eigenvector is unique up to sign (both sides take sum_i v_i >= 0)
+    A = _diffusion(20, 17)
+    mu_o, V_o = oracle.eig_smallest(A.row_ptr, A.col_idx, A.values, k + 1)
+    tol = 1e-10
+    mu, V, info = sla.sla_eigsh(to_dev(A), k, tol=tol, precond=precond)
+    assert info.status == sla.SLA_OK, info
+    assert info.residual <= tol * float(mu[-1])
+    Vg = V.cpu().numpy()
+    assert np.linalg.norm(Vg @ Vg.T - np.eye(k)) <= 1e-12
+    for s in range(k):
+        gap = min(mu_o[s + 1] - mu_o[s], mu_o[s] - mu_o[s - 1] if s > 0 else np.inf)
+        assert abs(float(mu[s]) - mu_o[s]) <= 1e-11 * mu_o[s]
+        assert Vg[s].sum() >= 0.0
+        assert np.linalg.norm(Vg[s] - V_o[s]) <= _vec_bound(tol, mu_o[s], gap, A.n)
+
+
+def test_eigsh_poisson_multiple_eigenvalue():
+    # the five-point Laplacian's 2nd and 3rd eigenvalues are equal (modes (1,2) and (2,1)): the
+    # eigenvalues are unique, the vectors only up to a basis of that eigenspace
+    m = 16
+    A = poisson_5pt(m)
+    th = np.pi / (m + 1)
+    lam = lambda p, q: 4.0 - 2.0 * np.cos(p * th) - 2.0 * np.cos(q * th)  # noqa: E731
+    exact = np.array([lam(1, 1), lam(1, 2), lam(2, 1), lam(2, 2)])
+    mu, V, info = sla.sla_eigsh(to_dev(A), 4, tol=1e-10)
+    assert info.status == sla.SLA_OK, info
+    assert np.all(np.abs(mu.numpy() - exact) <= 1e-11 * exact)
+    mu_o, V_o = oracle.eig_smallest(A.row_ptr, A.col_idx, A.values, 5)
+    Vg = V.cpu().numpy()
+    P, P_o = Vg[1:3].T @ Vg[1:3], V_o[1:3].T @ V_o[1:3]  # projectors onto the double eigenspace
+    gap = min(exact[1] - exact[0], exact[3] - exact[1])
+    assert np.linalg.norm(P - P_o) <= 2 * _vec_bound(1e-10, exact[1], gap, A.n)
+    for s in (0, 3):
+        assert np.linalg.norm(Vg[s] - V_o[s]) <= _vec_bound(1e-10, exact[s], gap, A.n)
+
+
+def test_eigsh_gradient_of_weighted_eigenvalues():
+    A = _diffusion(16, 23)
+    k, w = 3, np.array([1.5, -0.5, 2.0])
+    vals = t(A.values).requires_grad_(True)
+    dA = sla.CSRMatrix(t(A.row_ptr), t(A.col_idx), vals)
+    mu, V = sla.eigsh(dA, k, tol=1e-11)
+    assert mu.requires_grad and not V.requires_grad
+    (mu * t(w)).sum().backward()
+    mu_o, V_o = oracle.eig_smallest(A.row_ptr, A.col_idx, A.values, k + 1)
+    assert np.all(np.abs(mu.detach().cpu().numpy() - mu_o[:k]) <= 1e-11 * mu_o[:k])
+    ref = oracle.eig_grad_values(A.row_ptr, A.col_idx, V_o[:k], w)
+    assert rel(vals.grad.cpu().numpy(), ref) <= 1e-8
+    # the same through the method-style interface
+    mu2, _ = dA.eigsh(k=k, tol=1e-11)
+    assert torch.allclose(mu2.detach(), mu.detach(), rtol=1e-12, atol=0)
+
+
+def test_eigsh_k1_agrees_with_eig_smallest():
+    A = _diffusion(24, 7)
+    mu1, v1, _ = sla.sla_eig_smallest(to_dev(A), tol=1e-11)
+    mu, V, info = sla.sla_eigsh(to_dev(A), 1, tol=1e-11)
+    assert info.status == sla.SLA_OK
+    assert abs(float(mu[0]) - mu1) <= 1e-12 * mu1
+    assert np.linalg.norm(V[0].cpu().numpy() - v1.cpu().numpy()) <= 1e-8
+
+
+def test_eigsh_float32():
+    m = 20
+    A = poisson_5pt(m)
+    th = np.pi / (m + 1)
+    mu, V, info = sla.sla_eigsh(to_dev(A, np.float32), 2, tol=1e-5)
+    assert info.status == sla.SLA_OK, info
+    exact = np.array([4.0 - 4.0 * np.cos(th), 4.0 - 2.0 * np.cos(th) - 2.0 * np.cos(2 * th)])
+    assert np.all(np.abs(mu.numpy() - exact) <= 1e-4 * exact)
+    assert V.dtype == torch.float32
+
+
+def test_eigsh_status_and_argument_cases():
+    A = poisson_5pt(10)
+    dA = to_dev(A)
+    for k in (0, 17, A.n + 1):
+        with pytest.raises(sla.SlaError):
+            sla.sla_eigsh(dA, k, V0=None if k == 0 or k > 16 else torch.zeros(k, A.n, dtype=torch.float64,
+                                                                              device="cuda:0"))
+    # a rank-deficient start block: two equal rows
+    V0 = np.random.default_rng(1).standard_normal((3, A.n))
+    V0[2] = V0[1]
+    _, _, info = sla.sla_eigsh(dA, 3, V0=t(V0))
+    assert info.status == sla.SLA_BREAKDOWN and info.iters == 0
+    # negative definite: the first Ritz values are negative, before any solve
+    neg = sla.CSRMatrix.from_numpy(A.row_ptr, A.col_idx, -A.values, "cuda:0")
+    _, _, info = sla.sla_eigsh(neg, 2)
+    assert info.status == sla.SLA_BREAKDOWN and info.iters == 0 and info.inner_iters == 0
+    # maxit = 0: the Ritz pairs of the start block, not converged
+    mu, V, info = sla.sla_eigsh(dA, 2, maxit=0)
+    assert info.status == sla.SLA_NOT_CONVERGED and info.iters == 0
+    Vg = V.cpu().numpy()
+    assert np.linalg.norm(Vg @ Vg.T - np.eye(2)) <= 1e-12
