@@ -584,7 +584,11 @@ sla_status eigk_run(const sla_csr *A, int k, V *Vout, double *mu, const sla_eig_
     if (!(theta[0] > 0.0)) { status = SLA_BREAKDOWN; break; }
     if (conv) { status = SLA_OK; break; }
     if (it >= o->maxit) { status = SLA_NOT_CONVERGED; break; }
-    // Y = A^{-1} X for the k vectors at once (one matrix: values stride 0), from X diag(1/theta)
+    // Y = A^{-1} X from Y = X diag(1/theta), every vector to the rtol inner_factor * max_s
+    // residual_s / theta_s (per-vector tolerances, tighter for the vectors nearer convergence,
+    // took about a quarter more CG iterations for the same outer steps).  When one system fits
+    // the resident engine the k solves run one after another there; otherwise together in the
+    // batched CG (one matrix: values stride 0).
     M.assign((size_t)k * k, 0.0);
     for (int s = 0; s < k; ++s) M[(size_t)s * k + s] = 1.0 / theta[s];
     if ((e = combine(buf[cur], M, buf[t1])) != cudaSuccess) return fail(e);
@@ -596,9 +600,21 @@ sla_status eigk_run(const sla_csr *A, int k, V *Vout, double *mu, const sla_eig_
     co.loop = o->loop;
     co.reserved = 0;
     std::vector<sla_cg_info> ci((size_t)k);
-    const sla_status cs = cg_entry(A, k, A->values, 0, buf[cur], buf[t1], &co, buf[t1], ci.data(), nullptr,
-                                   ws + L.cg, st);
-    if (cs != SLA_OK) return cs;
+    const bool one_by_one = (o->loop == SLA_LOOP_AUTO || o->loop == SLA_LOOP_RESIDENT) &&
+                            resident_fits(n, 1, A->dtype, o->precond, o->inner_maxit);
+    if (one_by_one) {
+      const size_t vb = sizeof(V) * (size_t)n;
+      for (int s = 0; s < k; ++s) {
+        const char *xs = (const char *)buf[cur] + vb * s;
+        char *ys = (char *)buf[t1] + vb * s;
+        const sla_status cs = cg_entry(A, 1, A->values, 0, xs, ys, &co, ys, &ci[s], nullptr, ws + L.cg, st);
+        if (cs != SLA_OK) return cs;
+      }
+    } else {
+      const sla_status cs = cg_entry(A, k, A->values, 0, buf[cur], buf[t1], &co, buf[t1], ci.data(), nullptr,
+                                     ws + L.cg, st);
+      if (cs != SLA_OK) return cs;
+    }
     int32_t inner_bad = SLA_OK;
     for (int s = 0; s < k; ++s) {
       info->inner_iters += ci[s].iters;

@@ -315,10 +315,12 @@ SLA_API size_t sla_eigsh_workspace_bytes(int64_t n, int64_t k, int32_t dtype, in
  * with a Rayleigh-Ritz step (subspace iteration on A^{-1}): the start block is orthonormalised
  * (Cholesky QR, twice); every step forms W = A X and H = X^T W, takes H's eigenvectors Q
  * (theta ascending) to the Ritz vectors X Q and their images W Q, and, until every residual
- * ||A x_s - theta_s x_s|| is at most tol * theta_s, solves A Y = X for the k vectors at once by
- * CG from Y = X diag(1 / theta) with the rtol inner_factor * max_s residual_s / theta_s, then
- * orthonormalises Y into the next X.  The vector s converges at the rate theta_s / theta_{k+1}
- * per step, so a block somewhat larger than the eigenpairs needed converges faster.  Within a
+ * ||A x_s - theta_s x_s|| is at most tol * theta_s, solves A Y = X by CG from Y = X diag(1 / theta)
+ * to the rtol inner_factor * max_s residual_s / theta_s, and orthonormalises Y into the next X.
+ * When one system fits the resident engine (opts->loop AUTO or RESIDENT) the k solves run there
+ * one after another; otherwise together in the batched CG.  The vector s converges at the rate
+ * theta_s / theta_{k+1} per step, so a block somewhat larger than the eigenpairs needed converges
+ * faster.  Within a
  * multiple eigenvalue the vectors are some orthonormal basis of its eigenspace.
  *   V      device, k x n entries of A->dtype, row-major: the start block on entry (linearly
  *          independent), the unit eigenvectors on return (orthonormal to rounding), each with its

@@ -211,14 +211,16 @@ def _diffusion(m, seed):
     return diffusion_dirichlet(m, np.random.default_rng(seed).lognormal(0.0, 0.5, 2 * m * (m + 1)))
 
 
+@pytest.mark.parametrize("loop", [sla.SLA_LOOP_AUTO, sla.SLA_LOOP_GRAPH])
 @pytest.mark.parametrize("precond", [0, 1])
 @pytest.mark.parametrize("k", [1, 3, 6])
-def test_eigsh_k_matches_dense_oracle(k, precond):
-    # distinct eigenvalues: each eigenvector is unique up to sign (both sides take sum_i v_i >= 0)
+def test_eigsh_k_matches_dense_oracle(k, precond, loop):
+    # distinct eigenvalues: each eigenvector is unique up to sign (both sides take sum_i v_i >= 0).
+    # AUTO: the k inner solves one by one; GRAPH: together in the batched CG
     A = _diffusion(20, 17)
     mu_o, V_o = oracle.eig_smallest(A.row_ptr, A.col_idx, A.values, k + 1)
     tol = 1e-10
-    mu, V, info = sla.sla_eigsh(to_dev(A), k, tol=tol, precond=precond)
+    mu, V, info = sla.sla_eigsh(to_dev(A), k, tol=tol, precond=precond, loop=loop)
     assert info.status == sla.SLA_OK, info
     assert info.residual <= tol * float(mu[-1])
     Vg = V.cpu().numpy()
