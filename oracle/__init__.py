@@ -81,6 +81,14 @@ def _bind(lib):
     lib.orc_matvec_grad_values.restype = None
     lib.orc_threads.argtypes = [ctypes.c_int]
     lib.orc_threads.restype = ctypes.c_int
+    lib.orc_transpose.argtypes = [i64, p, p, p, p, p, p]
+    lib.orc_transpose.restype = None
+    lib.orc_bicgstab.argtypes = [i64, p, p, p, p, p, ctypes.c_double, i64, p, p, ctypes.POINTER(i64),
+                                 ctypes.POINTER(ctypes.c_double)]
+    lib.orc_bicgstab.restype = ctypes.c_int
+    lib.orc_bicgstab_adjoint.argtypes = [i64, p, p, p, p, p, ctypes.c_double, i64, p, p, ctypes.POINTER(i64),
+                                         ctypes.POINTER(ctypes.c_double)]
+    lib.orc_bicgstab_adjoint.restype = ctypes.c_int
     return lib
 
 
@@ -212,6 +220,56 @@ def cg_adjoint(row_ptr, col_idx, values, x, g, rtol: float = 1e-10, maxit: int =
     rr = ctypes.c_double(0.0)
     st = lib.orc_cg_adjoint(n, _ptr(rp), _ptr(ci), _ptr(v), _ptr(x), _ptr(g), float(rtol), int(maxit),
                             int(precond), _ptr(gb), _ptr(gv), ctypes.byref(it), ctypes.byref(rr))
+    return {"grad_b": gb, "grad_values": gv, "iters": int(it.value), "rel_res": float(rr.value),
+            "status": int(st)}
+
+
+def transpose(row_ptr, col_idx, values, lib=None):
+    """A^T as CSR (row_ptr int64, col_idx int32, values): each column's entries in increasing row order."""
+    lib = lib or load()
+    rp, ci, v = _csr(row_ptr, col_idx, values)
+    n = rp.shape[0] - 1
+    trp = np.empty(n + 1, dtype=np.int64)
+    tci = np.empty(ci.shape[0], dtype=np.int32)
+    tv = np.empty(ci.shape[0], dtype=np.float64)
+    lib.orc_transpose(n, _ptr(rp), _ptr(ci), _ptr(v), _ptr(trp), _ptr(tci), _ptr(tv))
+    return trp, tci, tv
+
+
+def bicgstab(row_ptr, col_idx, values, b, x0=None, rtol: float = 1e-10, maxit: int = 100000,
+             history: bool = False, lib=None) -> dict:
+    """Solve a general A x = b by BiCGStab; returns dict(x, iters, rel_res, status, history)."""
+    lib = lib or load()
+    rp, ci, v = _csr(row_ptr, col_idx, values)
+    n = rp.shape[0] - 1
+    b = np.ascontiguousarray(b, dtype=np.float64)
+    x0c = None if x0 is None else np.ascontiguousarray(x0, dtype=np.float64)
+    x = np.empty(n, dtype=np.float64)
+    h = np.full(maxit + 1, np.nan) if history else None
+    it = ctypes.c_int64(0)
+    rr = ctypes.c_double(0.0)
+    st = lib.orc_bicgstab(n, _ptr(rp), _ptr(ci), _ptr(v), _ptr(b), _ptr(x0c), float(rtol), int(maxit), _ptr(x),
+                          _ptr(h), ctypes.byref(it), ctypes.byref(rr))
+    out = {"x": x, "iters": int(it.value), "rel_res": float(rr.value), "status": int(st)}
+    if history:
+        out["history"] = h[: it.value + 1].copy()
+    return out
+
+
+def bicgstab_adjoint(row_ptr, col_idx, values, x, g, rtol: float = 1e-10, maxit: int = 100000, lib=None) -> dict:
+    """Adjoint backward of the BiCGStab solve: dict(grad_b = lambda (A^T lambda = g), grad_values, iters,
+    rel_res, status)."""
+    lib = lib or load()
+    rp, ci, v = _csr(row_ptr, col_idx, values)
+    n = rp.shape[0] - 1
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    gb = np.empty(n, dtype=np.float64)
+    gv = np.empty(ci.shape[0], dtype=np.float64)
+    it = ctypes.c_int64(0)
+    rr = ctypes.c_double(0.0)
+    st = lib.orc_bicgstab_adjoint(n, _ptr(rp), _ptr(ci), _ptr(v), _ptr(x), _ptr(g), float(rtol), int(maxit),
+                                  _ptr(gb), _ptr(gv), ctypes.byref(it), ctypes.byref(rr))
     return {"grad_b": gb, "grad_values": gv, "iters": int(it.value), "rel_res": float(rr.value),
             "status": int(st)}
 

@@ -284,3 +284,148 @@ void orc_eig_grad_values(int64_t n, const int64_t *row_ptr, const int32_t *col_i
       grad_values[e] = acc;
     }
 }
+
+/*
+ * A^T as a CSR matrix (general pattern): for every column c of A, its entries taken row by row in
+ * increasing row order.  tr_row_ptr: n+1; tr_col_idx, tr_values: nnz.
+ */
+void orc_transpose(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const double *values,
+                   int64_t *tr_row_ptr, int32_t *tr_col_idx, double *tr_values) {
+  for (int64_t c = 0; c <= n; ++c) tr_row_ptr[c] = 0;
+  for (int64_t e = 0; e < row_ptr[n]; ++e) tr_row_ptr[col_idx[e] + 1] += 1;
+  for (int64_t c = 0; c < n; ++c) tr_row_ptr[c + 1] += tr_row_ptr[c];
+  int64_t *fill = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+  for (int64_t c = 0; c < n; ++c) fill[c] = tr_row_ptr[c];
+  for (int64_t i = 0; i < n; ++i)
+    for (int64_t e = row_ptr[i]; e < row_ptr[i + 1]; ++e) {
+      const int64_t c = col_idx[e];
+      tr_col_idx[fill[c]] = (int32_t)i;
+      tr_values[fill[c]] = values[e];
+      fill[c] += 1;
+    }
+  free(fill);
+}
+
+/*
+ * BiCGStab for a general (non-symmetric) A x = b, unpreconditioned (H. A. van der Vorst,
+ * "Bi-CGSTAB", SIAM J. Sci. Stat. Comput. 13, 1992).  The torch-sla pages list BiCGStab among
+ * the solvers of the .solve API; they give no variant, so the textbook one:
+ *   r = b - A x0 (r = b when x0 is NULL); rhat = r (fixed shadow residual); rho_prev = alpha =
+ *   omega = 1; stop at once when ||r|| <= rtol ||b||.
+ *   repeat: rho = rhat.r; (rho == 0: BREAKDOWN)
+ *           p = r on the first iteration, else beta = (rho / rho_prev) (alpha / omega),
+ *             p = r + beta (p - omega v);
+ *           v = A p; (rhat.v == 0: BREAKDOWN) alpha = rho / (rhat.v); s = r - alpha v;
+ *           when ||s|| <= rtol ||b||: x = x + alpha p, r = s, stop (converged);
+ *           t = A s; (t.t == 0: BREAKDOWN) omega = (t.s) / (t.t);
+ *           x = (x + alpha p) + omega s; r = s - omega t;
+ *           stop when ||r|| <= rtol ||b||; (omega == 0: BREAKDOWN); rho_prev = rho.
+ * One iteration = one pass of the loop (two products with A).  history[k] = ||r_k|| / ||b||.
+ * b == 0 gives x = 0 after 0 iterations; non-finite sums stop with NONFINITE.
+ */
+int orc_bicgstab(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const double *values,
+                 const double *b, const double *x0, double rtol, int64_t maxit, double *x, double *history,
+                 int64_t *iters, double *rel_res) {
+  const size_t sz = sizeof(double) * (size_t)(n > 0 ? n : 1);
+  double *r = (double *)malloc(sz), *rh = (double *)malloc(sz), *p = (double *)malloc(sz);
+  double *v = (double *)malloc(sz), *s = (double *)malloc(sz), *t = (double *)malloc(sz);
+  int status = ORC_NOT_CONVERGED;
+  *iters = 0;
+  *rel_res = 0.0;
+  double nb = sqrt(orc_dot(n, b, b));
+  if (x0) memcpy(x, x0, sizeof(double) * (size_t)n);
+  else memset(x, 0, sizeof(double) * (size_t)n);
+  if (!isfinite(nb)) { status = ORC_NONFINITE; goto done; }
+  if (nb == 0.0) {
+    for (int64_t i = 0; i < n; ++i) x[i] = 0.0;
+    if (history != NULL) history[0] = 0.0;
+    status = ORC_OK;
+    goto done;
+  }
+  if (x0) {
+    orc_spmv(n, row_ptr, col_idx, values, x, t);
+    ORC_PARALLEL_FOR
+    for (int64_t i = 0; i < n; ++i) r[i] = b[i] - t[i];
+  } else {
+    memcpy(r, b, sizeof(double) * (size_t)n);
+  }
+  memcpy(rh, r, sizeof(double) * (size_t)n);
+  double rr = orc_dot(n, r, r);
+  *rel_res = sqrt(rr) / nb;
+  if (history != NULL) history[0] = *rel_res;
+  if (!isfinite(rr)) { status = ORC_NONFINITE; goto done; }
+  if (sqrt(rr) <= rtol * nb) { status = ORC_OK; goto done; }
+  double rho_prev = 1.0, alpha = 1.0, omega = 1.0;
+  for (int64_t k = 0; k < maxit; ++k) {
+    const double rho = orc_dot(n, rh, r);
+    if (!isfinite(rho)) { status = ORC_NONFINITE; goto done; }
+    if (rho == 0.0) { status = ORC_BREAKDOWN; goto done; }
+    if (k == 0) {
+      memcpy(p, r, sizeof(double) * (size_t)n);
+    } else {
+      const double beta = (rho / rho_prev) * (alpha / omega);
+      ORC_PARALLEL_FOR
+      for (int64_t i = 0; i < n; ++i) p[i] = r[i] + beta * (p[i] - omega * v[i]);
+    }
+    orc_spmv(n, row_ptr, col_idx, values, p, v);
+    const double rv = orc_dot(n, rh, v);
+    if (!isfinite(rv)) { status = ORC_NONFINITE; goto done; }
+    if (rv == 0.0) { status = ORC_BREAKDOWN; goto done; }
+    alpha = rho / rv;
+    ORC_PARALLEL_FOR
+    for (int64_t i = 0; i < n; ++i) s[i] = r[i] - alpha * v[i];
+    const double ss = orc_dot(n, s, s);
+    if (!isfinite(ss)) { status = ORC_NONFINITE; goto done; }
+    if (sqrt(ss) <= rtol * nb) {
+      ORC_PARALLEL_FOR
+      for (int64_t i = 0; i < n; ++i) x[i] += alpha * p[i];
+      memcpy(r, s, sizeof(double) * (size_t)n);
+      *iters = k + 1;
+      *rel_res = sqrt(ss) / nb;
+      if (history != NULL) history[k + 1] = *rel_res;
+      status = ORC_OK;
+      goto done;
+    }
+    orc_spmv(n, row_ptr, col_idx, values, s, t);
+    const double tt = orc_dot(n, t, t);
+    const double ts = orc_dot(n, t, s);
+    if (!isfinite(tt) || !isfinite(ts)) { status = ORC_NONFINITE; goto done; }
+    if (tt == 0.0) { status = ORC_BREAKDOWN; goto done; }
+    omega = ts / tt;
+    ORC_PARALLEL_FOR
+    for (int64_t i = 0; i < n; ++i) x[i] = (x[i] + alpha * p[i]) + omega * s[i];
+    ORC_PARALLEL_FOR
+    for (int64_t i = 0; i < n; ++i) r[i] = s[i] - omega * t[i];
+    rr = orc_dot(n, r, r);
+    *iters = k + 1;
+    *rel_res = sqrt(rr) / nb;
+    if (history != NULL) history[k + 1] = *rel_res;
+    if (!isfinite(rr)) { status = ORC_NONFINITE; goto done; }
+    if (sqrt(rr) <= rtol * nb) { status = ORC_OK; goto done; }
+    if (omega == 0.0) { status = ORC_BREAKDOWN; goto done; }
+    rho_prev = rho;
+  }
+  status = ORC_NOT_CONVERGED;
+done:
+  free(r); free(rh); free(p); free(v); free(s); free(t);
+  return status;
+}
+
+/*
+ * Adjoint backward of x = A^{-1} b for a general A (Methodology, 2: A^T lambda = dL/dx, then
+ * grad_b = lambda and grad_values = -lambda_i x_j on A's pattern): lambda by the same BiCGStab,
+ * rtol and maxit on the explicit transpose A^T, from lambda = 0.  Returns that solve's status.
+ */
+int orc_bicgstab_adjoint(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const double *values,
+                         const double *x, const double *g, double rtol, int64_t maxit, double *grad_b,
+                         double *grad_values, int64_t *iters, double *rel_res) {
+  const int64_t nnz = row_ptr[n];
+  int64_t *trp = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  int32_t *tci = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nnz > 0 ? nnz : 1));
+  double *tv = (double *)malloc(sizeof(double) * (size_t)(nnz > 0 ? nnz : 1));
+  orc_transpose(n, row_ptr, col_idx, values, trp, tci, tv);
+  int st = orc_bicgstab(n, trp, tci, tv, g, NULL, rtol, maxit, grad_b, NULL, iters, rel_res);
+  orc_grad_values(n, row_ptr, col_idx, grad_b, x, grad_values);
+  free(trp); free(tci); free(tv);
+  return st;
+}

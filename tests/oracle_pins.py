@@ -37,7 +37,7 @@ from fractions import Fraction
 import numpy as np
 
 import oracle
-from workloads import poisson_5pt, diffusion_dirichlet, diffusion_interior, random_spd, config1
+from workloads import poisson_5pt, diffusion_dirichlet, diffusion_interior, random_spd, config1, convection_diffusion
 
 EPS = np.finfo(np.float64).eps
 
@@ -531,6 +531,111 @@ def pin_eig_grad_rayleigh_identity(lib):
     assert not oracle.eig_grad_values(A.row_ptr, A.col_idx, np.zeros((0, A.n)), lib=lib).any()
 
 
+# --------------------------------------------------------------------------- BiCGStab (general A)
+
+def _nonsym_dominant(n, seed):
+    """A random non-symmetric CSR matrix with every row's diagonal 1 + the row's absolute sum:
+    strictly diagonally dominant, so nonsingular, and far from symmetric."""
+    rp, ci, v = _random_csr(n, 6, seed)
+    D = _dense(rp, ci, v, n)
+    D += np.diag(np.abs(D).sum(axis=1) + 1.0 - np.diag(D))
+    rows, cols = np.nonzero(D)
+    order = np.lexsort((cols, rows))
+    rows, cols = rows[order], cols[order]
+    rp2 = np.concatenate([[0], np.cumsum(np.bincount(rows, minlength=n))]).astype(np.int64)
+    return rp2, cols.astype(np.int32), D[rows, cols]
+
+
+def pin_transpose_dense(lib):
+    rp, ci, v = _nonsym_dominant(37, 3)
+    trp, tci, tv = oracle.transpose(rp, ci, v, lib=lib)
+    assert np.array_equal(_dense(trp, tci, tv, 37), _dense(rp, ci, v, 37).T)
+    for c in range(37):  # each column's entries in increasing row order
+        assert np.all(np.diff(tci[trp[c]:trp[c + 1]]) > 0)
+
+
+def pin_bicgstab_vs_dense(lib):
+    cd = convection_diffusion(9, 0.6, -0.3)
+    cases = [(cd.row_ptr, cd.col_idx, cd.values, cd.n), (*_nonsym_dominant(60, 5), 60)]
+    for rp, ci, v, n in cases:
+        D = _dense(np.asarray(rp, dtype=np.int64), ci, v, n)
+        assert not np.allclose(D, D.T)
+        b = np.random.default_rng(n).standard_normal(n)
+        r = oracle.bicgstab(rp, ci, v, b, rtol=1e-13, maxit=1000, history=True, lib=lib)
+        xd = np.linalg.solve(D, b)
+        assert r["status"] == 0 and r["iters"] > 1
+        assert np.linalg.norm(r["x"] - xd) <= 1e-10 * np.linalg.norm(xd)
+        true_res = np.linalg.norm(b - D @ r["x"]) / np.linalg.norm(b)
+        assert true_res <= 1e-12 and r["rel_res"] <= 1e-13
+        assert r["history"][0] == 1.0 and abs(r["history"][-1] - r["rel_res"]) == 0.0
+
+
+def pin_bicgstab_equals_cg_on_spd(lib):
+    A = diffusion_dirichlet(8, np.random.default_rng(6).lognormal(0.0, 0.5, 2 * 8 * 9))
+    b = np.random.default_rng(7).standard_normal(A.n)
+    rb = oracle.bicgstab(A.row_ptr, A.col_idx, A.values, b, rtol=1e-13, lib=lib)
+    rc = oracle.cg(A.row_ptr, A.col_idx, A.values, b, rtol=1e-13, lib=lib)
+    assert rb["status"] == rc["status"] == 0
+    assert np.linalg.norm(rb["x"] - rc["x"]) <= 1e-10 * np.linalg.norm(rc["x"])
+
+
+def pin_bicgstab_adjoint_fd(lib):
+    # L = g . x(A, b) for a non-symmetric A: grad_b = lambda with A^T lambda = g (so g.x = lambda.b),
+    # grad_values = -lambda_i x_j, each against central differences of the dense solve
+    rp, ci, v = _nonsym_dominant(30, 8)
+    n = 30
+    D = _dense(rp, ci, v, n)
+    rng = np.random.default_rng(9)
+    b, g = rng.standard_normal(n), rng.standard_normal(n)
+    x = oracle.bicgstab(rp, ci, v, b, rtol=1e-14, lib=lib)["x"]
+    adj = oracle.bicgstab_adjoint(rp, ci, v, x, g, rtol=1e-14, lib=lib)
+    assert adj["status"] == 0
+    lam = adj["grad_b"]
+    assert abs(g @ x - lam @ b) <= 1e-12 * (np.abs(g) @ np.abs(x))
+    assert np.linalg.norm(D.T @ lam - g) <= 1e-12 * np.linalg.norm(g)
+    L = lambda DD, bb: g @ np.linalg.solve(DD, bb)  # noqa: E731
+    h = 1e-6
+    for k in (0, 11, 29):
+        e = np.zeros(n)
+        e[k] = h
+        assert abs((L(D, b + e) - L(D, b - e)) / (2 * h) - lam[k]) <= 1e-7
+    rows = np.repeat(np.arange(n), np.diff(rp))
+    for q in (0, len(ci) // 2, len(ci) - 1, int(np.argmax(np.abs(adj["grad_values"])))):
+        E = np.zeros((n, n))
+        E[rows[q], ci[q]] = h
+        fd = (L(D + E, b) - L(D - E, b)) / (2 * h)
+        assert abs(fd - adj["grad_values"][q]) <= 1e-7, (q, fd, adj["grad_values"][q])
+
+
+def pin_bicgstab_finite_termination(lib):
+    # A diagonalisable non-symmetric matrix with three distinct eigenvalues: BiCG's polynomial
+    # reaches the minimal polynomial at degree 3 and BiCGStab's residual carries it as a factor,
+    # so in exact arithmetic the third iteration gives r = 0 (here: below 1e-9 relative)
+    rng = np.random.default_rng(11)
+    n = 12
+    S = np.eye(n) + 0.3 * rng.standard_normal((n, n))
+    D = S @ np.diag(np.repeat([1.0, 2.0, 3.0], 4)) @ np.linalg.inv(S)
+    rp = np.arange(0, n * n + 1, n, dtype=np.int64)
+    ci = np.tile(np.arange(n, dtype=np.int32), n)
+    for seed in range(3):
+        b = np.random.default_rng(seed).standard_normal(n)
+        r = oracle.bicgstab(rp, ci, D.reshape(-1), b, rtol=1e-9, maxit=50, lib=lib)
+        assert r["status"] == 0 and r["iters"] == 3, r["iters"]
+
+
+def pin_bicgstab_status(lib):
+    cd = convection_diffusion(6)
+    rp, ci, v = cd.row_ptr, cd.col_idx, cd.values
+    r = oracle.bicgstab(rp, ci, v, np.zeros(cd.n), lib=lib)
+    assert r["status"] == 0 and r["iters"] == 0 and not r["x"].any()
+    b = np.random.default_rng(2).standard_normal(cd.n)
+    r = oracle.bicgstab(rp, ci, v, b, maxit=0, lib=lib)
+    assert r["status"] == 1 and r["iters"] == 0 and not r["x"].any()
+    xs = np.linalg.solve(_dense(np.asarray(rp, dtype=np.int64), ci, v, cd.n), b)
+    r = oracle.bicgstab(rp, ci, v, b, x0=xs, rtol=1e-8, lib=lib)  # started at the solution
+    assert r["status"] == 0 and r["iters"] == 0 and np.array_equal(r["x"], xs)
+
+
 ALL_PINS = [
     pin_spmv_dense, pin_spmv_exact_integers, pin_dot, pin_spmv_transpose_dense, pin_matvec_grad_values,
     pin_cg_vs_dense, pin_cg_several_chunks_true_residual, pin_cg_exact_rational, pin_finite_termination, pin_eigen_closed_form_and_bound,
@@ -539,4 +644,6 @@ ALL_PINS = [
     pin_adjoint_identity, pin_adjoint_fd, pin_adjoint_config1_loss, pin_adjoint_invariants,
     pin_adjoint_zero_gradient,
     pin_eig_smallest_closed_form, pin_eig_grad_fd, pin_eig_grad_weighted_fd, pin_eig_grad_rayleigh_identity,
+    pin_transpose_dense, pin_bicgstab_vs_dense, pin_bicgstab_equals_cg_on_spd, pin_bicgstab_adjoint_fd,
+    pin_bicgstab_finite_termination, pin_bicgstab_status,
 ]

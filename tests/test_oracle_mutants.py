@@ -52,6 +52,15 @@ MUTANTS = [
      "acc = acc + ws * (V[s * n + i] * V[s * n + i]);"),
     ("eig_grad_wrong_vector", "acc = acc + ws * (V[s * n + i] * V[s * n + j]);",
      "acc = acc + ws * (V[i] * V[j]);"),
+    ("transpose_keeps_column", "tr_col_idx[fill[c]] = (int32_t)i;", "tr_col_idx[fill[c]] = (int32_t)c;"),
+    ("bicg_beta_ratio_transposed", "const double beta = (rho / rho_prev) * (alpha / omega);",
+     "const double beta = (rho / rho_prev) * (omega / alpha);"),
+    ("bicg_direction_sign", "p[i] = r[i] + beta * (p[i] - omega * v[i]);", "p[i] = r[i] + beta * (p[i] + omega * v[i]);"),
+    ("bicg_s_sign", "s[i] = r[i] - alpha * v[i];", "s[i] = r[i] + alpha * v[i];"),
+    ("bicg_omega_transposed", "omega = ts / tt;", "omega = tt / ts;"),
+    ("bicg_x_drops_s", "x[i] = (x[i] + alpha * p[i]) + omega * s[i];", "x[i] = x[i] + alpha * p[i];"),
+    ("bicg_adjoint_untransposed", "int st = orc_bicgstab(n, trp, tci, tv, g, NULL,",
+     "int st = orc_bicgstab(n, row_ptr, col_idx, values, g, NULL,"),
 ]
 
 

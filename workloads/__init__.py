@@ -108,6 +108,19 @@ def poisson_5pt(m: int, rowptr64: bool = False) -> CSR:
     return CSR(m * m, rp, ci, vals)
 
 
+def convection_diffusion(m: int, cx: float = 0.4, cy: float = 0.25, rowptr64: bool = False) -> CSR:
+    """2D convection-diffusion on the five-point pattern, central differences: diagonal 4, west
+    -1 - cx, east -1 + cx, north (i - m) -1 - cy, south (i + m) -1 + cy, missing neighbours dropped.
+
+    Non-symmetric (for cx or cy nonzero) on a structurally symmetric pattern; for |cx|, |cy| < 1
+    every off-diagonal entry is negative and each row sums to at least 0, so it is a nonsingular
+    M-matrix.  The input of the non-symmetric (BiCGStab) path.
+    """
+    rp, ci, slot = _pattern_5pt(m, rowptr64)
+    off = np.array([-1.0 - cy, -1.0 - cx, 4.0, -1.0 + cx, -1.0 + cy])
+    return CSR(m * m, rp, ci, off[slot.astype(np.int64)])
+
+
 def _edge_values(m: int, slot: np.ndarray, rp: np.ndarray, kN, kW, kE, kS, shift: float) -> np.ndarray:
     """Fill CSR values from per-unknown edge conductivities (each an m x m array).
 
