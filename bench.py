@@ -14,7 +14,9 @@ GB/s of the fused CG iteration against the measured copy bandwidth, and the adjo
 
 NAME: poisson64, poisson1000 (default), diffusion128_batch64, diffusion4096_jacobi,
 poisson13000_int64 (short aliases config1 .. config5); eig_poisson: the smallest eigenpair
-of the 1M-DOF Poisson matrix by inverse iteration on the CG plus its eigenvalue gradient.
+of the 1M-DOF Poisson matrix by inverse iteration on the CG plus its eigenvalue gradient;
+convdiff1000_bicgstab: the 1M-DOF convection-diffusion operator (non-symmetric) by BiCGStab,
+forward and adjoint.
 
 With N > 1 the script runs under torch.distributed.run; every rank solves its own
 independent system of the same size (replicas, weak scaling).  --dist splits one system
@@ -52,6 +54,20 @@ def b_iter_batched(batch, n, nnz, s_v):
     return batch * (nnz * s_v + 9 * n * s_v) + nnz * 4 + (n + 1) * 4
 
 
+def b_iter_bicgstab(n, nnz, s_v, s_p):
+    """Algorithmic bytes of one BiCGStab iteration: two matrix streams (A p and A s) and 17 vector
+    passes (p and A p: r, p_prev, v_prev, rhat read, p, v written; s and A s: r, v read, s, t
+    written; update: x, p, s, t, rhat read, x, r written)."""
+    return 2 * (nnz * (s_v + 4) + (n + 1) * s_p) + 17 * n * s_v
+
+
+def flops_iter_bicgstab(n, nnz):
+    """fp64 flops of one BiCGStab iteration, 2 per multiply-add: the products A p and A s (2 nnz
+    each) and 12 multiply-adds per row (p 2, s 1, x 2, r 1, and the dot products rhat.v, s.s, t.s,
+    t.t, rhat.r, r.r)."""
+    return 4 * nnz + 24 * n
+
+
 def b_gradvalues(n, nnz, s_v, s_p):
     """One grad_values pass: col_idx read + gv write, row pointers, lambda and x reads."""
     return nnz * (s_v + 4) + (n + 1) * s_p + 2 * n * s_v
@@ -79,11 +95,12 @@ def fp64_peak_tflops(clocks=None):
 # the gradient and eigenvalue kernels and the other engines' files hold none of them.
 KERNEL_SOURCES = {
     "cluster": ("sla_common.cuh", "sla_onchip.cuh", "sla_cluster.cu"),
-    "resident": ("sla_common.cuh", "sla_onchip.cuh", "sla_resident.cu"),
+    "resident": ("sla_common.cuh", "sla_grid.cuh", "sla_onchip.cuh", "sla_resident.cu"),
     "streaming": ("sla_common.cuh", "sla_tma.cuh", "sla_stream.cuh"),
+    "bicgstab": ("sla_common.cuh", "sla_grid.cuh", "sla_bicgstab.cu"),
 }
 ENGINE_OF = {"config1": "cluster", "config3": "cluster", "config2": "resident", "config4": "streaming",
-             "config5": "streaming"}
+             "config5": "streaming", "convdiff1000_bicgstab": "bicgstab"}
 
 
 def csrc_sha256(engine):
@@ -592,7 +609,7 @@ def local_rank_of(dev):
     return dev.index if dev.index is not None else 0
 
 
-def run_e2e(args, w, dev, precond, sla, torch):
+def run_e2e(args, w, dev, precond, sla, torch, method="cg"):
     """The same step through the public autograd API, inputs from pinned host memory, results back."""
     h_rp = torch.from_numpy(w.A.row_ptr).pin_memory()
     h_ci = torch.from_numpy(w.A.col_idx).pin_memory()
@@ -616,7 +633,7 @@ def run_e2e(args, w, dev, precond, sla, torch):
         b = h_b.to(dev, non_blocking=True).requires_grad_(True)
         g = h_g.to(dev, non_blocking=True)
         A = sla.CSRMatrix(rp, ci, v)
-        xx = sla.solve(A, b, rtol=w.rtol, maxit=w.maxit, precond=precond)
+        xx = sla.solve(A, b, rtol=w.rtol, maxit=w.maxit, precond=precond, method=method)
         xx.backward(g)
         o_x.copy_(xx.detach(), non_blocking=True)
         o_gb.copy_(b.grad, non_blocking=True)
@@ -639,13 +656,17 @@ def run_e2e(args, w, dev, precond, sla, torch):
         total += e0.elapsed_time(e1) / 1e3
     peak_mem = torch.cuda.max_memory_allocated(dev) - mem_base
     # iterations of the autograd path equal those of the direct calls on the same data
-    _, fi, _ = sla.sla_cg_solve(sla.CSRMatrix(h_rp.to(dev), h_ci.to(dev), h_v.to(dev)), h_b.to(dev), rtol=w.rtol,
-                                maxit=w.maxit, precond=precond)
-    _, _, ai = sla.sla_cg_adjoint(sla.CSRMatrix(h_rp.to(dev), h_ci.to(dev), h_v.to(dev)),
-                                  o_x.to(dev), h_g.to(dev), rtol=w.rtol, maxit=w.maxit, precond=precond)
+    Ad = sla.CSRMatrix(h_rp.to(dev), h_ci.to(dev), h_v.to(dev))
+    if method == "bicgstab":
+        _, fi, _ = sla.sla_bicgstab_solve(Ad, h_b.to(dev), rtol=w.rtol, maxit=w.maxit)
+        _, _, ai = sla.sla_bicgstab_adjoint(Ad, o_x.to(dev), h_g.to(dev), rtol=w.rtol, maxit=w.maxit)
+    else:
+        _, fi, _ = sla.sla_cg_solve(Ad, h_b.to(dev), rtol=w.rtol, maxit=w.maxit, precond=precond)
+        _, _, ai = sla.sla_cg_adjoint(Ad, o_x.to(dev), h_g.to(dev), rtol=w.rtol, maxit=w.maxit, precond=precond)
     per_step_iters = fi.iters + ai.iters
     return {"value": per_step_iters * args.steps / total, "unit": "iters/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "api": "differentiable_sparse_iterative_gb300.solve + backward",
+            "d2h_bytes_per_step": d2h,
+            "api": f"differentiable_sparse_iterative_gb300.solve(method={method!r}) + backward",
             "peak_mem_mb": peak_mem / 2**20}
 
 
@@ -657,19 +678,34 @@ def cpu_baseline(w, iters):
     lib = oracle.load_parallel()
     cores = lib.orc_threads(0)
     g = w.g if w.g is not None else np.random.default_rng(1).standard_normal(w.A.n)
+    fwd, adj, what = _oracle_pair(w, lib)
     if iters <= 0:
         t0 = time.perf_counter()
-        oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=0.0, maxit=20, precond=w.precond, lib=lib)
+        fwd(20)
         per_it = (time.perf_counter() - t0) / 20
         iters = int(min(20000, max(100, 7.5 / max(per_it, 1e-6))))
     t0 = time.perf_counter()
-    f = oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=0.0, maxit=iters, precond=w.precond, lib=lib)
-    a = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, w.A.values, f["x"], g, rtol=0.0, maxit=iters,
-                          precond=w.precond, lib=lib)
+    f = fwd(iters)
+    a = adj(f["x"], g, iters)
     dt = time.perf_counter() - t0
     return {"value": (f["iters"] + a["iters"]) / dt, "unit": "iters/s", "cores": cores, "kind": "oracle",
-            "sample": f"{w.name}: {iters} forward + {iters} adjoint CG iterations (rtol 0) and one grad_values "
+            "sample": f"{w.name}: {iters} forward + {iters} adjoint {what} iterations (rtol 0) and one grad_values "
                       f"pass, {dt:.1f} s on {cores} host cores (the oracle's multi-core build)"}
+
+
+def _oracle_pair(w, lib):
+    """The oracle's forward solve and adjoint for a workload, as functions of the iteration count."""
+    import oracle
+    A = w.A
+    if w.meta.get("method") == "bicgstab":
+        return (lambda k: oracle.bicgstab(A.row_ptr, A.col_idx, A.values, w.b, rtol=0.0, maxit=k, lib=lib),
+                lambda x, g, k: oracle.bicgstab_adjoint(A.row_ptr, A.col_idx, A.values, x, g, rtol=0.0, maxit=k,
+                                                        lib=lib),
+                "BiCGStab")
+    return (lambda k: oracle.cg(A.row_ptr, A.col_idx, A.values, w.b, rtol=0.0, maxit=k, precond=w.precond, lib=lib),
+            lambda x, g, k: oracle.cg_adjoint(A.row_ptr, A.col_idx, A.values, x, g, rtol=0.0, maxit=k,
+                                              precond=w.precond, lib=lib),
+            "CG")
 
 
 EIG_METRIC = "smallest eigenpair (inverse iteration on CG) + eigenvalue gradient, 2D Poisson fp64: CG iters/sec"
@@ -790,6 +826,107 @@ def run_eig(args, rank, world, local_rank):
     return out
 
 
+BICG_METRIC = ("BiCGStab iters/sec (forward + adjoint) and HBM GB/s (% of roofline), 1M-DOF 2D convection-diffusion "
+               "fp64; adjoint ms")
+
+
+def run_bicgstab(args, rank, world, local_rank):
+    """Non-symmetric workload: BiCGStab forward solve and its adjoint (A^T lambda = g by the same solver
+    on the partner-permuted values, then grad_values) on the convection-diffusion operator."""
+    import torch
+    import differentiable_sparse_iterative_gb300 as sla
+    from workloads import config_by_name
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = config_by_name(args.config, **({"m": args.grid_m} if args.grid_m else {}))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    A = sla.CSRMatrix.from_numpy(w.A.row_ptr, w.A.col_idx, w.A.values, dev)
+    b, g = torch.from_numpy(w.b).to(dev), torch.from_numpy(w.g).to(dev)
+    n, nnz = w.A.n, w.A.nnz
+    s_v, s_p = 8, w.A.row_ptr.dtype.itemsize
+    ws = torch.empty(sla.sla_bicgstab_workspace_bytes(n, nnz, torch.float64), dtype=torch.uint8, device=dev)
+    x = torch.empty(n, dtype=torch.float64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        _, fi, _ = sla.sla_bicgstab_solve(A, b, rtol=w.rtol, maxit=w.maxit, x=x, workspace=ws)
+        e1.record(stream)
+        _, _, ai = sla.sla_bicgstab_adjoint(A, x, g, rtol=w.rtol, maxit=w.maxit, workspace=ws)
+        e2.record(stream)
+        return e0, e1, e2, fi, ai
+
+    for _ in range(args.warmup):
+        flush_l2(flush)
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = sla.sla_launch_count()
+    recs = []
+    with ClockSampler(local_rank) as clk:
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            flush_l2(flush)
+            recs.append(step())
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    launches = sla.sla_launch_count() - launches0
+    fwd_ms = [r[0].elapsed_time(r[1]) for r in recs]
+    adj_ms = [r[1].elapsed_time(r[2]) for r in recs]
+    iters_f = [r[3].iters for r in recs]
+    iters_a = [r[4].iters for r in recs]
+    status = {r[3].status for r in recs} | {r[4].status for r in recs}
+    tot_s = (sum(fwd_ms) + sum(adj_ms)) / 1e3
+    tot_s_all, tot_iters_all = aggregate_over_ranks(tot_s, sum(iters_f) + sum(iters_a), world, dev)
+    Bi = b_iter_bicgstab(n, nnz, s_v, s_p)
+    peak, peak_kind = measured_peaks()
+    fwd_s = sum(fwd_ms) / 1e3
+    achieved = Bi * sum(iters_f) / fwd_s / 1e9
+    tr = None if args.grid_m else profiled_traffic(args.config)
+    clocks = clk.summary()
+    flops_it = flops_iter_bicgstab(n, nnz)
+    fp64_peak = fp64_peak_tflops(clocks)
+    fp64_ach = flops_it * sum(iters_f) / fwd_s / 1e12
+    path = recs[-1][3].path
+    kernel_name = {"resident": "bi_resident (one persistent cooperative kernel per solve)",
+                   "host": "bi_dir_apply + bi_s_apply + bi_update (host loop)"}.get(path, path)
+    e2e = None if args.no_e2e else run_e2e(args, w, dev, 0, sla, torch, method="bicgstab")
+    out = {
+        "metric": BICG_METRIC, "value": tot_iters_all / tot_s_all, "unit": "iters/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.mean([a + c for a, c in zip(fwd_ms, adj_ms)]),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generators; no dataset on the pages)",
+        "config": {"workload": w.name, "n": n, "nnz": nnz, "rtol": w.rtol, "precond": "none",
+                   "step": "forward BiCGStab solve + adjoint (A^T lambda = g by BiCGStab; grad_b, grad_values)",
+                   "l2": "flushed between steps (256 MB write); within a solve the iterations reuse L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "iters_forward": statistics.mean(iters_f), "iters_adjoint": statistics.mean(iters_a),
+        "time_to_tolerance_ms": statistics.mean(fwd_ms), "adjoint_ms": statistics.mean(adj_ms),
+        "status": sorted(status), "path": path,
+        "fp64": {"achieved_tflops": fp64_ach, "peak_tflops": fp64_peak, "frac": fp64_ach / fp64_peak,
+                 "flops_per_iter": flops_it,
+                 "peak_basis": "152 SMs x 2 fp64 FMA/clock x 2 flops x max SM clock"},
+        "roofline": {"kernel": kernel_name,
+                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": peak_kind, "bytes_per_iter": Bi,
+                     "traffic": (tr["dram_bytes_per_iter"] if tr else None),
+                     "traffic_unit": "DRAM bytes per BiCGStab iteration (ncu dram__bytes_read + write)",
+                     "traffic_source": (tr.get("source") if tr else None)},
+        "gpu_launches": int(launches), "wall_s": wall, "clocks": clocks,
+    }
+    if e2e:
+        out["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline(w, args.cpu_iters)
+    return out
+
+
 def run_reference(args, rank, world):
     """The oracle arm: the fp64 CPU oracle timed on the host, on bounded samples of the workload."""
     from workloads import config_by_name
@@ -805,10 +942,11 @@ def run_reference(args, rank, world):
     g = w.g if w.g is not None else np.random.default_rng(1).standard_normal(w.A.n)
     k = args.ref_iters
 
+    fwd, adj, what = _oracle_pair(w, lib)
+
     def step():
-        f = oracle.cg(w.A.row_ptr, w.A.col_idx, w.A.values, w.b, rtol=0.0, maxit=k, precond=w.precond, lib=lib)
-        a = oracle.cg_adjoint(w.A.row_ptr, w.A.col_idx, w.A.values, f["x"], g, rtol=0.0, maxit=k,
-                              precond=w.precond, lib=lib)
+        f = fwd(k)
+        a = adj(f["x"], g, k)
         return f["iters"] + a["iters"]
 
     for _ in range(args.warmup):
@@ -817,9 +955,10 @@ def run_reference(args, rank, world):
     its = sum(step() for _ in range(args.steps))
     dt = time.perf_counter() - t0
     v = its / dt
-    sample = (f"{w.name}: each step {k} forward + {k} adjoint CG iterations (rtol 0) + grad_values, on {cores} "
-              f"host cores (the oracle's multi-core build)")
-    return {"impl": "reference", "metric": EIG_METRIC if eig else METRIC, "value": v, "unit": "iters/s",
+    sample = (f"{w.name}: each step {k} forward + {k} adjoint {what} iterations (rtol 0) + grad_values, on "
+              f"{cores} host cores (the oracle's multi-core build)")
+    metric = EIG_METRIC if eig else (BICG_METRIC if what == "BiCGStab" else METRIC)
+    return {"impl": "reference", "metric": metric, "value": v, "unit": "iters/s",
             "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -837,7 +976,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="poisson1000",
                     help="workload: poisson64, poisson1000 (default), diffusion128_batch64, diffusion4096_jacobi, "
-                         "poisson13000_int64 (or config1 .. config5)")
+                         "poisson13000_int64 (or config1 .. config5), eig_poisson, convdiff1000_bicgstab")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-iters", type=int, default=0, help="oracle sample size (0: about 15 s of host time)")
@@ -873,6 +1012,8 @@ def main():
         out = run_dist(args, rank, world, local_rank)
     elif args.config == "eig_poisson":
         out = run_eig(args, rank, world, local_rank)
+    elif args.config == "convdiff1000_bicgstab":
+        out = run_bicgstab(args, rank, world, local_rank)
     else:
         out = run_ours(args, rank, world, local_rank)
     if world > 1 or args.dist:

@@ -32,7 +32,8 @@ from ._abi import (SLA_OK, SLA_NOT_CONVERGED, SLA_BREAKDOWN, SLA_INVALID_ARG, SL
 __all__ = [
     "CSRMatrix", "SlaError", "CGInfo", "lib", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
     "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_validate_csr", "sla_cg_workspace_bytes",
-    "sla_status_string", "sla_launch_count", "sla_version", "CGSolve", "solve", "CGSolveBatched", "solve_batched", "sla_eigsh", "sla_eigsh_workspace_bytes", "Eigsh", "eigsh",
+    "sla_status_string", "sla_launch_count", "sla_version", "CGSolve", "solve", "CGSolveBatched", "solve_batched", "sla_bicgstab_workspace_bytes", "sla_bicgstab_solve",
+    "sla_bicgstab_adjoint", "BiCGStabSolve", "sla_eigsh", "sla_eigsh_workspace_bytes", "Eigsh", "eigsh",
     "matvec",
     "SLA_PRECOND_NONE", "SLA_PRECOND_JACOBI", "SLA_LOOP_AUTO", "SLA_LOOP_HOST", "SLA_LOOP_GRAPH",
     "SLA_LOOP_RESIDENT", "SLA_LOOP_CLUSTER", "SLA_OK", "SLA_NOT_CONVERGED", "SLA_BREAKDOWN", "SLA_INVALID_ARG",
@@ -103,9 +104,10 @@ class CSRMatrix:
 
     # The method-style interface of the pages' sparse tensor (A.solve(f), A.matvec(x), A.eigsh()),
     # each the differentiable module function of the same name.
-    def solve(self, b: torch.Tensor, rtol: float = 1e-8, maxit: int = 10000, precond: int = 0) -> torch.Tensor:
+    def solve(self, b: torch.Tensor, rtol: float = 1e-8, maxit: int = 10000, precond: int = 0,
+              method: str = "cg") -> torch.Tensor:
         """Differentiable x = A^{-1} b (see solve)."""
-        return solve(self, b, rtol=rtol, maxit=maxit, precond=precond)
+        return solve(self, b, rtol=rtol, maxit=maxit, precond=precond, method=method)
 
     def matvec(self, x: torch.Tensor) -> torch.Tensor:
         """Differentiable y = A x (see matvec)."""
@@ -372,10 +374,92 @@ class CGSolve(torch.autograd.Function):
         return None, None, (grad_v if need_v else None), (grad_b if need_b else None), None, None, None
 
 
+def sla_bicgstab_workspace_bytes(n: int, nnz: int, dtype: torch.dtype) -> int:
+    return lib().sla_bicgstab_workspace_bytes(int(n), int(nnz), _DT[dtype])
+
+
+def _bi_workspace(A: CSRMatrix, ws: Optional[torch.Tensor]) -> torch.Tensor:
+    need = sla_bicgstab_workspace_bytes(A.n, A.nnz, A.values.dtype)
+    if ws is not None and ws.numel() * ws.element_size() >= need:
+        return ws
+    return torch.empty(max(need, 256), dtype=torch.uint8, device=A.values.device)
+
+
+def sla_bicgstab_solve(A: CSRMatrix, b: torch.Tensor, x0: Optional[torch.Tensor] = None, rtol: float = 1e-8,
+                       maxit: int = 10000, x: Optional[torch.Tensor] = None, history: bool = False,
+                       workspace: Optional[torch.Tensor] = None, unroll: int = 0, loop: int = SLA_LOOP_AUTO):
+    """BiCGStab solve of a general A x = b.  Returns (x, CGInfo, history tensor or None).  loop:
+    SLA_LOOP_HOST runs the host-driven kernel loop, any other value the resident kernel (the host
+    loop when it cannot be launched)."""
+    dt, dev = A.values.dtype, A.values.device
+    if x is None:
+        x = torch.empty(A.n, dtype=dt, device=dev)
+    hist = torch.full((int(maxit) + 1,), float("nan"), dtype=torch.float64, device=dev) if history else None
+    ws = _bi_workspace(A, workspace)
+    info = _abi.sla_cg_info()
+    st = lib().sla_bicgstab_solve(ctypes.byref(_csr_struct(A)), _dev_ptr(b, dt, "b"), _dev_ptr(x0, dt, "x0"),
+                                  ctypes.byref(_opts(rtol, maxit, SLA_PRECOND_NONE, unroll, loop)), _dev_ptr(x, dt, "x"),
+                                  ctypes.byref(info), _dev_ptr(hist, torch.float64, "history"), ws.data_ptr(),
+                                  ws.numel() * ws.element_size(), _stream(dev))
+    _check(st, "sla_bicgstab_solve")
+    return x, _info(info), hist
+
+
+def sla_bicgstab_adjoint(A: CSRMatrix, x: torch.Tensor, g: torch.Tensor, rtol: float = 1e-8, maxit: int = 10000,
+                         want_grad_values: bool = True, workspace: Optional[torch.Tensor] = None, unroll: int = 0,
+                         loop: int = SLA_LOOP_AUTO):
+    """Adjoint of the BiCGStab solve: A^T lambda = g; returns (grad_b = lambda, grad_values or None, CGInfo).
+    A's pattern must be structurally symmetric (status SLA_BAD_CSR otherwise)."""
+    dt, dev = A.values.dtype, A.values.device
+    grad_b = torch.empty(A.n, dtype=dt, device=dev)
+    grad_values = torch.empty(A.nnz, dtype=dt, device=dev) if want_grad_values else None
+    ws = _bi_workspace(A, workspace)
+    info = _abi.sla_cg_info()
+    st = lib().sla_bicgstab_adjoint(ctypes.byref(_csr_struct(A)), _dev_ptr(x, dt, "x"), _dev_ptr(g, dt, "g"),
+                                    ctypes.byref(_opts(rtol, maxit, SLA_PRECOND_NONE, unroll, loop)),
+                                    _dev_ptr(grad_b, dt, "grad_b"), _dev_ptr(grad_values, dt, "grad_values"),
+                                    ctypes.byref(info), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(dev))
+    _check(st, "sla_bicgstab_adjoint")
+    return grad_b, grad_values, _info(info)
+
+
+class BiCGStabSolve(torch.autograd.Function):
+    """x = A^{-1} b for a general A by BiCGStab, with the adjoint backward A^T lambda = dL/dx by the
+    same solver: grad_values = -lambda_i x_j on the pattern, grad_b = lambda."""
+
+    @staticmethod
+    def forward(ctx, row_ptr, col_idx, values, b, rtol, maxit):
+        A = CSRMatrix(row_ptr, col_idx, values)
+        x, info, _ = sla_bicgstab_solve(A, b.contiguous(), rtol=rtol, maxit=maxit)
+        _raise_on_failure(info, "BiCGStabSolve.forward")
+        ctx.save_for_backward(row_ptr, col_idx, values, x)
+        ctx.opts = (rtol, maxit)
+        return x
+
+    @staticmethod
+    def backward(ctx, g):
+        row_ptr, col_idx, values, x = ctx.saved_tensors
+        rtol, maxit = ctx.opts
+        A = CSRMatrix(row_ptr, col_idx, values)
+        need_v, need_b = ctx.needs_input_grad[2], ctx.needs_input_grad[3]
+        grad_b, grad_v, info = sla_bicgstab_adjoint(A, x, g.contiguous(), rtol=rtol, maxit=maxit,
+                                                    want_grad_values=need_v)
+        _raise_on_failure(info, "BiCGStabSolve.backward")
+        return None, None, (grad_v if need_v else None), (grad_b if need_b else None), None, None
+
+
 def solve(A: CSRMatrix, b: torch.Tensor, rtol: float = 1e-8, maxit: int = 10000,
-          precond: int = SLA_PRECOND_NONE) -> torch.Tensor:
-    """Differentiable x = A^{-1} b (gradients flow to A.values and b)."""
-    return CGSolve.apply(A.row_ptr, A.col_idx, A.values, b, rtol, maxit, precond)
+          precond: int = SLA_PRECOND_NONE, method: str = "cg") -> torch.Tensor:
+    """Differentiable x = A^{-1} b (gradients flow to A.values and b).  method "cg": symmetric
+    positive definite A (optionally Jacobi preconditioned); "bicgstab": general A, unpreconditioned
+    (its backward needs a structurally symmetric pattern)."""
+    if method == "cg":
+        return CGSolve.apply(A.row_ptr, A.col_idx, A.values, b, rtol, maxit, precond)
+    if method == "bicgstab":
+        if precond != SLA_PRECOND_NONE:
+            raise ValueError("bicgstab takes no preconditioner")
+        return BiCGStabSolve.apply(A.row_ptr, A.col_idx, A.values, b, rtol, maxit)
+    raise ValueError(f"unknown method {method!r} (cg or bicgstab)")
 
 
 class CGSolveBatched(torch.autograd.Function):

@@ -22,7 +22,8 @@ EXPORTS = [
     "sla_eig_grad_values", "sla_set_spmv_variant", "sla_test_set_barrier_wait", "sla_dist_state_bytes",
     "sla_dist_cg_begin", "sla_dist_cg_start", "sla_dist_cg_spmv", "sla_dist_cg_update", "sla_dist_cg_direction",
     "sla_dist_pack", "sla_dist_cg_info", "sla_spmv_transpose", "sla_matvec_grad_values", "sla_dist_scatter_add",
-    "sla_graph_cache_stats", "sla_eigsh_workspace_bytes", "sla_eigsh",
+    "sla_graph_cache_stats", "sla_eigsh_workspace_bytes", "sla_eigsh", "sla_bicgstab_workspace_bytes",
+    "sla_bicgstab_solve", "sla_bicgstab_adjoint",
 ]
 SLA_SPMV_PLAIN, SLA_SPMV_TMA = 0, 1
 
@@ -78,6 +79,10 @@ def bind(lib):
     lib.sla_eig_workspace_bytes.restype = sz
     lib.sla_eig_smallest.argtypes = [C, P, ctypes.POINTER(sla_eig_opts), ctypes.POINTER(sla_eig_info), P, sz, P]
     lib.sla_eig_grad_values.argtypes = [C, i64, P, ctypes.POINTER(ctypes.c_double), P, P]
+    lib.sla_bicgstab_workspace_bytes.argtypes = [i64, i64, i32]
+    lib.sla_bicgstab_workspace_bytes.restype = sz
+    lib.sla_bicgstab_solve.argtypes = [C, P, P, O, P, I, P, P, sz, P]
+    lib.sla_bicgstab_adjoint.argtypes = [C, P, P, O, P, P, I, P, sz, P]
     lib.sla_eigsh_workspace_bytes.argtypes = [i64, i64, i32, i32]
     lib.sla_eigsh_workspace_bytes.restype = sz
     lib.sla_eigsh.argtypes = [C, i64, P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(sla_eig_opts),
@@ -101,7 +106,7 @@ def bind(lib):
                  "sla_dist_cg_direction", "sla_dist_pack", "sla_dist_cg_info",
                  "sla_set_spmv_variant", "sla_graph_cache_stats", "sla_test_set_barrier_wait", "sla_validate_csr", "sla_spmv", "sla_cg_solve", "sla_cg_adjoint", "sla_grad_values",
                  "sla_cg_solve_batched", "sla_cg_adjoint_batched", "sla_cg_solve_static", "sla_eig_smallest",
-                 "sla_eig_grad_values", "sla_eigsh"]:
+                 "sla_eig_grad_values", "sla_eigsh", "sla_bicgstab_solve", "sla_bicgstab_adjoint"]:
         getattr(lib, name).restype = i32
     return lib
 

@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsla.so")
-SOURCES = ["sla_cg.cu", "sla_api.cu", "sla_static.cu", "sla_resident.cu", "sla_cluster.cu", "sla_eig.cu", "sla_dist.cu"]
+SOURCES = ["sla_cg.cu", "sla_api.cu", "sla_static.cu", "sla_resident.cu", "sla_cluster.cu", "sla_eig.cu", "sla_dist.cu",
+           "sla_bicgstab.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--cudart", "shared", "-I" + INCLUDE, "-I" + CSRC]

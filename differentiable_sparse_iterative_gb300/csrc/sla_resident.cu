@@ -25,6 +25,7 @@
 
 #include "sla_common.cuh"
 #include "sla_host.h"
+#include "sla_grid.cuh"
 #include "sla_onchip.cuh"
 
 namespace sla {
@@ -32,132 +33,13 @@ namespace sla {
 namespace {
 
 constexpr int kResBlock = 1024;
+static_assert(kResBlock == kPublishBlock, "block sums go through block_publish");
 constexpr int kStage = 8;  // rows per thread whose global loads are issued together
 constexpr long long kSpinLimit = 1ll << 26;  // ~seconds of polling before a barrier gives up
 
 // Grid-barrier wait bounds of the next launches (sla_test_set_barrier_wait; normally 0 and kSpinLimit).
 std::atomic<unsigned> g_wait_extra{0u};
 std::atomic<long long> g_wait_limit{kSpinLimit};
-
-// Bounds of the grid barrier's wait.  `extra` arrivals are expected beyond the G blocks: 0 in
-// use; a test sets 1 (an arrival that never comes) with a short `limit` to drive the timeout path
-// on the GPU and check that the solve returns SLA_TIMEOUT with the context still usable.
-struct WaitCfg {
-  unsigned extra;
-  long long limit;
-};
-
-__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Split-phase grid barrier over a monotone arrival counter.  grid_arrive: after the block's
-// writes (ordered by __syncthreads), thread 0 adds 1 with release semantics (no round trip).
-// grid_wait: thread 0 polls with acquire loads until all G blocks of this epoch have arrived, then
-// the block synchronises.  The wait is bounded: on expiry (or when another block has timed out) it
-// raises the timeout flag and returns false.  Work that needs neither side may run in between.
-__device__ __forceinline__ void grid_arrive(unsigned *arrive, unsigned &epoch) {
-  __syncthreads();
-  ++epoch;
-  if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(arrive), "r"(1u) : "memory");
-}
-
-__device__ __forceinline__ bool grid_wait(unsigned *arrive, unsigned *timeout, unsigned G, unsigned epoch,
-                                          const WaitCfg &wc) {
-  __shared__ int s_ok;
-  if (threadIdx.x == 0) {
-    const unsigned target = epoch * G + wc.extra;
-    int ok = 1;
-    long long spins = 0;
-    while (ld_acquire(arrive) < target) {
-      if (*(volatile unsigned *)timeout) { ok = 0; break; }
-      if (++spins > wc.limit) {
-        atomicExch(timeout, 1u);
-        ok = 0;
-        break;
-      }
-      if (spins > 256) __nanosleep(32);
-    }
-    s_ok = ok;
-  }
-  __syncthreads();
-  return s_ok != 0;
-}
-
-__device__ __forceinline__ bool grid_barrier(unsigned *arrive, unsigned *timeout, unsigned G, unsigned &epoch,
-                                             const WaitCfg &wc) {
-  grid_arrive(arrive, epoch);
-  return grid_wait(arrive, timeout, G, epoch, wc);
-}
-
-// Deterministic all-reduce across the G blocks, in three steps so that the fp64 work on the
-// critical path is short:
-//  1. block_publish: every thread's value goes through shared memory; warps 0-3 (one per SM
-//     sub-partition) each add 256 of them (a depth-3 pairwise tree per lane, then a shuffle
-//     tree) and thread 0 adds the four warp sums; the block sum goes to part[j][bid];
-//  2. grid_barrier;
-//  3. warp_totals (warp 0 only): lane l adds part[j][l], part[j][l+32], ... in order, then a
-//     butterfly leaves the identical total in every lane.
-// Every block adds the same numbers in the same order, so all blocks hold bit-identical totals.
-template <int NV>
-__device__ __forceinline__ void block_publish(const double (&v)[NV], double *sbuf, double *part) {
-  static_assert(kResBlock == 1024, "four warps of 256 values each");
-  __shared__ double s4[2][4];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-#pragma unroll
-  for (int j0 = 0; j0 < NV; j0 += 2) {
-    const int nj = (NV - j0) < 2 ? (NV - j0) : 2;
-#pragma unroll
-    for (int j = 0; j < nj; ++j) sbuf[j * kResBlock + tid] = v[j0 + j];
-    __syncthreads();
-    if (warp < 4) {
-#pragma unroll
-      for (int j = 0; j < nj; ++j) {
-        const double *b = sbuf + j * kResBlock + warp * 256 + lane;
-        const double a0 = b[0] + b[32], a1 = b[64] + b[96], a2 = b[128] + b[160], a3 = b[192] + b[224];
-        const double t = warp_sum((a0 + a1) + (a2 + a3));
-        if (lane == 0) s4[j][warp] = t;
-      }
-    }
-    __syncthreads();
-    if (tid == 0) {
-#pragma unroll
-      for (int j = 0; j < nj; ++j)
-        part[(size_t)(j0 + j) * kMaxBlocksPerSystem + blockIdx.x] = (s4[j][0] + s4[j][1]) + (s4[j][2] + s4[j][3]);
-    }
-  }
-}
-
-__device__ __forceinline__ double warp_allsum(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Warp 0 only: the grid totals, identical in every lane.
-template <int NV>
-__device__ __forceinline__ void warp_totals(const double *part, int G, double (&tot)[NV]) {
-  const int lane = threadIdx.x & 31;
-  // all loads of a 256-block slab first (one L2 round trip instead of one per 32 blocks), then a
-  // fixed pairwise tree per lane: the order depends only on G, so every block gets the same bits
-#pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    const double *pj = part + (size_t)j * kMaxBlocksPerSystem;
-    double t = 0.0;
-    for (int b0 = 0; b0 < G; b0 += 256) {
-      double v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int b = b0 + lane + 32 * u;
-        v[u] = b < G ? __ldcg(pj + b) : 0.0;
-      }
-      t += ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
-    }
-    tot[j] = warp_allsum(t);
-  }
-}
 
 // p_k at a column outside the block's chunk, from the published r_k and p_{k-1}.
 template <typename V, bool JAC>
@@ -576,7 +458,7 @@ sla_status run_resident(Prob<V, I> P, cudaStream_t stream, sla_cg_info *info) {
   if (e == cudaSuccess && P.halo)
     e = cudaMemsetAsync(P.halo, 0, sizeof(uint32_t) * (size_t)((P.n + 31) / 32), stream);
   if (e != cudaSuccess) return fail(e);
-  WaitCfg wc{g_wait_extra.load(), g_wait_limit.load()};
+  WaitCfg wc = launch_wait_cfg();
   void *args[] = {(void *)&P, (void *)&cap, (void *)&wc};
   e = cudaLaunchCooperativeKernel(fn, dim3(G), dim3(kResBlock), args, smem, stream);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
@@ -611,6 +493,10 @@ extern "C" SLA_API int sla_phase_cycles(unsigned long long *host, int nblocks) {
   return (int)cudaMemcpyFromSymbol(host, sla::g_phase_cycles, sizeof(unsigned long long) * 8 * (size_t)nblocks);
 }
 #endif
+
+namespace sla {
+WaitCfg launch_wait_cfg() { return WaitCfg{g_wait_extra.load(), g_wait_limit.load()}; }
+}  // namespace sla
 
 extern "C" sla_status sla_test_set_barrier_wait(uint32_t extra, int64_t spin_limit) {
   if (extra > 1u || spin_limit < 0 || spin_limit > sla::kSpinLimit) return SLA_INVALID_ARG;

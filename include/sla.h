@@ -255,6 +255,50 @@ SLA_API sla_status sla_cg_adjoint_batched(const sla_csr *pattern, int64_t batch,
                                   const void *g, const sla_cg_opts *opts, void *grad_b, void *grad_values,
                                   sla_cg_info *info, void *workspace, size_t ws_bytes, void *stream);
 
+/* ---------------------------------------------------------------- general (non-symmetric) A */
+
+/*
+ * Bytes of device workspace sla_bicgstab_solve and sla_bicgstab_adjoint need (0 for invalid
+ * arguments): eight n-vectors (r, rhat, two p, two v, s, t), the adjoint's transposed values (nnz)
+ * and the reductions' scratch.
+ */
+SLA_API size_t sla_bicgstab_workspace_bytes(int64_t n, int64_t nnz, int32_t dtype);
+
+/*
+ * BiCGStab solve of a general A x = b (TS Methodology 1: BiCGStab is among the solvers behind
+ * .solve; the iteration is the textbook one, van der Vorst, SIAM J. Sci. Stat. Comput. 13, 1992,
+ * unpreconditioned): r = b - A x0, rhat = r; per iteration rho = rhat.r, p = r (first) or
+ * r + beta (p - omega v) with beta = (rho / rho_prev)(alpha / omega), v = A p,
+ * alpha = rho / rhat.v, s = r - alpha v (stop with x += alpha p when ||s|| <= rtol ||b||), t = A s,
+ * omega = t.s / t.t, x += alpha p + omega s, r = s - omega t, stop when ||r|| <= rtol ||b||.
+ * Zero rhat.v, t.t, omega or rhat.r is SLA_BREAKDOWN (x left at the last iterate).
+ * Arguments as for sla_cg_solve, except: opts->precond must be SLA_PRECOND_NONE (else
+ * SLA_INVALID_ARG), and opts->loop picks one of two engines.  SLA_LOOP_HOST: three kernels per
+ * iteration, the host enqueueing opts->unroll iterations (default 8) between two reads of the
+ * device state.  Any other value: the whole solve in one cooperative kernel (one block per SM,
+ * three grid barriers per iteration, each wait bounded: an expired wait ends the solve with
+ * info->status SLA_TIMEOUT), or the host loop when the cooperative launch cannot be made here.
+ * info->path reports the engine that ran (SLA_LOOP_RESIDENT or SLA_LOOP_HOST); info->iters
+ * counts iterations (two products with A each).  Dot products are fp64 sums in a fixed order,
+ * so an engine gives the same bits run to run.
+ */
+SLA_API sla_status sla_bicgstab_solve(const sla_csr *A, const void *b, const void *x0, const sla_cg_opts *opts,
+                                      void *x, sla_cg_info *info, double *history, void *workspace,
+                                      size_t ws_bytes, void *stream);
+
+/*
+ * Adjoint backward of x = A^{-1} b for a general A (TS Methodology 2): lambda solves
+ * A^T lambda = g by the same BiCGStab (same rtol, maxit) from lambda = 0, written into grad_b;
+ * then grad_values[e] = -lambda[row(e)] * x[col(e)] on A's pattern (NULL: skipped).  A^T is formed
+ * on A's pattern, every value taken from its partner entry (j, i): the pattern must be
+ * structurally symmetric (a stored (j, i) for every stored (i, j), columns sorted within rows),
+ * else info->status is SLA_BAD_CSR and nothing is solved.  Arguments and workspace as for
+ * sla_bicgstab_solve; x, g, grad_b device n-vectors, grad_values device nnz entries.
+ */
+SLA_API sla_status sla_bicgstab_adjoint(const sla_csr *A, const void *x, const void *g, const sla_cg_opts *opts,
+                                        void *grad_b, void *grad_values, sla_cg_info *info, void *workspace,
+                                        size_t ws_bytes, void *stream);
+
 /* ---------------------------------------------------------------- eigenvalue problems */
 
 /* Options of sla_eig_smallest. */

@@ -77,4 +77,12 @@ def test_traffic_hash_covers_each_engines_kernel_sources_only(monkeypatch, tmp_p
             assert (bench.csrc_sha256(engine) != h0) == (name in files), (engine, name)
             (csrc / name).write_text(name)
         assert bench.csrc_sha256(engine) == h0
-    assert set(bench.ENGINE_OF) == {"config1", "config2", "config3", "config4", "config5"}
+    assert set(bench.ENGINE_OF) == {"config1", "config2", "config3", "config4", "config5", "convdiff1000_bicgstab"}
+
+
+def test_bicgstab_iteration_bytes():
+    # two matrix streams (values + col_idx, row pointers) and 17 vector passes of 8 bytes per row
+    n, nnz = 1_000_000, 4_996_000
+    assert bench.b_iter_bicgstab(n, nnz, 8, 4) == 2 * (nnz * 12 + (n + 1) * 4) + 17 * n * 8
+    # 2 nnz flops per product, two products, and 12 multiply-adds per row
+    assert bench.flops_iter_bicgstab(n, nnz) == 2 * 2 * nnz + 2 * 12 * n

@@ -341,6 +341,16 @@ def config5(m: int = 13000, iters: int = 1000) -> Workload:
     return Workload(f"poisson{m}_cg_fixed{iters}", A, b, g, 0.0, iters, meta={"m": m})
 
 
+def convdiff_bicgstab(m: int = 1000) -> Workload:
+    """2D convection-diffusion m=1000 (n=1e6, nnz=4,996,000; cx = 0.4, cy = 0.25, central
+    differences), b ~ N(0,1) seed 0, g ~ N(0,1) seed 1; BiCGStab rtol 1e-8 forward and adjoint."""
+    A = convection_diffusion(m)
+    n = m * m
+    b = np.random.default_rng(0).standard_normal(n)
+    g = np.random.default_rng(1).standard_normal(n)
+    return Workload(f"convdiff{m}_bicgstab_rtol1e-8", A, b, g, 1e-8, 100000, meta={"m": m, "method": "bicgstab"})
+
+
 def small_poisson(m: int, seed: int = 0, rowptr64: bool = False) -> Workload:
     """Small Poisson problem with b, g ~ N(0,1) (parity cases spanning several tiles)."""
     A = poisson_5pt(m, rowptr64)
@@ -366,4 +376,4 @@ def canonical_name(name: str) -> str:
 
 def config_by_name(name: str, **kw) -> Workload:
     return {"config1": config1, "config2": config2, "config3": config3, "config4": config4,
-            "config5": config5}[canonical_name(name)](**kw)
+            "config5": config5, "convdiff1000_bicgstab": convdiff_bicgstab}[canonical_name(name)](**kw)
