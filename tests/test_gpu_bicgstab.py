@@ -113,6 +113,15 @@ def test_bicgstab_engines_agree_at_1m_rows():
         res = np.linalg.norm(b - M @ xx.cpu().numpy()) / np.linalg.norm(b)
         assert res <= 1.05e-8 and abs(res - info.rel_res) <= 1e-3 * 1e-8, (res, info)
     assert rel(xr.cpu().numpy(), xh.cpu().numpy()) <= 1e-6
+    # the adjoint at the same size: A^T lambda = g to tolerance (true residual), and grad_values is
+    # -lambda_i x_j entry by entry (one rounded product: exact)
+    g = np.random.default_rng(1).standard_normal(A.n)
+    gb, gv, ai = sla.sla_bicgstab_adjoint(dA, xr, t(g), rtol=1e-8)
+    assert ai.status == 0 and ai.path == "resident"
+    lam, x_np = gb.cpu().numpy(), xr.cpu().numpy()
+    assert np.linalg.norm(g - M.T @ lam) / np.linalg.norm(g) <= 1.05e-8
+    rows = np.repeat(np.arange(A.n), np.diff(A.row_ptr.astype(np.int64)))
+    assert np.array_equal(gv.cpu().numpy(), -(lam[rows] * x_np[A.col_idx]))
 
 
 def test_bicgstab_resident_barrier_timeout_returns_status():
@@ -166,22 +175,24 @@ def test_bicgstab_float32():
     assert rel(x.cpu().numpy(), ref["x"]) <= TOL_F32
 
 
-def test_bicgstab_status_cases():
+@pytest.mark.parametrize("loop", list(LOOPS))
+def test_bicgstab_status_cases(loop):
+    lp = LOOPS[loop]
     A = convection_diffusion(12)
     dA = to_dev(A)
     # b = 0: x = 0 after no iteration, whatever x0
-    x, info, _ = sla.sla_bicgstab_solve(dA, t(np.zeros(A.n)), x0=t(np.ones(A.n)))
+    x, info, _ = sla.sla_bicgstab_solve(dA, t(np.zeros(A.n)), x0=t(np.ones(A.n)), loop=lp)
     assert info.status == 0 and info.iters == 0 and not x.cpu().numpy().any()
     b = np.random.default_rng(1).standard_normal(A.n)
     # maxit = 0: not converged, x = x0 (0)
-    x, info, _ = sla.sla_bicgstab_solve(dA, t(b), maxit=0)
+    x, info, _ = sla.sla_bicgstab_solve(dA, t(b), maxit=0, loop=lp)
     assert info.status == sla.SLA_NOT_CONVERGED and info.iters == 0 and not x.cpu().numpy().any()
     # started at the oracle's solution: converged before the first iteration
     xs = oracle.bicgstab(A.row_ptr, A.col_idx, A.values, b, rtol=1e-14)["x"]
-    x, info, _ = sla.sla_bicgstab_solve(dA, t(b), x0=t(xs), rtol=1e-8)
+    x, info, _ = sla.sla_bicgstab_solve(dA, t(b), x0=t(xs), rtol=1e-8, loop=lp)
     assert info.status == 0 and info.iters == 0 and np.array_equal(x.cpu().numpy(), xs)
     # fixed iteration count, against the oracle's
-    x, info, _ = sla.sla_bicgstab_solve(dA, t(b), rtol=1e-30, maxit=7)
+    x, info, _ = sla.sla_bicgstab_solve(dA, t(b), rtol=1e-30, maxit=7, loop=lp)
     r = oracle.bicgstab(A.row_ptr, A.col_idx, A.values, b, rtol=1e-30, maxit=7)
     assert info.status == r["status"] == sla.SLA_NOT_CONVERGED and info.iters == r["iters"] == 7
     assert rel(x.cpu().numpy(), r["x"]) <= 1e-12
