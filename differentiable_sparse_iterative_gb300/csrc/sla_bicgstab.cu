@@ -479,17 +479,30 @@ constexpr int kBrVec = 4;   // rows per thread whose loads the p and s passes is
 constexpr int kBrProd = 2;  // the product passes
 constexpr int kBrUpd = 2;   // the update (five vectors per row)
 
-// Publish the block sums, barrier, grid totals (valid in warp 0).  False when the barrier's wait
-// expired; the solve then ends.
+// An all-reduce in two halves, so that a block can do work that needs neither side while the
+// other blocks arrive: publish the block sums and arrive; then wait and form the grid totals
+// (valid in warp 0).  The wait returns false when it expired; the solve then ends.
+template <int NV>
+__device__ __forceinline__ void br_publish_arrive(const double (&v)[NV], double *sbuf, double *part, int slot,
+                                                  unsigned *arrive, unsigned &epoch) {
+  block_publish<NV>(v, sbuf, part + (size_t)slot * kMaxBlocksPerSystem);
+  grid_arrive(arrive, epoch);
+}
+
+template <int NV>
+__device__ __forceinline__ bool br_wait_totals(const double *part, int slot, unsigned *arrive, unsigned *timeout,
+                                               unsigned epoch, const WaitCfg &wc, double (&tot)[NV]) {
+  if (!grid_wait(arrive, timeout, gridDim.x, epoch, wc)) return false;
+  if (threadIdx.x < 32) warp_totals<NV>(part + (size_t)slot * kMaxBlocksPerSystem, (int)gridDim.x, tot);
+  return true;
+}
+
 template <int NV>
 __device__ __forceinline__ bool br_allreduce(const double (&v)[NV], double *sbuf, double *part, int slot,
                                              unsigned *arrive, unsigned *timeout, unsigned &epoch, const WaitCfg &wc,
                                              double (&tot)[NV]) {
-  double *rows = part + (size_t)slot * kMaxBlocksPerSystem;
-  block_publish<NV>(v, sbuf, rows);
-  if (!grid_barrier(arrive, timeout, gridDim.x, epoch, wc)) return false;
-  if (threadIdx.x < 32) warp_totals<NV>(rows, (int)gridDim.x, tot);
-  return true;
+  br_publish_arrive<NV>(v, sbuf, part, slot, arrive, epoch);
+  return br_wait_totals<NV>(part, slot, arrive, timeout, epoch, wc, tot);
 }
 
 template <typename I>
@@ -602,21 +615,21 @@ __global__ void __launch_bounds__(kBrBlock, 1) bi_resident(BiProb<V, I> P, WaitC
     V *__restrict__ pn = P.p[par];
     V *__restrict__ vn = P.v[par];
 
-    // p on the chunk's rows
+    // p on the chunk's rows: r (first iteration) or r + beta w, with w = p_prev - omega v_prev
+    // already in pn from the previous iteration's last wait (the same two roundings as p_at)
     for (int64_t g0 = c0 + threadIdx.x; g0 < c1; g0 += (int64_t)kBrVec * kBrBlock) {
-      V rv[kBrVec], pv[kBrVec], vv[kBrVec];
+      V rv[kBrVec], wv[kBrVec];
 #pragma unroll
       for (int u = 0; u < kBrVec; ++u) {
         const int64_t i = g0 + (int64_t)u * kBrBlock;
         const bool in = i < c1;
         rv[u] = in ? r[i] : V(0);
-        pv[u] = (in && !first) ? po[i] : V(0);
-        vv[u] = (in && !first) ? vo[i] : V(0);
+        wv[u] = (in && !first) ? pn[i] : V(0);
       }
 #pragma unroll
       for (int u = 0; u < kBrVec; ++u) {
         const int64_t i = g0 + (int64_t)u * kBrBlock;
-        if (i < c1) pn[i] = p_at<V>(rv[u], pv[u], vv[u], first, vbeta, vomega);
+        if (i < c1) pn[i] = first ? rv[u] : fmav<V>(vbeta, wv[u], rv[u]);
       }
     }
     __syncthreads();
@@ -732,7 +745,27 @@ __global__ void __launch_bounds__(kBrBlock, 1) bi_resident(BiProb<V, I> P, WaitC
       }
     }
     double t2[3];
-    const bool ok2 = br_allreduce<3>(a2, sbuf, P.part, 3, arrive, timeout, epoch, wc, t2);
+    br_publish_arrive<3>(a2, sbuf, P.part, 3, arrive, epoch);
+    // while the other blocks arrive: xh = x + alpha p, the part of the x update that does not need
+    // omega, into v_prev's buffer (every block read v_prev before the last barrier); x itself
+    // stays the last iterate until the update
+    V *__restrict__ xh = P.v[par ^ 1];
+    for (int64_t g0 = c0 + threadIdx.x; g0 < c1; g0 += (int64_t)kBrVec * kBrBlock) {
+      V xv[kBrVec], pv[kBrVec];
+#pragma unroll
+      for (int u = 0; u < kBrVec; ++u) {
+        const int64_t i = g0 + (int64_t)u * kBrBlock;
+        const bool in = i < c1;
+        xv[u] = in ? x[i] : V(0);
+        pv[u] = in ? pn[i] : V(0);
+      }
+#pragma unroll
+      for (int u = 0; u < kBrVec; ++u) {
+        const int64_t i = g0 + (int64_t)u * kBrBlock;
+        if (i < c1) xh[i] = fmav<V>(valpha, pv[u], xv[u]);
+      }
+    }
+    const bool ok2 = br_wait_totals<3>(P.part, 3, arrive, timeout, epoch, wc, t2);
     if (lead) {
       S.go = 0;
       S.exit_s = 0;
@@ -758,16 +791,15 @@ __global__ void __launch_bounds__(kBrBlock, 1) bi_resident(BiProb<V, I> P, WaitC
     if (!S.go && !exit_s) break;
     const V vom = exit_s ? V(0) : (V)S.omega;
 
-    // x += alpha p + omega s, r = s - omega t (x += alpha p, r = s after the early test); rhat.r, r.r
+    // x = xh + omega s, r = s - omega t (x = xh, r = s after the early test); rhat.r, r.r
     double a3[2] = {0.0, 0.0};
     for (int64_t g0 = c0 + threadIdx.x; g0 < c1; g0 += (int64_t)kBrUpd * kBrBlock) {
-      V xv[kBrUpd], pv[kBrUpd], sv[kBrUpd], tv[kBrUpd], hv[kBrUpd];
+      V xv[kBrUpd], sv[kBrUpd], tv[kBrUpd], hv[kBrUpd];
 #pragma unroll
       for (int u = 0; u < kBrUpd; ++u) {
         const int64_t i = g0 + (int64_t)u * kBrBlock;
         const bool in = i < c1;
-        xv[u] = in ? x[i] : V(0);
-        pv[u] = in ? pn[i] : V(0);
+        xv[u] = in ? xh[i] : V(0);
         sv[u] = in ? sg[i] : V(0);
         tv[u] = (in && !exit_s) ? tg[i] : V(0);
         hv[u] = in ? rh[i] : V(0);
@@ -778,10 +810,10 @@ __global__ void __launch_bounds__(kBrBlock, 1) bi_resident(BiProb<V, I> P, WaitC
         if (i < c1) {
           V ri;
           if (exit_s) {
-            x[i] = fmav<V>(valpha, pv[u], xv[u]);
+            x[i] = xv[u];
             ri = sv[u];
           } else {
-            x[i] = fmav<V>(vom, sv[u], fmav<V>(valpha, pv[u], xv[u]));
+            x[i] = fmav<V>(vom, sv[u], xv[u]);
             ri = fmav<V>(-vom, tv[u], sv[u]);
           }
           r[i] = ri;
@@ -799,7 +831,29 @@ __global__ void __launch_bounds__(kBrBlock, 1) bi_resident(BiProb<V, I> P, WaitC
       break;
     }
     double t3[2];
-    const bool ok3 = br_allreduce<2>(a3, sbuf, P.part, 6, arrive, timeout, epoch, wc, t3);
+    br_publish_arrive<2>(a3, sbuf, P.part, 6, arrive, epoch);
+    // while the other blocks arrive: w = p - omega v, the part of the next p that does not need
+    // beta, into p_prev's buffer (the next iteration's p; every block read p_prev before the first
+    // barrier of this iteration).  Wasted if the solve stops here.
+    {
+      V *__restrict__ wn = P.p[par ^ 1];
+      for (int64_t g0 = c0 + threadIdx.x; g0 < c1; g0 += (int64_t)kBrVec * kBrBlock) {
+        V pv[kBrVec], vv[kBrVec];
+#pragma unroll
+        for (int u = 0; u < kBrVec; ++u) {
+          const int64_t i = g0 + (int64_t)u * kBrBlock;
+          const bool in = i < c1;
+          pv[u] = in ? pn[i] : V(0);
+          vv[u] = in ? vn[i] : V(0);
+        }
+#pragma unroll
+        for (int u = 0; u < kBrVec; ++u) {
+          const int64_t i = g0 + (int64_t)u * kBrBlock;
+          if (i < c1) wn[i] = fmav<V>(-vom, vv[u], pv[u]);
+        }
+      }
+    }
+    const bool ok3 = br_wait_totals<2>(P.part, 6, arrive, timeout, epoch, wc, t3);
     if (lead) {
       S.go = 0;
       if (ok3) {
