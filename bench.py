@@ -689,8 +689,9 @@ def cpu_baseline(w, iters):
     a = adj(f["x"], g, iters)
     dt = time.perf_counter() - t0
     return {"value": (f["iters"] + a["iters"]) / dt, "unit": "iters/s", "cores": cores, "kind": "oracle",
-            "sample": f"{w.name}: {iters} forward + {iters} adjoint {what} iterations (rtol 0) and one grad_values "
-                      f"pass, {dt:.1f} s on {cores} host cores (the oracle's multi-core build)"}
+            "sample": f"{w.name}: {f['iters']} forward + {a['iters']} adjoint {what} iterations (rtol 0, at most "
+                      f"{iters} each) and one grad_values pass, {dt:.1f} s on {cores} host cores (the oracle's "
+                      f"multi-core build)"}
 
 
 def _oracle_pair(w, lib):
@@ -955,7 +956,8 @@ def run_reference(args, rank, world):
     its = sum(step() for _ in range(args.steps))
     dt = time.perf_counter() - t0
     v = its / dt
-    sample = (f"{w.name}: each step {k} forward + {k} adjoint {what} iterations (rtol 0) + grad_values, on "
+    sample = (f"{w.name}: each step at most {k} forward + {k} adjoint {what} iterations (rtol 0; the value counts "
+              f"those run) + grad_values, on "
               f"{cores} host cores (the oracle's multi-core build)")
     metric = EIG_METRIC if eig else (BICG_METRIC if what == "BiCGStab" else METRIC)
     return {"impl": "reference", "metric": metric, "value": v, "unit": "iters/s",
