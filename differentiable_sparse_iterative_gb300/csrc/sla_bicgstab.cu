@@ -11,9 +11,11 @@
 //   t = A s; omega = t.s / t.t; x += alpha p + omega s; r = s - omega t; stop when
 //   ||r|| <= rtol ||b||.  Zero rhat.v, t.t, omega or rho is a breakdown.
 //
-// GB300 design.  An iteration is three kernels.  bi_dir_apply forms the direction p and v = A p
-// with rhat.v; bi_s_apply forms s = r - alpha v and t = A s with s.s, t.s and t.t; bi_update the x
-// and r updates with rhat.r and r.r.  The two product kernels walk the rows in tiles dealt to the
+// GB300 design.  Two engines.  The default runs the whole solve in one cooperative kernel
+// (bi_resident, described with it below).  The host loop, for profiling and for GPUs where the
+// cooperative launch is refused, runs three kernels per iteration: bi_dir_apply forms the
+// direction p and v = A p with rhat.v; bi_s_apply forms s = r - alpha v and t = A s with s.s, t.s
+// and t.t; bi_update the x and r updates with rhat.r and r.r.  The two product kernels walk the rows in tiles dealt to the
 // blocks round-robin (a band sweep: a stencil's off-tile neighbours were just read by the blocks
 // beside it and hit in L2); a tile's own p (or s) stays in shared memory for the product, and a
 // neighbour's is recomputed from r, p_prev and v_prev (or r and v) by the same expression, so
@@ -473,7 +475,10 @@ __global__ void __launch_bounds__(kBlock, kBiUpdBlocks) bi_update(BiProb<V, I> P
 // order, so all blocks hold bit-identical scalars and take the same branch.  In the products a
 // column in the block's chunk reads the block's own p (or s); a column outside it recomputes
 // p = r + beta (p_prev - omega v_prev) (or s = r - alpha v) from values the barrier published, read
-// through L2 (another SM may hold a stale copy of them in its L1).  Every barrier wait is bounded.
+// through L2 (another SM may hold a stale copy of them in its L1).  The barriers before omega and
+// beta are split: while the other blocks arrive, a block forms x + alpha p and p - omega v, the
+// parts of the next updates that need no pending scalar (each into a buffer free by then, with the
+// roundings of the fused expressions).  Every barrier wait is bounded.
 constexpr int kBrBlock = 1024;
 constexpr int kBrVec = 4;   // rows per thread whose loads the p and s passes issue together
 constexpr int kBrProd = 2;  // the product passes
