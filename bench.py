@@ -848,13 +848,15 @@ def run_bicgstab(args, rank, world, local_rank):
     ws = torch.empty(sla.sla_bicgstab_workspace_bytes(n, nnz, torch.float64), dtype=torch.uint8, device=dev)
     x = torch.empty(n, dtype=torch.float64, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # --loop host: the three-kernel host loop; anything else: the resident kernel
+    loop = sla.SLA_LOOP_HOST if args.loop == "host" else sla.SLA_LOOP_AUTO
 
     def step():
         e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         e0.record(stream)
-        _, fi, _ = sla.sla_bicgstab_solve(A, b, rtol=w.rtol, maxit=w.maxit, x=x, workspace=ws)
+        _, fi, _ = sla.sla_bicgstab_solve(A, b, rtol=w.rtol, maxit=w.maxit, x=x, workspace=ws, loop=loop)
         e1.record(stream)
-        _, _, ai = sla.sla_bicgstab_adjoint(A, x, g, rtol=w.rtol, maxit=w.maxit, workspace=ws)
+        _, _, ai = sla.sla_bicgstab_adjoint(A, x, g, rtol=w.rtol, maxit=w.maxit, workspace=ws, loop=loop)
         e2.record(stream)
         return e0, e1, e2, fi, ai
 
@@ -888,12 +890,13 @@ def run_bicgstab(args, rank, world, local_rank):
     peak, peak_kind = measured_peaks()
     fwd_s = sum(fwd_ms) / 1e3
     achieved = Bi * sum(iters_f) / fwd_s / 1e9
-    tr = None if args.grid_m else profiled_traffic(args.config)
+    path = recs[-1][3].path
+    # the traffic record is the resident kernel's
+    tr = None if (args.grid_m or path != "resident") else profiled_traffic(args.config)
     clocks = clk.summary()
     flops_it = flops_iter_bicgstab(n, nnz)
     fp64_peak = fp64_peak_tflops(clocks)
     fp64_ach = flops_it * sum(iters_f) / fwd_s / 1e12
-    path = recs[-1][3].path
     kernel_name = {"resident": "bi_resident (one persistent cooperative kernel per solve)",
                    "host": "bi_dir_apply + bi_s_apply + bi_update (host loop)"}.get(path, path)
     e2e = None if args.no_e2e else run_e2e(args, w, dev, 0, sla, torch, method="bicgstab")
@@ -906,7 +909,7 @@ def run_bicgstab(args, rank, world, local_rank):
         "config": {"workload": w.name, "n": n, "nnz": nnz, "rtol": w.rtol, "precond": "none",
                    "step": "forward BiCGStab solve + adjoint (A^T lambda = g by BiCGStab; grad_b, grad_values)",
                    "l2": "flushed between steps (256 MB write); within a solve the iterations reuse L2",
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU", "loop": args.loop},
         "iters_forward": statistics.mean(iters_f), "iters_adjoint": statistics.mean(iters_a),
         "time_to_tolerance_ms": statistics.mean(fwd_ms), "adjoint_ms": statistics.mean(adj_ms),
         "status": sorted(status), "path": path,

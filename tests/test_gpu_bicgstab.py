@@ -76,6 +76,20 @@ def test_bicgstab_and_adjoint_match_the_oracle(name, loop):
     assert rel(gv.cpu().numpy(), adj["grad_values"]) <= GRAD_TOL_F64
 
 
+@pytest.mark.parametrize("loop", list(LOOPS))
+def test_bicgstab_from_a_start_vector(loop):
+    # r0 = b - A x0 and rhat = r0 from a random x0, against the oracle from the same x0
+    A = CASES["cd45_i64"]
+    rng = np.random.default_rng(11)
+    b, x0 = rng.standard_normal(A.n), rng.standard_normal(A.n)
+    x, info, hist = sla.sla_bicgstab_solve(to_dev(A), t(b), x0=t(x0), rtol=1e-10, history=True, loop=LOOPS[loop])
+    ref = oracle.bicgstab(A.row_ptr, A.col_idx, A.values, b, x0=x0, rtol=1e-10, history=True)
+    assert info.status == ref["status"] == 0 and info.path == loop
+    assert abs(info.iters - ref["iters"]) <= 1 + max(ref["iters"] // 20, iteration_spread(A, b, 1e-10, 100000))
+    assert rel(x.cpu().numpy(), ref["x"]) <= X_TOL_F64
+    check_history(hist.cpu().numpy(), ref["history"], k=min(8, ref["iters"]))
+
+
 def test_bicgstab_on_spd_equals_the_cg_solution():
     A = poisson_5pt(40)
     b = np.random.default_rng(3).standard_normal(A.n)
