@@ -409,7 +409,7 @@ def sla_bicgstab_adjoint(A: CSRMatrix, x: torch.Tensor, g: torch.Tensor, rtol: f
                          want_grad_values: bool = True, workspace: Optional[torch.Tensor] = None, unroll: int = 0,
                          loop: int = SLA_LOOP_AUTO):
     """Adjoint of the BiCGStab solve: A^T lambda = g; returns (grad_b = lambda, grad_values or None, CGInfo).
-    A's pattern must be structurally symmetric (status SLA_BAD_CSR otherwise)."""
+    A^T shares A's pattern when that is structurally symmetric, and is built explicitly otherwise."""
     dt, dev = A.values.dtype, A.values.device
     grad_b = torch.empty(A.n, dtype=dt, device=dev)
     grad_values = torch.empty(A.nnz, dtype=dt, device=dev) if want_grad_values else None
@@ -452,7 +452,7 @@ def solve(A: CSRMatrix, b: torch.Tensor, rtol: float = 1e-8, maxit: int = 10000,
           precond: int = SLA_PRECOND_NONE, method: str = "cg") -> torch.Tensor:
     """Differentiable x = A^{-1} b (gradients flow to A.values and b).  method "cg": symmetric
     positive definite A (optionally Jacobi preconditioned); "bicgstab": general A, unpreconditioned
-    (its backward needs a structurally symmetric pattern)."""
+    (its backward solves A^T lambda = dL/dx by the same method)."""
     if method == "cg":
         return CGSolve.apply(A.row_ptr, A.col_idx, A.values, b, rtol, maxit, precond)
     if method == "bicgstab":

@@ -25,8 +25,8 @@
 // last block to arrive adds the block sums in index order) and every scalar decision is taken by
 // that block on the device, so the host only enqueues `unroll` iterations at a time and reads the
 // state between them; the kernels of a finished solve return at once.  The adjoint runs the same
-// kernels on A's pattern with every value taken from its partner entry (j, i): A^T on a
-// structurally symmetric pattern.
+// kernels on A's pattern with every value taken from its partner entry (j, i) when the pattern is
+// structurally symmetric, and on an explicitly built A^T otherwise.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -51,6 +51,7 @@ struct BiCtl {
   uint32_t bad;     // a row range, a column index or (adjoint) a partner entry was missing
   uint32_t arrive;  // grid-barrier arrivals of the resident kernel
   uint32_t timeout; // a grid-barrier wait of the resident kernel expired
+  uint32_t nopartner;  // (adjoint) an entry (i, j) has no stored (j, i): A^T is built explicitly
 };
 
 // Rows of block partial sums: the streaming kernels use rows 0-2; the resident kernel gives each
@@ -58,8 +59,13 @@ struct BiCtl {
 // already in the next phase never overwrites sums that another block is still reading.
 constexpr int kBiSlots = 8;
 
+// Rows of the explicit transpose's column-count scan handled by one block.
+constexpr int64_t kTrChunk = 4096;
+
 struct BiLayout {
-  size_t ctl, part, r, rh, p[2], v[2], s, t, vt, total;
+  size_t ctl, part, r, rh, p[2], v[2], s, t, vt;
+  size_t tp, tci, cnt, bsum;  // the adjoint's explicit A^T (patterns without partner entries)
+  size_t total;
 };
 
 BiLayout bi_layout(int64_t n, int64_t nnz, size_t vsz) {
@@ -77,6 +83,10 @@ BiLayout bi_layout(int64_t n, int64_t nnz, size_t vsz) {
   L.s = off; off += vec;
   L.t = off; off += vec;
   L.vt = off; off += align256(vsz * (size_t)nnz);  // the adjoint's transposed values
+  L.tp = off; off += align256(sizeof(int64_t) * ((size_t)n + 1));  // A^T row pointers (as A's type)
+  L.tci = off; off += align256(sizeof(int32_t) * (size_t)nnz);     // A^T column indices
+  L.cnt = off; off += align256(sizeof(int32_t) * (size_t)n);       // column counts, then cursors
+  L.bsum = off; off += align256(sizeof(int64_t) * (size_t)((n + kTrChunk - 1) / kTrChunk + 1));
   L.total = off;
   return L;
 }
@@ -924,12 +934,13 @@ __global__ void __launch_bounds__(kBlock) bi_finish(BiProb<V, I> P) {
 }
 
 // vt[e] = val[e'] for the entry e' = (j, i) partnering e = (i, j): A^T's values on A's pattern when
-// the pattern is structurally symmetric; a missing partner sets the bad flag (and vt[e] = 0).
+// the pattern is structurally symmetric (columns sorted within rows).  A missing partner sets
+// `nopartner` (A^T is then built explicitly); a malformed row range or column sets `bad`.
 template <typename V, typename I>
 __global__ void __launch_bounds__(kBlock) bi_transpose_values(int64_t n, int64_t nnz, const I *__restrict__ rp,
                                                               const int32_t *__restrict__ ci,
                                                               const V *__restrict__ val, V *__restrict__ vt,
-                                                              uint32_t *bad) {
+                                                              uint32_t *bad, uint32_t *nopartner) {
   for (int64_t i = blockIdx.x * (int64_t)kBlock + threadIdx.x; i < n; i += (int64_t)gridDim.x * kBlock) {
     int64_t e0, e1;
     row_range(rp, i, nnz, e0, e1, bad);
@@ -937,7 +948,8 @@ __global__ void __launch_bounds__(kBlock) bi_transpose_values(int64_t n, int64_t
       const int32_t j = ci[e];
       V out = V(0);
       bool found = false;
-      if (col_ok(j, (int32_t)n, bad)) {
+      const bool jok = col_ok(j, (int32_t)n, bad);
+      if (jok) {
         int64_t j0, j1;
         row_range(rp, j, nnz, j0, j1, bad);
         int64_t lo = j0, hi = j1;
@@ -951,10 +963,171 @@ __global__ void __launch_bounds__(kBlock) bi_transpose_values(int64_t n, int64_t
           found = true;
         }
       }
-      if (!found) atomicOr(bad, 1u);
+      if (jok && !found) atomicOr(nopartner, 1u);
       vt[e] = out;
     }
   }
+}
+
+// ---- explicit A^T for patterns without partner entries (run only on a well-formed CSR)
+//
+// Column counts, an exclusive scan of them into A^T's row pointers (per-chunk sums, a scan of the
+// chunk sums, per-chunk scans), a scatter through per-column cursors, and a sort of every A^T row
+// by column: the scatter's order depends on the atomics' timing, the sorted rows do not (given no
+// duplicate entries), so the adjoint solve sums every row of A^T in the same order each time.
+
+template <typename I>
+__global__ void __launch_bounds__(kBlock) tr_count(int64_t n, const I *__restrict__ rp, const int32_t *__restrict__ ci,
+                                                   int32_t *cnt) {
+  for (int64_t i = blockIdx.x * (int64_t)kBlock + threadIdx.x; i < n; i += (int64_t)gridDim.x * kBlock)
+    for (int64_t e = (int64_t)rp[i]; e < (int64_t)rp[i + 1]; ++e) atomicAdd(cnt + ci[e], 1);
+}
+
+// Block sum of one int64 per thread of a 1024-thread block, in thread 0.
+__device__ __forceinline__ int64_t tr_block_sum(int64_t v, int64_t *s_w) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int64_t t = 0;
+  if (threadIdx.x < 32) {
+    t = s_w[threadIdx.x];
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_down_sync(0xffffffffu, t, o);
+  }
+  __syncthreads();
+  return t;
+}
+
+// Exclusive scan of one int64 per thread of a 1024-thread block; every thread gets its prefix.
+__device__ __forceinline__ int64_t tr_block_exscan(int64_t v, int64_t *s_w) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t inc = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) s_w[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = s_w[lane], winc = w;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, winc, o);
+      if (lane >= o) winc += y;
+    }
+    s_w[lane] = winc - w;  // exclusive prefix of the warp sums
+  }
+  __syncthreads();
+  const int64_t out = s_w[warp] + inc - v;
+  __syncthreads();
+  return out;
+}
+
+// bsum[b] = sum of cnt over chunk b (kTrChunk rows: 1024 threads x 4).
+__global__ void __launch_bounds__(1024) tr_chunk_sums(int64_t n, const int32_t *__restrict__ cnt, int64_t *bsum) {
+  __shared__ int64_t s_w[32];
+  const int64_t base = blockIdx.x * kTrChunk + (int64_t)threadIdx.x * 4;
+  int64_t v = 0;
+  for (int u = 0; u < 4; ++u)
+    if (base + u < n) v += cnt[base + u];
+  const int64_t t = tr_block_sum(v, s_w);
+  if (threadIdx.x == 0) bsum[blockIdx.x] = t;
+}
+
+// bsum[0..nb) replaced by its exclusive scan, and bsum[nb] = the total; one block.
+__global__ void __launch_bounds__(1024) tr_scan_sums(int64_t nb, int64_t *bsum) {
+  __shared__ int64_t s_w[32];
+  const int64_t per = (nb + 1023) / 1024;
+  const int64_t a = (int64_t)threadIdx.x * per, b = a + per < nb ? a + per : nb;
+  int64_t v = 0;
+  for (int64_t k = a; k < b; ++k) v += bsum[k];
+  int64_t run = tr_block_exscan(v, s_w);
+  __syncthreads();
+  for (int64_t k = a; k < b; ++k) {
+    const int64_t c = bsum[k];
+    bsum[k] = run;
+    run += c;
+  }
+  if (b == nb && a < b) bsum[nb] = run;  // the thread holding the last chunk
+  if (nb == 0 && threadIdx.x == 0) bsum[0] = 0;
+}
+
+// tp[j] = bsum[chunk] + the exclusive prefix of cnt within the chunk; tp[n] = the total.
+template <typename I>
+__global__ void __launch_bounds__(1024) tr_chunk_scan(int64_t n, const int32_t *__restrict__ cnt,
+                                                      const int64_t *__restrict__ bsum, I *tp) {
+  __shared__ int64_t s_w[32];
+  const int64_t base = blockIdx.x * kTrChunk + (int64_t)threadIdx.x * 4;
+  int64_t c[4], v = 0;
+  for (int u = 0; u < 4; ++u) {
+    c[u] = base + u < n ? cnt[base + u] : 0;
+    v += c[u];
+  }
+  int64_t run = bsum[blockIdx.x] + tr_block_exscan(v, s_w);
+  for (int u = 0; u < 4; ++u) {
+    if (base + u < n) tp[base + u] = (I)run;
+    run += c[u];
+    if (base + u == n - 1) tp[n] = (I)run;
+  }
+}
+
+// Scatter every entry (i, j) of A into row j of A^T through the column's cursor.
+template <typename V, typename I>
+__global__ void __launch_bounds__(kBlock) tr_scatter(int64_t n, const I *__restrict__ rp, const int32_t *__restrict__ ci,
+                                                     const V *__restrict__ val, const I *__restrict__ tp,
+                                                     int32_t *cur, int32_t *__restrict__ tci, V *__restrict__ tval) {
+  for (int64_t i = blockIdx.x * (int64_t)kBlock + threadIdx.x; i < n; i += (int64_t)gridDim.x * kBlock)
+    for (int64_t e = (int64_t)rp[i]; e < (int64_t)rp[i + 1]; ++e) {
+      const int32_t j = ci[e];
+      const int64_t pos = (int64_t)tp[j] + atomicAdd(cur + j, 1);
+      tci[pos] = (int32_t)i;
+      tval[pos] = val[e];
+    }
+}
+
+// Sort every row of A^T by column (insertion sort, one thread per row), values alongside.
+template <typename V, typename I>
+__global__ void __launch_bounds__(kBlock) tr_sort_rows(int64_t n, const I *__restrict__ tp, int32_t *__restrict__ tci,
+                                                       V *__restrict__ tval) {
+  for (int64_t j = blockIdx.x * (int64_t)kBlock + threadIdx.x; j < n; j += (int64_t)gridDim.x * kBlock) {
+    const int64_t a = (int64_t)tp[j], b = (int64_t)tp[j + 1];
+    for (int64_t k = a + 1; k < b; ++k) {
+      const int32_t key = tci[k];
+      const V kv = tval[k];
+      int64_t m = k - 1;
+      while (m >= a && tci[m] > key) {
+        tci[m + 1] = tci[m];
+        tval[m + 1] = tval[m];
+        --m;
+      }
+      tci[m + 1] = key;
+      tval[m + 1] = kv;
+    }
+  }
+}
+
+// Builds A^T (row pointers tp of A's index type, columns tci, values tval) from a well-formed A.
+template <typename V, typename I>
+sla_status tr_build(const sla_csr *A, const BiLayout &L, char *ws, cudaStream_t st) {
+  const int64_t n = A->n;
+  int32_t *cnt = (int32_t *)(ws + L.cnt);
+  int64_t *bsum = (int64_t *)(ws + L.bsum);
+  I *tp = (I *)(ws + L.tp);
+  const I *rp = (const I *)A->row_ptr;
+  const int G = bi_grid(n);
+  const int64_t nb = (n + kTrChunk - 1) / kTrChunk;
+  cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * (size_t)n, st);
+  if (e != cudaSuccess) return fail(e);
+  tr_count<I><<<G, kBlock, 0, st>>>(n, rp, A->col_idx, cnt);
+  tr_chunk_sums<<<(unsigned)nb, 1024, 0, st>>>(n, cnt, bsum);
+  tr_scan_sums<<<1, 1024, 0, st>>>(nb, bsum);
+  tr_chunk_scan<I><<<(unsigned)nb, 1024, 0, st>>>(n, cnt, bsum, tp);
+  if ((e = cudaGetLastError()) != cudaSuccess) return fail(e);
+  if ((e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * (size_t)n, st)) != cudaSuccess) return fail(e);
+  tr_scatter<V, I><<<G, kBlock, 0, st>>>(n, rp, A->col_idx, (const V *)A->values, tp, cnt, (int32_t *)(ws + L.tci),
+                                         (V *)(ws + L.vt));
+  tr_sort_rows<V, I><<<G, kBlock, 0, st>>>(n, tp, (int32_t *)(ws + L.tci), (V *)(ws + L.vt));
+  if ((e = cudaGetLastError()) != cudaSuccess) return fail(e);
+  count_launches(6);
+  return SLA_OK;
 }
 
 // The resident engine: one cooperative launch for the whole solve.  SLA_INVALID_ARG when it cannot
@@ -1085,20 +1258,27 @@ sla_status bi_adjoint_t(const sla_csr *A, const void *x, const void *g, const sl
   if (e != cudaSuccess) return fail(e);
   const int G = bi_grid(A->n);
   bi_transpose_values<V, I><<<G, kBlock, 0, st>>>(A->n, A->nnz, (const I *)A->row_ptr, A->col_idx,
-                                                   (const V *)A->values, (V *)(ws + L.vt), &P.C->bad);
+                                                   (const V *)A->values, (V *)(ws + L.vt), &P.C->bad,
+                                                   &P.C->nopartner);
   if ((e = cudaGetLastError()) != cudaSuccess) return fail(e);
   count_launches(1);
-  uint32_t hbad = 0;
-  if ((e = cudaMemcpyAsync(&hbad, &P.C->bad, sizeof(hbad), cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+  BiCtl h;
+  if ((e = cudaMemcpyAsync(&h, P.C, sizeof(h), cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
       (e = cudaStreamSynchronize(st)) != cudaSuccess)
     return fail(e);
-  if (hbad) {
+  if (h.bad) {
     if (info) {
       memset(info, 0, sizeof(*info));
       info->status = SLA_BAD_CSR;
       info->path = SLA_LOOP_HOST;
     }
     return SLA_OK;
+  }
+  if (h.nopartner) {
+    // the pattern is not structurally symmetric: solve on an explicitly built A^T
+    SLA_CHECK((tr_build<V, I>(A, L, ws, st)));
+    P.rp = (const I *)(ws + L.tp);
+    P.ci = (const int32_t *)(ws + L.tci);
   }
   sla_status s = bi_run<V, I>(P, o, st, info);
   if (s != SLA_OK) return s;

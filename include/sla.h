@@ -259,8 +259,8 @@ SLA_API sla_status sla_cg_adjoint_batched(const sla_csr *pattern, int64_t batch,
 
 /*
  * Bytes of device workspace sla_bicgstab_solve and sla_bicgstab_adjoint need (0 for invalid
- * arguments): eight n-vectors (r, rhat, two p, two v, s, t), the adjoint's transposed values (nnz)
- * and the reductions' scratch.
+ * arguments): eight n-vectors (r, rhat, two p, two v, s, t), the adjoint's A^T (values, column
+ * indices and row pointers) with its construction scratch, and the reductions' scratch.
  */
 SLA_API size_t sla_bicgstab_workspace_bytes(int64_t n, int64_t nnz, int32_t dtype);
 
@@ -289,11 +289,13 @@ SLA_API sla_status sla_bicgstab_solve(const sla_csr *A, const void *b, const voi
 /*
  * Adjoint backward of x = A^{-1} b for a general A (TS Methodology 2): lambda solves
  * A^T lambda = g by the same BiCGStab (same rtol, maxit) from lambda = 0, written into grad_b;
- * then grad_values[e] = -lambda[row(e)] * x[col(e)] on A's pattern (NULL: skipped).  A^T is formed
- * on A's pattern, every value taken from its partner entry (j, i): the pattern must be
- * structurally symmetric (a stored (j, i) for every stored (i, j), columns sorted within rows),
- * else info->status is SLA_BAD_CSR and nothing is solved.  Arguments and workspace as for
- * sla_bicgstab_solve; x, g, grad_b device n-vectors, grad_values device nnz entries.
+ * then grad_values[e] = -lambda[row(e)] * x[col(e)] on A's pattern (NULL: skipped).  When the
+ * pattern is structurally symmetric (a stored (j, i) for every stored (i, j), columns sorted
+ * within rows), A^T is used on A's own pattern, every value taken from its partner entry (j, i);
+ * otherwise A^T is built explicitly in the workspace (each row's entries in column order, so the
+ * result does not depend on the build's atomics; A without duplicate entries).  A malformed row
+ * range or column gives info->status SLA_BAD_CSR and nothing is solved.  Arguments and workspace
+ * as for sla_bicgstab_solve; x, g, grad_b device n-vectors, grad_values device nnz entries.
  */
 SLA_API sla_status sla_bicgstab_adjoint(const sla_csr *A, const void *x, const void *g, const sla_cg_opts *opts,
                                         void *grad_b, void *grad_values, sla_cg_info *info, void *workspace,

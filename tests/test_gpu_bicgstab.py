@@ -1,8 +1,9 @@
 """BiCGStab for a general A (libsla, through the C ABI) against the fp64 oracle.
 
 Non-symmetric inputs: the convection-diffusion operator on the five-point pattern (central
-differences, structurally symmetric) and a random diagonally dominant pattern with non-symmetric
-values.  Checked: the solution at 1e-9, the iteration count, the first residual-history entries
+differences, structurally symmetric), a random diagonally dominant pattern with non-symmetric
+values, and structurally non-symmetric patterns (random rows, upper bidiagonal) whose adjoint
+builds A^T explicitly.  Checked: the solution at 1e-9, the iteration count, the first residual-history entries
 at 1e-8, the adjoint (A^T lambda = g) gradients grad_b and grad_values at 1e-7 with the oracle's
 adjoint chained from its own solution, and the status cases.
 """
@@ -225,7 +226,50 @@ def test_bicgstab_status_cases(loop):
     assert st == sla.SLA_INVALID_ARG
 
 
-def test_bicgstab_adjoint_needs_a_structurally_symmetric_pattern():
+def _nonsym_pattern(n, seed):
+    """A structurally non-symmetric, strictly diagonally dominant matrix: every row its diagonal
+    and 0-5 random off-diagonal columns (every 97th row 40), values U(-1, 1), the diagonal
+    1 + the row's absolute off-diagonal sum."""
+    rng = np.random.default_rng(seed)
+    rp, ci, vals = [0], [], []
+    for i in range(n):
+        k = 40 if i % 97 == 0 else int(rng.integers(0, 6))
+        off = rng.choice(np.delete(np.arange(n), i), size=min(k, n - 1), replace=False)
+        ov = rng.uniform(-1.0, 1.0, off.size)
+        cols = np.concatenate([off, [i]])
+        v = np.concatenate([ov, [1.0 + np.abs(ov).sum()]])
+        order = np.argsort(cols)
+        ci.extend(cols[order])
+        vals.extend(v[order])
+        rp.append(len(ci))
+    return CSR(n, np.array(rp, dtype=np.int32), np.array(ci, dtype=np.int32), np.array(vals))
+
+
+@pytest.mark.parametrize("loop", list(LOOPS))
+def test_bicgstab_adjoint_on_a_pattern_without_partners(loop):
+    # no stored (j, i) for most (i, j): the adjoint builds A^T explicitly, as the oracle does
+    A = _nonsym_pattern(3000, 4)
+    rp64 = A.row_ptr.astype(np.int64)
+    rows = np.repeat(np.arange(A.n), np.diff(rp64))
+    assert not set(zip(rows.tolist(), A.col_idx.tolist())) <= set(zip(A.col_idx.tolist(), rows.tolist()))
+    rng = np.random.default_rng(12)
+    b, g = rng.standard_normal(A.n), rng.standard_normal(A.n)
+    dA = to_dev(A)
+    x, info, _ = sla.sla_bicgstab_solve(dA, t(b), rtol=1e-11, loop=LOOPS[loop])
+    ref = oracle.bicgstab(A.row_ptr, A.col_idx, A.values, b, rtol=1e-11)
+    assert info.status == ref["status"] == 0 and rel(x.cpu().numpy(), ref["x"]) <= X_TOL_F64
+    gb, gv, ai = sla.sla_bicgstab_adjoint(dA, x, t(g), rtol=1e-11, loop=LOOPS[loop])
+    adj = oracle.bicgstab_adjoint(A.row_ptr, A.col_idx, A.values, ref["x"], g, rtol=1e-11)
+    assert ai.status == adj["status"] == 0 and ai.path == loop
+    assert abs(ai.iters - adj["iters"]) <= 2 + adj["iters"] // 10, (ai.iters, adj["iters"])
+    assert rel(gb.cpu().numpy(), adj["grad_b"]) <= GRAD_TOL_F64
+    assert rel(gv.cpu().numpy(), adj["grad_values"]) <= GRAD_TOL_F64
+    # the transpose's rows are sorted after the scatter: the same bits every time
+    gb2, gv2, _ = sla.sla_bicgstab_adjoint(dA, x, t(g), rtol=1e-11, loop=LOOPS[loop])
+    assert torch.equal(gb, gb2) and torch.equal(gv, gv2)
+
+
+def test_bicgstab_adjoint_upper_bidiagonal():
     # an upper-bidiagonal pattern, (i, i+1) stored and (i+1, i) not, with random values and b.
     # (Constant values with b = ones is a degenerate case for the method itself: there rhat.r is zero
     # in exact arithmetic from the third iteration on, and the trajectory is decided by rounding.)
@@ -239,12 +283,31 @@ def test_bicgstab_adjoint_needs_a_structurally_symmetric_pattern():
     A = CSR(n, rp, ci, v)
     dA = to_dev(A)
     x, info, _ = sla.sla_bicgstab_solve(dA, t(b), rtol=1e-12)
-    assert info.status == 0  # the forward solve does not need it
+    assert info.status == 0
     ref = oracle.bicgstab(rp, ci, v, b, rtol=1e-12)
     assert rel(x.cpu().numpy(), ref["x"]) <= X_TOL_F64
     assert rel(x.cpu().numpy(), np.linalg.solve(A.dense(), b)) <= 1e-10
-    _, _, ainfo = sla.sla_bicgstab_adjoint(dA, x, t(b), rtol=1e-12)
+    gb, gv, ainfo = sla.sla_bicgstab_adjoint(dA, x, t(b), rtol=1e-12)
+    adj = oracle.bicgstab_adjoint(rp, ci, v, ref["x"], b, rtol=1e-12)
+    assert ainfo.status == adj["status"] == 0
+    assert rel(gb.cpu().numpy(), np.linalg.solve(A.dense().T, b)) <= 1e-10
+    assert rel(gv.cpu().numpy(), adj["grad_values"]) <= GRAD_TOL_F64
+    # through autograd
+    vals = dA.values.clone().requires_grad_(True)
+    sla.solve(dA.with_values(vals), t(b), rtol=1e-12, method="bicgstab").backward(t(b))
+    assert torch.equal(vals.grad, gv)
+
+
+@pytest.mark.parametrize("loop", list(LOOPS))
+def test_bicgstab_reports_a_malformed_pattern(loop):
+    # a column index past n: every kernel checks columns before it reads, skips the entry and
+    # raises the flag; the solve and the adjoint both report SLA_BAD_CSR
+    A = convection_diffusion(10)
+    ci = A.col_idx.copy()
+    ci[7] = A.n
+    dA = sla.CSRMatrix.from_numpy(A.row_ptr, ci, A.values, "cuda:0")
+    b = t(np.random.default_rng(2).standard_normal(A.n))
+    x, info, _ = sla.sla_bicgstab_solve(dA, b, rtol=1e-10, loop=LOOPS[loop])
+    assert info.status == sla.SLA_BAD_CSR
+    _, _, ainfo = sla.sla_bicgstab_adjoint(dA, x, b, rtol=1e-10, loop=LOOPS[loop])
     assert ainfo.status == sla.SLA_BAD_CSR
-    with pytest.raises(sla.SlaError):
-        vals = dA.values.clone().requires_grad_(True)
-        sla.solve(dA.with_values(vals), t(b), rtol=1e-12, method="bicgstab").sum().backward()
