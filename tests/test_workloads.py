@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 from workloads import (poisson_5pt, diffusion_interior, diffusion_dirichlet, random_spd, config1, config3,
-                       small_poisson)
+                       small_poisson, convection_diffusion, config_by_name)
 from oracle_pins import poisson_eigs
 
 
@@ -97,3 +97,39 @@ def test_config3_small_batch():
 def test_small_poisson_seeded():
     a, b = small_poisson(10, 3), small_poisson(10, 3)
     assert np.array_equal(a.b, b.b) and np.array_equal(a.g, b.g)
+
+
+@pytest.mark.parametrize("m", [1, 2, 6, 11])
+def test_convection_diffusion_structure(m):
+    # the five-point pattern of the Poisson matrix; with no convection, the Poisson matrix itself;
+    # otherwise its symmetric part is the Poisson matrix and its skew part +-cx (east / west),
+    # +-cy (south / north); a nonsingular M-matrix for |cx|, |cy| < 1
+    cx, cy = 0.4, 0.25
+    A = convection_diffusion(m, cx, cy)
+    P = poisson_5pt(m)
+    _canonical(A)
+    assert np.array_equal(A.row_ptr, P.row_ptr) and np.array_equal(A.col_idx, P.col_idx)
+    assert np.array_equal(convection_diffusion(m, 0.0, 0.0).values, P.values)
+    D, DP = A.dense(), P.dense()
+    assert np.allclose(0.5 * (D + D.T), DP, rtol=0, atol=1e-15)
+    K = 0.5 * (D - D.T)
+    i = np.arange(A.n)
+    a, c = np.divmod(i, m)
+    east = c < m - 1
+    south = a < m - 1
+    assert np.allclose(K[i[east], i[east] + 1], cx, rtol=0, atol=1e-15)
+    assert np.allclose(K[i[south], i[south] + m], cy, rtol=0, atol=1e-15)
+    assert np.count_nonzero(np.abs(K) > 1e-15) == 2 * (np.count_nonzero(east) + np.count_nonzero(south))
+    off = D - np.diag(np.diag(D))
+    assert np.all(off <= 0) and np.all(D.sum(axis=1) >= -1e-15)
+    if A.n > 1:
+        assert np.min(np.linalg.eigvals(D).real) > 0
+    B = convection_diffusion(m, cx, cy, rowptr64=True)
+    assert B.row_ptr.dtype == np.int64 and np.array_equal(B.values, A.values)
+
+
+def test_convdiff_bicgstab_workload():
+    w = config_by_name("convdiff1000_bicgstab", m=30)
+    assert w.A.n == 900 and w.A.nnz == 5 * 900 - 4 * 30 and w.rtol == 1e-8 and w.meta["method"] == "bicgstab"
+    assert np.array_equal(w.b, np.random.default_rng(0).standard_normal(900))
+    assert np.array_equal(w.g, np.random.default_rng(1).standard_normal(900))
