@@ -1,6 +1,7 @@
 """BiCGStab for a general A (libsla, through the C ABI) against the fp64 oracle.
 
-Non-symmetric inputs: the convection-diffusion operator on the five-point pattern (central
+Non-symmetric inputs (residual history compared over the first 20 iterations, or up to where the
+oracle parts from itself under rounding-level changes): the convection-diffusion operator on the five-point pattern (central
 differences, structurally symmetric), a random diagonally dominant pattern with non-symmetric
 values, and structurally non-symmetric patterns (random rows, upper bidiagonal) whose adjoint
 builds A^T explicitly.  Checked: the solution at 1e-9, the iteration count, the first residual-history entries
@@ -39,6 +40,27 @@ CASES = {
 LOOPS = {"resident": sla.SLA_LOOP_AUTO, "host": sla.SLA_LOOP_HOST}
 
 
+def history_horizon(A, b, rtol, maxit, k=20, trials=3):
+    """The first k residual-history entries, cut before the oracle parts from itself by more than the
+    history bar: under one-ulp changes of b (every entry up or down at random), and between its two
+    builds, which differ only in the dot products' summation order, as the GPU does.  BiCGStab
+    amplifies rounding quickly on some matrices: on the random non-symmetric case one-ulp changes
+    of b part the oracle from itself at iteration 9."""
+    def apart(h, h0):
+        m = min(len(h), len(h0), k + 1)
+        idx = np.nonzero(np.abs(h[:m] - h0[:m]) > 1e-8 * np.abs(h0[:m]) + 1e-13)[0]
+        return int(idx[0]) - 1 if idx.size else k
+
+    run = lambda bb, lib=None: oracle.bicgstab(A.row_ptr, A.col_idx, A.values, bb, rtol=rtol, maxit=maxit,
+                                               history=True, lib=lib)["history"]
+    h0 = run(b)
+    horizon = apart(run(b, oracle.load_parallel()), h0)
+    for tr in range(trials):
+        sgn = np.where(np.random.default_rng(200 + tr).random(A.n) < 0.5, -1.0, 1.0)
+        horizon = min(horizon, apart(run(b + sgn * np.spacing(b)), h0))
+    return horizon
+
+
 def iteration_spread(A, b, rtol, maxit, trials=4):
     """How far the oracle's own stopping iteration moves when every entry of b moves by one ulp
     (up or down at random): BiCGStab's residual is not monotone, and near the threshold two
@@ -68,7 +90,7 @@ def test_bicgstab_and_adjoint_match_the_oracle(name, loop):
     assert abs(info.iters - ref["iters"]) <= slack, (info.iters, ref["iters"], slack)
     assert rel(x.cpu().numpy(), ref["x"]) <= X_TOL_F64
     h = hist.cpu().numpy()
-    check_history(h, ref["history"], k=min(8, ref["iters"]))
+    check_history(h, ref["history"], k=min(ref["iters"], history_horizon(A, b, rtol, maxit)))
     assert np.isnan(h[info.iters + 1:]).all()
     gb, gv, ainfo = sla.sla_bicgstab_adjoint(dA, x, t(g), rtol=rtol, maxit=maxit, loop=LOOPS[loop])
     adj = oracle.bicgstab_adjoint(A.row_ptr, A.col_idx, A.values, ref["x"], g, rtol=rtol, maxit=maxit)
