@@ -183,3 +183,15 @@ def test_library_reads_no_environment_variables():
     csrc = os.path.join(ROOT, "differentiable_sparse_iterative_gb300", "csrc")
     for f in os.listdir(csrc):
         assert "getenv" not in open(os.path.join(csrc, f)).read(), f
+
+
+def test_bicgstab_workspace_bytes(lib):
+    f = lib.sla_bicgstab_workspace_bytes
+    assert f(-1, 0, 1) == 0 and f(10, -1, 1) == 0 and f(10, 10, 7) == 0
+    n, nnz = 100_000, 500_000
+    f64, f32 = f(n, nnz, 1), f(n, nnz, 0)
+    # eight n-vectors, the transposed values, A^T's column indices, row pointers and column counts
+    assert f64 >= 8 * 8 * n + 8 * nnz + 4 * nnz + 8 * (n + 1) + 4 * n
+    assert f32 >= 8 * 4 * n + 4 * nnz + 4 * nnz + 8 * (n + 1) + 4 * n
+    assert f64 > f32 and f(n, 2 * nnz, 1) - f64 >= (8 + 4) * nnz - 512
+    assert f(0, 0, 1) > 0  # the control block and the reductions' scratch
